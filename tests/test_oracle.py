@@ -1,0 +1,315 @@
+"""Pins for the CPU oracle: closed forms, invariants, brute force and the
+numbers printed in the guide. None of these calls the CUDA library."""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import msa_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+RNG = np.random.default_rng(12345)
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# --------------------------------------------------------------------------- rounding
+
+def test_bf16_rounding_matches_torch_conversion():
+    # torch's float32 -> bfloat16 conversion is round-to-nearest-even
+    x = np.concatenate([
+        RNG.standard_normal(20000).astype(np.float32),
+        (RNG.standard_normal(2000) * 1e-30).astype(np.float32),
+        (RNG.standard_normal(2000) * 1e30).astype(np.float32),
+        np.array([0.0, -0.0, 1.0, -1.0, 3.0e38, -3.0e38, 1e-40, np.inf, -np.inf], dtype=np.float32),
+    ])
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.round_f32_to_bf16(x)
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_rounding_ties_to_even():
+    ulp = 2.0 ** -7  # bf16 spacing in [1, 2)
+    cases = {
+        1.0 + ulp / 2: 1.0,                    # tie, 1.0 is even
+        1.0 + ulp + ulp / 2: 1.0 + 2 * ulp,    # tie, 1+ulp is odd -> up
+        1.0 + ulp / 2 + 2.0 ** -20: 1.0 + ulp,  # just above the tie
+        -(1.0 + ulp / 2): -1.0,
+    }
+    for x, want in cases.items():
+        assert O.round_f32_to_bf16(np.float32(x)) == want
+    assert np.isnan(O.round_f32_to_bf16(np.float32(np.nan)))
+
+
+# --------------------------------------------------------------------------- pooling
+
+def test_pool_constant_block_is_exact():
+    d = O.HEAD_DIM
+    k = np.full((256, d), 0.3125)
+    for store in ("bf16", "f32"):
+        stored, exact = O.pool_block_keys(k, 256, store)
+        assert stored.shape == (4, d)
+        assert np.all(stored == 0.3125) and np.all(exact == 0.3125)
+
+
+def test_pool_closed_form_index_pattern():
+    # K[t, d] = 1024*block + (t mod 64) + d  ->  mean = 1024*block + 31.5 + d exactly
+    d = O.HEAD_DIM
+    t = np.arange(5 * 64 + 17)
+    k = (1024.0 * (t // 64))[:, None] + (t % 64)[:, None] + np.arange(d)[None, :]
+    stored, exact = O.pool_block_keys(k, len(t), "f32")
+    assert stored.shape == (5, d)             # the partial sixth block is not pooled
+    want = (1024.0 * np.arange(5))[:, None] + 31.5 + np.arange(d)[None, :]
+    assert np.array_equal(stored, want) and np.array_equal(exact, want)
+
+
+def test_pool_stored_value_within_rounding_bound_of_mean():
+    d = O.HEAD_DIM
+    k = O.round_f32_to_bf16(RNG.standard_normal((64 * 40, d)).astype(np.float32))
+    stored, exact = O.pool_block_keys(k, k.shape[0], "bf16")
+    # fp32 sum of 64 terms: |err| <= 63 * 2^-24 * sum|x|; then a half bf16 ulp
+    absmean = np.abs(k).reshape(40, 64, d).mean(axis=1)
+    bound = 63 * 2.0 ** -24 * absmean + np.abs(exact) * 2.0 ** -8 + 1e-30
+    assert np.all(np.abs(stored - exact) <= bound)
+
+
+def test_mean_pooled_key_score_equals_mean_of_token_scores():
+    # the reading of the guide's block pooling used here: scoring the mean key is
+    # the mean of the token-level scores (linearity), exact in float64
+    d = O.HEAD_DIM
+    k = RNG.standard_normal((64 * 8, d))
+    q = RNG.standard_normal(d)
+    _, exact = O.pool_block_keys(k, k.shape[0], "f32")
+    tok = (k @ q).reshape(8, 64).mean(axis=1)
+    assert np.allclose(exact @ q, tok, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- index query
+
+def test_index_query_sums_group_heads():
+    d = O.HEAD_DIM
+    g = 3
+    q = np.zeros((g, d))
+    for j in range(g):
+        q[j, 5 * j] = 1.0
+        q[j, 7] = 2.0
+    qi = O.index_query(q)
+    want = np.zeros(d)
+    want[[0, 5, 10]] = 1.0
+    want[7] = 2.0 * g
+    assert np.array_equal(qi, want)
+    # a prefill tile: rows x heads
+    qt = np.ones((64, 8, d))
+    assert np.all(O.index_query(qt) == 512.0)
+
+
+# --------------------------------------------------------------------------- selection
+
+def _brute_force_topk(scores, k):
+    """The unique k-subset whose every member beats every non-member under
+    (higher score, then lower index)."""
+    n = len(scores)
+    beats = lambda i, j: scores[i] > scores[j] or (scores[i] == scores[j] and i < j)  # noqa: E731
+    found = []
+    for sub in itertools.combinations(range(n), min(k, n)):
+        s = set(sub)
+        if all(beats(i, j) for i in s for j in range(n) if j not in s):
+            found.append(sorted(sub))
+    assert len(found) == 1
+    return found[0]
+
+
+@pytest.mark.parametrize("trial", range(60))
+def test_select_matches_brute_force(trial):
+    rng = np.random.default_rng(trial)
+    n = int(rng.integers(1, 11))
+    k = int(rng.integers(1, 6))
+    if trial % 3 == 0:
+        scores = rng.integers(-2, 3, size=n).astype(np.float64)   # many exact ties
+    else:
+        scores = rng.standard_normal(n)
+    forced = n if trial % 2 == 0 else None
+    k_total = k + 1
+    sel = O.select_blocks(scores, k, forced, k_total)
+    want = _brute_force_topk(list(scores), k)
+    if forced is not None:
+        want = sorted(want + [forced])
+    want = want + [-1] * (k_total - len(want))
+    assert list(sel) == want
+
+
+def test_select_pads_when_few_candidates():
+    sel = O.select_blocks(np.array([0.5, 2.0]), 5, 2, 6)
+    assert list(sel) == [0, 1, 2, -1, -1, -1]
+    sel = O.select_blocks(np.zeros(0), 3, 0, 4)
+    assert list(sel) == [0, -1, -1, -1]
+
+
+def test_planted_needles_are_selected():
+    from synth import make_decode_inputs
+    inp = make_decode_inputs([4096], 1, 4, "f32", "contiguous", needles=2, seed=1001)
+    q = inp.q[0].double().numpy()
+    k = inp.kv_rows(0, 0, "k").double().numpy()
+    v = inp.kv_rows(0, 0, "v").double().numpy()
+    res = O.decode_unit(q, k, v, 4096, 8, 9, 1 / math.sqrt(128), "f32")
+    for b in inp.needles[(0, 0)]:
+        assert b in res["selected"]
+    assert res["selected"][-1] == 63          # newest block always kept
+    assert sorted(res["selected"]) == list(res["selected"])
+
+
+# --------------------------------------------------------------------------- attention
+
+def test_attend_zero_query_is_mean_of_values():
+    d = O.HEAD_DIM
+    k = RNG.standard_normal((300, d))
+    v = RNG.standard_normal((300, d))
+    toks = np.array([3, 10, 11, 299])
+    o, lse, p = O.attend(np.zeros((2, d)), k, v, toks, 0.1)
+    assert np.allclose(o, v[toks].mean(axis=0), atol=1e-14)
+    assert np.allclose(lse, math.log(4), atol=1e-14)
+    assert np.allclose(p, 0.25, atol=1e-15)
+
+
+def test_attend_two_tokens_closed_form():
+    d = O.HEAD_DIM
+    k = np.zeros((2, d))
+    k[0, 0], k[1, 1] = 2.0, -1.0
+    v = np.zeros((2, d))
+    v[0, 3], v[1, 4] = 1.0, 1.0
+    q = np.zeros((1, d))
+    q[0, 0], q[0, 1] = 1.5, 0.5
+    scale = 0.25
+    z0, z1 = 1.5 * 2.0 * scale, 0.5 * -1.0 * scale
+    p0 = 1.0 / (1.0 + math.exp(z1 - z0))
+    o, lse, _ = O.attend(q, k, v, np.array([0, 1]), scale)
+    assert abs(o[0, 3] - p0) < 1e-15 and abs(o[0, 4] - (1 - p0)) < 1e-15
+    assert abs(lse[0] - math.log(math.exp(z0) + math.exp(z1))) < 1e-14
+
+
+def test_attend_invariants():
+    d = O.HEAD_DIM
+    k = RNG.standard_normal((500, d))
+    v = RNG.standard_normal((500, d))
+    q = RNG.standard_normal((4, d))
+    toks = np.sort(RNG.choice(500, size=130, replace=False))
+    o, lse, p = O.attend(q, k, v, toks, 1 / math.sqrt(d))
+    assert np.allclose(p.sum(axis=1), 1.0, atol=1e-12)
+    perm = RNG.permutation(len(toks))
+    o2, lse2, _ = O.attend(q, k, v, toks[perm], 1 / math.sqrt(d))
+    assert np.allclose(o, o2, atol=1e-12) and np.allclose(lse, lse2, atol=1e-12)
+    vc = np.tile(RNG.standard_normal(d), (500, 1))
+    o3, _, _ = O.attend(q, k, vc, toks, 1 / math.sqrt(d))
+    assert np.allclose(o3, vc[0], atol=1e-12)
+    o4, _, _ = O.attend(q, k, v, np.array([77]), 1 / math.sqrt(d))
+    assert np.allclose(o4, v[77], atol=1e-15)
+
+
+def test_dense_closed_form_zero_query():
+    d = O.HEAD_DIM
+    v = RNG.standard_normal((200, d))
+    k = RNG.standard_normal((200, d))
+    o, lse = O.dense_gqa(np.zeros((3, d)), k, v, 150, 0.3)
+    assert np.allclose(o, v[:151].mean(axis=0), atol=1e-13)
+    assert np.allclose(lse, math.log(151), atol=1e-13)
+
+
+@pytest.mark.parametrize("seq_len", [64 * 12, 64 * 12 + 1, 64 * 12 + 37])
+def test_all_blocks_selected_equals_dense_decode(seq_len):
+    d = O.HEAD_DIM
+    rng = np.random.default_rng(seq_len)
+    k = rng.standard_normal((64 * 13, d))
+    v = rng.standard_normal((64 * 13, d))
+    q = rng.standard_normal((4, d))
+    nb = O.num_blocks(seq_len)
+    res = O.decode_unit(q, k, v, seq_len, k_scored=nb, k_total=nb, scale=1 / math.sqrt(d), store="f32")
+    assert list(res["selected"]) == list(range(nb))
+    od, ld = O.dense_gqa(q, k, v, seq_len - 1, 1 / math.sqrt(d))
+    assert np.allclose(res["o"], od, rtol=0, atol=1e-12)
+    assert np.allclose(res["lse"], ld, rtol=0, atol=1e-12)
+
+
+def test_all_blocks_selected_equals_dense_prefill():
+    d = O.HEAD_DIM
+    rng = np.random.default_rng(7)
+    q_start, n_new, g = 128, 70, 2
+    total = q_start + n_new
+    k = rng.standard_normal((total, d))
+    v = rng.standard_normal((total, d))
+    q = rng.standard_normal((n_new, g, d))
+    pooled, _ = O.pool_block_keys(k, total, "f32")
+    for tile in range(2):
+        rows = q[tile * 64:(tile + 1) * 64]
+        sel = O.prefill_tile_select(rows, tile, q_start, pooled, k_scored=64, k_total=5)
+        diag = q_start // 64 + tile
+        assert list(sel["selected"][: diag + 1]) == list(range(diag + 1))
+        pos = q_start + tile * 64 + np.arange(rows.shape[0])
+        o, lse = O.prefill_rows(rows, pos, k, v, total, sel["selected"], 1 / math.sqrt(d))
+        for i in range(rows.shape[0]):
+            od, ld = O.dense_gqa(rows[i], k, v, pos[i], 1 / math.sqrt(d))
+            assert np.allclose(o[i], od, atol=1e-12) and np.allclose(lse[i], ld, atol=1e-12)
+
+
+def test_prefill_tile_excludes_future_blocks():
+    d = O.HEAD_DIM
+    rng = np.random.default_rng(3)
+    k = rng.standard_normal((64 * 10, d))
+    pooled, _ = O.pool_block_keys(k, 64 * 10, "f32")
+    q = rng.standard_normal((64, 2, d))
+    sel = O.prefill_tile_select(q, 2, 5 * 64, pooled, k_scored=3, k_total=4)
+    assert sel["diag"] == 7 and len(sel["scores"]) == 7
+    assert sel["selected"][-1] == 7 and all(0 <= b < 7 for b in sel["selected"][:-1])
+
+
+# --------------------------------------------------------------------------- the guide's numbers
+
+def test_golden_block_arithmetic():
+    rows = _golden_rows("block_arithmetic.txt")
+    for r in rows[:-1]:
+        ctx, bs, want = int(r[0]), int(r[1]), int(r[2])
+        assert bs == O.BLOCK and O.num_blocks(ctx) == want
+    sp, flo, fhi, tlo, thi = map(float, rows[-1])
+    nb = O.num_blocks(1048576)
+    touched = 1.0 / sp
+    assert flo <= touched <= fhi
+    assert tlo <= touched * nb * O.BLOCK <= thi
+
+
+def test_golden_diagram_groups_share_one_selection():
+    """Six heads, two KV heads: heads 1-3 must use I1 and heads 4-6 use I2."""
+    rows = _golden_rows("diagram_groups.txt")
+    d = O.HEAD_DIM
+    rng = np.random.default_rng(11)
+    hq, hkv = 6, 2
+    grp = hq // hkv
+    seq_len = 64 * 16
+    k = rng.standard_normal((hkv, seq_len, d))
+    v = rng.standard_normal((hkv, seq_len, d))
+    q = rng.standard_normal((hq, d))
+    # plant a different needle block in each KV head, aligned with its group's mean query
+    needles = {0: 3, 1: 11}
+    for h, b in needles.items():
+        k[h, b * 64:(b + 1) * 64] = 3 * q[h * grp:(h + 1) * grp].mean(axis=0)
+    sel = {}
+    for h in range(hkv):
+        res = O.decode_unit(q[h * grp:(h + 1) * grp], k[h], v[h], seq_len, 2, 3, 1 / math.sqrt(d), "f32")
+        sel[h] = res
+        assert needles[h] in res["selected"]
+    for head1, list1 in rows:
+        j, h = int(head1) - 1, int(list1) - 1
+        assert j // grp == h
+        toks = O.tokens_of_blocks(sel[h]["selected"], seq_len)
+        o, _, _ = O.attend(q[j:j + 1], k[h], v[h], toks, 1 / math.sqrt(d))
+        assert np.allclose(o[0], sel[h]["o"][j - h * grp], atol=1e-13)
+    assert list(sel[0]["selected"]) != list(sel[1]["selected"])
