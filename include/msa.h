@@ -1,0 +1,210 @@
+/*
+ * msa.h -- C ABI of a single-GPU (sm_103a) library for two-stage GQA
+ * block-sparse attention, the "MiniMax Sparse Attention" block.
+ *
+ * Source of the method: the Atlas Cloud guide "MiniMax goes sparse: decoding
+ * M3's attention from a single diagram" (Portuguese, Spanish and French
+ * editions), section 1:
+ *   Step 1 (index branch): each GQA group has one index query; block-level
+ *     scores are formed from token keys pooled per fixed-size block; a top-k
+ *     keeps a short list of KV blocks per layer and per group.
+ *   Step 2 (sparse branch): every query head of a group attends, with ordinary
+ *     softmax attention, over the real (uncompressed) K/V of the blocks its
+ *     group selected.
+ * Where the guide leaves a step open, this library fixes it as a parameter:
+ *   - block size 64 tokens;
+ *   - block summary key = mean of the block's 64 keys of the KV head itself
+ *     (scoring it equals the block mean of the token scores);
+ *   - group index query = sum of the group's query heads (decode) or of the
+ *     tile's 64 tokens x group heads (prefill);
+ *   - the block holding the newest token (decode) or the tile's diagonal block
+ *     (prefill) is always kept and never scored;
+ *   - top-k ties go to the lower block index.
+ *
+ * Conventions for every call:
+ *   - Every pointer argument is a DEVICE pointer unless marked "host".
+ *   - The caller owns and allocates every buffer (inputs, outputs, workspace);
+ *     the library never allocates device memory and never synchronises the
+ *     stream, except msa_read_device_status.
+ *   - Calls are asynchronous on `stream`. Calls that share a workspace must be
+ *     ordered on one stream; distinct workspaces make calls independent.
+ *   - Argument errors are found on the host before any launch and return
+ *     MSA_ERR_INVALID_ARG / MSA_ERR_UNSUPPORTED / MSA_ERR_WORKSPACE with no
+ *     work queued. A failed launch returns MSA_ERR_CUDA.
+ *   - Data-dependent errors (a page id outside [0, num_pages), a sequence
+ *     length above the cache capacity) never fault: the kernel skips the access
+ *     and sets a sticky status word in the workspace, read with
+ *     msa_read_device_status.
+ *   - Head dimension D = 128 and block size 64 are the only supported values.
+ *
+ * Layouts (row-major, innermost last):
+ *   q (decode)   [batch, num_q_heads, 128]         KV dtype
+ *   q (prefill)  [n_q_tokens, num_q_heads, 128]    KV dtype
+ *   KV contiguous  k, v: [batch, num_kv_heads, max_tokens, 128]
+ *   KV paged       k, v: [num_pages, num_kv_heads, 64, 128], page_table
+ *                  [batch, max_pages_per_seq] int32 (logical block -> page)
+ *   pooled keys (same dtype as KV):
+ *     contiguous   [batch, num_kv_heads, max_tokens/64, 128]
+ *     paged        [num_pages, num_kv_heads, 128]  (one summary per page)
+ *   Query head j belongs to KV head j / G, G = num_q_heads / num_kv_heads.
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* msa_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum msa_status {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent shapes */
+  MSA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head_dim != 128) */
+  MSA_ERR_WORKSPACE = 3,     /* workspace null or smaller than msa_workspace_size */
+  MSA_ERR_CUDA = 4,          /* a CUDA launch or API call failed */
+  MSA_ERR_DEVICE_BOUNDS = 5, /* (device status) a page id or length was out of range */
+  MSA_ERR_TIMEOUT = 6        /* (device status) a bounded wait gave up */
+} msa_status;
+
+typedef enum msa_dtype { MSA_DTYPE_F32 = 0, MSA_DTYPE_BF16 = 1 } msa_dtype;
+typedef enum msa_kv_layout { MSA_KV_CONTIGUOUS = 0, MSA_KV_PAGED = 1 } msa_kv_layout;
+
+/* The block-scoring operator of Step 1. Only the mean-pooled-key score is
+ * implemented; it is the block mean of token scores q_idx . k_t. */
+typedef enum msa_score_mode { MSA_SCORE_MEAN_POOLED_KEYS = 0 } msa_score_mode;
+
+/* Description of a KV cache. All pointers are device pointers. */
+typedef struct msa_kv_desc {
+  int32_t layout;            /* msa_kv_layout */
+  int32_t dtype;             /* msa_dtype of k, v, q, pooled keys and outputs */
+  int32_t batch;             /* number of sequences */
+  int32_t num_kv_heads;      /* Hkv */
+  int32_t head_dim;          /* must be 128 */
+  int32_t block_size;        /* must be 64 */
+  const void* k;             /* keys, layout above */
+  const void* v;             /* values, same layout as k */
+  int64_t max_tokens;        /* contiguous: token capacity per sequence, a multiple of 64 */
+  const int32_t* page_table; /* paged: [batch, max_pages_per_seq] */
+  int32_t max_pages_per_seq; /* paged */
+  int32_t num_pages;         /* paged: number of pages in k and v */
+  const int32_t* seq_lens;   /* [batch] tokens present per sequence (device) */
+} msa_kv_desc;
+
+/* Step-1 selection parameters. */
+typedef struct msa_select_cfg {
+  int32_t k_scored;    /* number of scored blocks to keep per unit, >= 0 */
+  int32_t force_local; /* 1: always keep the newest / diagonal block (not scored) */
+  int32_t q_tile;      /* 1: decode (one token per sequence); 64: prefill tiles */
+  int32_t mode;        /* msa_score_mode */
+  int64_t q_start;     /* prefill: absolute position of the first query token, a multiple of 64 */
+} msa_select_cfg;
+
+/* Operation ids for msa_workspace_size. */
+typedef enum msa_op {
+  MSA_OP_POOL = 0,
+  MSA_OP_SELECT = 1,         /* msa_select_topk_blocks with q_tile 1 (decode) */
+  MSA_OP_DECODE = 2,
+  MSA_OP_PREFILL = 3,
+  MSA_OP_DENSE_DECODE = 4,
+  MSA_OP_DENSE_PREFILL = 5,
+  MSA_OP_SELECT_PREFILL = 6  /* msa_select_topk_blocks with q_tile 64 */
+} msa_op;
+
+/* Bytes of workspace `op` needs for these shapes (host call, no GPU work).
+ * n_q_tokens is 1 for decode ops; k_total is the index-list length (ignored by
+ * dense ops). Returns 0 when the arguments are invalid. A workspace must be
+ * zero-filled once before its first use (msa_workspace_init); the library
+ * leaves it ready for the next call. One workspace of the largest size serves
+ * every op. */
+size_t msa_workspace_size(int32_t op, const msa_kv_desc* kv /* host */, int32_t num_q_heads,
+                          int32_t n_q_tokens, int32_t k_total);
+
+/* Zero-fill `bytes` of workspace on `stream` (a memset; no allocation). */
+msa_status msa_workspace_init(void* ws, size_t bytes, msa_stream_t stream);
+
+/* Step 1a -- block summary keys (guide §1, Step 1, block pooling of the index
+ * branch). For every complete block b (64 b + 63 < seq_len) of every
+ * (sequence, KV head) with first_block <= b < first_block + n_blocks
+ * (n_blocks = -1: all), writes pooled[b] = (1/64) * sum_{i<64} K[64 b + i]:
+ * fp32 sum in row order, one multiply by 1/64, rounded to nearest even into
+ * the KV dtype. Partial blocks are left untouched. Bad page ids set
+ * MSA_ERR_DEVICE_BOUNDS in the status word when `ws` is given (ws may be NULL:
+ * then bad pages are skipped silently). */
+msa_status msa_pool_block_keys(const msa_kv_desc* kv /* host */, int64_t first_block, int64_t n_blocks,
+                               void* pooled, void* ws, size_t ws_bytes, msa_stream_t stream);
+
+/* Step 1b/1c -- group index query, block scores and top-k (guide §1, Step 1:
+ * one index query per GQA group, scores per block, TopK keeps the k best
+ * blocks per layer and group).
+ * Decode (cfg->q_tile == 1): q [batch, Hq, 128]; unit = (sequence, KV head);
+ *   q_idx = sum of the group's G query heads (fp32); candidates are the
+ *   complete blocks, minus the newest block nb-1 (nb = ceil(seq_len/64)) when
+ *   force_local. Output idx_out [batch, Hkv, k_total].
+ * Prefill (cfg->q_tile == 64, batch 1): q [n_q_tokens, Hq, 128]; unit =
+ *   (tile j, KV head); q_idx = sum over the tile's tokens and the group's
+ *   heads; candidates are the blocks before the diagonal block
+ *   q_start/64 + j. Output idx_out [ceil(n_q_tokens/64), Hkv, k_total].
+ * Scores are q_idx . pooled[b] in fp32 (unscaled). The top min(k_scored, n)
+ * candidates by (score descending, block ascending) plus the forced block are
+ * written sorted ascending, padded with -1; k_total >= k_scored + force_local.
+ * scores_out (nullable): [units, max_blocks] fp32 raw scores, -inf for
+ * non-candidates (max_blocks = max_tokens/64 or max_pages_per_seq). */
+msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_q_tokens,
+                                  const void* pooled, const msa_kv_desc* kv /* host */,
+                                  const msa_select_cfg* cfg /* host */, int32_t* idx_out, int32_t k_total,
+                                  float* scores_out, void* ws, size_t ws_bytes, msa_stream_t stream);
+
+/* Step 2, decode (guide §1, Step 2: attention over the gathered selected
+ * blocks; all heads of a group share the group's list).
+ * For each sequence s and query head j (KV head h = j / G):
+ *   o = sum_t softmax_t(scale * q_j . K[t]) V[t]
+ * over the tokens t < seq_len[s] of the blocks idx[s, h, 0..k_total) (-1
+ * entries ignored; duplicates are not allowed). out [batch, Hq, 128] in the KV
+ * dtype; lse (nullable) [batch, Hq] fp32 natural-log sum of exp(scale q.k).
+ * An empty selection gives out = 0 and lse = -inf. */
+msa_status msa_sparse_attn_decode(const void* q, int32_t num_q_heads, const msa_kv_desc* kv /* host */,
+                                  const int32_t* idx, int32_t k_total, float scale, void* out,
+                                  float* lse, void* ws, size_t ws_bytes, msa_stream_t stream);
+
+/* Step 2, chunked prefill (guide §1, Step 2, and §3: during prefill the
+ * savings fall on the main attention). Batch 1; query token r sits at
+ * absolute position p = q_start + r and attends to the tokens t <= p of the
+ * blocks idx[r / 64, h, :] (idx from msa_select_topk_blocks with q_tile 64).
+ * out [n_q_tokens, Hq, 128] KV dtype; lse (nullable) [n_q_tokens, Hq] fp32. */
+msa_status msa_sparse_attn_prefill(const void* q, int32_t num_q_heads, int32_t n_q_tokens, int64_t q_start,
+                                   const msa_kv_desc* kv /* host */, const int32_t* idx, int32_t k_total,
+                                   float scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                                   msa_stream_t stream);
+
+/* Dense causal GQA decode: the full-attention comparator (guide §3 quotes
+ * the sparse speed-ups against full attention). Same as msa_sparse_attn_decode
+ * with every block 0..ceil(seq_len/64)-1 selected. */
+msa_status msa_dense_gqa_decode(const void* q, int32_t num_q_heads, const msa_kv_desc* kv /* host */,
+                                float scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                                msa_stream_t stream);
+
+/* Dense causal GQA prefill: msa_sparse_attn_prefill with every block up to the
+ * diagonal selected for every tile. */
+msa_status msa_dense_gqa_prefill(const void* q, int32_t num_q_heads, int32_t n_q_tokens, int64_t q_start,
+                                 const msa_kv_desc* kv /* host */, float scale, void* out, float* lse,
+                                 void* ws, size_t ws_bytes, msa_stream_t stream);
+
+/* Reads (and clears) the sticky device status word of `ws`: synchronises
+ * `stream`, stores an msa_status in *status_out (host). */
+msa_status msa_read_device_status(const void* ws, msa_stream_t stream, int32_t* status_out /* host */);
+
+/* Static English text for a status code. */
+const char* msa_status_string(int32_t status);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int32_t msa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

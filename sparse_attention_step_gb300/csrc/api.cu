@@ -1,0 +1,386 @@
+// Host side of the C ABI declared in include/msa.h: argument validation,
+// workspace layout, TMA descriptors and kernel launches. No device memory is
+// allocated here and no call synchronises, except msa_read_device_status.
+#include <mutex>
+
+#include "kernels.cuh"
+
+namespace msa {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxTopkCandidates = 49152;  // shared-memory key array of the top-k kernel
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  size_t topk_smem = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+// Per-device setup: SM count and the dynamic shared-memory opt-ins.
+msa_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MSA_ERR_CUDA;
+    if (set_decode_smem() != cudaSuccess) return MSA_ERR_CUDA;
+    if (set_prefill_smem() != cudaSuccess) return MSA_ERR_CUDA;
+    d.topk_smem = kMaxTopkCandidates * sizeof(uint32_t);
+    if (set_topk_smem(d.topk_smem) != cudaSuccess) return MSA_ERR_CUDA;
+    d.ready = true;
+  }
+  *out = &d;
+  return MSA_OK;
+}
+
+// SM count for workspace sizing (host call without launches).
+int num_sms_current() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D view [rows, 128] of a bf16 K or V buffer; boxes of 64 rows x 64 columns
+// (128 bytes) with 128-byte swizzling.
+msa_status make_kv_map(CUtensorMap* map, const void* base, int64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return MSA_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0) return MSA_ERR_INVALID_ARG;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * 2};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MSA_OK : MSA_ERR_CUDA;
+}
+
+msa_status validate_kv(const msa_kv_desc* kv) {
+  if (kv == nullptr) return MSA_ERR_INVALID_ARG;
+  if (kv->layout != MSA_KV_CONTIGUOUS && kv->layout != MSA_KV_PAGED) return MSA_ERR_INVALID_ARG;
+  if (kv->dtype != MSA_DTYPE_F32 && kv->dtype != MSA_DTYPE_BF16) return MSA_ERR_INVALID_ARG;
+  if (kv->batch <= 0 || kv->num_kv_heads <= 0) return MSA_ERR_INVALID_ARG;
+  if (kv->k == nullptr || kv->v == nullptr || kv->seq_lens == nullptr) return MSA_ERR_INVALID_ARG;
+  if (kv->head_dim != kHeadDim || kv->block_size != kBlock) return MSA_ERR_UNSUPPORTED;
+  if (kv->layout == MSA_KV_CONTIGUOUS) {
+    if (kv->max_tokens <= 0 || kv->max_tokens % kBlock != 0) return MSA_ERR_INVALID_ARG;
+  } else {
+    if (kv->page_table == nullptr || kv->max_pages_per_seq <= 0 || kv->num_pages <= 0) return MSA_ERR_INVALID_ARG;
+  }
+  return MSA_OK;
+}
+
+int64_t kv_rows(const msa_kv_desc* kv) {
+  return kv->layout == MSA_KV_CONTIGUOUS ? static_cast<int64_t>(kv->batch) * kv->num_kv_heads * kv->max_tokens
+                                         : static_cast<int64_t>(kv->num_pages) * kv->num_kv_heads * kBlock;
+}
+int64_t kv_max_blocks(const msa_kv_desc* kv) {
+  return kv->layout == MSA_KV_CONTIGUOUS ? kv->max_tokens / kBlock : kv->max_pages_per_seq;
+}
+
+KvView view_of(const msa_kv_desc* kv) {
+  KvView v;
+  v.layout = kv->layout;
+  v.hkv = kv->num_kv_heads;
+  v.max_tokens = kv->max_tokens;
+  v.page_table = kv->page_table;
+  v.max_pages = kv->max_pages_per_seq;
+  v.num_pages = kv->num_pages;
+  v.seq_lens = kv->seq_lens;
+  return v;
+}
+
+int32_t* ws_status(void* ws) { return ws == nullptr ? nullptr : reinterpret_cast<int32_t*>(ws); }
+uint8_t* ws_region(void* ws) { return reinterpret_cast<uint8_t*>(ws) + kWsRegion; }
+
+// ---- workspace layouts (bytes after the header) ----
+struct SelectLayout {
+  size_t scores = 0, qidx = 0, total = 0;
+};
+SelectLayout select_layout(const msa_kv_desc* kv, int n_q_tokens, int prefill) {
+  SelectLayout L;
+  const int64_t units = prefill ? static_cast<int64_t>((n_q_tokens + kBlock - 1) / kBlock) * kv->num_kv_heads
+                                : static_cast<int64_t>(kv->batch) * kv->num_kv_heads;
+  L.scores = 0;
+  size_t off = align_up(static_cast<size_t>(units) * kv_max_blocks(kv) * sizeof(float), 256);
+  L.qidx = off;
+  if (prefill) off += align_up(static_cast<size_t>(units) * kHeadDim * sizeof(float), 256);
+  L.total = kWsRegion + off;
+  return L;
+}
+
+struct DecodeLayout {
+  int n_splits = 1, bps = 1;
+  size_t tickets = 0, partials = 0, total = 0;
+};
+DecodeLayout decode_layout(const msa_kv_desc* kv, int64_t list_len, int num_sms) {
+  DecodeLayout L;
+  const int64_t units = static_cast<int64_t>(kv->batch) * kv->num_kv_heads;
+  decode_splits(units, list_len, num_sms > 0 ? num_sms : 1, &L.n_splits, &L.bps);
+  L.tickets = 0;
+  L.partials = align_up(static_cast<size_t>(units) * sizeof(int32_t), 256);
+  L.total = kWsRegion + L.partials + decode_partials_bytes(units, L.n_splits);
+  return L;
+}
+
+msa_status check_ws(void* ws, size_t have, size_t need) {
+  if (ws == nullptr || have < need) return MSA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MSA_ERR_WORKSPACE;
+  return MSA_OK;
+}
+
+msa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
+
+msa_status check_q_heads(const msa_kv_desc* kv, int hq) {
+  if (hq <= 0 || hq % kv->num_kv_heads != 0) return MSA_ERR_INVALID_ARG;
+  if (hq / kv->num_kv_heads > 8) return MSA_ERR_UNSUPPORTED;
+  return MSA_OK;
+}
+
+msa_status decode_common(const void* q, int hq, const msa_kv_desc* kv, const int32_t* idx, int k_total, float scale,
+                         void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  msa_status st = validate_kv(kv);
+  if (st != MSA_OK) return st;
+  if ((st = check_q_heads(kv, hq)) != MSA_OK) return st;
+  if (q == nullptr || out == nullptr) return MSA_ERR_INVALID_ARG;
+  if (idx != nullptr && k_total <= 0) return MSA_ERR_INVALID_ARG;
+  if (!(scale > 0.f)) return MSA_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != MSA_OK) return st;
+  const int64_t list_len = idx != nullptr ? k_total : kv_max_blocks(kv);
+  DecodeLayout L = decode_layout(kv, list_len, dev->num_sms);
+  if ((st = check_ws(ws, ws_bytes, L.total)) != MSA_OK) return st;
+  DecodeArgs a;
+  a.q = q;
+  a.hq = hq;
+  a.hkv = kv->num_kv_heads;
+  a.grp = hq / kv->num_kv_heads;
+  a.idx = idx;
+  a.k_total = idx != nullptr ? k_total : 0;
+  a.n_splits = L.n_splits;
+  a.bps = L.bps;
+  a.scale_log2 = scale * kLog2e;
+  a.out = out;
+  a.lse = lse;
+  a.tickets = reinterpret_cast<int32_t*>(ws_region(ws) + L.tickets);
+  a.partials = reinterpret_cast<float*>(ws_region(ws) + L.partials);
+  a.status = ws_status(ws);
+  KvView view = view_of(kv);
+  if (kv->dtype == MSA_DTYPE_BF16) {
+    const int64_t rows = kv_rows(kv);
+    if (rows >= (int64_t(1) << 31)) return MSA_ERR_UNSUPPORTED;
+    CUtensorMap tmk, tmv;
+    if ((st = make_kv_map(&tmk, kv->k, rows)) != MSA_OK) return st;
+    if ((st = make_kv_map(&tmv, kv->v, rows)) != MSA_OK) return st;
+    return cuda_status(launch_decode_bf16(tmk, tmv, view, kv->batch, a, stream));
+  }
+  return cuda_status(launch_decode_f32(static_cast<const float*>(kv->k), static_cast<const float*>(kv->v), view,
+                                       kv->batch, a, stream));
+}
+
+msa_status prefill_common(const void* q, int hq, int n_q_tokens, int64_t q_start, const msa_kv_desc* kv,
+                          const int32_t* idx, int k_total, float scale, void* out, float* lse, void* ws,
+                          size_t ws_bytes, cudaStream_t stream) {
+  msa_status st = validate_kv(kv);
+  if (st != MSA_OK) return st;
+  if ((st = check_q_heads(kv, hq)) != MSA_OK) return st;
+  if (q == nullptr || out == nullptr || n_q_tokens <= 0 || q_start < 0) return MSA_ERR_INVALID_ARG;
+  if (idx != nullptr && k_total <= 0) return MSA_ERR_INVALID_ARG;
+  if (!(scale > 0.f)) return MSA_ERR_INVALID_ARG;
+  if (kv->batch != 1 || kv->layout != MSA_KV_CONTIGUOUS || kv->dtype != MSA_DTYPE_BF16) return MSA_ERR_UNSUPPORTED;
+  if (q_start % kBlock != 0) return MSA_ERR_UNSUPPORTED;
+  if (q_start + n_q_tokens > kv->max_tokens) return MSA_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != MSA_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, kWsRegion)) != MSA_OK) return st;
+  PrefillArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.hq = hq;
+  a.hkv = kv->num_kv_heads;
+  a.grp = hq / kv->num_kv_heads;
+  a.n_q_tokens = n_q_tokens;
+  a.q_start = q_start;
+  a.idx = idx;
+  a.k_total = idx != nullptr ? k_total : 0;
+  a.scale_log2 = scale * kLog2e;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  a.status = ws_status(ws);
+  const int64_t rows = kv_rows(kv);
+  if (rows >= (int64_t(1) << 31)) return MSA_ERR_UNSUPPORTED;
+  CUtensorMap tmk, tmv;
+  if ((st = make_kv_map(&tmk, kv->k, rows)) != MSA_OK) return st;
+  if ((st = make_kv_map(&tmv, kv->v, rows)) != MSA_OK) return st;
+  return cuda_status(launch_prefill_bf16(tmk, tmv, view_of(kv), a, stream));
+}
+
+}  // namespace
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" {
+
+int32_t msa_version(void) { return 0x000100; }
+
+const char* msa_status_string(int32_t status) {
+  switch (status) {
+    case MSA_OK: return "ok";
+    case MSA_ERR_INVALID_ARG: return "invalid argument";
+    case MSA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MSA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MSA_ERR_CUDA: return "CUDA error";
+    case MSA_ERR_DEVICE_BOUNDS: return "device: page id, block index or length out of range";
+    case MSA_ERR_TIMEOUT: return "device: bounded wait timed out";
+    default: return "unknown status";
+  }
+}
+
+size_t msa_workspace_size(int32_t op, const msa_kv_desc* kv, int32_t num_q_heads, int32_t n_q_tokens,
+                          int32_t k_total) {
+  if (validate_kv(kv) != MSA_OK) return 0;
+  switch (op) {
+    case MSA_OP_POOL: return kWsRegion;
+    case MSA_OP_SELECT: return select_layout(kv, 1, 0).total;
+    case MSA_OP_SELECT_PREFILL: return n_q_tokens > 0 ? select_layout(kv, n_q_tokens, 1).total : 0;
+    case MSA_OP_DECODE:
+      if (k_total <= 0) return 0;
+      return decode_layout(kv, k_total, num_sms_current()).total;
+    case MSA_OP_DENSE_DECODE: return decode_layout(kv, kv_max_blocks(kv), num_sms_current()).total;
+    case MSA_OP_PREFILL:
+    case MSA_OP_DENSE_PREFILL: return kWsRegion;
+    default: return 0;
+  }
+  (void)num_q_heads;
+}
+
+msa_status msa_workspace_init(void* ws, size_t bytes, msa_stream_t stream) {
+  if (ws == nullptr) return MSA_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(ws, 0, bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+msa_status msa_pool_block_keys(const msa_kv_desc* kv, int64_t first_block, int64_t n_blocks, void* pooled, void* ws,
+                               size_t ws_bytes, msa_stream_t stream) {
+  msa_status st = validate_kv(kv);
+  if (st != MSA_OK) return st;
+  if (pooled == nullptr || first_block < 0 || n_blocks < -1) return MSA_ERR_INVALID_ARG;
+  if (ws != nullptr && ws_bytes < kWsRegion) return MSA_ERR_WORKSPACE;
+  KvView view = view_of(kv);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (kv->dtype == MSA_DTYPE_BF16)
+    return cuda_status(launch_pool<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(kv->k), view, kv->batch,
+                                                  first_block, n_blocks, static_cast<__nv_bfloat16*>(pooled),
+                                                  ws_status(ws), s));
+  return cuda_status(launch_pool<float>(static_cast<const float*>(kv->k), view, kv->batch, first_block, n_blocks,
+                                        static_cast<float*>(pooled), ws_status(ws), s));
+}
+
+msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_q_tokens, const void* pooled,
+                                  const msa_kv_desc* kv, const msa_select_cfg* cfg, int32_t* idx_out,
+                                  int32_t k_total, float* scores_out, void* ws, size_t ws_bytes,
+                                  msa_stream_t stream) {
+  msa_status st = validate_kv(kv);
+  if (st != MSA_OK) return st;
+  if (cfg == nullptr || q == nullptr || pooled == nullptr || idx_out == nullptr) return MSA_ERR_INVALID_ARG;
+  if ((st = check_q_heads(kv, num_q_heads)) != MSA_OK) return st;
+  if (cfg->mode != MSA_SCORE_MEAN_POOLED_KEYS) return MSA_ERR_UNSUPPORTED;
+  if (cfg->k_scored < 0 || k_total <= 0 || k_total < cfg->k_scored + (cfg->force_local ? 1 : 0))
+    return MSA_ERR_INVALID_ARG;
+  if (cfg->force_local != 0 && cfg->force_local != 1) return MSA_ERR_INVALID_ARG;
+  const int prefill = cfg->q_tile == kBlock;
+  if (!prefill && cfg->q_tile != 1) return MSA_ERR_UNSUPPORTED;
+  if (prefill) {
+    if (kv->batch != 1 || n_q_tokens <= 0 || cfg->q_start < 0) return MSA_ERR_INVALID_ARG;
+    if (cfg->q_start % kBlock != 0) return MSA_ERR_UNSUPPORTED;
+    if (kv->layout != MSA_KV_CONTIGUOUS) return MSA_ERR_UNSUPPORTED;
+    if (cfg->q_start + n_q_tokens > kv->max_tokens) return MSA_ERR_INVALID_ARG;
+  } else if (n_q_tokens != 1 && n_q_tokens != kv->batch) {
+    return MSA_ERR_INVALID_ARG;
+  }
+  if (kv_max_blocks(kv) > kMaxTopkCandidates) return MSA_ERR_UNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != MSA_OK) return st;
+  SelectLayout L = select_layout(kv, prefill ? n_q_tokens : 1, prefill);
+  if ((st = check_ws(ws, ws_bytes, L.total)) != MSA_OK) return st;
+  float* scores = scores_out != nullptr ? scores_out : reinterpret_cast<float*>(ws_region(ws) + L.scores);
+  float* qidx = reinterpret_cast<float*>(ws_region(ws) + L.qidx);
+  KvView view = view_of(kv);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (kv->dtype == MSA_DTYPE_BF16)
+    return cuda_status(launch_select<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(q), num_q_heads, n_q_tokens,
+                                                    static_cast<const __nv_bfloat16*>(pooled), view, kv->batch,
+                                                    *cfg, idx_out, k_total, scores, qidx, ws_status(ws), s));
+  return cuda_status(launch_select<float>(static_cast<const float*>(q), num_q_heads, n_q_tokens,
+                                          static_cast<const float*>(pooled), view, kv->batch, *cfg, idx_out,
+                                          k_total, scores, qidx, ws_status(ws), s));
+}
+
+msa_status msa_sparse_attn_decode(const void* q, int32_t num_q_heads, const msa_kv_desc* kv, const int32_t* idx,
+                                  int32_t k_total, float scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                                  msa_stream_t stream) {
+  if (idx == nullptr) return MSA_ERR_INVALID_ARG;
+  return decode_common(q, num_q_heads, kv, idx, k_total, scale, out, lse, ws, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_dense_gqa_decode(const void* q, int32_t num_q_heads, const msa_kv_desc* kv, float scale, void* out,
+                                float* lse, void* ws, size_t ws_bytes, msa_stream_t stream) {
+  return decode_common(q, num_q_heads, kv, nullptr, 0, scale, out, lse, ws, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_sparse_attn_prefill(const void* q, int32_t num_q_heads, int32_t n_q_tokens, int64_t q_start,
+                                   const msa_kv_desc* kv, const int32_t* idx, int32_t k_total, float scale,
+                                   void* out, float* lse, void* ws, size_t ws_bytes, msa_stream_t stream) {
+  if (idx == nullptr) return MSA_ERR_INVALID_ARG;
+  return prefill_common(q, num_q_heads, n_q_tokens, q_start, kv, idx, k_total, scale, out, lse, ws, ws_bytes,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_dense_gqa_prefill(const void* q, int32_t num_q_heads, int32_t n_q_tokens, int64_t q_start,
+                                 const msa_kv_desc* kv, float scale, void* out, float* lse, void* ws,
+                                 size_t ws_bytes, msa_stream_t stream) {
+  return prefill_common(q, num_q_heads, n_q_tokens, q_start, kv, nullptr, 0, scale, out, lse, ws, ws_bytes,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_read_device_status(const void* ws, msa_stream_t stream, int32_t* status_out) {
+  if (ws == nullptr || status_out == nullptr) return MSA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t word[2] = {0, 0};
+  if (cudaMemcpyAsync(word, ws, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MSA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MSA_ERR_CUDA;
+  *status_out = word[0];
+  if (word[0] != 0) {
+    if (cudaMemsetAsync(const_cast<void*>(ws), 0, sizeof(word), s) != cudaSuccess) return MSA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MSA_ERR_CUDA;
+  }
+  return MSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,208 @@
+// Shared device helpers: inline-PTX wrappers (mbarrier, TMA bulk tensor copies,
+// ldmatrix, mma.sync, movmatrix), bf16 packing and the workspace layout.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/msa.h"
+
+namespace msa {
+
+constexpr int kHeadDim = 128;
+constexpr int kBlock = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------------------
+// Workspace layout. Bytes [0, 256) hold the header; the op-specific region
+// starts at kWsRegion. Ticket counters (zero between calls) come first in each
+// op's region.
+// ---------------------------------------------------------------------------
+constexpr size_t kWsHeader = 256;
+constexpr size_t kWsRegion = 256;
+
+struct WsHeader {
+  int32_t status;  // sticky msa_status set by kernels (0 = ok)
+  int32_t where;   // diagnostic: kernel id that set it
+  int32_t pad[62];
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Record the first device-side error (a no-op when no workspace is given).
+__device__ inline void set_status(int32_t* status, int32_t code, int32_t where) {
+  if (status == nullptr) return;
+  if (atomicCAS(status, 0, code) == 0) status[1] = where;
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory addresses
+// ---------------------------------------------------------------------------
+__device__ inline uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ inline void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ inline void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ inline void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ inline void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ inline void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ inline bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete, giving up after about
+// `kWaitCycles` SM cycles (then the device status gets MSA_ERR_TIMEOUT and the
+// caller must stop using the buffer the barrier guards).
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+__device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status, int where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  while (true) {
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > kWaitCycles) {
+      set_status(status, MSA_ERR_TIMEOUT, where);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA: 2-D tiled bulk tensor copy global -> shared, completing on an mbarrier.
+// x is the innermost coordinate (elements), y the row.
+// ---------------------------------------------------------------------------
+__device__ inline void tma_load_2d(void* smem_dst, const CUtensorMap* map, int32_t x, int32_t y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ inline void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Warp-level tensor-core fragments (m16n8k16, bf16 in, fp32 accumulate).
+// Lane l: g = l >> 2 (row group), c = l & 3 (column pair).
+// ---------------------------------------------------------------------------
+__device__ inline void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ inline void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ inline void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ inline uint32_t movm_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+__device__ inline uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Byte offset of (row, 16-byte chunk) in a tile written by TMA with 128-byte
+// swizzling: rows of 128 bytes, chunk index XOR (row mod 8).
+__device__ inline uint32_t swz128(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ inline float bf16_bits_to_f32(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+// Scores as order-preserving unsigned keys: a larger float gives a larger key.
+__device__ inline uint32_t float_to_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;  // -0 ranks with +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ---------------------------------------------------------------------------
+// KV cache addressing shared by every kernel. Rows are 128-element (D) rows.
+// ---------------------------------------------------------------------------
+struct KvView {
+  int32_t layout;       // MSA_KV_CONTIGUOUS / MSA_KV_PAGED
+  int32_t hkv;          // KV heads
+  int64_t max_tokens;   // contiguous capacity per sequence
+  const int32_t* page_table;
+  int32_t max_pages;    // paged: table row length
+  int32_t num_pages;
+  const int32_t* seq_lens;
+
+  __device__ int64_t capacity() const {
+    return layout == MSA_KV_CONTIGUOUS ? max_tokens : static_cast<int64_t>(max_pages) * kBlock;
+  }
+  // Length of sequence s, clamped to [0, capacity]; an out-of-range length
+  // sets MSA_ERR_DEVICE_BOUNDS.
+  __device__ int64_t seq_len(int s, int32_t* status, int where) const {
+    int64_t n = seq_lens[s];
+    int64_t cap = capacity();
+    if (n < 0 || n > cap) {
+      set_status(status, MSA_ERR_DEVICE_BOUNDS, where);
+      n = n < 0 ? 0 : cap;
+    }
+    return n;
+  }
+  // Page holding logical block b of sequence s (paged), or -1 (status set).
+  __device__ int32_t page(int s, int64_t b, int32_t* status, int where) const {
+    int32_t p = page_table[static_cast<int64_t>(s) * max_pages + b];
+    if (p < 0 || p >= num_pages) {
+      set_status(status, MSA_ERR_DEVICE_BOUNDS, where);
+      return -1;
+    }
+    return p;
+  }
+  // First K/V row of logical block b of (s, h), or -1 for a bad page.
+  __device__ int64_t block_row(int s, int h, int64_t b, int32_t* status, int where) const {
+    if (layout == MSA_KV_CONTIGUOUS) return (static_cast<int64_t>(s) * hkv + h) * max_tokens + b * kBlock;
+    int32_t p = page(s, b, status, where);
+    return p < 0 ? -1 : (static_cast<int64_t>(p) * hkv + h) * kBlock;
+  }
+  // Row of the pooled summary key of block b of (s, h), or -1 for a bad page.
+  __device__ int64_t pooled_row(int s, int h, int64_t b, int32_t* status, int where) const {
+    if (layout == MSA_KV_CONTIGUOUS) return (static_cast<int64_t>(s) * hkv + h) * (max_tokens / kBlock) + b;
+    int32_t p = page(s, b, status, where);
+    return p < 0 ? -1 : static_cast<int64_t>(p) * hkv + h;
+  }
+  __host__ __device__ int64_t max_blocks() const {
+    return layout == MSA_KV_CONTIGUOUS ? max_tokens / kBlock : static_cast<int64_t>(max_pages);
+  }
+};
+
+// Kernel ids recorded with a device status (WsHeader::where).
+enum KernelId { kIdPool = 1, kIdQidx = 2, kIdScore = 3, kIdTopk = 4, kIdDecode = 5, kIdPrefill = 6 };
+
+}  // namespace msa

@@ -1,0 +1,62 @@
+// Argument blocks and host launchers of the kernels, shared by the kernel
+// files and the C-ABI layer.
+#pragma once
+
+#include "common.cuh"
+
+namespace msa {
+
+// ---- Step 1a: pooling (pool.cu) ----
+template <typename T>
+cudaError_t launch_pool(const T* k, const KvView& kv, int batch, int64_t first_block, int64_t n_blocks, T* pooled,
+                        int32_t* status, cudaStream_t stream);
+
+// ---- Step 1b/1c: index query, scores, top-k (select.cu) ----
+template <typename T>
+cudaError_t launch_select(const T* q, int hq, int n_q_tokens, const T* pooled, const KvView& kv, int batch,
+                          const msa_select_cfg& cfg, int32_t* idx_out, int k_total, float* scores, float* qidx_ws,
+                          int32_t* status, cudaStream_t stream);
+cudaError_t set_topk_smem(size_t bytes);
+
+// ---- Step 2, decode (decode.cu) ----
+struct DecodeArgs {
+  const void* q;
+  int hq, hkv, grp;
+  const int32_t* idx;   // [batch, hkv, k_total] or nullptr (dense)
+  int k_total;
+  int n_splits;
+  int bps;              // list entries (sparse) or blocks (dense) per split
+  float scale_log2;     // scale * log2(e)
+  void* out;
+  float* lse;
+  float* partials;      // [units, n_splits, kPartFloats]
+  int32_t* tickets;     // [units], zero between calls
+  int32_t* status;
+};
+cudaError_t set_decode_smem();
+size_t decode_smem_bytes();
+void decode_splits(int64_t units, int64_t list_len, int num_sms, int* n_splits, int* bps);
+size_t decode_partials_bytes(int64_t units, int n_splits);
+cudaError_t launch_decode_bf16(const CUtensorMap& tmk, const CUtensorMap& tmv, const KvView& kv, int batch,
+                               const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_f32(const float* k, const float* v, const KvView& kv, int batch, const DecodeArgs& a,
+                              cudaStream_t stream);
+
+// ---- Step 2, prefill (prefill.cu) ----
+struct PrefillArgs {
+  const __nv_bfloat16* q;  // [n_q_tokens, hq, 128]
+  int hq, hkv, grp;
+  int n_q_tokens;
+  int64_t q_start;
+  const int32_t* idx;  // [n_tiles, hkv, k_total] or nullptr (dense)
+  int k_total;
+  float scale_log2;
+  __nv_bfloat16* out;
+  float* lse;
+  int32_t* status;
+};
+cudaError_t set_prefill_smem();
+cudaError_t launch_prefill_bf16(const CUtensorMap& tmk, const CUtensorMap& tmv, const KvView& kv,
+                                const PrefillArgs& a, cudaStream_t stream);
+
+}  // namespace msa

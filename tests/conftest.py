@@ -14,6 +14,7 @@ def pytest_configure(config):
 
 @pytest.fixture(scope="session")
 def lib():
-    """The built C-ABI library (loads the shared object; no GPU needed)."""
-    from sparse_attention_step_gb300 import msa
+    """The built C-ABI library (builds it in-tree if needed; no GPU needed)."""
+    from sparse_attention_step_gb300 import build, msa
+    build.build()
     return msa.load()

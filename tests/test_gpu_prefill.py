@@ -1,0 +1,117 @@
+"""GPU parity of the chunked-prefill path (tile selection + causal sparse
+attention, and the dense comparator) against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import msa_oracle as O
+from synth import make_prefill_inputs, make_workload, WORKLOADS
+from tests.parity import SCALE, SelectionStats, check_lse, check_output, check_selection, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev(lib):
+    assert torch.cuda.is_available()
+    return torch.device("cuda:0")
+
+
+def run_prefill(inp, k_scored, k_total, dense=False, sparse=True):
+    from sparse_attention_step_gb300 import msa
+    dev = inp.q.device
+    desc = msa.kv_desc(inp.k, inp.v, inp.seq_lens)
+    hq, n = inp.num_q_heads, inp.n_new
+    n_tiles = (n + 63) // 64
+    need = max(msa.msa_workspace_size(msa.MSA_OP_SELECT_PREFILL, desc, hq, n, k_total),
+               msa.msa_workspace_size(msa.MSA_OP_PREFILL, desc, hq, n, k_total))
+    ws = msa.Workspace(need, dev)
+    pooled = torch.full(msa.pooled_shape(desc), float("nan"), dtype=inp.k.dtype, device=dev)
+    idx = torch.full((n_tiles, inp.num_kv_heads, k_total), -7, dtype=torch.int32, device=dev)
+    scores = torch.empty(n_tiles * inp.num_kv_heads, desc.max_tokens // 64, dtype=torch.float32, device=dev)
+    out = torch.full_like(inp.q, float("nan"))
+    lse = torch.full((n, hq), float("nan"), dtype=torch.float32, device=dev)
+    msa.msa_pool_block_keys(desc, 0, -1, pooled, ws.buf, ws.nbytes)
+    cfg = msa.select_cfg(k_scored, True, 64, inp.q_start)
+    msa.msa_select_topk_blocks(inp.q, hq, n, pooled, desc, cfg, idx, k_total, scores, ws.buf, ws.nbytes)
+    if sparse:
+        msa.msa_sparse_attn_prefill(inp.q, hq, n, inp.q_start, desc, idx, k_total, SCALE, out, lse, ws.buf,
+                                    ws.nbytes)
+    res = dict(pooled=pooled, idx=idx, scores=scores, out=out, lse=lse)
+    if dense:
+        dout = torch.full_like(inp.q, float("nan"))
+        dlse = torch.full((n, hq), float("nan"), dtype=torch.float32, device=dev)
+        msa.msa_dense_gqa_prefill(inp.q, hq, n, inp.q_start, desc, SCALE, dout, dlse, ws.buf, ws.nbytes)
+        res.update(dense_out=dout, dense_lse=dlse)
+    torch.cuda.synchronize()
+    res["status"] = msa.msa_read_device_status(ws.buf)
+    return res
+
+
+def verify_tiles(inp, res, tiles, heads, k_scored, k_total, rows_per_tile=None, stats=None, check_dense=False,
+                 check_sparse=True):
+    grp = inp.num_q_heads // inp.num_kv_heads
+    total = inp.q_start + inp.n_new
+    for h in heads:
+        kr = to64(inp.k[0, h])
+        vr = to64(inp.v[0, h])
+        pooled, _ = O.pool_block_keys(kr, total, inp.dtype)
+        assert np.array_equal(to64(res["pooled"][0, h, :total // 64]), pooled), f"pooled keys differ, head {h}"
+        for j in tiles:
+            r0, r1 = 64 * j, min(inp.n_new, 64 * j + 64)
+            q_tile = to64(inp.q[r0:r1, h * grp:(h + 1) * grp])
+            sel = O.prefill_tile_select(q_tile, j, inp.q_start, pooled, k_scored, k_total)
+            got_idx = res["idx"][j, h].cpu().numpy()
+            check_selection(got_idx, sel["scores"], k_scored, sel["diag"], k_total, stats)
+            rows = np.arange(r1 - r0) if rows_per_tile is None else \
+                np.unique(np.linspace(0, r1 - r0 - 1, rows_per_tile).astype(int))
+            pos = inp.q_start + r0 + rows
+            if check_sparse:
+                o, lse = O.prefill_rows(q_tile[rows], pos, kr, vr, total, got_idx, SCALE)
+                got = to64(res["out"][r0 + rows, h * grp:(h + 1) * grp])
+                check_output(got, o, inp.dtype, f"prefill tile {j} head {h}")
+                check_lse(to64(res["lse"][r0 + rows, h * grp:(h + 1) * grp]), lse)
+            if check_dense:
+                for i, r in enumerate(rows):
+                    od, ld = O.dense_gqa(q_tile[r], kr, vr, pos[i], SCALE)
+                    check_output(to64(res["dense_out"][r0 + r, h * grp:(h + 1) * grp]), od, inp.dtype,
+                                 f"dense prefill row {r0 + r} head {h}")
+                    check_lse(to64(res["dense_lse"][r0 + r, h * grp:(h + 1) * grp]), ld, "dense lse")
+
+
+@pytest.mark.parametrize("hq,hkv", [(16, 2), (8, 8), (16, 4)])
+def test_prefill_small(dev, hq, hkv):
+    inp = make_prefill_inputs(64 * 10, 64 * 3 + 37, hkv, hq, "bf16", seed=hq + hkv, device=dev)
+    res = run_prefill(inp, 4, 5, dense=True)
+    assert res["status"] == 0
+    n_tiles = (inp.n_new + 63) // 64
+    verify_tiles(inp, res, range(n_tiles), range(hkv), 4, 5, check_dense=True)
+
+
+def test_prefill_all_blocks_equals_dense(dev):
+    inp = make_prefill_inputs(64 * 6, 64 * 2 + 5, 2, 16, "bf16", seed=3, device=dev)
+    res = run_prefill(inp, 1000, 1001, dense=True)
+    assert res["status"] == 0
+    d = (res["out"].float() - res["dense_out"].float()).abs().max().item()
+    assert d <= 2e-2
+    verify_tiles(inp, res, range(3), range(2), 1000, 1001, check_dense=True)
+
+
+def test_prefill_from_empty_prefix(dev):
+    inp = make_prefill_inputs(0, 64 * 4, 2, 16, "bf16", seed=8, device=dev)
+    res = run_prefill(inp, 2, 3, dense=True)
+    assert res["status"] == 0
+    verify_tiles(inp, res, range(4), range(2), 2, 3, check_dense=True)
+
+
+def test_full_chunked_prefill(dev):
+    """8192 new tokens on a 131072-token prefix, 8 KV heads, 64 query heads,
+    top-32 + diagonal: tiles and rows sampled across the chunk."""
+    w = WORKLOADS["prefill_8k_on_128k"]
+    inp = make_workload("prefill_8k_on_128k", device=dev)
+    res = run_prefill(inp, w["k_scored"], w["k_total"], dense=True)
+    assert res["status"] == 0
+    stats = SelectionStats()
+    verify_tiles(inp, res, [0, 57, 127], [0, 5], w["k_scored"], w["k_total"], rows_per_tile=6, stats=stats,
+                 check_dense=True)
+    print("prefill selection", stats)
