@@ -150,7 +150,8 @@ msa_status msa_pool_block_keys(const msa_kv_desc* kv /* host */, int64_t first_b
  *   q_start/64 + j. Output idx_out [ceil(n_q_tokens/64), Hkv, k_total].
  * Scores are q_idx . pooled[b] in fp32 (unscaled). The top min(k_scored, n)
  * candidates by (score descending, block ascending) plus the forced block are
- * written sorted ascending, padded with -1; k_total >= k_scored + force_local.
+ * written sorted ascending, padded with -1;
+ * k_total >= min(k_scored, max_blocks) + force_local.
  * scores_out (nullable): [units, max_blocks] fp32 raw scores, -inf for
  * non-candidates (max_blocks = max_tokens/64 or max_pages_per_seq). */
 msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_q_tokens,

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/msa.h: argument validation,
 // workspace layout, TMA descriptors and kernel launches. No device memory is
 // allocated here and no call synchronises, except msa_read_device_status.
+#include <algorithm>
 #include <mutex>
 
 #include "kernels.cuh"
@@ -30,6 +31,7 @@ msa_status device_info(DeviceInfo** out) {
     if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MSA_ERR_CUDA;
     if (set_decode_smem() != cudaSuccess) return MSA_ERR_CUDA;
     if (set_prefill_smem() != cudaSuccess) return MSA_ERR_CUDA;
+    if (set_prefill_tc_smem() != cudaSuccess) return MSA_ERR_CUDA;
     d.topk_smem = kMaxTopkCandidates * sizeof(uint32_t);
     if (set_topk_smem(d.topk_smem) != cudaSuccess) return MSA_ERR_CUDA;
     d.ready = true;
@@ -75,6 +77,23 @@ msa_status make_kv_map(CUtensorMap* map, const void* base, int64_t rows) {
   cuuint32_t box[2] = {64, 64};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MSA_OK : MSA_ERR_CUDA;
+}
+
+// 3-D view [tokens, heads, 128] of a bf16 query buffer; boxes of 16 tokens x
+// 8 heads x 64 columns (128 rows of 128 bytes) with 128-byte swizzling.
+msa_status make_q_map(CUtensorMap* map, const void* base, int64_t n_tokens, int hq) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return MSA_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0) return MSA_ERR_INVALID_ARG;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(hq),
+                        static_cast<cuuint64_t>(n_tokens)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2, static_cast<cuuint64_t>(hq) * kHeadDim * 2};
+  cuuint32_t box[3] = {64, 8, 16};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MSA_OK : MSA_ERR_CUDA;
@@ -236,6 +255,11 @@ msa_status prefill_common(const void* q, int hq, int n_q_tokens, int64_t q_start
   CUtensorMap tmk, tmv;
   if ((st = make_kv_map(&tmk, kv->k, rows)) != MSA_OK) return st;
   if ((st = make_kv_map(&tmv, kv->v, rows)) != MSA_OK) return st;
+  if (a.grp == 8) {
+    CUtensorMap tmq;
+    if ((st = make_q_map(&tmq, q, n_q_tokens, hq)) != MSA_OK) return st;
+    return cuda_status(launch_prefill_tc(tmq, tmk, tmv, view_of(kv), a, stream));
+  }
   return cuda_status(launch_prefill_bf16(tmk, tmv, view_of(kv), a, stream));
 }
 
@@ -309,7 +333,8 @@ msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_
   if (cfg == nullptr || q == nullptr || pooled == nullptr || idx_out == nullptr) return MSA_ERR_INVALID_ARG;
   if ((st = check_q_heads(kv, num_q_heads)) != MSA_OK) return st;
   if (cfg->mode != MSA_SCORE_MEAN_POOLED_KEYS) return MSA_ERR_UNSUPPORTED;
-  if (cfg->k_scored < 0 || k_total <= 0 || k_total < cfg->k_scored + (cfg->force_local ? 1 : 0))
+  if (cfg->k_scored < 0 || k_total <= 0) return MSA_ERR_INVALID_ARG;
+  if (k_total < std::min<int64_t>(cfg->k_scored, kv_max_blocks(kv)) + (cfg->force_local ? 1 : 0))
     return MSA_ERR_INVALID_ARG;
   if (cfg->force_local != 0 && cfg->force_local != 1) return MSA_ERR_INVALID_ARG;
   const int prefill = cfg->q_tile == kBlock;

@@ -56,6 +56,10 @@ struct PrefillArgs {
   int32_t* status;
 };
 cudaError_t set_prefill_smem();
+cudaError_t set_prefill_tc_smem();
+// tcgen05 kernel: 8 query heads per KV head only
+cudaError_t launch_prefill_tc(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                              const KvView& kv, const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_bf16(const CUtensorMap& tmk, const CUtensorMap& tmv, const KvView& kv,
                                 const PrefillArgs& a, cudaStream_t stream);
 

@@ -1,0 +1,334 @@
+// Step 2, chunked prefill on the 5th-generation tensor cores ("MiniMax goes
+// sparse", §1 Step 2: the heads of a group share one list of KV blocks, the
+// set is staged on chip in one pass and attended with a flash-style kernel).
+//
+// One CTA owns 256 query rows of a (64-token tile, KV head) unit: 32 tokens x
+// the 8 heads of the group, as two M = 128 tiles (rows token-major,
+// head-minor). For every selected 64-key block:
+//   S_t = Q_t K^T      tcgen05.mma M128 N64 K16 x 8, bf16 -> fp32 in TMEM
+//   softmax            one thread per row: tcgen05.ld of its 64 scores, causal
+//                      mask on the diagonal block, online max with lazy
+//                      rescaling (O is rescaled in TMEM only when the running
+//                      max grows by more than 2^8), exp2, P (bf16) written to
+//                      shared memory in the 128-byte-swizzled K-major layout
+//   O_t += P_t V       tcgen05.mma M128 N128 K16 x 4, V read MN-major
+// Warp roles: warps 0-3 softmax of tile 0, warps 4-7 softmax of tile 1 (warp
+// w reaches TMEM lanes 32 (w mod 4) ..), warp 8 TMA producer (Q once, then a
+// 3-stage K/V ring), warp 9 TMEM allocator and MMA issuer. The two tiles
+// ping-pong: the tensor core runs one tile's MMAs while the other tile's
+// softmax runs. TMEM: S_0 [0,64), S_1 [64,128), O_0 [128,256), O_1 [256,384).
+#include <float.h>
+
+#include "kernels.cuh"
+#include "tc.cuh"
+
+namespace msa {
+
+namespace {
+
+constexpr int kTcTiles = 2;
+constexpr int kTcStages = 3;
+constexpr int kTcThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kQBytes = kTcTiles * 2 * 16384;   // two tiles x two 64-dim halves
+constexpr int kKVBytes = kTcStages * 32768;
+constexpr int kPBytes = kTcTiles * 16384;
+constexpr int kMaxList = 512;
+constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
+
+struct TcTail {
+  uint64_t q_full;
+  uint64_t kv_full[kTcStages];
+  uint64_t kv_empty[kTcStages];
+  uint64_t s_full[kTcTiles];
+  uint64_t p_full[kTcTiles];
+  uint64_t o_final[kTcTiles];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int32_t n_blocks;
+  int32_t abort;
+  int32_t blocks[kMaxList];
+};
+
+constexpr size_t kTcSmem = 1024 + kQBytes + kKVBytes + kPBytes + sizeof(TcTail);
+
+__device__ inline bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int32_t* abort, int32_t* status) {
+  if (*abort) return false;
+  if (!mbar_wait(bar, parity, status, kIdPrefill)) {
+    *abort = 1;
+    return false;
+  }
+  return true;
+}
+
+}  // namespace
+
+// grid (2 row halves, Hkv, n_tiles); requires G = 8.
+__global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq,
+                                                                  const __grid_constant__ CUtensorMap tmk,
+                                                                  const __grid_constant__ CUtensorMap tmv, KvView kv,
+                                                                  PrefillArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* qs = base;
+  uint8_t* kvs = base + kQBytes;
+  uint8_t* ps = kvs + kKVBytes;
+  TcTail& st = *reinterpret_cast<TcTail*>(ps + kPBytes);
+
+  const int rh = blockIdx.x, h = blockIdx.y, tile = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t diag = a.q_start / kBlock + tile;
+
+  if (tid == 0) {
+    int n = 0;
+    if (a.idx != nullptr) {
+      const int32_t* list = a.idx + (static_cast<int64_t>(tile) * a.hkv + h) * a.k_total;
+      for (int i = 0; i < a.k_total && n < kMaxList; ++i) {
+        const int32_t b = list[i];
+        if (b < 0) continue;
+        if (b > diag) {
+          set_status(a.status, MSA_ERR_DEVICE_BOUNDS, kIdPrefill);
+          continue;
+        }
+        st.blocks[n++] = b;
+      }
+    } else {
+      n = static_cast<int>(diag + 1);
+    }
+    st.n_blocks = n;
+    st.abort = 0;
+    mbar_init(&st.q_full, 1);
+    for (int i = 0; i < kTcStages; ++i) {
+      mbar_init(&st.kv_full[i], 1);
+      mbar_init(&st.kv_empty[i], 1);
+    }
+    for (int t = 0; t < kTcTiles; ++t) {
+      mbar_init(&st.s_full[t], 1);
+      mbar_init(&st.p_full[t], 4);
+      mbar_init(&st.o_final[t], 1);
+    }
+    mbar_init(&st.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tc::alloc(&st.tmem_base, kTmemCols);
+    tc::relinquish();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const int nblk = st.n_blocks;
+  const bool dense = a.idx == nullptr;
+  const uint32_t tmem = st.tmem_base;
+  volatile int32_t* abort = &st.abort;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmq);
+      tma_prefetch_desc(&tmk);
+      tma_prefetch_desc(&tmv);
+      mbar_arrive_expect_tx(&st.q_full, kQBytes);
+      const int32_t tok0 = tile * kBlock + rh * (kTcTiles * 16);
+      for (int t = 0; t < kTcTiles; ++t)
+        for (int half = 0; half < 2; ++half)
+          tma_load_3d(qs + t * 32768 + half * 16384, &tmq, 64 * half, h * 8, tok0 + 16 * t, &st.q_full);
+      int issued = 0;
+      for (int i = 0; i < nblk; ++i) {
+        const int stg = i % kTcStages;
+        if (i >= kTcStages && !wait_or_abort(&st.kv_empty[stg], ((i / kTcStages) - 1) & 1, abort, a.status)) break;
+        const int b = dense ? i : st.blocks[i];
+        const int64_t row = kv.block_row(0, h, b, a.status, kIdPrefill);
+        const int32_t y = static_cast<int32_t>(row < 0 ? 0 : row);
+        uint8_t* dst = kvs + stg * 32768;
+        mbar_arrive_expect_tx(&st.kv_full[stg], 32768);
+        tma_load_2d(dst, &tmk, 0, y, &st.kv_full[stg]);
+        tma_load_2d(dst + 8192, &tmk, 64, y, &st.kv_full[stg]);
+        tma_load_2d(dst + 16384, &tmv, 0, y, &st.kv_full[stg]);
+        tma_load_2d(dst + 24576, &tmv, 64, y, &st.kv_full[stg]);
+        issued = i + 1;
+      }
+      // drain: every load this thread issued has landed before the CTA may exit
+      mbar_wait(&st.q_full, 0, a.status, kIdPrefill);
+      for (int i = issued - kTcStages < 0 ? 0 : issued - kTcStages; i < issued; ++i)
+        mbar_wait(&st.kv_full[i % kTcStages], (i / kTcStages) & 1, a.status, kIdPrefill);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = tc::idesc_bf16(128, 64, 0, 0);
+      constexpr uint32_t kIdO = tc::idesc_bf16(128, 128, 0, 1);
+      const uint32_t q_addr = smem_u32(qs), kv_addr = smem_u32(kvs), p_addr = smem_u32(ps);
+      auto issue_s = [&](int t, int stg) {
+        const uint32_t d = tmem + t * 64;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          const uint64_t ad = tc::sdesc_sw128(q_addr + t * 32768 + off, 16, 1024);
+          const uint64_t bd = tc::sdesc_sw128(kv_addr + stg * 32768 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+          tc::mma_ss(d, ad, bd, kIdS, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int stg, bool acc) {
+        const uint32_t d = tmem + 128 + t * 128;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t ad = tc::sdesc_sw128(p_addr + t * 16384 + ks * 32, 16, 1024);
+          const uint64_t bd = tc::sdesc_sw128(kv_addr + stg * 32768 + 16384 + ks * 2048, 8192, 1024);
+          tc::mma_ss(d, ad, bd, kIdO, (acc || ks > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = wait_or_abort(&st.q_full, 0, abort, a.status);
+      tc::fence_after();
+      for (int i = 0; ok && i < nblk; ++i) {
+        const int stg = i % kTcStages;
+        if (!(ok = wait_or_abort(&st.kv_full[stg], (i / kTcStages) & 1, abort, a.status))) break;
+        tc::fence_after();
+        for (int t = 0; t < kTcTiles; ++t) {
+          if (i > 0) {
+            if (!(ok = wait_or_abort(&st.p_full[t], (i - 1) & 1, abort, a.status))) break;
+            tc::fence_after();
+            issue_pv(t, (i - 1) % kTcStages, i - 1 > 0);
+            if (t == kTcTiles - 1) tc::commit(&st.kv_empty[(i - 1) % kTcStages]);
+          }
+          issue_s(t, stg);
+          tc::commit(&st.s_full[t]);
+        }
+      }
+      if (ok && nblk > 0) {
+        for (int t = 0; t < kTcTiles; ++t) {
+          if (!(ok = wait_or_abort(&st.p_full[t], (nblk - 1) & 1, abort, a.status))) break;
+          tc::fence_after();
+          issue_pv(t, (nblk - 1) % kTcStages, nblk - 1 > 0);
+        }
+      }
+      for (int t = 0; t < kTcTiles; ++t) tc::commit(&st.o_final[t]);
+      tc::commit(&st.drain);
+      mbar_wait(&st.drain, 0, a.status, kIdPrefill);  // nothing of ours is left in flight
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;               // tile
+    const int r = 32 * (warp & 3) + lane;  // row within the tile = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int tt = rh * (kTcTiles * 16) + 16 * t + (r >> 3);  // token within the 64-token tile
+    const int head = h * 8 + (r & 7);
+    const int64_t tq = static_cast<int64_t>(tile) * kBlock + tt;  // token within the chunk
+    const bool live = tq < a.n_q_tokens;
+    float m = -INFINITY, l = 0.f;
+    uint8_t* prow = ps + t * 16384 + r * 128;
+    bool ok = true;
+    for (int i = 0; i < nblk; ++i) {
+      if (!(ok = wait_or_abort(&st.s_full[t], i & 1, abort, a.status))) break;
+      tc::fence_after();
+      uint32_t sr[64];
+      tc::ld32(tmem + lane_base + t * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tc::ld32(tmem + lane_base + t * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tc::wait_ld();
+      const int b = dense ? i : st.blocks[i];
+      const bool diag_blk = b == diag;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        float z = __uint_as_float(sr[c]) * a.scale_log2;
+        if (diag_blk && c > tt) z = -INFINITY;
+        sr[c] = __float_as_uint(z);
+        mx = fmaxf(mx, z);
+      }
+      const float m_new = fmaxf(m, mx);
+      const bool need = (m == -INFINITY) ? (m_new != -INFINITY) : (m_new > m + kRescaleLog2);
+      if (__any_sync(0xffffffffu, need)) {
+        const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - m_new);
+        if (i > 0) {
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o[32];
+            const uint32_t oa = tmem + lane_base + 128 + t * 128 + cc * 32;
+            tc::ld32(oa, o);
+            tc::wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            tc::st32(oa, o);
+          }
+          tc::wait_st();
+        }
+        l *= alpha;
+        m = m_new;
+      }
+      const float ref = (m == -INFINITY) ? 0.f : m;
+      float sum = 0.f;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          p[e] = exp2f(__uint_as_float(sr[8 * c8 + e]) - ref);
+          sum += p[e];
+        }
+        uint4 v;
+        v.x = pack_bf16(p[0], p[1]);
+        v.y = pack_bf16(p[2], p[3]);
+        v.z = pack_bf16(p[4], p[5]);
+        v.w = pack_bf16(p[6], p[7]);
+        *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) = v;
+      }
+      l += sum;
+      fence_proxy_async();  // P is read by the tensor core (async proxy)
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&st.p_full[t]);
+    }
+    // epilogue: O / l in bf16 and lse
+    if (ok) ok = wait_or_abort(&st.o_final[t], 0, abort, a.status);
+    tc::fence_after();
+    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+    __nv_bfloat16* dst = a.out + (tq * a.hq + head) * kHeadDim;
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+      uint32_t o[32];
+      tc::ld32(tmem + lane_base + 128 + t * 128 + cc * 32, o);
+      tc::wait_ld();
+      if (live) {
+        if (nblk == 0 || !ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+          uint4 v;
+          v.x = pack_bf16(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv);
+          v.y = pack_bf16(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
+          v.z = pack_bf16(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv);
+          v.w = pack_bf16(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv);
+          *reinterpret_cast<uint4*>(dst + cc * 32 + j) = v;
+        }
+      }
+    }
+    if (live && a.lse != nullptr) a.lse[tq * a.hq + head] = (l > 0.f) ? (m * kLn2 + logf(l)) : -INFINITY;
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::fence_after();
+    tc::dealloc(tmem, kTmemCols);
+  }
+}
+
+size_t prefill_tc_smem_bytes() { return kTcSmem; }
+
+cudaError_t set_prefill_tc_smem() {
+  return cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kTcSmem));
+}
+
+cudaError_t launch_prefill_tc(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                              const KvView& kv, const PrefillArgs& a, cudaStream_t stream) {
+  const int n_tiles = (a.n_q_tokens + kBlock - 1) / kBlock;
+  dim3 grid(2, kv.hkv, n_tiles);
+  prefill_tc_kernel<<<grid, kTcThreads, kTcSmem, stream>>>(tmq, tmk, tmv, kv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace msa
