@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="time only the headline workload")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--batch", type=int, default=8,
+                    help="sequences of the 131072-token decode workload (8 = the benchmark; fewer for profiling)")
     return ap.parse_args()
 
 
@@ -386,7 +388,12 @@ def run_ours(args):
 
     name = "decode_128k"
     w = WORKLOADS[name]
-    inp = make_workload(name, device="cuda")
+    if args.batch == len(w["lens"]):
+        inp = make_workload(name, device="cuda")
+    else:
+        from synth import make_decode_inputs
+        inp = make_decode_inputs(w["lens"][:1] * args.batch, w["hkv"], w["hq"], w["dtype"], w["layout"],
+                                 w["needles"], w["seed"], "cuda")
     st = decode_setup(torch, msa, inp, w["k_scored"], w["k_total"])
     pool_ms = time_op(torch, timer, lambda: msa.msa_pool_block_keys(st["desc"], 0, -1, st["pooled"], st["ws"].buf,
                                                                      st["ws"].nbytes), 5, 2)
@@ -428,13 +435,13 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 6), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {
-            "workload": "decode_128k: 8 sequences x 131072 tokens, 8 KV heads, 64 query heads, head dim 128, "
+            "workload": f"decode_128k: {args.batch} sequences x 131072 tokens, 8 KV heads, 64 query heads, head dim 128, "
                         "64-token blocks, top-31 scored blocks + newest block, 16 needle blocks per (seq, head)",
-            "global_batch": 8 * world, "seq_len": 131072, "parallelism": f"replicas x{world}",
+            "global_batch": args.batch * world, "seq_len": 131072, "parallelism": f"replicas x{world}",
             "l2": "flushed (512 MB write) before every timed step",
             "step": "select (scores + top-k) + sparse flash-decode; summary keys pooled beforehand",
         },
-        "tokens_per_s": round(8 * world / (step_ms * 1e-3), 1),
+        "tokens_per_s": round(args.batch * world / (step_ms * 1e-3), 1),
         "step_GBps": round((pooled_b + sel_b + qo_b) / (step_ms * 1e-3) / 1e9, 1),
         "step_bytes": pooled_b + sel_b + qo_b,
         "select_us": round(sel_ms * 1e3, 3), "attend_us": round(att_ms * 1e3, 3),

@@ -164,7 +164,8 @@ msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_
  * For each sequence s and query head j (KV head h = j / G):
  *   o = sum_t softmax_t(scale * q_j . K[t]) V[t]
  * over the tokens t < seq_len[s] of the blocks idx[s, h, 0..k_total) (-1
- * entries ignored; duplicates are not allowed). out [batch, Hq, 128] in the KV
+ * entries ignored; duplicates are not allowed); batch * Hkv <= 16384 units
+ * (MSA_ERR_UNSUPPORTED above). out [batch, Hq, 128] in the KV
  * dtype; lse (nullable) [batch, Hq] fp32 natural-log sum of exp(scale q.k).
  * An empty selection gives out = 0 and lse = -inf. */
 msa_status msa_sparse_attn_decode(const void* q, int32_t num_q_heads, const msa_kv_desc* kv /* host */,

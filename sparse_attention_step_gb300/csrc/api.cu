@@ -135,7 +135,6 @@ KvView view_of(const msa_kv_desc* kv) {
 }
 
 int32_t* ws_status(void* ws) { return ws == nullptr ? nullptr : reinterpret_cast<int32_t*>(ws); }
-uint8_t* ws_region(void* ws) { return reinterpret_cast<uint8_t*>(ws) + kWsRegion; }
 
 // ---- workspace layouts (bytes after the header) ----
 struct SelectLayout {
@@ -145,14 +144,15 @@ SelectLayout select_layout(const msa_kv_desc* kv, int n_q_tokens, int prefill) {
   SelectLayout L;
   const int64_t units = prefill ? static_cast<int64_t>((n_q_tokens + kBlock - 1) / kBlock) * kv->num_kv_heads
                                 : static_cast<int64_t>(kv->batch) * kv->num_kv_heads;
-  L.scores = 0;
-  size_t off = align_up(static_cast<size_t>(units) * kv_max_blocks(kv) * sizeof(float), 256);
+  L.scores = kWsRegion;
+  size_t off = kWsRegion + align_up(static_cast<size_t>(units) * kv_max_blocks(kv) * sizeof(float), 256);
   L.qidx = off;
   if (prefill) off += align_up(static_cast<size_t>(units) * kHeadDim * sizeof(float), 256);
-  L.total = kWsRegion + off;
+  L.total = off;
   return L;
 }
 
+// Offsets below are from the start of the workspace.
 struct DecodeLayout {
   int n_splits = 1, bps = 1;
   size_t tickets = 0, partials = 0, total = 0;
@@ -161,10 +161,13 @@ DecodeLayout decode_layout(const msa_kv_desc* kv, int64_t list_len, int num_sms)
   DecodeLayout L;
   const int64_t units = static_cast<int64_t>(kv->batch) * kv->num_kv_heads;
   decode_splits(units, list_len, num_sms > 0 ? num_sms : 1, &L.n_splits, &L.bps);
-  L.tickets = 0;
-  L.partials = align_up(static_cast<size_t>(units) * sizeof(int32_t), 256);
-  L.total = kWsRegion + L.partials + decode_partials_bytes(units, L.n_splits);
+  L.tickets = kWsHeader;
+  L.partials = kWsRegion;
+  L.total = L.partials + decode_partials_bytes(units, L.n_splits);
   return L;
+}
+bool decode_units_fit(const msa_kv_desc* kv) {
+  return static_cast<int64_t>(kv->batch) * kv->num_kv_heads <= static_cast<int64_t>(kWsMaxTicketUnits);
 }
 
 msa_status check_ws(void* ws, size_t have, size_t need) {
@@ -189,6 +192,7 @@ msa_status decode_common(const void* q, int hq, const msa_kv_desc* kv, const int
   if (q == nullptr || out == nullptr) return MSA_ERR_INVALID_ARG;
   if (idx != nullptr && k_total <= 0) return MSA_ERR_INVALID_ARG;
   if (!(scale > 0.f)) return MSA_ERR_INVALID_ARG;
+  if (!decode_units_fit(kv)) return MSA_ERR_UNSUPPORTED;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != MSA_OK) return st;
   const int64_t list_len = idx != nullptr ? k_total : kv_max_blocks(kv);
@@ -206,8 +210,8 @@ msa_status decode_common(const void* q, int hq, const msa_kv_desc* kv, const int
   a.scale_log2 = scale * kLog2e;
   a.out = out;
   a.lse = lse;
-  a.tickets = reinterpret_cast<int32_t*>(ws_region(ws) + L.tickets);
-  a.partials = reinterpret_cast<float*>(ws_region(ws) + L.partials);
+  a.tickets = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + L.tickets);
+  a.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.partials);
   a.status = ws_status(ws);
   KvView view = view_of(kv);
   if (kv->dtype == MSA_DTYPE_BF16) {
@@ -236,7 +240,7 @@ msa_status prefill_common(const void* q, int hq, int n_q_tokens, int64_t q_start
   if (q_start + n_q_tokens > kv->max_tokens) return MSA_ERR_INVALID_ARG;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != MSA_OK) return st;
-  if ((st = check_ws(ws, ws_bytes, kWsRegion)) != MSA_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, kWsHeader)) != MSA_OK) return st;
   PrefillArgs a;
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.hq = hq;
@@ -289,7 +293,7 @@ size_t msa_workspace_size(int32_t op, const msa_kv_desc* kv, int32_t num_q_heads
                           int32_t k_total) {
   if (validate_kv(kv) != MSA_OK) return 0;
   switch (op) {
-    case MSA_OP_POOL: return kWsRegion;
+    case MSA_OP_POOL: return kWsHeader;
     case MSA_OP_SELECT: return select_layout(kv, 1, 0).total;
     case MSA_OP_SELECT_PREFILL: return n_q_tokens > 0 ? select_layout(kv, n_q_tokens, 1).total : 0;
     case MSA_OP_DECODE:
@@ -297,7 +301,7 @@ size_t msa_workspace_size(int32_t op, const msa_kv_desc* kv, int32_t num_q_heads
       return decode_layout(kv, k_total, num_sms_current()).total;
     case MSA_OP_DENSE_DECODE: return decode_layout(kv, kv_max_blocks(kv), num_sms_current()).total;
     case MSA_OP_PREFILL:
-    case MSA_OP_DENSE_PREFILL: return kWsRegion;
+    case MSA_OP_DENSE_PREFILL: return kWsHeader;
     default: return 0;
   }
   (void)num_q_heads;
@@ -313,7 +317,7 @@ msa_status msa_pool_block_keys(const msa_kv_desc* kv, int64_t first_block, int64
   msa_status st = validate_kv(kv);
   if (st != MSA_OK) return st;
   if (pooled == nullptr || first_block < 0 || n_blocks < -1) return MSA_ERR_INVALID_ARG;
-  if (ws != nullptr && ws_bytes < kWsRegion) return MSA_ERR_WORKSPACE;
+  if (ws != nullptr && ws_bytes < kWsHeader) return MSA_ERR_WORKSPACE;
   KvView view = view_of(kv);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (kv->dtype == MSA_DTYPE_BF16)
@@ -352,8 +356,8 @@ msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_
   if ((st = device_info(&dev)) != MSA_OK) return st;
   SelectLayout L = select_layout(kv, prefill ? n_q_tokens : 1, prefill);
   if ((st = check_ws(ws, ws_bytes, L.total)) != MSA_OK) return st;
-  float* scores = scores_out != nullptr ? scores_out : reinterpret_cast<float*>(ws_region(ws) + L.scores);
-  float* qidx = reinterpret_cast<float*>(ws_region(ws) + L.qidx);
+  float* scores = scores_out != nullptr ? scores_out : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.scores);
+  float* qidx = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.qidx);
   KvView view = view_of(kv);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (kv->dtype == MSA_DTYPE_BF16)
@@ -409,3 +413,4 @@ msa_status msa_read_device_status(const void* ws, msa_stream_t stream, int32_t* 
 }
 
 }  // extern "C"
+

@@ -17,12 +17,18 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // ---------------------------------------------------------------------------
-// Workspace layout. Bytes [0, 256) hold the header; the op-specific region
-// starts at kWsRegion. Ticket counters (zero between calls) come first in each
-// op's region.
+// Workspace layout, shared by every op so one zero-filled workspace serves all:
+//   [0, 256)                     header (sticky device status)
+//   [256, 256 + kWsTicketBytes)  split-K ticket counters, one int32 per decode
+//                                unit; zero between calls (the last CTA of a
+//                                unit resets its counter) and written by
+//                                nothing else
+//   [kWsRegion, ...)             op-specific scratch (scores, q_idx, partials)
 // ---------------------------------------------------------------------------
 constexpr size_t kWsHeader = 256;
-constexpr size_t kWsRegion = 256;
+constexpr size_t kWsMaxTicketUnits = 16384;
+constexpr size_t kWsTicketBytes = kWsMaxTicketUnits * sizeof(int32_t);
+constexpr size_t kWsRegion = kWsHeader + kWsTicketBytes;
 
 struct WsHeader {
   int32_t status;  // sticky msa_status set by kernels (0 = ok)

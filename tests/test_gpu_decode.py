@@ -155,6 +155,19 @@ def test_decode_k_extremes(dev, k_scored):
         assert d <= 2e-2
 
 
+@pytest.mark.parametrize("layout", ["contiguous", "paged"])
+def test_decode_one_workspace_for_every_step(dev, layout):
+    """Select keeps its scores in the workspace (no scores_out) and decode
+    then uses the same workspace, twice in a row: the split-K counters must
+    survive the scorer's scratch and reset themselves."""
+    lens = [64 * 300 + 5, 64 * 77, 64 * 1024]
+    inp = make_decode_inputs(lens, 2, 16, "bf16", layout, needles=3, seed=31, device=dev)
+    for _ in range(2):
+        res = run_decode(inp, 47, 48, want_scores=False, dense=True)
+        assert res["status"] == 0
+        verify_units(inp, res, all_units(inp), 47, 48, check_dense=True)
+
+
 def test_decode_without_forced_block(dev):
     lens = [64 * 20, 64 * 20 + 9]
     inp = make_decode_inputs(lens, 2, 8, "bf16", "contiguous", needles=2, seed=4, device=dev)
@@ -208,7 +221,8 @@ def _sampled_full(name, units_fn):
     w = WORKLOADS[name]
     dev = torch.device("cuda:0")
     inp = make_workload(name, device=dev)
-    res = run_decode(inp, w["k_scored"], w["k_total"], dense=True)
+    # scores stay in the workspace, as in the benchmark
+    res = run_decode(inp, w["k_scored"], w["k_total"], dense=True, want_scores=False)
     assert res["status"] == 0
     stats = SelectionStats()
     units = units_fn(inp)
