@@ -195,6 +195,28 @@ msa_status msa_dense_gqa_prefill(const void* q, int32_t num_q_heads, int32_t n_q
                                  const msa_kv_desc* kv /* host */, float scale, void* out, float* lse,
                                  void* ws, size_t ws_bytes, msa_stream_t stream);
 
+/* msa_sparse_attn_decode without a workspace argument, for callers that
+ * cannot allocate device memory (an engine or plugin host that owns every
+ * allocation, or a serving loop that must not call cudaMalloc/cudaFree once
+ * running, since those can synchronise the device). The guide has no
+ * counterpart to this call; it only changes where the split-K scratch lives.
+ * Same arguments, layouts and results as msa_sparse_attn_decode, minus ws.
+ *  - Scratch: a fixed 4 MiB device array inside this library, held by every
+ *    GPU that loads it until the process exits. Shapes whose
+ *    msa_workspace_size(MSA_OP_DECODE, ...) exceeds 4 MiB are rejected with
+ *    MSA_ERR_WORKSPACE before any work is queued.
+ *  - The first call on a device looks up the array's device address (a
+ *    one-time set-up per device); make that first call before any stream
+ *    capture.
+ *  - Every call on a device shares the one array and clears its counters at
+ *    the start (a memset on `stream`): calls whose work overlaps on the GPU
+ *    race; order them on one stream.
+ *  - No device memory is allocated or freed. Data-dependent errors (bad page
+ *    ids, lengths above capacity) are skipped without a status report. */
+msa_status msa_sparse_attn_decode_noalloc(const void* q, int32_t num_q_heads, const msa_kv_desc* kv /* host */,
+                                          const int32_t* idx, int32_t k_total, float scale, void* out, float* lse,
+                                          msa_stream_t stream);
+
 /* Reads (and clears) the sticky device status word of `ws`: synchronises
  * `stream`, stores an msa_status in *status_out (host). */
 msa_status msa_read_device_status(const void* ws, msa_stream_t stream, int32_t* status_out /* host */);

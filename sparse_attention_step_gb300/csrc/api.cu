@@ -414,3 +414,95 @@ msa_status msa_read_device_status(const void* ws, msa_stream_t stream, int32_t* 
 
 }  // extern "C"
 
+// ---------------------------------------------------------------------------
+// Sparse decode without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory: an inference engine or plugin
+// host that owns every device allocation and hands its kernels no scratch,
+// or a serving loop that must not allocate once it is running, because
+// cudaMalloc/cudaFree can synchronise the device and stall every stream.
+// msa_sparse_attn_decode_noalloc serves them: its split-K scratch (tickets
+// and partial results) lives in the fixed array below, which every GPU that
+// loads this library keeps until the process exits.
+// ---------------------------------------------------------------------------
+namespace msa {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB per device
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDevice {
+  bool ready = false;
+  uint8_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+};
+NoAllocDevice g_noalloc[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Once per device, with that device current: look up the device address of
+// the scratch array (its host-side name is only a stand-in, not an address a
+// kernel may use).
+msa_status noalloc_scratch(uint8_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocDevice& d = g_noalloc[dev];
+  if (!d.ready) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return MSA_ERR_CUDA;
+    d.scratch = static_cast<uint8_t*>(p);
+    d.ready = true;
+  }
+  *out = d.scratch;
+  return MSA_OK;
+}
+
+}  // namespace
+}  // namespace msa
+
+extern "C" msa_status msa_sparse_attn_decode_noalloc(const void* q, int32_t num_q_heads, const msa_kv_desc* kv,
+                                                     const int32_t* idx, int32_t k_total, float scale, void* out,
+                                                     float* lse, msa_stream_t stream) {
+  using namespace msa;
+  msa_status st = validate_kv(kv);
+  if (st != MSA_OK) return st;
+  if ((st = check_q_heads(kv, num_q_heads)) != MSA_OK) return st;
+  if (q == nullptr || out == nullptr || idx == nullptr || k_total <= 0) return MSA_ERR_INVALID_ARG;
+  if (!(scale > 0.f)) return MSA_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != MSA_OK) return st;
+  uint8_t* ws = nullptr;
+  if ((st = noalloc_scratch(&ws)) != MSA_OK) return st;
+  if (!decode_units_fit(kv)) return MSA_ERR_UNSUPPORTED;
+  const DecodeLayout L = decode_layout(kv, k_total, dev->num_sms);
+  if (L.total > kNoAllocScratchBytes) return MSA_ERR_WORKSPACE;  // beyond the fixed scratch
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: the tickets must start at zero
+  const size_t units = static_cast<size_t>(kv->batch) * kv->num_kv_heads;
+  if (cudaMemsetAsync(ws + L.tickets, 0, units * sizeof(int32_t), s) != cudaSuccess) return MSA_ERR_CUDA;
+  DecodeArgs a;
+  a.q = q;
+  a.hq = num_q_heads;
+  a.hkv = kv->num_kv_heads;
+  a.grp = num_q_heads / kv->num_kv_heads;
+  a.idx = idx;
+  a.k_total = k_total;
+  a.n_splits = L.n_splits;
+  a.bps = L.bps;
+  a.scale_log2 = scale * kLog2e;
+  a.out = out;
+  a.lse = lse;
+  a.tickets = reinterpret_cast<int32_t*>(ws + L.tickets);
+  a.partials = reinterpret_cast<float*>(ws + L.partials);
+  a.status = nullptr;  // bad page ids / lengths are skipped without a report
+  const KvView view = view_of(kv);
+  if (kv->dtype == MSA_DTYPE_BF16) {
+    const int64_t rows = kv_rows(kv);
+    if (rows >= (int64_t(1) << 31)) return MSA_ERR_UNSUPPORTED;
+    CUtensorMap tmk, tmv;
+    if ((st = make_kv_map(&tmk, kv->k, rows)) != MSA_OK) return st;
+    if ((st = make_kv_map(&tmv, kv->v, rows)) != MSA_OK) return st;
+    return cuda_status(launch_decode_bf16(tmk, tmv, view, kv->batch, a, s));
+  }
+  return cuda_status(launch_decode_f32(static_cast<const float*>(kv->k), static_cast<const float*>(kv->v), view,
+                                       kv->batch, a, s));
+}

@@ -29,7 +29,7 @@ MSA_SCORE_MEAN_POOLED_KEYS = 0
 # every symbol include/msa.h declares
 EXPORTS = ["msa_workspace_size", "msa_workspace_init", "msa_pool_block_keys", "msa_select_topk_blocks",
            "msa_sparse_attn_decode", "msa_sparse_attn_prefill", "msa_dense_gqa_decode", "msa_dense_gqa_prefill",
-           "msa_read_device_status", "msa_status_string", "msa_version"]
+           "msa_read_device_status", "msa_status_string", "msa_version", "msa_sparse_attn_decode_noalloc"]
 
 
 class MsaError(RuntimeError):
@@ -68,6 +68,7 @@ _SIGS = {
     "msa_dense_gqa_decode": (_I32, [_P, _I32, _DESC, ctypes.c_float, _P, _P, _P, _SZ, _P]),
     "msa_dense_gqa_prefill": (_I32, [_P, _I32, _I32, _I64, _DESC, ctypes.c_float, _P, _P, _P, _SZ, _P]),
     "msa_read_device_status": (_I32, [_P, _P, ctypes.POINTER(_I32)]),
+    "msa_sparse_attn_decode_noalloc": (_I32, [_P, _I32, _DESC, _P, _I32, ctypes.c_float, _P, _P, _P]),
     "msa_status_string": (ctypes.c_char_p, [_I32]),
     "msa_version": (_I32, []),
 }
@@ -203,6 +204,15 @@ def msa_dense_gqa_prefill(q, num_q_heads: int, n_q_tokens: int, q_start: int, de
     _check(load().msa_dense_gqa_prefill(_ptr(q), num_q_heads, n_q_tokens, q_start, ctypes.byref(desc), scale,
                                         _ptr(out), _ptr(lse), _ptr(ws), ws_bytes, _stream(stream)),
            "msa_dense_gqa_prefill")
+
+
+def msa_sparse_attn_decode_noalloc(q, num_q_heads: int, desc: KvDesc, idx, k_total: int, scale: float, out, lse,
+                                   stream=None) -> None:
+    """msa_sparse_attn_decode for callers that cannot allocate device memory:
+    the split-K scratch is a fixed 4 MiB array inside the library."""
+    _check(load().msa_sparse_attn_decode_noalloc(_ptr(q), num_q_heads, ctypes.byref(desc), _ptr(idx), k_total, scale,
+                                                 _ptr(out), _ptr(lse), _stream(stream)),
+           "msa_sparse_attn_decode_noalloc")
 
 
 def msa_read_device_status(ws, stream=None) -> int:
