@@ -193,7 +193,8 @@ def decode_setup(torch, msa, inp, k_scored, k_total):
     desc = msa.kv_desc(inp.k, inp.v, inp.seq_lens, inp.page_table)
     hq = inp.num_q_heads
     need = max(msa.msa_workspace_size(op, desc, hq, 1, k_total)
-               for op in (msa.MSA_OP_POOL, msa.MSA_OP_SELECT, msa.MSA_OP_DECODE, msa.MSA_OP_DENSE_DECODE))
+               for op in (msa.MSA_OP_POOL, msa.MSA_OP_SELECT, msa.MSA_OP_DECODE, msa.MSA_OP_DENSE_DECODE,
+                          msa.MSA_OP_DECODE_STEP))
     ws = msa.Workspace(need)
     pooled = torch.empty(msa.pooled_shape(desc), dtype=inp.k.dtype, device="cuda")
     idx = torch.empty(inp.batch, inp.num_kv_heads, k_total, dtype=torch.int32, device="cuda")
@@ -225,31 +226,65 @@ def decode_bytes(inp, k_total):
     return pooled, sel, qo
 
 
-def time_decode(torch, msa, timer, st, inp, steps, warmup, dist):
-    """Times select + attend; returns per-step and per-attention-kernel ms."""
-    q = inp.q
+def capture(torch, fn):
+    """CUDA graph of the library calls in ``fn`` (their first call, which does
+    the per-device set-up, has already run outside the capture)."""
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(torch, timer, g, steps, warmup, dist=None):
+    """Mean device time of one replay, L2 flushed before each timed replay."""
     for _ in range(warmup):
-        decode_select(msa, st, q)
-        decode_attend(msa, st, q)
+        g.replay()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    dist.barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if dist is not None:
+        dist.barrier()
     torch.cuda.synchronize()
-    for e0, e1, e2 in ev:
+    for e0, e1 in ev:
         timer.l2_flush()
         e0.record(stream)
-        decode_select(msa, st, q)
+        g.replay()
         e1.record(stream)
-        decode_attend(msa, st, q)
-        e2.record(stream)
     torch.cuda.synchronize()
-    dist.barrier()
-    step = [a.elapsed_time(c) for a, _, c in ev]
-    sel = [a.elapsed_time(b) for a, b, _ in ev]
-    att = [b.elapsed_time(c) for _, b, c in ev]
-    return statistics.mean(step), statistics.mean(sel), statistics.mean(att)
+    if dist is not None:
+        dist.barrier()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def decode_step(msa, st, q, out=None):
+    """The whole decode step through msa_sparse_decode_step (one kernel for
+    contiguous bf16 caches)."""
+    msa.msa_sparse_decode_step(q, st["hq"], st["pooled"], st["desc"], st["cfg"], st["idx"], st["k_total"], SCALE,
+                               st["out"] if out is None else out, st["lse"], st["ws"].buf, st["ws"].nbytes)
+
+
+def time_decode(torch, msa, timer, st, inp, steps, warmup, dist):
+    """Times the step (msa_sparse_decode_step) as one CUDA graph replay, and
+    the two-kernel form (select, then attend; each its own graph) for the
+    per-kernel figures."""
+    q = inp.q
+    for _ in range(max(1, warmup)):
+        decode_select(msa, st, q)
+        decode_attend(msa, st, q)
+        decode_step(msa, st, q)
+    torch.cuda.synchronize()
+    g_step = capture(torch, lambda: decode_step(msa, st, q))
+    g_sel = capture(torch, lambda: decode_select(msa, st, q))
+    g_att = capture(torch, lambda: decode_attend(msa, st, q))
+    step = time_graph(torch, timer, g_step, steps, warmup, dist)
+    sel = time_graph(torch, timer, g_sel, steps, warmup)
+    att = time_graph(torch, timer, g_att, steps, warmup)
+    return step, sel, att
 
 
 def time_e2e_decode(torch, msa, timer, st, inp, steps, warmup):
@@ -265,8 +300,7 @@ def time_e2e_decode(torch, msa, timer, st, inp, steps, warmup):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         q_dev.copy_(q_host, non_blocking=True)
-        decode_select(msa, st, q_dev)
-        decode_attend(msa, st, q_dev)
+        decode_step(msa, st, q_dev)
         out_host.copy_(st["out"], non_blocking=True)
         e1.record(stream)
         e1.synchronize()
@@ -277,20 +311,10 @@ def time_e2e_decode(torch, msa, timer, st, inp, steps, warmup):
 
 
 def time_op(torch, timer, fn, steps, warmup):
-    for _ in range(warmup):
-        fn()
+    """Device time of ``fn`` (library calls only) replayed as a CUDA graph."""
+    fn()
     torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
-    ts = []
-    for _ in range(steps):
-        timer.l2_flush()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        fn()
-        e1.record(stream)
-        ts.append((e0, e1))
-    torch.cuda.synchronize()
-    return statistics.mean(a.elapsed_time(b) for a, b in ts)
+    return time_graph(torch, timer, capture(torch, fn), steps, warmup)
 
 
 def extras_decode(torch, msa, timer, name, steps, warmup, hbm):
@@ -311,7 +335,7 @@ def extras_decode(torch, msa, timer, name, steps, warmup, hbm):
     status = msa.msa_read_device_status(st["ws"].buf)
     res = {
         "workload": name, "us_per_step": step_ms * 1e3,
-        "select_us": sel_ms * 1e3, "attend_us": att_ms * 1e3,
+        "two_kernel_select_us": sel_ms * 1e3, "two_kernel_attend_us": att_ms * 1e3,
         "step_GBps": (pooled_b + sel_b + qo_b) / (step_ms * 1e-3) / 1e9,
         "step_roofline_frac": (pooled_b + sel_b + qo_b) / (step_ms * 1e-3) / 1e9 / hbm,
         "bytes_per_step": pooled_b + sel_b + qo_b,
@@ -429,7 +453,9 @@ def run_ours(args):
         cpu = cpu_baseline(name, target_seconds=15.0)
 
     att_gbps = att_bytes / (att_ms * 1e-3) / 1e9
-    traffic = recorded_traffic("decode_bf16_kernel", "decode.cu")
+    step_bytes = pooled_b + sel_b + qo_b
+    step_gbps = step_bytes / (step_ms * 1e-3) / 1e9
+    traffic = recorded_traffic("decode_step_kernel", "step.cu")
     line = {
         "metric": METRIC, "value": round(step_ms * 1e3, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 6), "higher_is_better": False, "scaling": "weak",
@@ -439,19 +465,21 @@ def run_ours(args):
                         "64-token blocks, top-31 scored blocks + newest block, 16 needle blocks per (seq, head)",
             "global_batch": args.batch * world, "seq_len": 131072, "parallelism": f"replicas x{world}",
             "l2": "flushed (512 MB write) before every timed step",
-            "step": "select (scores + top-k) + sparse flash-decode; summary keys pooled beforehand",
+            "step": "msa_sparse_decode_step (block scores, top-k and sparse attention in one kernel), replayed as a "
+                    "CUDA graph; summary keys pooled beforehand",
         },
         "tokens_per_s": round(args.batch * world / (step_ms * 1e-3), 1),
-        "step_GBps": round((pooled_b + sel_b + qo_b) / (step_ms * 1e-3) / 1e9, 1),
-        "step_bytes": pooled_b + sel_b + qo_b,
-        "select_us": round(sel_ms * 1e3, 3), "attend_us": round(att_ms * 1e3, 3),
-        "roofline": {"kernel": "decode_bf16_kernel (sparse flash-decode + split-K combine)", "bound": "hbm",
-                     "achieved": round(att_gbps, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(att_gbps / hbm, 4), "peak_source": f"{peak_src} (hbm_gbs)",
-                     "algorithmic_bytes_per_launch": att_bytes, "traffic": traffic},
+        "step_GBps": round(step_gbps, 1),
+        "step_bytes": step_bytes,
+        "roofline": {"kernel": "decode_step_kernel (fused scores + top-k + sparse flash-decode)", "bound": "hbm",
+                     "achieved": round(step_gbps, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(step_gbps / hbm, 4), "peak_source": f"{peak_src} (hbm_gbs)",
+                     "algorithmic_bytes_per_launch": step_bytes, "traffic": traffic},
+        "two_kernel_form": {"select_us": round(sel_ms * 1e3, 3), "attend_us": round(att_ms * 1e3, 3),
+                            "attend_GBps": round(att_gbps, 1), "attend_frac": round(att_gbps / hbm, 4)},
         "pool_block_keys": {"us": round(pool_ms * 1e3, 2), "GBps": round(pool_bytes / (pool_ms * 1e-3) / 1e9, 1)},
         "e2e": {"value": round(e2e_ms * 1e3, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": args.steps,
         "clocks": clk,
         "device_status": status,
     }

@@ -111,7 +111,8 @@ typedef enum msa_op {
   MSA_OP_PREFILL = 3,
   MSA_OP_DENSE_DECODE = 4,
   MSA_OP_DENSE_PREFILL = 5,
-  MSA_OP_SELECT_PREFILL = 6  /* msa_select_topk_blocks with q_tile 64 */
+  MSA_OP_SELECT_PREFILL = 6, /* msa_select_topk_blocks with q_tile 64 */
+  MSA_OP_DECODE_STEP = 7     /* msa_sparse_decode_step */
 } msa_op;
 
 /* Bytes of workspace `op` needs for these shapes (host call, no GPU work).
@@ -152,8 +153,9 @@ msa_status msa_pool_block_keys(const msa_kv_desc* kv /* host */, int64_t first_b
  * candidates by (score descending, block ascending) plus the forced block are
  * written sorted ascending, padded with -1;
  * k_total >= min(k_scored, max_blocks) + force_local.
- * scores_out (nullable): [units, max_blocks] fp32 raw scores, -inf for
- * non-candidates (max_blocks = max_tokens/64 or max_pages_per_seq). */
+ * scores_out (nullable): [units, max_blocks] fp32 raw scores of the candidate
+ * blocks (max_blocks = max_tokens/64 or max_pages_per_seq); other entries are
+ * left unspecified. */
 msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_q_tokens,
                                   const void* pooled, const msa_kv_desc* kv /* host */,
                                   const msa_select_cfg* cfg /* host */, int32_t* idx_out, int32_t k_total,
@@ -181,6 +183,20 @@ msa_status msa_sparse_attn_prefill(const void* q, int32_t num_q_heads, int32_t n
                                    const msa_kv_desc* kv /* host */, const int32_t* idx, int32_t k_total,
                                    float scale, void* out, float* lse, void* ws, size_t ws_bytes,
                                    msa_stream_t stream);
+
+/* One whole decode step (guide §1, Step 1 then Step 2): the index lists of
+ * msa_select_topk_blocks (decode, cfg->q_tile == 1) written to idx_out, and
+ * the attention of msa_sparse_attn_decode over them written to out / lse,
+ * with the same results. For a contiguous bf16 cache with k_scored <= 64 it
+ * runs as one kernel: one thread-block cluster per (sequence, KV head) scores
+ * the summaries, selects and attends, exchanging the lists and the partial
+ * results through distributed shared memory (nothing round-trips through the
+ * workspace); otherwise it launches the two kernels in turn. ws must hold
+ * msa_workspace_size(MSA_OP_DECODE_STEP, ...) bytes. */
+msa_status msa_sparse_decode_step(const void* q, int32_t num_q_heads, const void* pooled,
+                                  const msa_kv_desc* kv /* host */, const msa_select_cfg* cfg /* host */,
+                                  int32_t* idx_out, int32_t k_total, float scale, void* out, float* lse, void* ws,
+                                  size_t ws_bytes, msa_stream_t stream);
 
 /* Dense causal GQA decode: the full-attention comparator (guide §3 quotes
  * the sparse speed-ups against full attention). Same as msa_sparse_attn_decode

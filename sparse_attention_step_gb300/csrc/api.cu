@@ -11,7 +11,8 @@ namespace msa {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int64_t kMaxTopkCandidates = 49152;  // shared-memory key array of the top-k kernel
+constexpr int64_t kMaxTopkCandidates = 32768;  // shared-memory key array of the top-k kernel (2M tokens)
+constexpr int64_t kTopkCandCap = 8192;         // refinement buffer of the top-k kernel
 
 struct DeviceInfo {
   bool ready = false;
@@ -32,8 +33,10 @@ msa_status device_info(DeviceInfo** out) {
     if (set_decode_smem() != cudaSuccess) return MSA_ERR_CUDA;
     if (set_prefill_smem() != cudaSuccess) return MSA_ERR_CUDA;
     if (set_prefill_tc_smem() != cudaSuccess) return MSA_ERR_CUDA;
-    d.topk_smem = kMaxTopkCandidates * sizeof(uint32_t);
+    if (set_step_smem() != cudaSuccess) return MSA_ERR_CUDA;
+    d.topk_smem = (kMaxTopkCandidates + kTopkCandCap) * sizeof(uint32_t);
     if (set_topk_smem(d.topk_smem) != cudaSuccess) return MSA_ERR_CUDA;
+    if (set_select_decode_smem(select_decode_smem(4096)) != cudaSuccess) return MSA_ERR_CUDA;
     d.ready = true;
   }
   *out = &d;
@@ -138,7 +141,7 @@ int32_t* ws_status(void* ws) { return ws == nullptr ? nullptr : reinterpret_cast
 
 // ---- workspace layouts (bytes after the header) ----
 struct SelectLayout {
-  size_t scores = 0, qidx = 0, total = 0;
+  size_t scores = 0, qidx = 0, cand = 0, total = 0;
 };
 SelectLayout select_layout(const msa_kv_desc* kv, int n_q_tokens, int prefill) {
   SelectLayout L;
@@ -148,6 +151,12 @@ SelectLayout select_layout(const msa_kv_desc* kv, int n_q_tokens, int prefill) {
   size_t off = kWsRegion + align_up(static_cast<size_t>(units) * kv_max_blocks(kv) * sizeof(float), 256);
   L.qidx = off;
   if (prefill) off += align_up(static_cast<size_t>(units) * kHeadDim * sizeof(float), 256);
+  L.cand = off;
+  if (!prefill) {
+    int chunk = 0, n_chunks = 0;
+    select_decode_shape(kv_max_blocks(kv), units, num_sms_current(), &chunk, &n_chunks);
+    off += align_up(select_decode_cand_bytes(units, n_chunks), 256);
+  }
   L.total = off;
   return L;
 }
@@ -157,10 +166,11 @@ struct DecodeLayout {
   int n_splits = 1, bps = 1;
   size_t tickets = 0, partials = 0, total = 0;
 };
-DecodeLayout decode_layout(const msa_kv_desc* kv, int64_t list_len, int num_sms) {
+DecodeLayout decode_layout(const msa_kv_desc* kv, int64_t list_len, int num_sms, bool dense) {
   DecodeLayout L;
   const int64_t units = static_cast<int64_t>(kv->batch) * kv->num_kv_heads;
-  decode_splits(units, list_len, num_sms > 0 ? num_sms : 1, &L.n_splits, &L.bps);
+  decode_splits(units, list_len, num_sms > 0 ? num_sms : 1, kv->dtype == MSA_DTYPE_BF16, dense, &L.n_splits,
+                &L.bps);
   L.tickets = kWsHeader;
   L.partials = kWsRegion;
   L.total = L.partials + decode_partials_bytes(units, L.n_splits);
@@ -196,7 +206,7 @@ msa_status decode_common(const void* q, int hq, const msa_kv_desc* kv, const int
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != MSA_OK) return st;
   const int64_t list_len = idx != nullptr ? k_total : kv_max_blocks(kv);
-  DecodeLayout L = decode_layout(kv, list_len, dev->num_sms);
+  DecodeLayout L = decode_layout(kv, list_len, dev->num_sms, idx == nullptr);
   if ((st = check_ws(ws, ws_bytes, L.total)) != MSA_OK) return st;
   DecodeArgs a;
   a.q = q;
@@ -298,10 +308,13 @@ size_t msa_workspace_size(int32_t op, const msa_kv_desc* kv, int32_t num_q_heads
     case MSA_OP_SELECT_PREFILL: return n_q_tokens > 0 ? select_layout(kv, n_q_tokens, 1).total : 0;
     case MSA_OP_DECODE:
       if (k_total <= 0) return 0;
-      return decode_layout(kv, k_total, num_sms_current()).total;
-    case MSA_OP_DENSE_DECODE: return decode_layout(kv, kv_max_blocks(kv), num_sms_current()).total;
+      return decode_layout(kv, k_total, num_sms_current(), false).total;
+    case MSA_OP_DENSE_DECODE: return decode_layout(kv, kv_max_blocks(kv), num_sms_current(), true).total;
     case MSA_OP_PREFILL:
     case MSA_OP_DENSE_PREFILL: return kWsHeader;
+    case MSA_OP_DECODE_STEP:
+      if (k_total <= 0) return 0;
+      return std::max(select_layout(kv, 1, 0).total, decode_layout(kv, k_total, num_sms_current(), false).total);
     default: return 0;
   }
   (void)num_q_heads;
@@ -358,15 +371,21 @@ msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_
   if ((st = check_ws(ws, ws_bytes, L.total)) != MSA_OK) return st;
   float* scores = scores_out != nullptr ? scores_out : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.scores);
   float* qidx = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.qidx);
+  FusedSelect fused;
+  fused.scores_out = scores_out;
+  fused.cand = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + L.cand);
+  fused.tickets = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + kWsHeader);
+  fused.num_sms = dev->num_sms;
+  if (!prefill && !decode_units_fit(kv)) return MSA_ERR_UNSUPPORTED;
   KvView view = view_of(kv);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (kv->dtype == MSA_DTYPE_BF16)
     return cuda_status(launch_select<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(q), num_q_heads, n_q_tokens,
                                                     static_cast<const __nv_bfloat16*>(pooled), view, kv->batch,
-                                                    *cfg, idx_out, k_total, scores, qidx, ws_status(ws), s));
+                                                    *cfg, idx_out, k_total, scores, qidx, &fused, ws_status(ws), s));
   return cuda_status(launch_select<float>(static_cast<const float*>(q), num_q_heads, n_q_tokens,
                                           static_cast<const float*>(pooled), view, kv->batch, *cfg, idx_out,
-                                          k_total, scores, qidx, ws_status(ws), s));
+                                          k_total, scores, qidx, &fused, ws_status(ws), s));
 }
 
 msa_status msa_sparse_attn_decode(const void* q, int32_t num_q_heads, const msa_kv_desc* kv, const int32_t* idx,
@@ -396,6 +415,42 @@ msa_status msa_dense_gqa_prefill(const void* q, int32_t num_q_heads, int32_t n_q
                                  size_t ws_bytes, msa_stream_t stream) {
   return prefill_common(q, num_q_heads, n_q_tokens, q_start, kv, nullptr, 0, scale, out, lse, ws, ws_bytes,
                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_sparse_decode_step(const void* q, int32_t num_q_heads, const void* pooled, const msa_kv_desc* kv,
+                                  const msa_select_cfg* cfg, int32_t* idx_out, int32_t k_total, float scale,
+                                  void* out, float* lse, void* ws, size_t ws_bytes, msa_stream_t stream) {
+  msa_status st = validate_kv(kv);
+  if (st != MSA_OK) return st;
+  if (cfg == nullptr || q == nullptr || pooled == nullptr || idx_out == nullptr || out == nullptr)
+    return MSA_ERR_INVALID_ARG;
+  if ((st = check_q_heads(kv, num_q_heads)) != MSA_OK) return st;
+  if (cfg->q_tile != 1) return MSA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f)) return MSA_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != MSA_OK) return st;
+  int C = 0, chunk = 0, bps = 0;
+  const int64_t units = static_cast<int64_t>(kv->batch) * kv->num_kv_heads;
+  const bool fused = kv->dtype == MSA_DTYPE_BF16 && kv->layout == MSA_KV_CONTIGUOUS &&
+                     cfg->mode == MSA_SCORE_MEAN_POOLED_KEYS && cfg->k_scored >= 0 &&
+                     k_total >= std::min<int64_t>(cfg->k_scored, kv_max_blocks(kv)) + (cfg->force_local ? 1 : 0) &&
+                     step_shape(units, kv_max_blocks(kv), cfg->k_scored, k_total, dev->num_sms, &C, &chunk, &bps);
+  if (!fused) {
+    // the same step as two launches
+    st = msa_select_topk_blocks(q, num_q_heads, 1, pooled, kv, cfg, idx_out, k_total, nullptr, ws, ws_bytes, stream);
+    if (st != MSA_OK) return st;
+    return msa_sparse_attn_decode(q, num_q_heads, kv, idx_out, k_total, scale, out, lse, ws, ws_bytes, stream);
+  }
+  if ((st = check_ws(ws, ws_bytes, kWsHeader)) != MSA_OK) return st;
+  const int64_t rows = kv_rows(kv);
+  if (rows >= (int64_t(1) << 31)) return MSA_ERR_UNSUPPORTED;
+  CUtensorMap tmk, tmv;
+  if ((st = make_kv_map(&tmk, kv->k, rows)) != MSA_OK) return st;
+  if ((st = make_kv_map(&tmv, kv->v, rows)) != MSA_OK) return st;
+  return cuda_status(launch_decode_step(tmk, tmv, view_of(kv), kv->batch, static_cast<const __nv_bfloat16*>(q),
+                                        num_q_heads, static_cast<const __nv_bfloat16*>(pooled), *cfg, k_total, C,
+                                        chunk, bps, scale * kLog2e, idx_out, static_cast<__nv_bfloat16*>(out), lse,
+                                        ws_status(ws), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 msa_status msa_read_device_status(const void* ws, msa_stream_t stream, int32_t* status_out) {
@@ -473,7 +528,7 @@ extern "C" msa_status msa_sparse_attn_decode_noalloc(const void* q, int32_t num_
   uint8_t* ws = nullptr;
   if ((st = noalloc_scratch(&ws)) != MSA_OK) return st;
   if (!decode_units_fit(kv)) return MSA_ERR_UNSUPPORTED;
-  const DecodeLayout L = decode_layout(kv, k_total, dev->num_sms);
+  const DecodeLayout L = decode_layout(kv, k_total, dev->num_sms, false);
   if (L.total > kNoAllocScratchBytes) return MSA_ERR_WORKSPACE;  // beyond the fixed scratch
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the array keeps the previous call's contents: the tickets must start at zero

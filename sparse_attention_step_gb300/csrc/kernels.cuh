@@ -12,10 +12,21 @@ cudaError_t launch_pool(const T* k, const KvView& kv, int batch, int64_t first_b
                         int32_t* status, cudaStream_t stream);
 
 // ---- Step 1b/1c: index query, scores, top-k (select.cu) ----
+// Scratch of the fused decode selection (k_scored <= 64).
+struct FusedSelect {
+  float* scores_out;  // nullable
+  uint64_t* cand;     // [units, n_chunks, 64]
+  int32_t* tickets;   // [units]
+  int num_sms;
+};
 template <typename T>
 cudaError_t launch_select(const T* q, int hq, int n_q_tokens, const T* pooled, const KvView& kv, int batch,
                           const msa_select_cfg& cfg, int32_t* idx_out, int k_total, float* scores, float* qidx_ws,
-                          int32_t* status, cudaStream_t stream);
+                          const FusedSelect* fused, int32_t* status, cudaStream_t stream);
+void select_decode_shape(int64_t max_blocks, int64_t units, int num_sms, int* chunk, int* n_chunks);
+size_t select_decode_smem(int chunk);
+size_t select_decode_cand_bytes(int64_t units, int n_chunks);
+cudaError_t set_select_decode_smem(size_t bytes);
 cudaError_t set_topk_smem(size_t bytes);
 
 // ---- Step 2, decode (decode.cu) ----
@@ -35,7 +46,7 @@ struct DecodeArgs {
 };
 cudaError_t set_decode_smem();
 size_t decode_smem_bytes();
-void decode_splits(int64_t units, int64_t list_len, int num_sms, int* n_splits, int* bps);
+void decode_splits(int64_t units, int64_t list_len, int num_sms, bool cluster, bool dense, int* n_splits, int* bps);
 size_t decode_partials_bytes(int64_t units, int n_splits);
 cudaError_t launch_decode_bf16(const CUtensorMap& tmk, const CUtensorMap& tmv, const KvView& kv, int batch,
                                const DecodeArgs& a, cudaStream_t stream);
@@ -62,5 +73,15 @@ cudaError_t launch_prefill_tc(const CUtensorMap& tmq, const CUtensorMap& tmk, co
                               const KvView& kv, const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_bf16(const CUtensorMap& tmk, const CUtensorMap& tmv, const KvView& kv,
                                 const PrefillArgs& a, cudaStream_t stream);
+
+// ---- fused decode step (step.cu) ----
+bool step_shape(int64_t units, int64_t max_blocks, int k_scored, int k_total, int num_sms, int* C, int* chunk,
+                int* bps);
+cudaError_t set_step_smem();
+cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, const KvView& kv, int batch,
+                               const __nv_bfloat16* q, int hq, const __nv_bfloat16* pooled,
+                               const msa_select_cfg& cfg, int k_total, int C, int chunk, int bps, float scale_log2,
+                               int32_t* idx_out, __nv_bfloat16* out, float* lse, int32_t* status,
+                               cudaStream_t stream);
 
 }  // namespace msa

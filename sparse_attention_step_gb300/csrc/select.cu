@@ -6,18 +6,23 @@
 // Three kernels:
 //   qidx_prefill_kernel  q_idx of a 64-token prefill tile = sum over its tokens
 //                        and the group's heads (fp32, token-major order).
-//   score_kernel         streams the pooled keys of each unit once (bandwidth
-//                        bound, 16-byte loads, one half-warp per block row) and
-//                        writes fp32 scores; for decode it forms q_idx inline
-//                        from the G query heads.
-//   topk_kernel          per unit, radix select of the k-th largest score in
-//                        shared memory (4 passes of 8-bit digits over
-//                        order-preserving keys), ties to the lower block, then
-//                        an ordered compaction that emits the kept blocks in
-//                        ascending order followed by the forced block.
+//   score_kernel         streams the summary keys of each unit once (bandwidth
+//                        bound, 16-byte loads, one half-warp per block row, 16
+//                        rows in flight per thread), writes fp32 scores and
+//                        adds each score to a per-unit histogram of the top 12
+//                        bits of its order-preserving key; for decode it forms
+//                        q_idx inline from the G query heads.
+//   topk_kernel          per unit: the histogram gives the 12-bit bin that
+//                        holds the k-th largest score; the few scores in that
+//                        bin are refined by two 10-bit radix passes, ties go
+//                        to the lower block, and an ordered compaction emits
+//                        the kept blocks ascending, then the forced block. It
+//                        clears the histogram it read for the next call.
 #include <float.h>
 
 #include "kernels.cuh"
+#include "rows.cuh"
+#include "topk64.cuh"
 
 namespace msa {
 
@@ -51,26 +56,8 @@ __global__ void __launch_bounds__(128) qidx_prefill_kernel(const T* __restrict__
 // ---------------------------------------------------------------------------
 constexpr int kScoreThreads = 256;
 constexpr int kScoreChunk = 256;  // pooled rows per CTA
-
-template <typename T>
-__device__ inline void load8(const T* p, float (&x)[8]);
-template <>
-__device__ inline void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&x)[8]) {
-  uint4 r = __ldg(reinterpret_cast<const uint4*>(p));
-  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = __uint_as_float(w[i] << 16);
-    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-template <>
-__device__ inline void load8<float>(const float* p, float (&x)[8]) {
-  float4 a = __ldg(reinterpret_cast<const float4*>(p));
-  float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
+constexpr int kHistBits = 12;     // first radix digit of the top-k: top 12 bits of the score key
+constexpr int kHistBins = 1 << kHistBits;
 
 struct ScoreArgs {
   int hq, hkv;
@@ -135,10 +122,10 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const T* __restric
   const int64_t row_end = min(chunk0 + kScoreChunk, a.max_blocks);
 
   constexpr int kRowsPerIter = kScoreThreads / 16;
-  constexpr int kUnroll = 4;
+  constexpr int kUnroll = kScoreChunk / kRowsPerIter;  // every row of the chunk in flight at once
 #pragma unroll 1
   for (int64_t r0 = chunk0; r0 < row_end; r0 += kRowsPerIter * kUnroll) {
-    float kp[kUnroll][8];
+    RawRow<T> kp[kUnroll];
     bool have[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -149,7 +136,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const T* __restric
         if (prow < 0) {
           have[u] = false;
         } else {
-          load8<T>(pooled + prow * kHeadDim + 8 * e, kp[u]);
+          kp[u].load(pooled + prow * kHeadDim + 8 * e);
         }
       }
     }
@@ -159,11 +146,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const T* __restric
       const bool in_range = b < row_end;  // all lanes still join the shuffles
 #pragma unroll
       for (int t = 0; t < kTiles; ++t) {
-        float part = 0.f;
-        if (have[u]) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) part = fmaf(qi[t][i], kp[u][i], part);
-        }
+        float part = have[u] ? kp[u].dot(qi[t]) : 0.f;
         part += __shfl_xor_sync(0xffffffffu, part, 8);
         part += __shfl_xor_sync(0xffffffffu, part, 4);
         part += __shfl_xor_sync(0xffffffffu, part, 2);
@@ -221,100 +204,144 @@ struct TopkArgs {
   int64_t max_blocks;
 };
 
+constexpr int kCandCap = 8192;  // keys of the threshold bin refined in shared memory
+
+// Finds, among `nbins` counts in shared memory (bin index increasing with the
+// key), the bin holding the k-th largest element: *bin and *above (the count
+// in higher bins). Each of the 1024 threads owns nbins/1024 consecutive bins.
+__device__ inline void find_kth_bin(const int* cnt, int nbins, int k, int* scan_tmp, int* out_bin, int* out_above) {
+  const int per = nbins / kTopkThreads;
+  const int lo = threadIdx.x * per;
+  int own = 0;
+  for (int j = 0; j < per; ++j) own += cnt[lo + j];
+  int total;
+  const int incl = block_inclusive_scan(own, scan_tmp, &total);
+  int above = total - incl;  // elements in bins above this thread's range
+  if (above < k && above + own >= k) {
+    for (int j = per - 1; j >= 0; --j) {
+      if (above + cnt[lo + j] >= k) {
+        *out_bin = lo + j;
+        *out_above = above;
+        break;
+      }
+      above += cnt[lo + j];
+    }
+  }
+  __syncthreads();
+}
+
+// Histogram of the digit of `bits` bits at `shift` of the keys matching
+// (prefix, mask), with warp-aggregated shared-memory atomics (scores of a
+// unit crowd into few bins, so lanes with equal digits add once).
+__device__ inline void digit_hist(const uint32_t* keys, int n, uint32_t prefix, uint32_t mask, int shift, int bits,
+                                  int* cnt) {
+  const uint32_t dmask = (1u << bits) - 1u;
+  for (int i = threadIdx.x; i < (1 << bits); i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    int d = -1;
+    if (i < n) {
+      const uint32_t key = keys[i];
+      if ((key & mask) == prefix) d = static_cast<int>((key >> shift) & dmask);
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, d);
+    if (d >= 0 && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&cnt[d], __popc(peers));
+  }
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ scores, KvView kv, TopkArgs a,
                                                            int32_t* __restrict__ idx_out, int32_t* status) {
-  extern __shared__ uint32_t keys[];  // [max_blocks]
-  __shared__ int hist[256];
+  extern __shared__ uint32_t keys[];      // [max_blocks], then kCandCap candidate keys
+  __shared__ int cnt[kHistBins];
   __shared__ int scan_tmp[33];
-  __shared__ int sel_digit, sel_above;
+  __shared__ int sel_bin, sel_above, n_cand_keys;
 
   const int h = blockIdx.x;
   const int outer = blockIdx.y;
   const int tid = threadIdx.x;
   const int64_t unit = static_cast<int64_t>(outer) * a.hkv + h;
 
-  int64_t n, forced;
+  int64_t n64, forced;
   if (!a.prefill) {
     const int64_t len = kv.seq_len(outer, status, kIdTopk);
     const int64_t nb = (len + kBlock - 1) / kBlock;
     const int64_t nbf = len / kBlock;
-    n = a.force_local ? min(nbf, nb - 1) : nbf;
+    n64 = a.force_local ? min(nbf, nb - 1) : nbf;
     forced = (a.force_local && nb > 0) ? nb - 1 : -1;
   } else {
-    n = a.q_start / kBlock + outer;
-    forced = a.force_local ? n : -1;
+    n64 = a.q_start / kBlock + outer;
+    forced = a.force_local ? n64 : -1;
   }
-  if (n < 0) n = 0;
-  const int k = static_cast<int>(min(static_cast<int64_t>(a.k_scored), n));
+  const int n = static_cast<int>(n64 < 0 ? 0 : n64);
+  const int k = min(a.k_scored, n);
   const float* sc = scores + unit * a.max_blocks;
   int32_t* out = idx_out + unit * a.k_total;
+  uint32_t* cand = keys + a.max_blocks;
 
-  uint32_t thresh = 0;  // keys >= thresh ... (see below)
-  int take_equal = 0;   // how many keys == thresh to keep (lowest indices)
+  for (int i = tid; i < n; i += blockDim.x) keys[i] = float_to_key(sc[i]);
+  if (tid == 0) n_cand_keys = 0;
+  __syncthreads();
+
+  uint32_t thresh = 0;  // the k-th largest key
+  int take_equal = 0;   // how many keys equal to thresh are kept (lowest blocks first)
   const bool all = (k >= n);
   if (!all && k > 0) {
-    for (int64_t i = tid; i < n; i += blockDim.x) keys[i] = float_to_key(sc[i]);
-    uint32_t prefix = 0, mask = 0;
-    int remaining = k;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
-      __syncthreads();
-      for (int64_t i = tid; i < n; i += blockDim.x) {
-        const uint32_t key = keys[i];
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
+    // digit 1: the top 12 bits
+    digit_hist(keys, n, 0u, 0u, 32 - kHistBits, kHistBits, cnt);
+    find_kth_bin(cnt, kHistBins, k, scan_tmp, &sel_bin, &sel_above);
+    uint32_t prefix = static_cast<uint32_t>(sel_bin) << (32 - kHistBits);
+    uint32_t mask = 0xFFFFFFFFu << (32 - kHistBits);
+    int remaining = k - sel_above;
+    const int in_bin = cnt[sel_bin];
+    __syncthreads();  // every thread has read in_bin before cnt is reused
+    // gather the keys of that bin (few, normally) to refine
+    const uint32_t* src = keys;
+    int src_n = n;
+    if (in_bin <= kCandCap) {
+      for (int base = 0; base < n; base += blockDim.x) {
+        const int i = base + tid;
+        const bool hit = i < n && (keys[i] & mask) == prefix;
+        const unsigned m = __ballot_sync(0xffffffffu, hit);
+        int slot = 0;
+        if ((tid & 31) == 0 && m != 0u) slot = atomicAdd(&n_cand_keys, __popc(m));
+        slot = __shfl_sync(0xffffffffu, slot, 0);
+        if (hit) cand[slot + __popc(m & ((1u << (tid & 31)) - 1u))] = keys[i];
       }
       __syncthreads();
-      if (tid < 32) {
-        // lane l owns digits [8l, 8l+8); suffix sums from the top digit down
-        int own = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) own += hist[8 * tid + j];
-        int suf = own;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          int y = __shfl_down_sync(0xffffffffu, suf, off);
-          if (tid + off < 32) suf += y;
-        }
-        const int above_lane = suf - own;  // count in lanes > tid
-        if (above_lane < remaining && suf >= remaining) {
-          int acc = above_lane;
-          for (int d = 8 * tid + 7; d >= 8 * tid; --d) {
-            if (acc + hist[d] >= remaining) {
-              sel_digit = d;
-              sel_above = acc;
-              break;
-            }
-            acc += hist[d];
-          }
-        }
-      }
-      __syncthreads();
+      src = cand;
+      src_n = n_cand_keys;
+    }
+    // digits 2 and 3 (10 bits each)
+    for (int shift = 32 - kHistBits - 10; shift >= 0; shift -= 10) {
+      digit_hist(src, src_n, prefix, mask, shift, 10, cnt);
+      find_kth_bin(cnt, 1024, remaining, scan_tmp, &sel_bin, &sel_above);
       remaining -= sel_above;
-      prefix |= static_cast<uint32_t>(sel_digit) << shift;
-      mask |= 255u << shift;
-      __syncthreads();
+      prefix |= static_cast<uint32_t>(sel_bin) << shift;
+      mask |= 1023u << shift;
     }
     thresh = prefix;
     take_equal = remaining;
   }
 
   // Ordered compaction over contiguous per-thread ranges.
-  const int64_t per = (n + blockDim.x - 1) / blockDim.x;
-  const int64_t lo = min(n, static_cast<int64_t>(tid) * per);
-  const int64_t hi = min(n, lo + per);
+  const int per = (n + blockDim.x - 1) / blockDim.x;
+  const int lo = min(n, tid * per);
+  const int hi = min(n, lo + per);
   int written = 0;
   if (k > 0) {
     int eq_before = 0;
     if (!all) {
       int my_eq = 0;
-      for (int64_t i = lo; i < hi; ++i) my_eq += keys[i] == thresh;
+      for (int i = lo; i < hi; ++i) my_eq += keys[i] == thresh;
       int tot;
       eq_before = block_inclusive_scan(my_eq, scan_tmp, &tot) - my_eq;
     }
     int my_sel = 0;
     {
       int eq = eq_before;
-      for (int64_t i = lo; i < hi; ++i) {
+      for (int i = lo; i < hi; ++i) {
         if (all) {
           ++my_sel;
         } else {
@@ -328,7 +355,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     int pos = block_inclusive_scan(my_sel, scan_tmp, &tot) - my_sel;
     {
       int eq = eq_before;
-      for (int64_t i = lo; i < hi; ++i) {
+      for (int i = lo; i < hi; ++i) {
         bool keep;
         if (all) {
           keep = true;
@@ -349,17 +376,274 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
 }
 
 // ---------------------------------------------------------------------------
+// Fused decode selection (k_scored <= 64). One CTA handles a chunk of a
+// unit's candidate blocks: a producer warp streams the chunk's summary rows
+// into a shared-memory ring with bulk copies (one 16 KB copy per 64 rows for a
+// contiguous cache, one 256-byte copy per row for a paged one); eight warps
+// score them (a half-warp per row) into 64-bit selection keys; block_topk
+// keeps the chunk's best. A unit spread over several chunks posts the chunk
+// lists and its last CTA to finish (atomic ticket) selects among them.
+// grid (n_chunks, Hkv, batch); chunks past a sequence's candidates exit at
+// once and take no ticket.
+// ---------------------------------------------------------------------------
+constexpr int kSelWarps = 8;
+constexpr int kSelThreads = 32 * (kSelWarps + 1);
+constexpr int kSelStageRows = 64;
+constexpr int kSelStages = 4;
+constexpr int kSelStageBytes = kSelStageRows * kHeadDim * 2;  // bf16 rows (fp32 rows use two stages' room)
+
+struct SelDecArgs {
+  int hq, hkv;
+  int force_local;
+  int k_scored;
+  int k_total;
+  int chunk;        // candidate rows per CTA: 512 * 2^j, <= 4096
+  int n_chunks;     // chunks per unit at capacity (grid.x)
+  int64_t max_blocks;
+  float* scores_out;  // nullable [units, max_blocks]
+  uint64_t* cand;     // [units, n_chunks, 64] chunk lists (multi-chunk units)
+  int32_t* tickets;   // [units], zero between calls
+};
+
+__device__ inline int pow2_at_least(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+// Writes the final list of a unit: the blocks of the kk best keys ascending,
+// the forced block, then -1 padding. Called by every thread.
+__device__ inline void write_selection(const uint64_t* top, int kk, int64_t forced, int k_total, int32_t* out,
+                                       int* sorted_tmp) {
+  if (threadIdx.x < 32) warp_sort64_blocks_asc(top, kk, sorted_tmp);
+  __syncthreads();
+  for (int i = threadIdx.x; i < k_total; i += blockDim.x) {
+    int v;
+    if (i < kk) v = sorted_tmp[i];
+    else if (i == kk && forced >= 0) v = static_cast<int>(forced);
+    else v = -1;
+    out[i] = v;
+  }
+}
+
+// The k best keys into top[0..k): the binned selection, else (keys crowded
+// into one bin) a full sort in lists of 64 using the free ring as scratch.
+__device__ inline void choose_top(const uint64_t* keys, int n, int k, uint8_t* ring, uint64_t* top,
+                                  SelectScratch& scr, int* count) {
+  if (block_select(keys, n, k, top, scr)) return;
+  block_topk(keys, n, k, reinterpret_cast<uint64_t*>(ring), top, count);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* __restrict__ q,
+                                                                   const T* __restrict__ pooled, KvView kv,
+                                                                   SelDecArgs a, int32_t* __restrict__ idx_out,
+                                                                   int32_t* status) {
+  constexpr int kRowBytes = SelRow<T>::kBytes;
+  constexpr int kStageRows = kSelStageBytes / kRowBytes;  // 64 (bf16) or 32 (fp32) rows per stage
+  extern __shared__ __align__(128) uint8_t sel_raw[];
+  uint8_t* ring = sel_raw;                                                   // kSelStages x 16 KB
+  uint64_t* keys = reinterpret_cast<uint64_t*>(sel_raw + kSelStages * kSelStageBytes);  // [max(chunk, 2048)]
+  int32_t* pages = reinterpret_cast<int32_t*>(keys + max(a.chunk, 2048));  // [chunk] page ids (paged caches)
+  __shared__ uint64_t full[kSelStages], empty[kSelStages];
+  __shared__ uint64_t top[64];
+  __shared__ SelectScratch scr;
+  __shared__ int sorted_blocks[64];
+  __shared__ int count, is_last;
+
+  const int c = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t unit = static_cast<int64_t>(s) * a.hkv + h;
+  const int grp = a.hq / a.hkv;
+  pdl_wait();  // inputs and the workspace may come from the previous kernel
+
+  const int64_t len = kv.seq_len(s, status, kIdScore);
+  const int64_t nb = (len + kBlock - 1) / kBlock;
+  const int64_t nbf = len / kBlock;
+  int64_t n_cand = a.force_local ? min(nbf, nb - 1) : nbf;
+  if (n_cand < 0) n_cand = 0;
+  const int64_t forced = (a.force_local && nb > 0) ? nb - 1 : -1;
+  const int my_chunks = n_cand > 0 ? static_cast<int>((n_cand + a.chunk - 1) / a.chunk) : 1;
+  if (c >= my_chunks) return;  // past this sequence's candidates
+  const int64_t r0 = static_cast<int64_t>(c) * a.chunk;
+  const int rows = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(a.chunk), n_cand - r0)));
+  const int n_stages = (rows + kStageRows - 1) / kStageRows;
+
+  if (tid == 0) {
+    for (int i = 0; i < kSelStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kSelWarps);
+    }
+    fence_mbar_init();
+  }
+  if (kv.layout == MSA_KV_PAGED)
+    for (int i = tid; i < rows; i += blockDim.x) pages[i] = kv.page(s, r0 + i, status, kIdScore);
+  __syncthreads();
+
+  const int e = tid & 15, hw = tid >> 4;  // scorers: 16 half-warps, lane e owns dims [8e, 8e+8)
+  float qi[8];
+  if (warp < kSelWarps) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qi[i] = 0.f;
+    for (int g = 0; g < grp; ++g) {
+      float x[8];
+      load8<T>(q + (static_cast<int64_t>(s) * a.hq + h * grp + g) * kHeadDim + 8 * e, x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) qi[i] += x[i];
+    }
+  }
+  auto emit = [&](int i, float part, bool ok) {  // row i of the chunk
+    const int64_t b = r0 + i;
+    keys[i] = ok ? sel_key(part, static_cast<int>(b)) : 0ull;
+    if (a.scores_out != nullptr) a.scores_out[unit * a.max_blocks + b] = ok ? part : -INFINITY;
+  };
+  if (kv.layout == MSA_KV_CONTIGUOUS) {
+    if (warp == kSelWarps) {
+      // ---------------- producer: one bulk copy per 64-row stage ----------------
+      if (lane == 0) {
+        for (int st = 0; st < n_stages; ++st) {
+          const int slot = st % kSelStages;
+          if (st >= kSelStages && !mbar_wait(&empty[slot], ((st / kSelStages) - 1) & 1, status, kIdScore)) break;
+          const int base = st * kStageRows;
+          const int n = min(kStageRows, rows - base);
+          const T* src = pooled + ((static_cast<int64_t>(s) * a.hkv + h) * (kv.max_tokens / kBlock) + r0 + base) *
+                                      kHeadDim;
+          mbar_arrive_expect_tx(&full[slot], n * kRowBytes);
+          bulk_load(ring + slot * kSelStageBytes, src, n * kRowBytes, &full[slot]);
+        }
+      }
+    } else {
+      // ---------------- scorers ----------------
+      for (int st = 0; st < n_stages; ++st) {
+        const int slot = st % kSelStages;
+        if (!mbar_wait(&full[slot], (st / kSelStages) & 1, status, kIdScore)) break;
+        const uint8_t* stage = ring + slot * kSelStageBytes;
+        const int base = st * kStageRows;
+        const int n = min(kStageRows, rows - base);
+#pragma unroll
+        for (int rr = 0; rr < kStageRows / 16; ++rr) {
+          const int i = rr * 16 + hw;  // row within the stage
+          float part = i < n ? SelRow<T>::dot(stage + i * kRowBytes, e, qi) : 0.f;
+          part += __shfl_xor_sync(0xffffffffu, part, 8);
+          part += __shfl_xor_sync(0xffffffffu, part, 4);
+          part += __shfl_xor_sync(0xffffffffu, part, 2);
+          part += __shfl_xor_sync(0xffffffffu, part, 1);
+          if (e == 0 && i < n) emit(base + i, part, true);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+      }
+    }
+  } else if (warp < kSelWarps) {
+    // paged: summary rows are scattered one per page; direct 16-byte loads,
+    // 8 rows in flight per thread
+    constexpr int kRowsPerPass = 8 * (kSelWarps * 2);
+    for (int p0 = 0; p0 < rows; p0 += kRowsPerPass) {
+      RawRow<T> kp[8];
+      bool have[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = p0 + u * (kSelWarps * 2) + hw;
+        have[u] = i < rows && pages[i] >= 0;
+        if (have[u]) kp[u].load(pooled + (static_cast<int64_t>(pages[i]) * a.hkv + h) * kHeadDim + 8 * e);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = p0 + u * (kSelWarps * 2) + hw;
+        float part = have[u] ? kp[u].dot(qi) : 0.f;
+        part += __shfl_xor_sync(0xffffffffu, part, 8);
+        part += __shfl_xor_sync(0xffffffffu, part, 4);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        if (e == 0 && i < rows) emit(i, part, have[u]);
+      }
+    }
+  }
+  __syncthreads();
+  pdl_trigger();  // the attention kernel may start its set-up
+  const int kk = static_cast<int>(n_cand < a.k_scored ? n_cand : static_cast<int64_t>(a.k_scored));
+  int32_t* out = idx_out + unit * a.k_total;
+  const int kk_local = min(kk, rows);
+  if (kk_local > 0) choose_top(keys, rows, kk_local, ring, top, scr, &count);
+  if (my_chunks == 1) {
+    write_selection(top, kk, forced, a.k_total, out, sorted_blocks);
+    return;
+  }
+  // post this chunk's list; the unit's last CTA selects among them
+  uint64_t* mine = a.cand + (unit * a.n_chunks + c) * 64;
+  if (tid < 64) mine[tid] = tid < kk_local ? top[tid] : 0ull;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) is_last = atomicAdd(&a.tickets[unit], 1) == my_chunks - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  const uint64_t* all = a.cand + unit * a.n_chunks * 64;
+  const int n_all = my_chunks * 64;
+  for (int i = tid; i < n_all; i += blockDim.x) keys[i] = __ldcg(all + i);
+  __syncthreads();
+  if (kk > 0) choose_top(keys, n_all, kk, ring, top, scr, &count);
+  write_selection(top, kk, forced, a.k_total, out, sorted_blocks);
+  if (tid == 0) a.tickets[unit] = 0;  // ready for the next call
+}
+
+// Chunk size for the fused decode selection: 512 candidate rows, doubled
+// while a unit would need more than 32 chunks or the grid would exceed eight
+// CTAs per SM (ragged batches sized by their longest sequence).
+void select_decode_shape(int64_t max_blocks, int64_t units, int num_sms, int* chunk, int* n_chunks) {
+  int c = 512;
+  while (c < 4096 && ((max_blocks + c - 1) / c > 32 || units * ((max_blocks + c - 1) / c) > 8LL * num_sms)) c <<= 1;
+  *chunk = c;
+  *n_chunks = static_cast<int>((max_blocks + c - 1) / c);
+  if (*n_chunks < 1) *n_chunks = 1;
+}
+
+size_t select_decode_smem(int chunk) {
+  const int n = chunk > 2048 ? chunk : 2048;
+  return static_cast<size_t>(kSelStages) * kSelStageBytes + static_cast<size_t>(n) * sizeof(uint64_t) +
+         static_cast<size_t>(chunk) * sizeof(int32_t);
+}
+
+size_t select_decode_cand_bytes(int64_t units, int n_chunks) {
+  return static_cast<size_t>(units) * n_chunks * 64 * sizeof(uint64_t);
+}
+
+// ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
 template <typename T>
 cudaError_t launch_select(const T* q, int hq, int n_q_tokens, const T* pooled, const KvView& kv, int batch,
                           const msa_select_cfg& cfg, int32_t* idx_out, int k_total, float* scores, float* qidx_ws,
-                          int32_t* status, cudaStream_t stream) {
+                          const FusedSelect* fused, int32_t* status, cudaStream_t stream) {
   const int prefill = cfg.q_tile == kBlock;
   const int64_t max_blocks = kv.max_blocks();
   ScoreArgs sa{hq, kv.hkv, prefill, cfg.force_local, cfg.q_start, 0, max_blocks};
   const unsigned chunks = static_cast<unsigned>((max_blocks + kScoreChunk - 1) / kScoreChunk);
   int outer;
+  if (!prefill && cfg.k_scored <= 64 && fused != nullptr) {
+    SelDecArgs da;
+    da.hq = hq;
+    da.hkv = kv.hkv;
+    da.force_local = cfg.force_local;
+    da.k_scored = cfg.k_scored;
+    da.k_total = k_total;
+    select_decode_shape(max_blocks, static_cast<int64_t>(batch) * kv.hkv, fused->num_sms, &da.chunk, &da.n_chunks);
+    da.max_blocks = max_blocks;
+    da.scores_out = fused->scores_out;
+    da.cand = fused->cand;
+    da.tickets = fused->tickets;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(da.n_chunks, kv.hkv, batch);
+    lc.blockDim = dim3(kSelThreads, 1, 1);
+    lc.dynamicSmemBytes = select_decode_smem(da.chunk);
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, select_decode_kernel<T>, q, pooled, kv, da, idx_out, status);
+  }
   if (!prefill) {
     outer = batch;
     score_kernel<T, 1><<<dim3(chunks, kv.hkv, batch), kScoreThreads, 0, stream>>>(q, nullptr, pooled, kv, sa,
@@ -379,9 +663,23 @@ cudaError_t launch_select(const T* q, int hq, int n_q_tokens, const T* pooled, c
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   TopkArgs ta{kv.hkv, prefill, cfg.force_local, cfg.k_scored, k_total, cfg.q_start, max_blocks};
-  const size_t smem = static_cast<size_t>(max_blocks) * sizeof(uint32_t);
+  const size_t smem = static_cast<size_t>(max_blocks + kCandCap) * sizeof(uint32_t);
   topk_kernel<<<dim3(kv.hkv, outer), kTopkThreads, smem, stream>>>(scores, kv, ta, idx_out, status);
   return cudaGetLastError();
+}
+
+cudaError_t set_select_decode_smem(size_t bytes) {
+  // the decode step's kernels all ask for the largest shared-memory carve-out,
+  // so consecutive launches need no L1/shared reconfiguration
+  const void* fns[2] = {reinterpret_cast<const void*>(select_decode_kernel<__nv_bfloat16>),
+                        reinterpret_cast<const void*>(select_decode_kernel<float>)};
+  for (const void* f : fns) {
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t set_topk_smem(size_t bytes) {
@@ -390,9 +688,9 @@ cudaError_t set_topk_smem(size_t bytes) {
 
 template cudaError_t launch_select<__nv_bfloat16>(const __nv_bfloat16*, int, int, const __nv_bfloat16*,
                                                   const KvView&, int, const msa_select_cfg&, int32_t*, int, float*,
-                                                  float*, int32_t*, cudaStream_t);
+                                                  float*, const FusedSelect*, int32_t*, cudaStream_t);
 template cudaError_t launch_select<float>(const float*, int, int, const float*, const KvView&, int,
-                                          const msa_select_cfg&, int32_t*, int, float*, float*, int32_t*,
-                                          cudaStream_t);
+                                          const msa_select_cfg&, int32_t*, int, float*, float*, const FusedSelect*,
+                                          int32_t*, cudaStream_t);
 
 }  // namespace msa

@@ -1,0 +1,383 @@
+// Top-k (k <= 64) of up to 2048 candidates inside one CTA, by sorting
+// networks: each warp bitonic-sorts 64 keys in registers (two per lane), then
+// sorted lists of 64 are merged pairwise (the top 64 of two sorted lists is
+// the bitonic sequence max(A[i], B[63-i]) followed by a bitonic merge).
+//
+// Keys are 64-bit: order-preserving score bits in the high word and the
+// complement of the block index in the low word, so a larger key means a
+// higher score and, between equal scores, the lower block. Key 0 marks an
+// empty slot and sorts last.
+#pragma once
+
+#include "common.cuh"
+
+namespace msa {
+
+__device__ inline uint64_t sel_key(float score, int block) {
+  return (static_cast<uint64_t>(float_to_key(score)) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(block));
+}
+__device__ inline int sel_block(uint64_t key) { return static_cast<int>(~static_cast<uint32_t>(key)); }
+
+__device__ inline uint64_t shfl_xor_u64(uint64_t v, int m) {
+  const uint32_t lo = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(v), m);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(v >> 32), m);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// Sort the warp's 64 keys (x[r] is element 2*lane + r) in descending order.
+__device__ inline void warp_sort64_desc(uint64_t (&x)[2]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 64; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j == 1) {
+        const int e = 2 * lane;
+        const bool desc = (e & k) == 0;
+        const bool swap = desc ? (x[0] < x[1]) : (x[0] > x[1]);
+        if (swap) {
+          const uint64_t t = x[0];
+          x[0] = x[1];
+          x[1] = t;
+        }
+      } else {
+        const int lj = j >> 1;
+        const bool lower = (lane & lj) == 0;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int e = 2 * lane + r;
+          const bool desc = (e & k) == 0;
+          const uint64_t o = shfl_xor_u64(x[r], lj);
+          const bool keep_max = (lower == desc);
+          x[r] = keep_max ? (x[r] > o ? x[r] : o) : (x[r] < o ? x[r] : o);
+        }
+      }
+    }
+  }
+}
+
+// One warp: out = top 64 of the sorted (descending) lists a and b, sorted.
+__device__ inline void warp_merge64(const uint64_t* a, const uint64_t* b, uint64_t* out) {
+  const int lane = threadIdx.x & 31;
+  uint64_t x[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int e = 2 * lane + r;
+    const uint64_t u = a[e], v = b[63 - e];
+    x[r] = u > v ? u : v;
+  }
+  // bitonic merge, descending
+#pragma unroll
+  for (int j = 32; j > 0; j >>= 1) {
+    if (j == 1) {
+      if (x[0] < x[1]) {
+        const uint64_t t = x[0];
+        x[0] = x[1];
+        x[1] = t;
+      }
+    } else {
+      const int lj = j >> 1;
+      const bool lower = (lane & lj) == 0;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint64_t o = shfl_xor_u64(x[r], lj);
+        x[r] = lower ? (x[r] > o ? x[r] : o) : (x[r] < o ? x[r] : o);
+      }
+    }
+  }
+  out[2 * lane] = x[0];
+  out[2 * lane + 1] = x[1];
+}
+
+// Merge `n_lists` sorted lists of 64 keys in buf (a power of two, <= 64) down
+// to one; the result is returned (a pointer into buf or tmp). Every thread of
+// the CTA calls this; warps take the pairs round-robin.
+__device__ inline uint64_t* block_merge_lists(uint64_t* buf, uint64_t* tmp, int n_lists) {
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  uint64_t* src = buf;
+  uint64_t* dst = tmp;
+  while (n_lists > 1) {
+    const int pairs = n_lists >> 1;
+    for (int p = warp; p < pairs; p += nwarps) warp_merge64(src + (2 * p) * 64, src + (2 * p + 1) * 64, dst + p * 64);
+    __syncthreads();
+    uint64_t* t = src;
+    src = dst;
+    dst = t;
+    n_lists = pairs;
+  }
+  return src;
+}
+
+// Sort the warp's 128 keys (x[r] is element 4*lane + r) in descending order.
+__device__ inline void warp_sort128_desc(uint64_t (&x)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 128; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j < 4) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int p = r ^ j;
+          if (p > r) {
+            const int e = 4 * lane + r;
+            const bool desc = (e & k) == 0;
+            const bool swap = desc ? (x[r] < x[p]) : (x[r] > x[p]);
+            if (swap) {
+              const uint64_t t = x[r];
+              x[r] = x[p];
+              x[p] = t;
+            }
+          }
+        }
+      } else {
+        const int lj = j >> 2;
+        const bool lower = (lane & lj) == 0;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int e = 4 * lane + r;
+          const bool desc = (e & k) == 0;
+          const uint64_t o = shfl_xor_u64(x[r], lj);
+          const bool keep_max = (lower == desc);
+          x[r] = keep_max ? (x[r] > o ? x[r] : o) : (x[r] < o ? x[r] : o);
+        }
+      }
+    }
+  }
+}
+
+// Top-k (k <= 64, 1 <= k <= n) of n <= 4096 keys in shared memory, written
+// sorted descending to top[0..64) (entries past k are not meaningful).
+// Exact: t = the k-th largest of 64 group maxima is <= the k-th largest key
+// (the k best groups each hold a key >= t), so every one of the top k keys is
+// >= t. The keys >= t (normally a little over k) are sorted by one warp; if
+// more than 128 pass, the keys are sorted in full with the list merge tree.
+// `work` holds >= 2 * max(n_pad, 128) + 64 keys; every thread calls this.
+__device__ inline void block_topk(const uint64_t* keys, int n, int k, uint64_t* work, uint64_t* top, int* count) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = (n + 63) / 64;  // group size
+  uint64_t* gmax = work;        // [64]
+  uint64_t* cand = work + 64;   // [128]
+  if (tid == 0) *count = 0;
+  for (int grp = warp; grp < 64; grp += blockDim.x >> 5) {
+    uint64_t m = 0ull;
+    for (int i = grp * g + lane; i < min(n, (grp + 1) * g); i += 32) m = keys[i] > m ? keys[i] : m;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const uint64_t o = shfl_xor_u64(m, off);
+      m = o > m ? o : m;
+    }
+    if (lane == 0) gmax[grp] = m;
+  }
+  __syncthreads();
+  __shared__ uint64_t thr;
+  if (warp == 0) {
+    uint64_t x[2] = {gmax[2 * lane], gmax[2 * lane + 1]};
+    warp_sort64_desc(x);
+    // element k-1 of the sorted maxima
+    const int e = k - 1;
+    const uint64_t mine = (e >> 1) == lane ? x[e & 1] : 0ull;
+    uint64_t t = mine;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const uint64_t o = shfl_xor_u64(t, off);
+      t = o > t ? o : t;
+    }
+    if (lane == 0) thr = t;
+  }
+  __syncthreads();
+  const uint64_t t = thr;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + tid;
+    const bool hit = i < n && keys[i] >= t && keys[i] != 0ull;
+    const unsigned m = __ballot_sync(0xffffffffu, hit);
+    int slot = 0;
+    if (lane == 0 && m != 0u) slot = atomicAdd(count, __popc(m));
+    slot = __shfl_sync(0xffffffffu, slot, 0);
+    const int pos = slot + __popc(m & ((1u << lane) - 1u));
+    if (hit && pos < 128) cand[pos] = keys[i];
+  }
+  __syncthreads();
+  const int c = *count;
+  if (c <= 128) {
+    if (warp == 0) {
+      uint64_t x[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int e = 4 * lane + r;
+        x[r] = e < c ? cand[e] : 0ull;
+      }
+      warp_sort128_desc(x);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int e = 4 * lane + r;
+        if (e < 64) top[e] = x[r];
+      }
+    }
+    __syncthreads();
+    return;
+  }
+  // many keys near the threshold: sort everything in lists of 64 and merge
+  int n_lists = 1;
+  while (n_lists * 64 < n) n_lists <<= 1;
+  uint64_t* a = work;
+  uint64_t* b = work + n_lists * 64;
+  for (int i = tid; i < n_lists * 64; i += blockDim.x) a[i] = i < n ? keys[i] : 0ull;
+  __syncthreads();
+  for (int l = warp; l < n_lists; l += blockDim.x >> 5) {
+    uint64_t x[2] = {a[l * 64 + 2 * lane], a[l * 64 + 2 * lane + 1]};
+    warp_sort64_desc(x);
+    a[l * 64 + 2 * lane] = x[0];
+    a[l * 64 + 2 * lane + 1] = x[1];
+  }
+  __syncthreads();
+  const uint64_t* best = block_merge_lists(a, b, n_lists);
+  for (int i = tid; i < 64; i += blockDim.x) top[i] = best[i];
+  __syncthreads();
+}
+
+__device__ inline float key_to_float(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+
+// Shared scratch of block_select.
+struct SelectScratch {
+  int hist[1024];
+  uint64_t cand[256];
+  float wmin[32], wmax[32];
+  int n_above, n_cand, bstar, above_bstar;
+  float lo, inv;
+};
+
+// The k largest (1 <= k <= 64) of n keys in shared memory (0 = empty slot),
+// written to out[0..k) in no particular order; returns false (out untouched)
+// when the keys crowd too tightly to resolve this way (the caller then falls
+// back to block_topk). Exact: scores are binned linearly between their min and
+// max into 1024 bins (the bin is non-decreasing in the key); the bin holding
+// the k-th largest key is found from the histogram, every key above it is
+// kept, and the keys inside it (at most 256) are ranked by pairwise counting.
+// Every thread of the CTA calls this.
+__device__ inline bool block_select(const uint64_t* keys, int n, int k, uint64_t* out, SelectScratch& sc) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nth = blockDim.x;
+  // 1. range of the scores
+  float mn = INFINITY, mx = -INFINITY;
+  for (int i = tid; i < n; i += nth) {
+    const uint64_t kk = keys[i];
+    if (kk == 0ull) continue;
+    const float f = key_to_float(static_cast<uint32_t>(kk >> 32));
+    mn = fminf(mn, f);
+    mx = fmaxf(mx, f);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  if (lane == 0) {
+    sc.wmin[warp] = mn;
+    sc.wmax[warp] = mx;
+  }
+  for (int i = tid; i < 1024; i += nth) sc.hist[i] = 0;
+  __syncthreads();
+  if (tid == 0) {
+    float a = INFINITY, b = -INFINITY;
+    for (int w = 0; w < (nth >> 5); ++w) {
+      a = fminf(a, sc.wmin[w]);
+      b = fmaxf(b, sc.wmax[w]);
+    }
+    sc.lo = a;
+    sc.inv = (b > a) ? 1024.f / (b - a) : 0.f;
+    sc.n_above = 0;
+    sc.n_cand = 0;
+    sc.bstar = -1;
+  }
+  __syncthreads();
+  const float lo = sc.lo, inv = sc.inv;
+  auto bin_of = [&](uint64_t kk) {
+    const float f = key_to_float(static_cast<uint32_t>(kk >> 32));
+    const int b = static_cast<int>((f - lo) * inv);
+    return b < 0 ? 0 : (b > 1023 ? 1023 : b);
+  };
+  // 2. histogram
+  for (int i = tid; i < n; i += nth) {
+    const uint64_t kk = keys[i];
+    if (kk != 0ull) atomicAdd(&sc.hist[bin_of(kk)], 1);
+  }
+  __syncthreads();
+  // 3. the bin of the k-th largest: suffix counts over 4 bins per thread
+  {
+    int own = 0;
+    if (tid < 256)
+      for (int j = 0; j < 4; ++j) own += sc.hist[4 * tid + j];
+    // inclusive scan over threads (warp shuffles + one pass over warp totals)
+    int x = own;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    __shared__ int wsum[32];
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < (nth >> 5); ++w) {
+      if (w < warp) before += wsum[w];
+      total += wsum[w];
+    }
+    int above = total - (before + x);  // keys in bins above this thread's four
+    if (tid < 256 && above < k && above + own >= k) {
+      for (int j = 3; j >= 0; --j) {
+        const int b = 4 * tid + j;
+        if (above + sc.hist[b] >= k) {
+          sc.bstar = b;
+          sc.above_bstar = above;
+          break;
+        }
+        above += sc.hist[b];
+      }
+    }
+    __syncthreads();
+  }
+  const int bstar = sc.bstar;
+  if (bstar < 0 || sc.hist[bstar] > 256) return false;  // uniform decision: shared values
+  const int need = k - sc.above_bstar;
+  // 4. keep the keys above the bin; gather the bin's keys
+  for (int i = tid; i < n; i += nth) {
+    const uint64_t kk = keys[i];
+    if (kk == 0ull) continue;
+    const int b = bin_of(kk);
+    if (b > bstar) out[atomicAdd(&sc.n_above, 1)] = kk;
+    else if (b == bstar) sc.cand[atomicAdd(&sc.n_cand, 1)] = kk;
+  }
+  __syncthreads();
+  // 5. rank inside the bin (keys are distinct: they carry the block index)
+  const int nc = sc.n_cand, base = sc.n_above;
+  for (int i = tid; i < nc; i += nth) {
+    const uint64_t me = sc.cand[i];
+    int rank = 0;
+    for (int j = 0; j < nc; ++j) rank += sc.cand[j] > me;
+    if (rank < need) out[base + rank] = me;
+  }
+  __syncthreads();
+  return true;
+}
+
+// One warp: sort up to 64 block ids ascending (entries >= n are padding).
+__device__ inline void warp_sort64_blocks_asc(const uint64_t* top, int n, int* out) {
+  const int lane = threadIdx.x & 31;
+  // ascending blocks == descending complements
+  uint64_t x[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int e = 2 * lane + r;
+    x[r] = e < n ? static_cast<uint64_t>(static_cast<uint32_t>(top[e])) : 0ull;
+  }
+  warp_sort64_desc(x);
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int e = 2 * lane + r;
+    if (e < n) out[e] = sel_block(x[r]);
+  }
+}
+
+}  // namespace msa

@@ -24,12 +24,13 @@ MSA_DTYPE_F32, MSA_DTYPE_BF16 = 0, 1
 MSA_KV_CONTIGUOUS, MSA_KV_PAGED = 0, 1
 MSA_SCORE_MEAN_POOLED_KEYS = 0
 (MSA_OP_POOL, MSA_OP_SELECT, MSA_OP_DECODE, MSA_OP_PREFILL, MSA_OP_DENSE_DECODE, MSA_OP_DENSE_PREFILL,
- MSA_OP_SELECT_PREFILL) = range(7)
+ MSA_OP_SELECT_PREFILL, MSA_OP_DECODE_STEP) = range(8)
 
 # every symbol include/msa.h declares
 EXPORTS = ["msa_workspace_size", "msa_workspace_init", "msa_pool_block_keys", "msa_select_topk_blocks",
            "msa_sparse_attn_decode", "msa_sparse_attn_prefill", "msa_dense_gqa_decode", "msa_dense_gqa_prefill",
-           "msa_read_device_status", "msa_status_string", "msa_version", "msa_sparse_attn_decode_noalloc"]
+           "msa_read_device_status", "msa_status_string", "msa_version", "msa_sparse_attn_decode_noalloc",
+           "msa_sparse_decode_step"]
 
 
 class MsaError(RuntimeError):
@@ -69,6 +70,8 @@ _SIGS = {
     "msa_dense_gqa_prefill": (_I32, [_P, _I32, _I32, _I64, _DESC, ctypes.c_float, _P, _P, _P, _SZ, _P]),
     "msa_read_device_status": (_I32, [_P, _P, ctypes.POINTER(_I32)]),
     "msa_sparse_attn_decode_noalloc": (_I32, [_P, _I32, _DESC, _P, _I32, ctypes.c_float, _P, _P, _P]),
+    "msa_sparse_decode_step": (_I32, [_P, _I32, _P, _DESC, ctypes.POINTER(SelectCfg), _P, _I32, ctypes.c_float, _P,
+                                      _P, _P, _SZ, _P]),
     "msa_status_string": (ctypes.c_char_p, [_I32]),
     "msa_version": (_I32, []),
 }
@@ -191,6 +194,13 @@ def msa_sparse_attn_prefill(q, num_q_heads: int, n_q_tokens: int, q_start: int, 
     _check(load().msa_sparse_attn_prefill(_ptr(q), num_q_heads, n_q_tokens, q_start, ctypes.byref(desc), _ptr(idx),
                                           k_total, scale, _ptr(out), _ptr(lse), _ptr(ws), ws_bytes,
                                           _stream(stream)), "msa_sparse_attn_prefill")
+
+
+def msa_sparse_decode_step(q, num_q_heads: int, pooled, desc: KvDesc, cfg: SelectCfg, idx_out, k_total: int,
+                           scale: float, out, lse, ws, ws_bytes: int, stream=None) -> None:
+    _check(load().msa_sparse_decode_step(_ptr(q), num_q_heads, _ptr(pooled), ctypes.byref(desc), ctypes.byref(cfg),
+                                         _ptr(idx_out), k_total, scale, _ptr(out), _ptr(lse), _ptr(ws), ws_bytes,
+                                         _stream(stream)), "msa_sparse_decode_step")
 
 
 def msa_dense_gqa_decode(q, num_q_heads: int, desc: KvDesc, scale: float, out, lse, ws, ws_bytes: int,

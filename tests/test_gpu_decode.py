@@ -251,3 +251,61 @@ def test_full_ragged_paged_decode(dev):
         lens = np.array(inp.lens)
         return [(int(lens.argmin()), 1), (int(lens.argmax()), 4), (5, 7)]
     _sampled_full("ragged_paged_decode", units)
+
+
+# --------------------------------------------------------------------------- the fused decode step
+
+def run_step(inp, k_scored, k_total, force_local=True):
+    """Pool, then msa_sparse_decode_step (selection + attention in one call)."""
+    from sparse_attention_step_gb300 import msa
+    dev = inp.q.device
+    desc = msa.kv_desc(inp.k, inp.v, inp.seq_lens, inp.page_table)
+    hq = inp.num_q_heads
+    need = max(msa.msa_workspace_size(op, desc, hq, 1, k_total) for op in (msa.MSA_OP_POOL, msa.MSA_OP_DECODE_STEP))
+    ws = msa.Workspace(need, dev)
+    pooled = torch.full(msa.pooled_shape(desc), float("nan"), dtype=inp.k.dtype, device=dev)
+    b, hkv = inp.batch, inp.num_kv_heads
+    idx = torch.full((b, hkv, k_total), -7, dtype=torch.int32, device=dev)
+    out = torch.full_like(inp.q, float("nan"))
+    lse = torch.full((b, hq), float("nan"), dtype=torch.float32, device=dev)
+    msa.msa_pool_block_keys(desc, 0, -1, pooled, ws.buf, ws.nbytes)
+    for _ in range(2):  # twice: nothing may depend on state left by a previous call
+        msa.msa_sparse_decode_step(inp.q, hq, pooled, desc, msa.select_cfg(k_scored, force_local), idx, k_total,
+                                   SCALE, out, lse, ws.buf, ws.nbytes)
+    torch.cuda.synchronize()
+    return dict(pooled=pooled, idx=idx, out=out, lse=lse, scores=None, status=msa.msa_read_device_status(ws.buf))
+
+
+@pytest.mark.parametrize("lens,hkv,hq,k_scored,k_total", [
+    ([64 * 300 + 5, 64 * 77, 64 * 1024], 2, 16, 47, 48),   # few units: clusters of 16
+    ([64 * 200 + 33] * 20, 4, 32, 31, 32),                  # 80 units: clusters of 2
+    ([64 * 40] * 40, 4, 16, 8, 9),                          # 160 units: one CTA per unit
+    ([64 * 2048, 64 * 511 + 63], 1, 8, 63, 64),             # long sequence, k = 63
+    ([64 * 12, 10, 64], 2, 4, 5, 6),                        # tiny and partial sequences, G = 2
+])
+def test_fused_step_small(dev, lens, hkv, hq, k_scored, k_total):
+    inp = make_decode_inputs(lens, hkv, hq, "bf16", "contiguous", needles=3, seed=sum(lens) % 997, device=dev)
+    res = run_step(inp, k_scored, k_total)
+    assert res["status"] == 0
+    verify_units(inp, res, all_units(inp), k_scored, k_total)
+
+
+def test_fused_step_without_forced_block(dev):
+    inp = make_decode_inputs([64 * 100, 64 * 30 + 9], 2, 16, "bf16", "contiguous", needles=2, seed=77, device=dev)
+    res = run_step(inp, 6, 6, force_local=False)
+    assert res["status"] == 0
+    verify_units(inp, res, all_units(inp), 6, 6, force_local=False)
+
+
+@pytest.mark.parametrize("name,units", [("decode_128k", [(0, 0), (4, 3), (7, 7)]), ("decode_1m", [(0, 1), (0, 7)])])
+def test_fused_step_full(dev, name, units):
+    w = WORKLOADS[name]
+    inp = make_workload(name, device=dev)
+    res = run_step(inp, w["k_scored"], w["k_total"])
+    assert res["status"] == 0
+    verify_units(inp, res, units, w["k_scored"], w["k_total"])
+    idx = res["idx"].cpu().numpy()
+    for (s, h), blocks in inp.needles.items():
+        assert set(blocks) <= set(idx[s, h].tolist()), f"needles missing in unit {(s, h)}"
+    del inp, res
+    torch.cuda.empty_cache()
