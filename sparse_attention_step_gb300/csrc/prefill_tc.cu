@@ -12,9 +12,12 @@
 //                      max grows by more than 2^8), exp2, P (bf16) written to
 //                      shared memory in the 128-byte-swizzled K-major layout
 //   O_t += P_t V       tcgen05.mma M128 N128 K16 x 4, V read MN-major
-// Warp roles: warps 0-3 softmax of tile 0, warps 4-7 softmax of tile 1 (warp
-// w reaches TMEM lanes 32 (w mod 4) ..), warp 8 TMA producer (Q once, then a
-// 3-stage K/V ring), warp 9 TMEM allocator and MMA issuer. The two tiles
+// Warp roles: warps 0-7 softmax of tile 0 and warps 8-15 of tile 1; within a
+// tile, warps 0-3 take score columns 0-31 and warps 4-7 columns 32-63 of the
+// rows in TMEM lanes 32 (w mod 4) .. (a warp reaches only those lanes); the
+// two halves of a row exchange their maxima and sums through shared memory
+// (a named barrier per tile). Warp 16 is the TMA producer (Q once, then a
+// 3-stage K/V ring), warp 17 the TMEM allocator and MMA issuer. The two tiles
 // ping-pong: the tensor core runs one tile's MMAs while the other tile's
 // softmax runs. TMEM: S_0 [0,64), S_1 [64,128), O_0 [128,256), O_1 [256,384).
 #include <float.h>
@@ -28,9 +31,10 @@ namespace {
 
 constexpr int kTcTiles = 2;
 constexpr int kTcStages = 3;
-constexpr int kTcThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kSoftmaxWarps = 16;
+constexpr int kTcThreads = 32 * (kSoftmaxWarps + 2);
+constexpr int kProducerWarp = kSoftmaxWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + 1;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kQBytes = kTcTiles * 2 * 16384;   // two tiles x two 64-dim halves
 constexpr int kKVBytes = kTcStages * 32768;
@@ -53,6 +57,15 @@ struct TcTail {
 };
 
 constexpr size_t kTcSmem = 1024 + kQBytes + kKVBytes + kPBytes + sizeof(TcTail);
+
+__device__ inline float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ inline void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 __device__ inline bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int32_t* abort, int32_t* status) {
   if (*abort) return false;
@@ -106,7 +119,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     }
     for (int t = 0; t < kTcTiles; ++t) {
       mbar_init(&st.s_full[t], 1);
-      mbar_init(&st.p_full[t], 4);
+      mbar_init(&st.p_full[t], kSoftmaxWarps / 2);
       mbar_init(&st.o_final[t], 1);
     }
     mbar_init(&st.drain, 1);
@@ -210,42 +223,56 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int t = warp >> 2;               // tile
-    const int r = 32 * (warp & 3) + lane;  // row within the tile = TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    __shared__ float xmax[2][kTcTiles][2][128];  // [block parity][tile][half][row]
+    __shared__ float xsum[kTcTiles][2][128];
+    const int t = warp >> 3;                // tile
+    const int hf = (warp >> 2) & 1;         // score columns [32 hf, 32 hf + 32)
+    const int q4 = warp & 3;                // TMEM lane quadrant
+    const int r = 32 * q4 + lane;           // row within the tile = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+    const int bar_id = 1 + t;               // the tile's 8 softmax warps
     const int tt = rh * (kTcTiles * 16) + 16 * t + (r >> 3);  // token within the 64-token tile
     const int head = h * 8 + (r & 7);
     const int64_t tq = static_cast<int64_t>(tile) * kBlock + tt;  // token within the chunk
     const bool live = tq < a.n_q_tokens;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;  // running max (log2 units) and this half's running sum
     uint8_t* prow = ps + t * 16384 + r * 128;
     bool ok = true;
+    // Every warp of the tile runs every iteration and every named barrier, even
+    // after a wait gave up (then it skips the work), so no partner warp can be
+    // left waiting at a barrier.
     for (int i = 0; i < nblk; ++i) {
-      if (!(ok = wait_or_abort(&st.s_full[t], i & 1, abort, a.status))) break;
+      ok = __all_sync(0xffffffffu, ok && wait_or_abort(&st.s_full[t], i & 1, abort, a.status));
       tc::fence_after();
-      uint32_t sr[64];
-      tc::ld32(tmem + lane_base + t * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tc::ld32(tmem + lane_base + t * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tc::wait_ld();
+      uint32_t sr[32];
+      if (ok) {
+        tc::ld32(tmem + lane_base + t * 64 + 32 * hf, sr);
+        tc::wait_ld();
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sr[c] = __float_as_uint(-INFINITY);
+      }
       const int b = dense ? i : st.blocks[i];
       const bool diag_blk = b == diag;
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float z = __uint_as_float(sr[c]) * a.scale_log2;
-        if (diag_blk && c > tt) z = -INFINITY;
-        sr[c] = __float_as_uint(z);
-        mx = fmaxf(mx, z);
+      for (int c = 0; c < 32; ++c) {
+        if (diag_blk && 32 * hf + c > tt) sr[c] = __float_as_uint(-INFINITY);
+        mx = fmaxf(mx, __uint_as_float(sr[c]));
       }
-      const float m_new = fmaxf(m, mx);
+      xmax[i & 1][t][hf][r] = mx;
+      named_bar_sync(bar_id, 256);
+      mx = fmaxf(mx, xmax[i & 1][t][hf ^ 1][r]);
+      const float m_blk = mx * a.scale_log2;  // -inf stays -inf
+      const float m_new = fmaxf(m, m_blk);
       const bool need = (m == -INFINITY) ? (m_new != -INFINITY) : (m_new > m + kRescaleLog2);
       if (__any_sync(0xffffffffu, need)) {
-        const float alpha = (m == -INFINITY) ? 0.f : exp2f(m - m_new);
-        if (i > 0) {
+        const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
+        if (i > 0 && ok) {
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < 2; ++cc) {
             uint32_t o[32];
-            const uint32_t oa = tmem + lane_base + 128 + t * 128 + cc * 32;
+            const uint32_t oa = tmem + lane_base + 128 + t * 128 + 64 * hf + cc * 32;
             tc::ld32(oa, o);
             tc::wait_ld();
 #pragma unroll
@@ -257,14 +284,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         l *= alpha;
         m = m_new;
       }
-      const float ref = (m == -INFINITY) ? 0.f : m;
+      const float neg_ref = (m == -INFINITY) ? 0.f : -m;
       float sum = 0.f;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
+      for (int c8 = 0; c8 < 4; ++c8) {
         float p[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          p[e] = exp2f(__uint_as_float(sr[8 * c8 + e]) - ref);
+          p[e] = ex2_approx(fmaf(__uint_as_float(sr[8 * c8 + e]), a.scale_log2, neg_ref));
           sum += p[e];
         }
         uint4 v;
@@ -272,23 +299,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         v.y = pack_bf16(p[2], p[3]);
         v.z = pack_bf16(p[4], p[5]);
         v.w = pack_bf16(p[6], p[7]);
-        *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) = v;
+        *reinterpret_cast<uint4*>(prow + (((4 * hf + c8) ^ (r & 7)) << 4)) = v;
       }
       l += sum;
       fence_proxy_async();  // P is read by the tensor core (async proxy)
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&st.p_full[t]);
+      if (lane == 0 && ok) mbar_arrive(&st.p_full[t]);
     }
-    // epilogue: O / l in bf16 and lse
+    // epilogue: the row's two half sums, then O / l in bf16 and the lse
+    xsum[t][hf][r] = l;
+    named_bar_sync(bar_id, 256);
+    const float L = l + xsum[t][hf ^ 1][r];
     if (ok) ok = wait_or_abort(&st.o_final[t], 0, abort, a.status);
     tc::fence_after();
-    const float inv = (l > 0.f) ? 1.f / l : 0.f;
-    __nv_bfloat16* dst = a.out + (tq * a.hq + head) * kHeadDim;
+    const float inv = (L > 0.f) ? 1.f / L : 0.f;
+    __nv_bfloat16* dst = a.out + (tq * a.hq + head) * kHeadDim + 64 * hf;
 #pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {
+    for (int cc = 0; cc < 2; ++cc) {
       uint32_t o[32];
-      tc::ld32(tmem + lane_base + 128 + t * 128 + cc * 32, o);
+      tc::ld32(tmem + lane_base + 128 + t * 128 + 64 * hf + cc * 32, o);
       tc::wait_ld();
       if (live) {
         if (nblk == 0 || !ok) {
@@ -306,7 +336,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         }
       }
     }
-    if (live && a.lse != nullptr) a.lse[tq * a.hq + head] = (l > 0.f) ? (m * kLn2 + logf(l)) : -INFINITY;
+    if (live && hf == 0 && a.lse != nullptr)
+      a.lse[tq * a.hq + head] = (L > 0.f) ? (m * kLn2 + logf(L)) : -INFINITY;
   }
   tc::fence_before();
   __syncthreads();
