@@ -8,10 +8,12 @@ sequence. The summary keys are pooled once beforehand (they change only when a
 block fills) and that pass is reported separately.
 
 Timing: W untimed warm-up steps, then K timed steps. The L2 (129 MB) is
-flushed by writing a 512 MB buffer before every timed step, outside the timed
-window; each step is bracketed by CUDA events on the launching stream (one
-event between Step 1 and Step 2 gives the per-kernel time of the attention
-kernel). Clocks are sampled with nvidia-smi during the timed region.
+flushed before every timed step, outside the timed window: a 512 MB buffer is
+written, then a separate 256 MB buffer is read, so the step starts with none of
+its inputs cached and with clean lines in L2 (a cache left full of dirty lines
+would bill the step for writing back the flush buffer). Each step is bracketed
+by CUDA events on the launching stream. Clocks are sampled with nvidia-smi
+during the timed region.
 
 Prints ONE JSON line on rank 0. Under torchrun (N > 1) every rank runs an
 independent replica on its own GPU (the path shards by sequence and head with
@@ -41,6 +43,7 @@ METRIC = "sparse-attn decode µs/step + HBM GB/s at 128K/1M ctx; prefill TFLOP/s
 UNIT = "µs/step"
 SCALE = 1.0 / math.sqrt(128)
 L2_FLUSH_BYTES = 512 << 20
+L2_CLEAN_BYTES = 256 << 20
 KV_BLOCK_BYTES = 64 * 128 * 2  # one 64-token K (or V) block in bf16
 
 
@@ -184,9 +187,11 @@ class Timer:
     def __init__(self, torch):
         self.torch = torch
         self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.clean = torch.ones(L2_CLEAN_BYTES // 4, dtype=torch.float32, device="cuda")
 
     def l2_flush(self):
         self.flush.zero_()
+        self.clean.sum()
 
 
 # --------------------------------------------------------------------------- our arm
@@ -466,7 +471,7 @@ def run_ours(args):
             "workload": f"decode_128k: {args.batch} sequences x 131072 tokens, 8 KV heads, 64 query heads, head dim 128, "
                         "64-token blocks, top-31 scored blocks + newest block, 16 needle blocks per (seq, head)",
             "global_batch": args.batch * world, "seq_len": 131072, "parallelism": f"replicas x{world}",
-            "l2": "flushed (512 MB write) before every timed step",
+            "l2": "flushed before every timed step (512 MB written, then 256 MB read)",
             "step": "msa_sparse_decode_step (block scores, top-k and sparse attention in one kernel), replayed as a "
                     "CUDA graph; summary keys pooled beforehand",
         },

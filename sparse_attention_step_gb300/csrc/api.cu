@@ -18,6 +18,7 @@ struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
   size_t topk_smem = 0;
+  int step_clusters[5] = {0, 0, 0, 0, 0};  // co-resident fused-step clusters of 1, 2, 4, 8, 16 CTAs
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -34,6 +35,7 @@ msa_status device_info(DeviceInfo** out) {
     if (set_prefill_smem() != cudaSuccess) return MSA_ERR_CUDA;
     if (set_prefill_tc_smem() != cudaSuccess) return MSA_ERR_CUDA;
     if (set_step_smem() != cudaSuccess) return MSA_ERR_CUDA;
+    for (int i = 0; i < 5; ++i) d.step_clusters[i] = step_max_clusters(1 << i);
     d.topk_smem = (kMaxTopkCandidates + kTopkCandCap) * sizeof(uint32_t);
     if (set_topk_smem(d.topk_smem) != cudaSuccess) return MSA_ERR_CUDA;
     if (set_select_decode_smem(select_decode_smem(4096)) != cudaSuccess) return MSA_ERR_CUDA;
@@ -434,7 +436,8 @@ msa_status msa_sparse_decode_step(const void* q, int32_t num_q_heads, const void
   const bool fused = kv->dtype == MSA_DTYPE_BF16 && kv->layout == MSA_KV_CONTIGUOUS &&
                      cfg->mode == MSA_SCORE_MEAN_POOLED_KEYS && cfg->k_scored >= 0 &&
                      k_total >= std::min<int64_t>(cfg->k_scored, kv_max_blocks(kv)) + (cfg->force_local ? 1 : 0) &&
-                     step_shape(units, kv_max_blocks(kv), cfg->k_scored, k_total, dev->num_sms, &C, &chunk, &bps);
+                     step_shape(units, kv_max_blocks(kv), cfg->k_scored, k_total, dev->num_sms, dev->step_clusters, &C,
+                                &chunk, &bps);
   if (!fused) {
     // the same step as two launches
     st = msa_select_topk_blocks(q, num_q_heads, 1, pooled, kv, cfg, idx_out, k_total, nullptr, ws, ws_bytes, stream);

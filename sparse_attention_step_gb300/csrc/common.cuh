@@ -97,6 +97,14 @@ __device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status
   }
 }
 
+// The whole warp waits, and leaves converged with the same result in every
+// lane. Lanes leave a spin on their own, so without the vote a warp can carry
+// on split in two, and every warp-collective instruction after it (shuffles,
+// ldmatrix, mma.sync, tcgen05.ld) then runs once per part.
+__device__ inline bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int32_t* status, int where) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, where));
+}
+
 // ---------------------------------------------------------------------------
 // TMA: 2-D tiled bulk tensor copy global -> shared, completing on an mbarrier.
 // x is the innermost coordinate (elements), y the row.
@@ -115,6 +123,13 @@ __device__ inline void bulk_load(void* smem_dst, const void* gsrc, uint32_t byte
           smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+// Pull one 2-D tile into L2 (no shared memory, no completion to wait for).
+__device__ inline void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 __device__ inline void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -191,6 +206,13 @@ __device__ inline uint32_t cluster_ctarank() {
 __device__ inline void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Named barrier `id` (1..15) for the first nthreads / 32 warps of the CTA.
+__device__ inline void bar_sync_warps(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// The two halves of cluster_sync, for work that fits between them.
+__device__ inline void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ inline void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 // Address of the same shared-memory location in the cluster's CTA `rank`.
 __device__ inline uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
   uint32_t r;
@@ -211,6 +233,10 @@ __device__ inline int32_t ld_dsmem_i32(uint32_t addr) {
   int32_t v;
   asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
+}
+__device__ inline void st_dsmem4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
 }
 __device__ inline float4 ld_dsmem4(uint32_t addr) {
   float4 v;

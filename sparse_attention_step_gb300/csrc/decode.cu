@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_bf16_kernel(const __grid_c
     const int vchunk = (lane >> 3) & 1;
     for (int i = 0; i < nblk; ++i) {
       const int stg = i % kStages;
-      if (!mbar_wait(&st.full[stg], (i / kStages) & 1, a.status, kIdDecode)) break;
+      if (!mbar_wait_warp(&st.full[stg], (i / kStages) & 1, a.status, kIdDecode)) break;
       const uint32_t kbase = smem_u32(ring + stg * kStageBytes);
       const uint32_t vbase = kbase + 16384;
       float sacc[4] = {0.f, 0.f, 0.f, 0.f};

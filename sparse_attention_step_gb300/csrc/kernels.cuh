@@ -75,8 +75,9 @@ cudaError_t launch_prefill_bf16(const CUtensorMap& tmk, const CUtensorMap& tmv, 
                                 const PrefillArgs& a, cudaStream_t stream);
 
 // ---- fused decode step (step.cu) ----
-bool step_shape(int64_t units, int64_t max_blocks, int k_scored, int k_total, int num_sms, int* C, int* chunk,
-                int* bps);
+bool step_shape(int64_t units, int64_t max_blocks, int k_scored, int k_total, int num_sms, const int* max_clusters,
+                int* C, int* chunk, int* bps);
+int step_max_clusters(int C);
 cudaError_t set_step_smem();
 cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, const KvView& kv, int batch,
                                const __nv_bfloat16* q, int hq, const __nv_bfloat16* pooled,

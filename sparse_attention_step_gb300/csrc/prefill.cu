@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_bf16_kernel(const __grid_c
 
   for (int i = 0; i < nblk; ++i) {
     const int stg = i % kPfStages;
-    if (!mbar_wait(&st.full[stg], (i / kPfStages) & 1, a.status, kIdPrefill)) break;
+    if (!mbar_wait_warp(&st.full[stg], (i / kPfStages) & 1, a.status, kIdPrefill)) break;
     const int b = dense ? i : st.blocks[i];
     const uint32_t kbase = smem_u32(ring + stg * kPfStageBytes);
     const uint32_t vbase = kbase + 16384;

@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     xsum[t][hf][r] = l;
     named_bar_sync(bar_id, 256);
     const float L = l + xsum[t][hf ^ 1][r];
-    if (ok) ok = wait_or_abort(&st.o_final[t], 0, abort, a.status);
+    ok = __all_sync(0xffffffffu, ok && wait_or_abort(&st.o_final[t], 0, abort, a.status));
     tc::fence_after();
     const float inv = (L > 0.f) ? 1.f / L : 0.f;
     __nv_bfloat16* dst = a.out + (tq * a.hq + head) * kHeadDim + 64 * hf;

@@ -516,7 +516,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
       // ---------------- scorers ----------------
       for (int st = 0; st < n_stages; ++st) {
         const int slot = st % kSelStages;
-        if (!mbar_wait(&full[slot], (st / kSelStages) & 1, status, kIdScore)) break;
+        if (!mbar_wait_warp(&full[slot], (st / kSelStages) & 1, status, kIdScore)) break;
         const uint8_t* stage = ring + slot * kSelStageBytes;
         const int base = st * kStageRows;
         const int n = min(kStageRows, rows - base);

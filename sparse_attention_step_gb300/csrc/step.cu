@@ -6,11 +6,12 @@
 // CTA ever synchronises through global memory:
 //   1. CTA r scores candidate blocks [r*chunk, (r+1)*chunk): a producer warp
 //      streams the summary rows (bulk copies, 128 rows per 32 KB stage, a
-//      3-stage ring) and eight warps dot them with the group's index query;
-//      the CTA keeps its best 64 (block_select).
-//   2. The leader (rank 0) gathers the C lists through distributed shared
-//      memory, selects the unit's top-k, writes the index list, and leaves it
-//      in its shared memory where every CTA reads its slice.
+//      3-stage ring) and eight warps dot them with the group's index query.
+//   2. The CTA keeps its best 64 keys (register bitonic sorts and merges);
+//      after one cluster barrier every CTA gathers the C lists through
+//      distributed shared memory and merges them identically, so each holds
+//      the unit's top-k and takes its slice of the index list (the leader
+//      writes the list out).
 //   3. CTA r attends over its slice: the producer streams each 64x128 K and V
 //      block with 2-D TMA copies (128-byte swizzle) into the 3-stage ring;
 //      warps 0-3 consume every block in order (each warp 16 tokens: S = K Q^T
@@ -18,7 +19,9 @@
 //      order keeps each warp at most one ring cycle ahead of a slot, so a
 //      parity wait can never match a stale phase.
 //   4. The C partial results (m, l, O) are combined through distributed
-//      shared memory: CTA r writes output pieces r, r + C, ...
+//      shared memory: every CTA pushes piece p (one head, 8 dims) of its
+//      partial into the shared memory of CTA p % C, and after one cluster
+//      barrier CTA r merges and writes output pieces r, r + C, ...
 #include <float.h>
 
 #include "kernels.cuh"
@@ -30,6 +33,7 @@ namespace msa {
 namespace {
 
 constexpr int kStWarps = 8;                     // compute warps
+constexpr int kStAttnWarps = 4;                 // warps that consume attention blocks
 constexpr int kStThreads = 32 * (kStWarps + 1);  // + producer warp
 constexpr int kStStages = 3;
 constexpr int kStStage = 32768;
@@ -37,13 +41,10 @@ constexpr int kStRowsPerStage = kStStage / (kHeadDim * 2);  // 128 bf16 summary 
 constexpr int kStMaxChunk = 1024;                           // candidate rows per CTA
 constexpr int kStMaxList = 64;                              // selected blocks per CTA
 constexpr int kStMaxCluster = 16;
+constexpr int kStPrefetchExtra = 2;             // L2 prefetches per CTA beyond kk / C
 constexpr int kStG = 8;                                     // heads per group handled
 constexpr int kStOS = kHeadDim + 4;                         // padded merge rows
-// offsets inside the ring while it is not streaming
-constexpr int kOffScratch = 0;          // SelectScratch (the selection)
-constexpr int kOffFallback = 16384;     // block_topk work space (<= 16 KB)
-constexpr int kOffXList = 65536;        // this CTA's best keys, read by the leader
-constexpr int kOffFinal = 65536 + 512;  // the leader's final list, read by every CTA
+constexpr int kStRecv = 12;                                 // floats per pushed piece: O[8], M, L, pad
 constexpr size_t kStSmem = 1024 + kStStages * kStStage + kStMaxChunk * sizeof(uint64_t);
 
 }  // namespace
@@ -70,11 +71,11 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(st_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* keys = reinterpret_cast<uint64_t*>(ring + kStStages * kStStage);  // [kStMaxChunk]
   __shared__ uint64_t full[kStStages], empty[kStStages];
-  __shared__ uint64_t top[64];
+  __shared__ uint64_t xlist[64];  // this CTA's best keys, read by the whole cluster
   __shared__ int32_t blocks[kStMaxList];
   __shared__ int sorted_blocks[64];
-  __shared__ int n_blocks, count;
-  __shared__ float wm[kStWarps][kStG], wl[kStWarps][kStG];
+  __shared__ int n_blocks;
+  __shared__ float wm[kStAttnWarps][kStG], wl[kStAttnWarps][kStG];
 
   const int rank = blockIdx.x, C = gridDim.x, h = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -102,6 +103,11 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   const int64_t r0 = static_cast<int64_t>(rank) * a.chunk;
   const int rows = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(a.chunk), n_cand - r0)));
   const int n_st = (rows + kStRowsPerStage - 1) / kStRowsPerStage;
+  if (rank == 0 && warp == kStWarps && lane >= 28 && forced >= 0) {
+    // the newest block is always attended: pull it into L2 during scoring
+    const int64_t row = kv.block_row(s, h, forced, a.status, kIdDecode);
+    if (row >= 0) tma_prefetch_2d((lane & 2) ? &tmv : &tmk, (lane & 1) * 64, static_cast<int32_t>(row));
+  }
   __syncthreads();
 
   // ---------------------------------------------------------------- 1. scores
@@ -130,7 +136,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     }
     for (int st = 0; st < n_st; ++st) {
       const int slot = st % kStStages;
-      if (!mbar_wait(&full[slot], (st / kStStages) & 1, a.status, kIdDecode)) break;
+      if (!mbar_wait_warp(&full[slot], (st / kStStages) & 1, a.status, kIdDecode)) break;
       const uint8_t* stage = ring + slot * kStStage;
       const int n = min(kStRowsPerStage, rows - st * kStRowsPerStage);
 #pragma unroll
@@ -150,48 +156,108 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   __syncthreads();  // every stage consumed: the ring is free until the attention phase
 
   // ---------------------------------------------------------------- 2. selection
-  SelectScratch& scr = *reinterpret_cast<SelectScratch*>(ring + kOffScratch);
-  uint8_t* fallback = ring + kOffFallback;
-  uint64_t* xlist = reinterpret_cast<uint64_t*>(ring + kOffXList);
-  int32_t* final_list = reinterpret_cast<int32_t*>(ring + kOffFinal);
+  // (a) this CTA's best 64: each warp bitonic-sorts batches of 64 keys in
+  // registers and merges them into a running list; the eight warp lists are
+  // then merged pairwise. Key 0 pads and sorts last.
+  uint64_t* lists = reinterpret_cast<uint64_t*>(ring);  // [kStMaxCluster][64]
+  uint64_t* tmp = lists + kStMaxCluster * 64;           // [kStMaxCluster / 2][64]
+  if (warp < kStWarps) {
+    __syncwarp();
+    uint64_t run[2] = {0ull, 0ull};
+    for (int b = warp * 64; b < rows; b += kStWarps * 64) {
+      uint64_t x[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int e = b + 2 * lane + r;
+        x[r] = e < rows ? keys[e] : 0ull;
+      }
+      warp_sort64_desc(x);
+      if (b == warp * 64) {
+        run[0] = x[0];
+        run[1] = x[1];
+      } else {
+        warp_merge64_reg(run, x);
+      }
+    }
+    lists[warp * 64 + 2 * lane] = run[0];
+    lists[warp * 64 + 2 * lane + 1] = run[1];
+  }
+  __syncthreads();
+  const uint64_t* mine = block_merge_lists(lists, tmp, kStWarps);
+  if (tid < 64) xlist[tid] = mine[tid];
   const int kk = static_cast<int>(n_cand < a.k_scored ? n_cand : static_cast<int64_t>(a.k_scored));
-  const int kk_local = min(kk, rows);
-  if (kk_local > 0) {
-    if (!block_select(keys, rows, kk_local, top, scr))
-      block_topk(keys, rows, kk_local, reinterpret_cast<uint64_t*>(fallback), top, &count);
+  // (b) every CTA of the cluster gathers the C lists through distributed
+  // shared memory and merges them the same way, so each one holds the same
+  // top 64 of the unit without a second cluster barrier. xlist is never
+  // written again, and no CTA exits before the closing cluster barrier.
+  // Meanwhile the producer warp starts pulling the K/V blocks of this CTA's
+  // own best candidates into L2: about kk / C of them end up selected, so the
+  // attention phase finds most of its blocks there. Its lanes take their keys
+  // (candidates lane and lane + 32) before the merge below reuses `mine`.
+  const int n_pf = min(kk, (kk + C - 1) / C + kStPrefetchExtra);
+  uint64_t pf_key[2] = {0ull, 0ull};
+  if (warp == kStWarps) {
+    pf_key[0] = lane < n_pf ? mine[lane] : 0ull;
+    pf_key[1] = lane + 32 < n_pf ? mine[lane + 32] : 0ull;
   }
-  if (tid < 64) xlist[tid] = tid < kk_local ? top[tid] : 0ull;
-  cluster_sync();
+  if (C > 1) cluster_arrive();
+  if (warp == kStWarps) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (pf_key[j] != 0ull) {
+        const int64_t row = kv.block_row(s, h, sel_block(pf_key[j]), a.status, kIdDecode);
+        if (row >= 0) {
+          const int32_t y = static_cast<int32_t>(row);
+          tma_prefetch_2d(&tmk, 0, y);
+          tma_prefetch_2d(&tmk, 64, y);
+          tma_prefetch_2d(&tmv, 0, y);
+          tma_prefetch_2d(&tmv, 64, y);
+        }
+      }
+    }
+    __syncwarp();
+    if (C > 1) cluster_wait();
+  } else {
+    if (C > 1) cluster_wait();
+    else bar_sync_warps(1, 32 * kStWarps);
+    for (int i = tid; i < C * 64; i += 32 * kStWarps)
+      lists[i] = C > 1 ? ld_dsmem_u64(dsmem_addr(smem_u32(xlist + (i & 63)), static_cast<uint32_t>(i >> 6)))
+                       : xlist[i];
+    bar_sync_warps(1, 32 * kStWarps);
+    const uint64_t* best = warps_merge_lists(lists, tmp, C, kStWarps, 1);
+    if (tid < 64) {
+      // ascending block order by counting: the blocks are distinct, so each
+      // one's position is the number of selected blocks below it
+      const int b = tid < kk ? sel_block(best[tid]) : 0;
+      int pos = 0;
+#pragma unroll 4
+      for (int j = 0; j < kk; ++j) pos += sel_block(best[j]) < b ? 1 : 0;
+      if (tid < kk) sorted_blocks[pos] = b;
+    }
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kStStages; ++i) {
+      mbar_inval(&full[i]);
+      mbar_inval(&empty[i]);
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kStAttnWarps);  // one warp quartet consumes each block
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // (c) the unit's list: kk blocks ascending, then the forced block, then -1.
+  // The leader writes it out; every CTA takes its slice.
   if (rank == 0) {
-    const int n_all = C * 64;
-    for (int i = tid; i < n_all; i += blockDim.x)
-      keys[i] = ld_dsmem_u64(dsmem_addr(smem_u32(xlist + (i & 63)), static_cast<uint32_t>(i >> 6)));
-    __syncthreads();
-    if (kk > 0) {
-      if (!block_select(keys, n_all, kk, top, scr))
-        block_topk(keys, n_all, kk, reinterpret_cast<uint64_t*>(fallback), top, &count);
-    }
-    if (tid < 32) warp_sort64_blocks_asc(top, kk, sorted_blocks);
-    __syncthreads();
     int32_t* out = a.idx_out + unit * a.k_total;
-    for (int i = tid; i < a.k_total; i += blockDim.x) {
-      int v;
-      if (i < kk) v = sorted_blocks[i];
-      else if (i == kk && forced >= 0) v = static_cast<int>(forced);
-      else v = -1;
-      out[i] = v;
-      final_list[i] = v;
-    }
+    for (int i = tid; i < a.k_total; i += blockDim.x)
+      out[i] = i < kk ? sorted_blocks[i] : (i == kk && forced >= 0 ? static_cast<int>(forced) : -1);
   }
-  cluster_sync();
   if (warp == 0) {
-    // this CTA's slice of the leader's list
-    const uint32_t fl = dsmem_addr(smem_u32(final_list), 0u);
     const int lo = rank * a.bps, hi = min(a.k_total, lo + a.bps);
     int n = 0;
     for (int b0 = lo; b0 < hi; b0 += 32) {
       const int i = b0 + lane;
-      const int32_t b = i < hi ? ld_dsmem_i32(fl + 4u * i) : -1;
+      const int32_t b = i >= hi ? -1 : i < kk ? sorted_blocks[i] : (i == kk && forced >= 0 ? static_cast<int>(forced) : -1);
       if (b >= nb) set_status(a.status, MSA_ERR_DEVICE_BOUNDS, kIdDecode);
       const bool ok = b >= 0 && b < nb;
       const unsigned m = __ballot_sync(0xffffffffu, ok);
@@ -200,22 +266,12 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     }
     if (lane == 0) n_blocks = n;
   }
-  cluster_sync();  // the leader's list has been read: its ring may be reused
-  if (tid == 0) {
-    for (int i = 0; i < kStStages; ++i) {
-      mbar_inval(&full[i]);
-      mbar_inval(&empty[i]);
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 4);  // one warp quartet consumes each block
-    }
-    fence_mbar_init();
-  }
   __syncthreads();
   const int nblk = n_blocks;
 
   // ---------------------------------------------------------------- 3. attention
   const int g = lane >> 2, c = lane & 3;
-  const int wq = warp & 3;  // token quarter of each block
+  const int wq = warp & 3;  // token quarter of each block (attention warps 0-3)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   float o[8][4];
 #pragma unroll
@@ -235,7 +291,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
         tma_load_2d(dst + 24576, &tmv, 64, y, &full[slot]);
       }
     }
-  } else if (warp < 4) {
+  } else if (warp < kStAttnWarps) {
     uint32_t qb[8][2];
     {
       const bool live = g < a.grp;
@@ -252,7 +308,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     const int vchunk = (lane >> 3) & 1;
     for (int i = 0; i < nblk; ++i) {
       const int slot = i % kStStages;
-      if (!mbar_wait(&full[slot], (i / kStStages) & 1, a.status, kIdDecode)) break;
+      if (!mbar_wait_warp(&full[slot], (i / kStStages) & 1, a.status, kIdDecode)) break;
       const uint32_t kbase = smem_u32(ring + slot * kStStage);
       const uint32_t vbase = kbase + 16384;
       float sacc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -307,9 +363,9 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   }
   pdl_trigger();
   __syncthreads();  // the ring is free again: warp states go there
-  float* obuf = reinterpret_cast<float*>(ring);                        // [8 warps][8 heads][132]
-  float* xch = obuf + kStWarps * kStG * kStOS;                         // M[8], L[8], O[8][128]
-  if (warp < kStWarps) {
+  float* obuf = reinterpret_cast<float*>(ring);  // [4 warps][8 heads][132]
+  float* recv = reinterpret_cast<float*>(keys);  // [C][128 / C][kStRecv]: pieces pushed by the cluster
+  if (warp < kStAttnWarps) {
     float* ob = obuf + warp * kStG * kStOS;
     if (g == 0) {
       wm[warp][2 * c] = m0;
@@ -332,12 +388,12 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     const int head = tid >> 4, d0 = (tid & 15) * 8;
     if (tid < 128 && head < a.grp) {
       float M = -INFINITY;
-      for (int w = 0; w < kStWarps; ++w) M = fmaxf(M, wm[w][head]);
+      for (int w = 0; w < kStAttnWarps; ++w) M = fmaxf(M, wm[w][head]);
       float L = 0.f, acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.f;
       if (M != -INFINITY) {
-        for (int w = 0; w < kStWarps; ++w) {
+        for (int w = 0; w < kStAttnWarps; ++w) {
           const float f = exp2f(wm[w][head] - M);
           L += f * wl[w][head];
           const float* src = obuf + (w * kStG + head) * kStOS + d0;
@@ -356,22 +412,25 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
         *reinterpret_cast<uint4*>(a.out + qrow * kHeadDim + d0) = v;
         if (a.lse != nullptr && d0 == 0) a.lse[qrow] = L > 0.f ? M * kLn2 + logf(L) : -INFINITY;
       } else {
-        if (d0 == 0) {
-          xch[head] = M;
-          xch[kStG + head] = L;
-        }
-        float* dst = xch + 2 * kStG + head * kHeadDim + d0;
-        reinterpret_cast<float4*>(dst)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        reinterpret_cast<float4*>(dst)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        // push this CTA's part of piece `tid` (head, 8 dims) to the piece's
+        // owner, rank tid % C: slot [rank][tid / C] of the owner's receive
+        // area, which (like all of `keys`) is free once the owner has passed
+        // the selection barrier, as every CTA pushing here has
+        const uint32_t dst = dsmem_addr(smem_u32(recv + (rank * (128 / C) + tid / C) * kStRecv),
+                                        static_cast<uint32_t>(tid % C));
+        st_dsmem4(dst, make_float4(acc[0], acc[1], acc[2], acc[3]));
+        st_dsmem4(dst + 16u, make_float4(acc[4], acc[5], acc[6], acc[7]));
+        st_dsmem4(dst + 32u, make_float4(M, L, 0.f, 0.f));
       }
     }
   }
   if (C == 1) return;
+  // every piece has arrived; after this no CTA touches another's shared memory
   cluster_sync();
   if (tid < 128) {
     const int n = C;
     const int pieces = a.grp * 16;
-    const int j = tid / n, i = tid % n;
+    const int j = tid / n, i = tid % n;  // owned slot j, from rank i
     const int piece = j * n + rank;
     const bool live = piece < pieces;
     const int head = live ? piece >> 4 : 0;
@@ -379,11 +438,12 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     float Mi = -INFINITY, Li = 0.f;
     float4 oa = make_float4(0.f, 0.f, 0.f, 0.f), ob = oa;
     if (live) {
-      const uint32_t base = dsmem_addr(smem_u32(xch), static_cast<uint32_t>(i));
-      Mi = ld_dsmem(base + 4u * head);
-      Li = ld_dsmem(base + 4u * (kStG + head));
-      oa = ld_dsmem4(base + 4u * (2 * kStG + head * kHeadDim + d0));
-      ob = ld_dsmem4(base + 4u * (2 * kStG + head * kHeadDim + d0 + 4));
+      const float* src = recv + (i * (128 / n) + j) * kStRecv;
+      oa = *reinterpret_cast<const float4*>(src);
+      ob = *reinterpret_cast<const float4*>(src + 4);
+      const float4 ml = *reinterpret_cast<const float4*>(src + 8);
+      Mi = ml.x;
+      Li = ml.y;
     }
     float Mx = Mi;
     for (int off = n >> 1; off > 0; off >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
@@ -405,7 +465,6 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
       if (a.lse != nullptr && d0 == 0) a.lse[qrow] = v[0] > 0.f ? Mx * kLn2 + logf(v[0]) : -INFINITY;
     }
   }
-  cluster_sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -414,14 +473,19 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
 
 // Cluster shape of the fused step, or false when it does not apply (then the
 // step runs as the two separate kernels). C is a power of two <= 16 with
-// units x C within two resident CTAs per SM, chunk = ceil(max_blocks / C)
-// rounded up to 128 rows (<= 1024), and ceil(k_total / C) <= 64 list entries.
-bool step_shape(int64_t units, int64_t max_blocks, int k_scored, int k_total, int num_sms, int* C, int* chunk,
-                int* bps) {
+// units x C within two resident CTAs per SM and, where max_clusters is given
+// (the device's co-resident cluster count for C = 1, 2, 4, 8, 16), every
+// unit's cluster resident at once; chunk = ceil(max_blocks / C) rounded up to
+// 128 rows (<= 1024), and ceil(k_total / C) <= 64 list entries.
+bool step_shape(int64_t units, int64_t max_blocks, int k_scored, int k_total, int num_sms, const int* max_clusters,
+                int* C, int* chunk, int* bps) {
   if (k_scored > 64) return false;
   const int64_t slots = 2LL * num_sms;
-  int c = 1;
-  while (c < kStMaxCluster && units * c * 2 <= slots) c *= 2;
+  int c = 1, lg = 0;
+  while (c < kStMaxCluster && units * c * 2 <= slots && (max_clusters == nullptr || units <= max_clusters[lg + 1])) {
+    c *= 2;
+    ++lg;
+  }
   while (c < kStMaxCluster && ((max_blocks + c - 1) / c > kStMaxChunk || (k_total + c - 1) / c > kStMaxList)) c *= 2;
   int64_t ch = (max_blocks + c - 1) / c;
   ch = (ch + kStRowsPerStage - 1) / kStRowsPerStage * kStRowsPerStage;
@@ -430,6 +494,28 @@ bool step_shape(int64_t units, int64_t max_blocks, int k_scored, int k_total, in
   *chunk = static_cast<int>(ch);
   *bps = (k_total + c - 1) / c;
   return true;
+}
+
+// How many clusters of C fused-step CTAs the current device keeps resident
+// at once (0 if the query fails). Needs set_step_smem() first.
+int step_max_clusters(int C) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, 1, 1);
+  cfg.blockDim = dim3(kStThreads, 1, 1);
+  cfg.dynamicSmemBytes = kStSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decode_step_kernel, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 cudaError_t set_step_smem() {

@@ -24,35 +24,60 @@ __device__ inline uint64_t shfl_xor_u64(uint64_t v, int m) {
   return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
-// Sort the warp's 64 keys (x[r] is element 2*lane + r) in descending order.
-__device__ inline void warp_sort64_desc(uint64_t (&x)[2]) {
+__device__ inline uint64_t shfl_xor_key(uint64_t v, int m) { return shfl_xor_u64(v, m); }
+__device__ inline uint32_t shfl_xor_key(uint32_t v, int m) { return __shfl_xor_sync(0xffffffffu, v, m); }
+
+// Sort the warp's 64 keys (x[r] is element 2*lane + r; 64- or 32-bit) in
+// descending order.
+// The stage loops stay rolled: this runs once or twice per CTA, so a compact
+// body that stays in the instruction cache beats straight-line code that is
+// fetched cold.
+template <typename T>
+__device__ inline void warp_sort64_desc(T (&x)[2]) {
   const int lane = threadIdx.x & 31;
-#pragma unroll
+#pragma unroll 1
   for (int k = 2; k <= 64; k <<= 1) {
+    // stages with partner distance j = 2 lj >= 2 pair different lanes
+#pragma unroll 1
+    for (int lj = k >> 2; lj > 0; lj >>= 1) {
+      const bool lower = (lane & lj) == 0;
 #pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      if (j == 1) {
-        const int e = 2 * lane;
+      for (int r = 0; r < 2; ++r) {
+        const int e = 2 * lane + r;
         const bool desc = (e & k) == 0;
-        const bool swap = desc ? (x[0] < x[1]) : (x[0] > x[1]);
-        if (swap) {
-          const uint64_t t = x[0];
-          x[0] = x[1];
-          x[1] = t;
-        }
-      } else {
-        const int lj = j >> 1;
-        const bool lower = (lane & lj) == 0;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int e = 2 * lane + r;
-          const bool desc = (e & k) == 0;
-          const uint64_t o = shfl_xor_u64(x[r], lj);
-          const bool keep_max = (lower == desc);
-          x[r] = keep_max ? (x[r] > o ? x[r] : o) : (x[r] < o ? x[r] : o);
-        }
+        const T o = shfl_xor_key(x[r], lj);
+        const bool keep_max = (lower == desc);
+        x[r] = keep_max ? (x[r] > o ? x[r] : o) : (x[r] < o ? x[r] : o);
       }
     }
+    // distance 1: the lane's own pair
+    const bool desc = ((2 * lane) & k) == 0;
+    const bool swap = desc ? (x[0] < x[1]) : (x[0] > x[1]);
+    if (swap) {
+      const T t = x[0];
+      x[0] = x[1];
+      x[1] = t;
+    }
+  }
+}
+
+// Bitonic merge of a warp's 64 keys (element e in lane e/2, slot e%2) that
+// form a bitonic sequence: afterwards they are sorted in descending order.
+__device__ inline void warp_bitonic_merge64_desc(uint64_t (&x)[2]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int lj = 16; lj > 0; lj >>= 1) {
+    const bool lower = (lane & lj) == 0;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const uint64_t o = shfl_xor_u64(x[r], lj);
+      x[r] = lower ? (x[r] > o ? x[r] : o) : (x[r] < o ? x[r] : o);
+    }
+  }
+  if (x[0] < x[1]) {
+    const uint64_t t = x[0];
+    x[0] = x[1];
+    x[1] = t;
   }
 }
 
@@ -66,27 +91,19 @@ __device__ inline void warp_merge64(const uint64_t* a, const uint64_t* b, uint64
     const uint64_t u = a[e], v = b[63 - e];
     x[r] = u > v ? u : v;
   }
-  // bitonic merge, descending
-#pragma unroll
-  for (int j = 32; j > 0; j >>= 1) {
-    if (j == 1) {
-      if (x[0] < x[1]) {
-        const uint64_t t = x[0];
-        x[0] = x[1];
-        x[1] = t;
-      }
-    } else {
-      const int lj = j >> 1;
-      const bool lower = (lane & lj) == 0;
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const uint64_t o = shfl_xor_u64(x[r], lj);
-        x[r] = lower ? (x[r] > o ? x[r] : o) : (x[r] < o ? x[r] : o);
-      }
-    }
-  }
+  warp_bitonic_merge64_desc(x);
   out[2 * lane] = x[0];
   out[2 * lane + 1] = x[1];
+}
+
+// One warp, registers only: a = top 64 of the sorted (descending) lists a and
+// b, sorted. Element e of a meets element 63 - e of b, which sits in lane
+// 31 - lane (= lane ^ 31), slot 1 - r.
+__device__ inline void warp_merge64_reg(uint64_t (&a)[2], const uint64_t (&b)[2]) {
+  const uint64_t v0 = shfl_xor_u64(b[1], 31), v1 = shfl_xor_u64(b[0], 31);
+  a[0] = a[0] > v0 ? a[0] : v0;
+  a[1] = a[1] > v1 ? a[1] : v1;
+  warp_bitonic_merge64_desc(a);
 }
 
 // Merge `n_lists` sorted lists of 64 keys in buf (a power of two, <= 64) down
@@ -108,41 +125,65 @@ __device__ inline uint64_t* block_merge_lists(uint64_t* buf, uint64_t* tmp, int 
   return src;
 }
 
-// Sort the warp's 128 keys (x[r] is element 4*lane + r) in descending order.
-__device__ inline void warp_sort128_desc(uint64_t (&x)[4]) {
+// block_merge_lists for the first `nwarps` warps of the CTA only: they meet
+// at named barrier `bar` (1..15) instead of __syncthreads, so the other warps
+// are free meanwhile.
+__device__ inline const uint64_t* warps_merge_lists(uint64_t* buf, uint64_t* tmp, int n_lists, int nwarps, int bar) {
+  const int warp = threadIdx.x >> 5;
+  uint64_t* src = buf;
+  uint64_t* dst = tmp;
+  while (n_lists > 1) {
+    const int pairs = n_lists >> 1;
+    for (int p = warp; p < pairs; p += nwarps) warp_merge64(src + (2 * p) * 64, src + (2 * p + 1) * 64, dst + p * 64);
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(32 * nwarps) : "memory");
+    uint64_t* t = src;
+    src = dst;
+    dst = t;
+    n_lists = pairs;
+  }
+  return src;
+}
+
+// Compare-exchange inside a lane for the 128-key sort: registers r and r ^ j
+// (j = 1 or 2), direction from the bitonic block size k.
+__device__ inline void lane_stage128(uint64_t (&x)[4], int k, int j) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int k = 2; k <= 128; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      if (j < 4) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int p = r ^ j;
-          if (p > r) {
-            const int e = 4 * lane + r;
-            const bool desc = (e & k) == 0;
-            const bool swap = desc ? (x[r] < x[p]) : (x[r] > x[p]);
-            if (swap) {
-              const uint64_t t = x[r];
-              x[r] = x[p];
-              x[p] = t;
-            }
-          }
-        }
-      } else {
-        const int lj = j >> 2;
-        const bool lower = (lane & lj) == 0;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int e = 4 * lane + r;
-          const bool desc = (e & k) == 0;
-          const uint64_t o = shfl_xor_u64(x[r], lj);
-          const bool keep_max = (lower == desc);
-          x[r] = keep_max ? (x[r] > o ? x[r] : o) : (x[r] < o ? x[r] : o);
-        }
+  for (int r = 0; r < 4; ++r) {
+    const int p = r ^ j;
+    if (p > r) {
+      const int e = 4 * lane + r;
+      const bool desc = (e & k) == 0;
+      const bool swap = desc ? (x[r] < x[p]) : (x[r] > x[p]);
+      if (swap) {
+        const uint64_t t = x[r];
+        x[r] = x[p];
+        x[p] = t;
       }
     }
+  }
+}
+
+// Sort the warp's 128 keys (x[r] is element 4*lane + r) in descending order
+// (stage loops rolled, as in warp_sort64_desc).
+__device__ inline void warp_sort128_desc(uint64_t (&x)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int k = 2; k <= 128; k <<= 1) {
+#pragma unroll 1
+    for (int lj = k >> 3; lj > 0; lj >>= 1) {  // partner distance 4 lj >= 4: another lane
+      const bool lower = (lane & lj) == 0;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int e = 4 * lane + r;
+        const bool desc = (e & k) == 0;
+        const uint64_t o = shfl_xor_u64(x[r], lj);
+        const bool keep_max = (lower == desc);
+        x[r] = keep_max ? (x[r] > o ? x[r] : o) : (x[r] < o ? x[r] : o);
+      }
+    }
+    if (k >= 4) lane_stage128(x, k, 2);
+    lane_stage128(x, k, 1);
   }
 }
 
@@ -365,18 +406,18 @@ __device__ inline bool block_select(const uint64_t* keys, int n, int k, uint64_t
 // One warp: sort up to 64 block ids ascending (entries >= n are padding).
 __device__ inline void warp_sort64_blocks_asc(const uint64_t* top, int n, int* out) {
   const int lane = threadIdx.x & 31;
-  // ascending blocks == descending complements
-  uint64_t x[2];
+  // ascending blocks == descending complements (the key's low word); 0 pads
+  uint32_t x[2];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const int e = 2 * lane + r;
-    x[r] = e < n ? static_cast<uint64_t>(static_cast<uint32_t>(top[e])) : 0ull;
+    x[r] = e < n ? static_cast<uint32_t>(top[e]) : 0u;
   }
   warp_sort64_desc(x);
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const int e = 2 * lane + r;
-    if (e < n) out[e] = sel_block(x[r]);
+    if (e < n) out[e] = static_cast<int>(~x[r]);
   }
 }
 
