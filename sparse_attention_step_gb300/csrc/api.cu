@@ -73,13 +73,13 @@ EncodeTiledFn encode_fn() {
 
 // 2-D view [rows, 128] of a bf16 K or V buffer; boxes of 64 rows x 64 columns
 // (128 bytes) with 128-byte swizzling.
-msa_status make_kv_map(CUtensorMap* map, const void* base, int64_t rows) {
+msa_status make_kv_map(CUtensorMap* map, const void* base, int64_t rows, uint32_t box_rows = 64) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return MSA_ERR_CUDA;
   if ((reinterpret_cast<uintptr_t>(base) & 15) != 0) return MSA_ERR_INVALID_ARG;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * 2};
-  cuuint32_t box[2] = {64, 64};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -447,13 +447,15 @@ msa_status msa_sparse_decode_step(const void* q, int32_t num_q_heads, const void
   if ((st = check_ws(ws, ws_bytes, kWsHeader)) != MSA_OK) return st;
   const int64_t rows = kv_rows(kv);
   if (rows >= (int64_t(1) << 31)) return MSA_ERR_UNSUPPORTED;
-  CUtensorMap tmk, tmv;
+  // summary rows: [batch * hkv * max_blocks, 128], 128-row boxes
+  CUtensorMap tmk, tmv, tmp;
   if ((st = make_kv_map(&tmk, kv->k, rows)) != MSA_OK) return st;
   if ((st = make_kv_map(&tmv, kv->v, rows)) != MSA_OK) return st;
-  return cuda_status(launch_decode_step(tmk, tmv, view_of(kv), kv->batch, static_cast<const __nv_bfloat16*>(q),
-                                        num_q_heads, static_cast<const __nv_bfloat16*>(pooled), *cfg, k_total, C,
-                                        chunk, bps, scale * kLog2e, idx_out, static_cast<__nv_bfloat16*>(out), lse,
-                                        ws_status(ws), reinterpret_cast<cudaStream_t>(stream)));
+  if ((st = make_kv_map(&tmp, pooled, units * kv_max_blocks(kv), 128)) != MSA_OK) return st;
+  return cuda_status(launch_decode_step(tmk, tmv, tmp, view_of(kv), kv->batch, static_cast<const __nv_bfloat16*>(q),
+                                        num_q_heads, *cfg, k_total, C, chunk, bps, scale * kLog2e, idx_out,
+                                        static_cast<__nv_bfloat16*>(out), lse, ws_status(ws),
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 msa_status msa_read_device_status(const void* ws, msa_stream_t stream, int32_t* status_out) {

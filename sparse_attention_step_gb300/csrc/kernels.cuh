@@ -79,9 +79,8 @@ bool step_shape(int64_t units, int64_t max_blocks, int k_scored, int k_total, in
                 int* C, int* chunk, int* bps);
 int step_max_clusters(int C);
 cudaError_t set_step_smem();
-cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, const KvView& kv, int batch,
-                               const __nv_bfloat16* q, int hq, const __nv_bfloat16* pooled,
-                               const msa_select_cfg& cfg, int k_total, int C, int chunk, int bps, float scale_log2,
+cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmpool,
+                               const KvView& kv, int batch, const __nv_bfloat16* q, int hq, const msa_select_cfg& cfg, int k_total, int C, int chunk, int bps, float scale_log2,
                                int32_t* idx_out, __nv_bfloat16* out, float* lse, int32_t* status,
                                cudaStream_t stream);
 

@@ -5,8 +5,9 @@
 // A thread-block cluster of C CTAs serves one (sequence, KV head) unit; no
 // CTA ever synchronises through global memory:
 //   1. CTA r scores candidate blocks [r*chunk, (r+1)*chunk): a producer warp
-//      streams the summary rows (bulk copies, 128 rows per 32 KB stage, a
-//      3-stage ring) and eight warps dot them with the group's index query.
+//      streams the summary rows (2-D TMA, 128 rows per 32 KB stage, a 3-stage
+//      ring) and eight warps dot them with the group's index query on the
+//      tensor cores (mma.sync, the query split into two bf16 parts).
 //   2. The CTA keeps its best 64 keys (register bitonic sorts and merges);
 //      after one cluster barrier every CTA gathers the C lists through
 //      distributed shared memory and merges them identically, so each holds
@@ -41,7 +42,7 @@ constexpr int kStRowsPerStage = kStStage / (kHeadDim * 2);  // 128 bf16 summary 
 constexpr int kStMaxChunk = 1024;                           // candidate rows per CTA
 constexpr int kStMaxList = 64;                              // selected blocks per CTA
 constexpr int kStMaxCluster = 16;
-constexpr int kStPrefetchExtra = 2;             // L2 prefetches per CTA beyond kk / C
+constexpr int kStPrefetchExtra = 0;             // L2 prefetches per CTA beyond ceil(kk / C)
 constexpr int kStG = 8;                                     // heads per group handled
 constexpr int kStOS = kHeadDim + 4;                         // padded merge rows
 constexpr int kStRecv = 12;                                 // floats per pushed piece: O[8], M, L, pad
@@ -51,7 +52,6 @@ constexpr size_t kStSmem = 1024 + kStStages * kStStage + kStMaxChunk * sizeof(ui
 
 struct StepArgs {
   const __nv_bfloat16* q;       // [batch, hq, 128]
-  const __nv_bfloat16* pooled;  // [batch, hkv, max_blocks, 128]
   int hq, hkv, grp;
   int k_scored, k_total, force_local;
   int chunk;  // candidate rows per CTA, a multiple of 128, <= kStMaxChunk
@@ -65,7 +65,8 @@ struct StepArgs {
 
 // grid (C, Hkv, batch), cluster (C, 1, 1).
 __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid_constant__ CUtensorMap tmk,
-                                                                   const __grid_constant__ CUtensorMap tmv, KvView kv,
+                                                                   const __grid_constant__ CUtensorMap tmv,
+                                                                   const __grid_constant__ CUtensorMap tmpool, KvView kv,
                                                                    StepArgs a) {
   extern __shared__ __align__(1024) uint8_t st_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(st_raw) + 1023) & ~uintptr_t(1023));
@@ -75,6 +76,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   __shared__ int32_t blocks[kStMaxList];
   __shared__ int sorted_blocks[64];
   __shared__ int n_blocks;
+  __shared__ float qsum[kHeadDim];  // the group's index query (sum of its query heads), fp32
   __shared__ float wm[kStAttnWarps][kStG], wl[kStAttnWarps][kStG];
 
   const int rank = blockIdx.x, C = gridDim.x, h = blockIdx.y, s = blockIdx.z;
@@ -92,6 +94,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   if (warp == kStWarps && lane == 0) {
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
+    tma_prefetch_desc(&tmpool);
   }
   pdl_wait();
   const int64_t len = kv.seq_len(s, a.status, kIdDecode);
@@ -103,6 +106,12 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   const int64_t r0 = static_cast<int64_t>(rank) * a.chunk;
   const int rows = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(a.chunk), n_cand - r0)));
   const int n_st = (rows + kStRowsPerStage - 1) / kStRowsPerStage;
+  if (tid < kHeadDim) {
+    const __nv_bfloat16* qg = a.q + (static_cast<int64_t>(s) * a.hq + h * a.grp) * kHeadDim + tid;
+    float acc = 0.f;
+    for (int g = 0; g < a.grp; ++g) acc += __bfloat162float(qg[g * kHeadDim]);
+    qsum[tid] = acc;
+  }
   if (rank == 0 && warp == kStWarps && lane >= 28 && forced >= 0) {
     // the newest block is always attended: pull it into L2 during scoring
     const int64_t row = kv.block_row(s, h, forced, a.status, kIdDecode);
@@ -113,41 +122,57 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   // ---------------------------------------------------------------- 1. scores
   if (warp == kStWarps) {
     if (lane == 0) {
-      const __nv_bfloat16* base = a.pooled + (unit * max_blocks + r0) * kHeadDim;
+      // 128 summary rows per stage as two 64-column boxes (128-byte swizzle);
+      // rows past the CTA's chunk are loaded but never scored
+      const int32_t y0 = static_cast<int32_t>(unit * max_blocks + r0);
       for (int st = 0; st < n_st; ++st) {
         const int slot = st % kStStages;
         if (st >= kStStages && !mbar_wait(&empty[slot], ((st / kStStages) - 1) & 1, a.status, kIdDecode)) break;
-        const int n = min(kStRowsPerStage, rows - st * kStRowsPerStage);
-        mbar_arrive_expect_tx(&full[slot], n * kHeadDim * 2);
-        bulk_load(ring + slot * kStStage, base + static_cast<int64_t>(st) * kStRowsPerStage * kHeadDim,
-                  n * kHeadDim * 2, &full[slot]);
+        uint8_t* dst = ring + slot * kStStage;
+        mbar_arrive_expect_tx(&full[slot], kStStage);
+        tma_load_2d(dst, &tmpool, 0, y0 + st * kStRowsPerStage, &full[slot]);
+        tma_load_2d(dst + kStStage / 2, &tmpool, 64, y0 + st * kStRowsPerStage, &full[slot]);
       }
     }
   } else {
-    const int e = tid & 15, hw = tid >> 4;  // 16 half-warps; lane e owns dims [8e, 8e+8)
-    float qi[8];
+    // S = K_pool q_idx on the tensor cores, warp w taking rows 16w..16w+15 of
+    // each stage. The B operand holds the fp32 index query split into a bf16
+    // head (column 0) and the bf16 of the remainder (column 1), so the two
+    // accumulator columns add up to the fp32 dot product to ~2^-16 relative.
+    const int g = lane >> 2, c = lane & 3;
+    uint32_t qb[8][2];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) qi[i] = 0.f;
-    for (int g = 0; g < a.grp; ++g) {
-      float x[8];
-      load8<__nv_bfloat16>(a.q + (static_cast<int64_t>(s) * a.hq + h * a.grp + g) * kHeadDim + 8 * e, x);
+    for (int kk2 = 0; kk2 < 8; ++kk2) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) qi[i] += x[i];
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int d = 16 * kk2 + 2 * c + 8 * hlf;
+        float x0 = qsum[d], x1 = qsum[d + 1];
+        if (g == 1) {
+          x0 -= __bfloat162float(__float2bfloat16_rn(x0));
+          x1 -= __bfloat162float(__float2bfloat16_rn(x1));
+        }
+        qb[kk2][hlf] = g < 2 ? pack_bf16(x0, x1) : 0u;
+      }
     }
+    const int krow = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int kchunk = lane >> 4;
     for (int st = 0; st < n_st; ++st) {
       const int slot = st % kStStages;
       if (!mbar_wait_warp(&full[slot], (st / kStStages) & 1, a.status, kIdDecode)) break;
-      const uint8_t* stage = ring + slot * kStStage;
+      const uint32_t sbase = smem_u32(ring + slot * kStStage);
       const int n = min(kStRowsPerStage, rows - st * kStRowsPerStage);
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int rr = 0; rr < kStRowsPerStage / 16; ++rr) {
-        const int i = rr * 16 + hw;
-        float part = i < n ? SelRow<__nv_bfloat16>::dot(stage + i * kHeadDim * 2, e, qi) : 0.f;
-        part += __shfl_xor_sync(0xffffffffu, part, 8);
-        part += __shfl_xor_sync(0xffffffffu, part, 4);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        if (e == 0 && i < n) keys[st * kStRowsPerStage + i] = sel_key(part, static_cast<int>(r0 + st * kStRowsPerStage + i));
+      for (int kk2 = 0; kk2 < 8; ++kk2) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(sbase + (kk2 >> 2) * (kStStage / 2) + swz128(krow, (kk2 & 3) * 2 + kchunk), a0, a1, a2, a3);
+        mma_bf16(sacc, a0, a1, a2, a3, qb[kk2][0], qb[kk2][1]);
+      }
+      if (c == 0) {
+        const int i0 = 16 * warp + g, i1 = i0 + 8;
+        const int base = st * kStRowsPerStage;
+        if (i0 < n) keys[base + i0] = sel_key(sacc[0] + sacc[1], static_cast<int>(r0 + base + i0));
+        if (i1 < n) keys[base + i1] = sel_key(sacc[2] + sacc[3], static_cast<int>(r0 + base + i1));
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
@@ -528,14 +553,12 @@ cudaError_t set_step_smem() {
   return cudaFuncSetAttribute(decode_step_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
-cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, const KvView& kv, int batch,
-                               const __nv_bfloat16* q, int hq, const __nv_bfloat16* pooled,
-                               const msa_select_cfg& cfg, int k_total, int C, int chunk, int bps, float scale_log2,
+cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmpool,
+                               const KvView& kv, int batch, const __nv_bfloat16* q, int hq, const msa_select_cfg& cfg, int k_total, int C, int chunk, int bps, float scale_log2,
                                int32_t* idx_out, __nv_bfloat16* out, float* lse, int32_t* status,
                                cudaStream_t stream) {
   StepArgs a;
   a.q = q;
-  a.pooled = pooled;
   a.hq = hq;
   a.hkv = kv.hkv;
   a.grp = hq / kv.hkv;
@@ -563,7 +586,7 @@ cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, c
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 2;
-  return cudaLaunchKernelEx(&lc, decode_step_kernel, tmk, tmv, kv, a);
+  return cudaLaunchKernelEx(&lc, decode_step_kernel, tmk, tmv, tmpool, kv, a);
 }
 
 }  // namespace msa
