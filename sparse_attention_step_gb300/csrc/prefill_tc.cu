@@ -19,7 +19,9 @@
 // (a named barrier per tile). Warp 16 is the TMA producer (Q once, then a
 // 3-stage K/V ring), warp 17 the TMEM allocator and MMA issuer. The two tiles
 // ping-pong: the tensor core runs one tile's MMAs while the other tile's
-// softmax runs. TMEM: S_0 [0,64), S_1 [64,128), O_0 [128,256), O_1 [256,384).
+// softmax runs, and S is double-buffered so S of the next block is computed
+// while the softmax of this one runs. TMEM: S of tile t in [128 t, 128 t +
+// 128) (two 64-column buffers), O_t in [256 + 128 t, 384 + 128 t).
 #include <float.h>
 
 #include "kernels.cuh"
@@ -46,8 +48,9 @@ struct TcTail {
   uint64_t q_full;
   uint64_t kv_full[kTcStages];
   uint64_t kv_empty[kTcStages];
-  uint64_t s_full[kTcTiles];
+  uint64_t s_full[kTcTiles][2];  // S of a tile, double-buffered
   uint64_t p_full[kTcTiles];
+  uint64_t pv_done[kTcTiles];    // O += P V of the tile's latest block has completed
   uint64_t o_final[kTcTiles];
   uint64_t drain;
   uint32_t tmem_base;
@@ -118,8 +121,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       mbar_init(&st.kv_empty[i], 1);
     }
     for (int t = 0; t < kTcTiles; ++t) {
-      mbar_init(&st.s_full[t], 1);
+      mbar_init(&st.s_full[t][0], 1);
+      mbar_init(&st.s_full[t][1], 1);
       mbar_init(&st.p_full[t], kSoftmaxWarps / 2);
+      mbar_init(&st.pv_done[t], 1);
       mbar_init(&st.o_final[t], 1);
     }
     mbar_init(&st.drain, 1);
@@ -174,8 +179,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       constexpr uint32_t kIdS = tc::idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t kIdO = tc::idesc_bf16(128, 128, 0, 1);
       const uint32_t q_addr = smem_u32(qs), kv_addr = smem_u32(kvs), p_addr = smem_u32(ps);
-      auto issue_s = [&](int t, int stg) {
-        const uint32_t d = tmem + t * 64;
+      auto issue_s = [&](int t, int buf, int stg) {
+        const uint32_t d = tmem + t * 128 + buf * 64;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -185,7 +190,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         }
       };
       auto issue_pv = [&](int t, int stg, bool acc) {
-        const uint32_t d = tmem + 128 + t * 128;
+        const uint32_t d = tmem + 256 + t * 128;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           const uint64_t ad = tc::sdesc_sw128(p_addr + t * 16384 + ks * 32, 16, 1024);
@@ -193,29 +198,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
           tc::mma_ss(d, ad, bd, kIdO, (acc || ks > 0) ? 1u : 0u);
         }
       };
-      bool ok = wait_or_abort(&st.q_full, 0, abort, a.status);
-      tc::fence_after();
-      for (int i = 0; ok && i < nblk; ++i) {
+      // S_{i+1} of both tiles is issued before O += P_i V_i, into the other S
+      // buffer, so a tile's softmax of block i+1 never waits for the tensor
+      // core to finish block i.
+      auto issue_s_all = [&](int i) -> bool {
         const int stg = i % kTcStages;
-        if (!(ok = wait_or_abort(&st.kv_full[stg], (i / kTcStages) & 1, abort, a.status))) break;
+        if (!wait_or_abort(&st.kv_full[stg], (i / kTcStages) & 1, abort, a.status)) return false;
         tc::fence_after();
         for (int t = 0; t < kTcTiles; ++t) {
-          if (i > 0) {
-            if (!(ok = wait_or_abort(&st.p_full[t], (i - 1) & 1, abort, a.status))) break;
-            tc::fence_after();
-            issue_pv(t, (i - 1) % kTcStages, i - 1 > 0);
-            if (t == kTcTiles - 1) tc::commit(&st.kv_empty[(i - 1) % kTcStages]);
-          }
-          issue_s(t, stg);
-          tc::commit(&st.s_full[t]);
+          issue_s(t, i & 1, stg);
+          tc::commit(&st.s_full[t][i & 1]);
         }
-      }
-      if (ok && nblk > 0) {
+        return true;
+      };
+      bool ok = wait_or_abort(&st.q_full, 0, abort, a.status);
+      tc::fence_after();
+      if (ok && nblk > 0) ok = issue_s_all(0);
+      for (int i = 0; ok && i < nblk; ++i) {
+        // buffer (i + 1) & 1 was last read by the softmax of block i - 1,
+        // whose P this thread has already waited for
+        if (i + 1 < nblk && !(ok = issue_s_all(i + 1))) break;
         for (int t = 0; t < kTcTiles; ++t) {
-          if (!(ok = wait_or_abort(&st.p_full[t], (nblk - 1) & 1, abort, a.status))) break;
+          if (!(ok = wait_or_abort(&st.p_full[t], i & 1, abort, a.status))) break;
           tc::fence_after();
-          issue_pv(t, (nblk - 1) % kTcStages, nblk - 1 > 0);
+          issue_pv(t, i % kTcStages, i > 0);
+          tc::commit(&st.pv_done[t]);
         }
+        if (!ok) break;
+        tc::commit(&st.kv_empty[i % kTcStages]);
       }
       for (int t = 0; t < kTcTiles; ++t) tc::commit(&st.o_final[t]);
       tc::commit(&st.drain);
@@ -242,11 +252,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     // after a wait gave up (then it skips the work), so no partner warp can be
     // left waiting at a barrier.
     for (int i = 0; i < nblk; ++i) {
-      ok = __all_sync(0xffffffffu, ok && wait_or_abort(&st.s_full[t], i & 1, abort, a.status));
+      ok = __all_sync(0xffffffffu, ok && wait_or_abort(&st.s_full[t][i & 1], (i >> 1) & 1, abort, a.status));
       tc::fence_after();
+      // O and this tile's P buffer are touched only once O += P V of block
+      // i - 1 has completed
+      bool pv_seen = i == 0;
+      auto wait_pv = [&]() {
+        if (pv_seen) return;
+        ok = __all_sync(0xffffffffu, ok && wait_or_abort(&st.pv_done[t], (i - 1) & 1, abort, a.status));
+        tc::fence_after();
+        pv_seen = true;
+      };
       uint32_t sr[32];
       if (ok) {
-        tc::ld32(tmem + lane_base + t * 64 + 32 * hf, sr);
+        tc::ld32(tmem + lane_base + t * 128 + (i & 1) * 64 + 32 * hf, sr);
         tc::wait_ld();
       } else {
 #pragma unroll
@@ -267,12 +286,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       const float m_new = fmaxf(m, m_blk);
       const bool need = (m == -INFINITY) ? (m_new != -INFINITY) : (m_new > m + kRescaleLog2);
       if (__any_sync(0xffffffffu, need)) {
+        wait_pv();
         const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
         if (i > 0 && ok) {
 #pragma unroll 1
           for (int cc = 0; cc < 2; ++cc) {
             uint32_t o[32];
-            const uint32_t oa = tmem + lane_base + 128 + t * 128 + 64 * hf + cc * 32;
+            const uint32_t oa = tmem + lane_base + 256 + t * 128 + 64 * hf + cc * 32;
             tc::ld32(oa, o);
             tc::wait_ld();
 #pragma unroll
@@ -286,19 +306,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       }
       const float neg_ref = (m == -INFINITY) ? 0.f : -m;
       float sum = 0.f;
+      uint32_t pk[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), a.scale_log2, neg_ref));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), a.scale_log2, neg_ref));
+        sum += p0 + p1;
+        pk[c >> 1] = pack_bf16(p0, p1);
+      }
+      wait_pv();
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
-        float p[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = ex2_approx(fmaf(__uint_as_float(sr[8 * c8 + e]), a.scale_log2, neg_ref));
-          sum += p[e];
-        }
         uint4 v;
-        v.x = pack_bf16(p[0], p[1]);
-        v.y = pack_bf16(p[2], p[3]);
-        v.z = pack_bf16(p[4], p[5]);
-        v.w = pack_bf16(p[6], p[7]);
+        v.x = pk[4 * c8];
+        v.y = pk[4 * c8 + 1];
+        v.z = pk[4 * c8 + 2];
+        v.w = pk[4 * c8 + 3];
         *reinterpret_cast<uint4*>(prow + (((4 * hf + c8) ^ (r & 7)) << 4)) = v;
       }
       l += sum;
@@ -318,7 +341,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
 #pragma unroll 1
     for (int cc = 0; cc < 2; ++cc) {
       uint32_t o[32];
-      tc::ld32(tmem + lane_base + 128 + t * 128 + 64 * hf + cc * 32, o);
+      tc::ld32(tmem + lane_base + 256 + t * 128 + 64 * hf + cc * 32, o);
       tc::wait_ld();
       if (live) {
         if (nblk == 0 || !ok) {
