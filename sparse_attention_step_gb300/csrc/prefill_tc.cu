@@ -66,6 +66,23 @@ __device__ inline float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Paired fp32 arithmetic (one instruction for two lanes of a float2).
+__device__ inline float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 pa, pb, pc, pd;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %5};\n mov.b64 pc, {%6, %7};\n"
+      " fma.rn.f32x2 pd, pa, pb, pc;\n mov.b64 {%0, %1}, pd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ inline float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 pa, pb, pd;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %5};\n add.rn.f32x2 pd, pa, pb;\n"
+      " mov.b64 {%0, %1}, pd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
 __device__ inline void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -272,12 +289,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         for (int c = 0; c < 32; ++c) sr[c] = __float_as_uint(-INFINITY);
       }
       const int b = dense ? i : st.blocks[i];
-      const bool diag_blk = b == diag;
-      float mx = -INFINITY;
+      if (b == diag) {  // causal mask inside the diagonal block
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        if (diag_blk && 32 * hf + c > tt) sr[c] = __float_as_uint(-INFINITY);
-        mx = fmaxf(mx, __uint_as_float(sr[c]));
+        for (int c = 0; c < 32; ++c)
+          if (32 * hf + c > tt) sr[c] = __float_as_uint(-INFINITY);
+      }
+      float mx;
+      {
+        float t16[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) t16[c] = fmaxf(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
+#pragma unroll
+        for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+          for (int c = 0; c < w; ++c) t16[c] = fmaxf(t16[c], t16[c + w]);
+        mx = t16[0];
       }
       xmax[i & 1][t][hf][r] = mx;
       named_bar_sync(bar_id, 256);
@@ -305,15 +331,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         m = m_new;
       }
       const float neg_ref = (m == -INFINITY) ? 0.f : -m;
-      float sum = 0.f;
+      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nr2 = make_float2(neg_ref, neg_ref);
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
       uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), a.scale_log2, neg_ref));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), a.scale_log2, neg_ref));
-        sum += p0 + p1;
-        pk[c >> 1] = pack_bf16(p0, p1);
+      for (int c = 0; c < 16; ++c) {
+        const float2 x = ffma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc2, nr2);
+        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        if (c & 1) acc1 = fadd2(acc1, pp);
+        else acc0 = fadd2(acc0, pp);
+        pk[c] = pack_bf16(pp.x, pp.y);
       }
+      const float2 acc = fadd2(acc0, acc1);
+      const float sum = acc.x + acc.y;
       wait_pv();
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
