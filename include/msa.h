@@ -178,6 +178,8 @@ msa_status msa_sparse_attn_decode(const void* q, int32_t num_q_heads, const msa_
  * savings fall on the main attention). Batch 1; query token r sits at
  * absolute position p = q_start + r and attends to the tokens t <= p of the
  * blocks idx[r / 64, h, :] (idx from msa_select_topk_blocks with q_tile 64).
+ * At most 512 entries of a list may be valid blocks (-1 padding is free); a
+ * longer list is cut there and the device status records MSA_ERR_UNSUPPORTED.
  * out [n_q_tokens, Hq, 128] KV dtype; lse (nullable) [n_q_tokens, Hq] fp32. */
 msa_status msa_sparse_attn_prefill(const void* q, int32_t num_q_heads, int32_t n_q_tokens, int64_t q_start,
                                    const msa_kv_desc* kv /* host */, const int32_t* idx, int32_t k_total,

@@ -21,7 +21,7 @@ constexpr int kPfThreads = 32 * (kPfWarps + 1);
 constexpr int kPfRows = 16 * kPfWarps;  // rows per CTA
 constexpr int kPfStageBytes = 4 * 8192;
 constexpr int kPfStages = 4;
-constexpr int kPfMaxList = 512;
+constexpr int kPfMaxList = 512;  // list entries per (tile, head); larger k_total is rejected on the host
 
 
 struct PrefillSmemTail {
@@ -48,12 +48,16 @@ __global__ void __launch_bounds__(kPfThreads) prefill_bf16_kernel(const __grid_c
     int n = 0;
     if (a.idx != nullptr) {
       const int32_t* list = a.idx + (static_cast<int64_t>(tile) * a.hkv + h) * a.k_total;
-      for (int i = 0; i < a.k_total && n < kPfMaxList; ++i) {
+      for (int i = 0; i < a.k_total; ++i) {
         const int32_t b = list[i];
         if (b < 0) continue;
         if (b > diag) {
           set_status(a.status, MSA_ERR_DEVICE_BOUNDS, kIdPrefill);
           continue;
+        }
+        if (n == kPfMaxList) {  // more valid entries than the kernel holds
+          set_status(a.status, MSA_ERR_UNSUPPORTED, kIdPrefill);
+          break;
         }
         st.blocks[n++] = b;
       }

@@ -118,12 +118,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     int n = 0;
     if (a.idx != nullptr) {
       const int32_t* list = a.idx + (static_cast<int64_t>(tile) * a.hkv + h) * a.k_total;
-      for (int i = 0; i < a.k_total && n < kMaxList; ++i) {
+      for (int i = 0; i < a.k_total; ++i) {
         const int32_t b = list[i];
         if (b < 0) continue;
         if (b > diag) {
           set_status(a.status, MSA_ERR_DEVICE_BOUNDS, kIdPrefill);
           continue;
+        }
+        if (n == kMaxList) {  // more valid entries than the kernel holds
+          set_status(a.status, MSA_ERR_UNSUPPORTED, kIdPrefill);
+          break;
         }
         st.blocks[n++] = b;
       }
