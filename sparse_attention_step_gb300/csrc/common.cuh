@@ -124,6 +124,18 @@ __device__ inline void bulk_load(void* smem_dst, const void* gsrc, uint32_t byte
       "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// Per-thread asynchronous 16-byte copy global -> shared (L2 only), grouped
+// with commit / wait_group; a barrier after the wait publishes the data to
+// the other threads.
+__device__ inline void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ inline void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ inline void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Pull one 2-D tile into L2 (no shared memory, no completion to wait for).
 __device__ inline void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(

@@ -480,6 +480,96 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
     for (int i = tid; i < rows; i += blockDim.x) pages[i] = kv.page(s, r0 + i, status, kIdScore);
   __syncthreads();
 
+  auto emit = [&](int i, float part, bool ok) {  // row i of the chunk
+    const int64_t b = r0 + i;
+    keys[i] = ok ? sel_key(part, static_cast<int>(b)) : 0ull;
+    if (a.scores_out != nullptr) a.scores_out[unit * a.max_blocks + b] = ok ? part : -INFINITY;
+  };
+  if constexpr (sizeof(T) == 2) {
+    // bf16: every compute thread gathers 16-byte pieces of the stage's 64
+    // summary rows with cp.async (contiguous or one row per page alike) into
+    // a 4-stage ring, 128-byte swizzled as [64-dim half][row][128 B]; warps
+    // 0-3 score 16 rows each on the tensor cores with the index query split
+    // into a bf16 head and remainder (as in the fused step).
+    __shared__ float qsum[kHeadDim];
+    if (tid < kHeadDim) {
+      const T* qg = q + (static_cast<int64_t>(s) * a.hq + h * grp) * kHeadDim + tid;
+      float acc = 0.f;
+      for (int g = 0; g < grp; ++g) acc += __bfloat162float(qg[g * kHeadDim]);
+      qsum[tid] = acc;
+    }
+    __syncthreads();
+    constexpr int kRows = kSelStageBytes / (kHeadDim * 2);  // 64 rows per stage
+    const int64_t contig0 = (static_cast<int64_t>(s) * a.hkv + h) * a.max_blocks + r0;
+    auto issue = [&](int st) {
+      if (st < n_stages && warp < kSelWarps) {
+        uint8_t* stage = ring + (st % kSelStages) * kSelStageBytes;
+        const int base = st * kRows;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = tid + 32 * kSelWarps * u;  // 1024 pieces: row j / 16, piece j % 16
+          const int row = j >> 4, pc = j & 15;
+          const int i = base + row;
+          if (i >= rows) continue;
+          int64_t grow;
+          if (kv.layout == MSA_KV_CONTIGUOUS) {
+            grow = contig0 + i;
+          } else {
+            if (pages[i] < 0) continue;
+            grow = static_cast<int64_t>(pages[i]) * a.hkv + h;
+          }
+          cp_async16(stage + (pc >> 3) * (kRows * 128) + row * 128 + (((pc & 7) ^ (row & 7)) << 4),
+                     pooled + grow * kHeadDim + 8 * pc);
+        }
+      }
+      cp_async_commit();
+    };
+    const int g = lane >> 2, c = lane & 3;
+    uint32_t qb[8][2];
+#pragma unroll
+    for (int kk2 = 0; kk2 < 8; ++kk2) {
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int d = 16 * kk2 + 2 * c + 8 * hlf;
+        float x0 = qsum[d], x1 = qsum[d + 1];
+        if (g == 1) {
+          x0 -= __bfloat162float(__float2bfloat16_rn(x0));
+          x1 -= __bfloat162float(__float2bfloat16_rn(x1));
+        }
+        qb[kk2][hlf] = g < 2 ? pack_bf16(x0, x1) : 0u;
+      }
+    }
+    const int krow = 16 * (warp & 3) + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int kchunk = lane >> 4;
+    for (int st = 0; st < kSelStages - 1; ++st) issue(st);
+    for (int st = 0; st < n_stages; ++st) {
+      cp_async_wait<kSelStages - 2>();
+      __syncthreads();  // stage st has landed for every thread; stage st - 1 is consumed
+      issue(st + kSelStages - 1);
+      if (warp < 4) {
+        const uint32_t sbase = smem_u32(ring + (st % kSelStages) * kSelStageBytes);
+        float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk2 = 0; kk2 < 8; ++kk2) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(sbase + (kk2 >> 2) * (kRows * 128) + swz128(krow, (kk2 & 3) * 2 + kchunk), a0, a1, a2, a3);
+          mma_bf16(sacc, a0, a1, a2, a3, qb[kk2][0], qb[kk2][1]);
+        }
+        if (c == 0) {
+          const int base = st * kRows;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int i = base + 16 * warp + g + 8 * hh;
+            if (i < rows) {
+              const bool ok = kv.layout == MSA_KV_CONTIGUOUS || pages[i] >= 0;
+              emit(i, sacc[2 * hh] + sacc[2 * hh + 1], ok);
+            }
+          }
+        }
+      }
+    }
+    cp_async_wait<0>();
+  } else {
   const int e = tid & 15, hw = tid >> 4;  // scorers: 16 half-warps, lane e owns dims [8e, 8e+8)
   float qi[8];
   if (warp < kSelWarps) {
@@ -492,11 +582,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
       for (int i = 0; i < 8; ++i) qi[i] += x[i];
     }
   }
-  auto emit = [&](int i, float part, bool ok) {  // row i of the chunk
-    const int64_t b = r0 + i;
-    keys[i] = ok ? sel_key(part, static_cast<int>(b)) : 0ull;
-    if (a.scores_out != nullptr) a.scores_out[unit * a.max_blocks + b] = ok ? part : -INFINITY;
-  };
   if (kv.layout == MSA_KV_CONTIGUOUS) {
     if (warp == kSelWarps) {
       // ---------------- producer: one bulk copy per 64-row stage ----------------
@@ -559,6 +644,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
       }
     }
   }
+  }  // fp32 rows
   __syncthreads();
   pdl_trigger();  // the attention kernel may start its set-up
   const int kk = static_cast<int>(n_cand < a.k_scored ? n_cand : static_cast<int64_t>(a.k_scored));
