@@ -673,14 +673,16 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
   if (tid == 0) a.tickets[unit] = 0;  // ready for the next call
 }
 
-// Chunk size for the decode selection kernel: 512 candidate rows, doubled
-// while a unit would need more than 32 chunks (the last chunk of a unit merges
-// at most 32 lists of 64). Chunks past a short sequence's candidates exit at
-// once, so a ragged batch sized by its longest sequence costs little.
+// Chunk size for the decode selection kernel: 2048 candidate rows (fewer,
+// longer CTAs amortise their fixed costs: page ids, index query, top-k),
+// halved down to 512 while the grid would hold fewer than two CTAs per SM,
+// then doubled while a unit would need more than 32 chunks (the last chunk of
+// a unit merges at most 32 lists of 64). Chunks past a short sequence's
+// candidates exit at once, so a ragged batch sized by its longest sequence
+// costs little.
 void select_decode_shape(int64_t max_blocks, int64_t units, int num_sms, int* chunk, int* n_chunks) {
-  (void)units;
-  (void)num_sms;
-  int c = 512;
+  int c = 2048;
+  while (c > 512 && units * ((max_blocks + c - 1) / c) < 2LL * num_sms) c >>= 1;
   while (c < 4096 && (max_blocks + c - 1) / c > 32) c <<= 1;
   *chunk = c;
   *n_chunks = static_cast<int>((max_blocks + c - 1) / c);
