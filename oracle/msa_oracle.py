@@ -158,6 +158,37 @@ def boundary_gap(scores: np.ndarray, k_scored: int):
     return float(s[k_scored - 1]), float(s[k_scored])
 
 
+def score_blocks_token_max(q_idx: np.ndarray, kidx_rows: np.ndarray, n_cand: int) -> np.ndarray:
+    """Guide-literal block score of candidate blocks 0..n_cand-1 (float64).
+
+    Guide §1, Step 1 as drawn: token-level scores q_idx . K_idx[t] against a
+    single index-key head shared by every group of the layer, then a max pool
+    over the 64 tokens of each block. ``kidx_rows``: [T, D] index keys of the
+    sequence. Candidates are complete blocks, so every one has 64 tokens.
+    """
+    q = np.asarray(q_idx, dtype=np.float64)
+    out = np.empty(int(n_cand))
+    for b in range(int(n_cand)):
+        rows = np.asarray(kidx_rows[b * BLOCK:(b + 1) * BLOCK], dtype=np.float64)
+        out[b] = (rows @ q).max()
+    return out
+
+
+def select_token_max(q_group, kidx_rows, seq_len, k_scored, k_total, force_local=True):
+    """Step 1 with the token-level max-pooled score for one (sequence, KV
+    head): index query (group sum), token scores against the shared index
+    keys, block max, top-k plus the newest block."""
+    nb = num_blocks(seq_len)
+    nbf = num_full_blocks(seq_len)
+    forced = nb - 1 if force_local else None
+    n_cand = min(nbf, nb - 1) if force_local else nbf
+    n_cand = max(n_cand, 0)
+    q_idx = index_query(q_group)
+    scores = score_blocks_token_max(q_idx, kidx_rows, n_cand)
+    sel = select_blocks(scores, k_scored, forced, k_total)
+    return dict(selected=sel, scores=scores, q_idx=q_idx, forced=forced, n_cand=n_cand)
+
+
 # ---------------------------------------------------------------------------
 # Step 2: sparse branch
 # ---------------------------------------------------------------------------

@@ -23,7 +23,7 @@ BLOCK = 64
 HEAD_DIM = 128
 
 # stream ids
-_S_Q, _S_K, _S_V, _S_NEEDLE_POS, _S_NEEDLE_NOISE, _S_LENS, _S_PAGES = range(7)
+_S_Q, _S_K, _S_V, _S_NEEDLE_POS, _S_NEEDLE_NOISE, _S_LENS, _S_PAGES, _S_KIDX, _S_KIDX_POS, _S_KIDX_NOISE = range(10)
 
 
 def _gen(seed: int, stream: int, device) -> torch.Generator:
@@ -153,6 +153,65 @@ def _plant_needles(inp: DecodeInputs, per_head: int, seed: int) -> None:
             else:
                 pages = inp.page_table[s, blocks].long()
                 inp.k[pages, h] = rows
+
+
+@dataclasses.dataclass
+class IndexKeys:
+    kidx: torch.Tensor   # contiguous [B, T, D] or paged [P, 64, D]: one index-key head per sequence
+    needles: dict        # (s, h) -> sorted list of needle block ids (one needle token each)
+    layout: str
+
+    def rows(self, inp: DecodeInputs, s: int) -> torch.Tensor:
+        """[capacity, D] index keys of sequence s in logical token order."""
+        if self.layout == "contiguous":
+            return self.kidx[s]
+        n_pages = -(-inp.lens[s] // BLOCK)
+        pages = inp.page_table[s, :n_pages].long()
+        return self.kidx[pages].reshape(n_pages * BLOCK, self.kidx.shape[-1])
+
+
+def make_index_keys(inp: DecodeInputs, needles: int = 0, seed: int = 0) -> IndexKeys:
+    """A single index-key head per sequence, laid out like one KV head of the
+    cache (contiguous [B, T, D] or paged [P, 64, D] on the same pages), with
+    values ~ N(0, 1) in the KV dtype. For every (sequence, KV head), ``needles``
+    distinct candidate blocks (distinct across the heads of the sequence) get
+    one token whose index key is 3 * q_mean + N(0, 0.1^2), q_mean the fp32 mean
+    of that group's query heads."""
+    dev = inp.q.device
+    d = inp.q.shape[-1]
+    if inp.layout == "contiguous":
+        shape = (inp.batch, inp.k.shape[2], d)
+    else:
+        shape = (inp.k.shape[0], BLOCK, d)
+    kidx = torch.empty(shape, dtype=inp.k.dtype, device=dev)
+    _randn_into(kidx, _gen(seed, _S_KIDX, dev))
+    out = IndexKeys(kidx=kidx, needles={}, layout=inp.layout)
+    if not needles:
+        return out
+    rng = np.random.default_rng([int(seed), _S_KIDX_POS])
+    g = _gen(seed, _S_KIDX_NOISE, dev)
+    hkv = inp.num_kv_heads
+    grp = inp.num_q_heads // hkv
+    for s, n in enumerate(inp.lens):
+        nb = -(-n // BLOCK)
+        n_cand = min(n // BLOCK, nb - 1)
+        cnt = min(needles, n_cand // hkv)
+        if cnt <= 0:
+            continue
+        chosen = rng.choice(n_cand, size=cnt * hkv, replace=False)
+        offs = rng.integers(0, BLOCK, size=cnt * hkv)
+        qm = inp.q[s].float().view(hkv, grp, d).mean(dim=1)
+        for h in range(hkv):
+            blocks = [int(x) for x in chosen[h * cnt:(h + 1) * cnt]]
+            out.needles[(s, h)] = sorted(blocks)
+            for j, b in enumerate(blocks):
+                t = b * BLOCK + int(offs[h * cnt + j])
+                row = (3.0 * qm[h] + 0.1 * torch.randn(d, generator=g, device=dev, dtype=torch.float32)).to(kidx.dtype)
+                if inp.layout == "contiguous":
+                    kidx[s, t] = row
+                else:
+                    kidx[int(inp.page_table[s, t // BLOCK]), t % BLOCK] = row
+    return out
 
 
 @dataclasses.dataclass

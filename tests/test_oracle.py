@@ -313,3 +313,69 @@ def test_golden_diagram_groups_share_one_selection():
         o, _, _ = O.attend(q[j:j + 1], k[h], v[h], toks, 1 / math.sqrt(d))
         assert np.allclose(o[0], sel[h]["o"][j - h * grp], atol=1e-13)
     assert list(sel[0]["selected"]) != list(sel[1]["selected"])
+
+
+# --------------------------------------------------------------------------- token-level max-pooled score
+
+def test_token_max_equals_summary_score_for_constant_blocks():
+    # a block whose 64 index keys are one row r: max_t q.k_t = q.r, the score of
+    # the summary key r (pooling 64 copies of r gives r exactly)
+    rng = np.random.default_rng(7)
+    nb = 5
+    r = O.round_f32_to_bf16(rng.standard_normal((nb, O.HEAD_DIM)).astype(np.float32))
+    kidx = np.repeat(r, O.BLOCK, axis=0)
+    q = rng.standard_normal(O.HEAD_DIM)
+    got = O.score_blocks_token_max(q, kidx, nb)
+    pooled, _ = O.pool_block_keys(kidx, nb * O.BLOCK, "bf16")
+    want = O.score_blocks(q, pooled, nb)
+    np.testing.assert_allclose(got, want, rtol=1e-14, atol=0)
+
+
+def test_token_max_brute_force_and_bounds():
+    rng = np.random.default_rng(8)
+    nb = 3
+    kidx = rng.standard_normal((nb * O.BLOCK, O.HEAD_DIM))
+    q = rng.standard_normal(O.HEAD_DIM)
+    got = O.score_blocks_token_max(q, kidx, nb)
+    for b in range(nb):
+        toks = [math.fsum(float(q[d]) * float(kidx[b * O.BLOCK + t, d]) for d in range(O.HEAD_DIM))
+                for t in range(O.BLOCK)]
+        assert abs(got[b] - max(toks)) <= 1e-12 * max(1.0, abs(max(toks)))
+        # the max of the token scores is at least their mean (the summary score)
+        assert got[b] >= math.fsum(toks) / O.BLOCK - 1e-12
+    # fewer candidates than blocks: only the first n_cand are scored
+    assert len(O.score_blocks_token_max(q, kidx, 2)) == 2
+
+
+def test_token_max_is_invariant_to_token_order_within_blocks():
+    rng = np.random.default_rng(9)
+    nb = 4
+    kidx = rng.standard_normal((nb * O.BLOCK, O.HEAD_DIM))
+    q = rng.standard_normal(O.HEAD_DIM)
+    perm = np.concatenate([b * O.BLOCK + rng.permutation(O.BLOCK) for b in range(nb)])
+    np.testing.assert_array_equal(O.score_blocks_token_max(q, kidx, nb), O.score_blocks_token_max(q, kidx[perm], nb))
+
+
+def test_token_max_single_hot_token_wins_its_block():
+    # one token aligned with the query lifts its block to the top even though the
+    # block mean barely moves (the case the guide's max pool is drawn for)
+    rng = np.random.default_rng(10)
+    nb = 12
+    kidx = rng.standard_normal((nb * O.BLOCK + 10, O.HEAD_DIM))
+    q_group = rng.standard_normal((4, O.HEAD_DIM))
+    q_idx = q_group.sum(axis=0)
+    kidx[5 * O.BLOCK + 17] = 3.0 * q_idx / np.linalg.norm(q_idx) * 4.0
+    res = O.select_token_max(q_group, kidx, nb * O.BLOCK + 10, 1, 2)
+    assert list(res["selected"]) == [5, nb]          # the hot block and the newest (partial) block
+    assert res["n_cand"] == nb
+
+
+def test_index_key_needles_are_selected_by_token_max():
+    from synth import make_decode_inputs, make_index_keys
+    inp = make_decode_inputs([64 * 40 + 3], 2, 8, "f32", "contiguous", seed=21)
+    ik = make_index_keys(inp, needles=3, seed=22)
+    kidx = ik.rows(inp, 0).double().numpy()
+    for h in range(2):
+        q = inp.q[0, 4 * h:4 * h + 4].double().numpy()
+        res = O.select_token_max(q, kidx, inp.lens[0], 3, 4)
+        assert sorted(ik.needles[(0, h)]) == [b for b in res["selected"] if b != 40]
