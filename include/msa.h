@@ -73,9 +73,15 @@ typedef enum msa_status {
 typedef enum msa_dtype { MSA_DTYPE_F32 = 0, MSA_DTYPE_BF16 = 1 } msa_dtype;
 typedef enum msa_kv_layout { MSA_KV_CONTIGUOUS = 0, MSA_KV_PAGED = 1 } msa_kv_layout;
 
-/* The block-scoring operator of Step 1. Only the mean-pooled-key score is
- * implemented; it is the block mean of token scores q_idx . k_t. */
-typedef enum msa_score_mode { MSA_SCORE_MEAN_POOLED_KEYS = 0 } msa_score_mode;
+/* The block-scoring operator of Step 1.
+ * MEAN_POOLED_KEYS: q_idx . pooled[b], the summary key being the mean of the
+ *   block's keys of the KV head itself -- by linearity the block mean of the
+ *   token scores q_idx . k_t.
+ * TOKEN_MAX: the guide's Step 1 as drawn (§1, Step 1: token-level scores
+ *   against a single index-key head shared by all groups, then a block max
+ *   pool): max over the block's 64 tokens of q_idx . K_idx[t], with K_idx a
+ *   caller-provided index-key cache passed in place of the summaries. */
+typedef enum msa_score_mode { MSA_SCORE_MEAN_POOLED_KEYS = 0, MSA_SCORE_TOKEN_MAX = 1 } msa_score_mode;
 
 /* Description of a KV cache. All pointers are device pointers. */
 typedef struct msa_kv_desc {
@@ -155,7 +161,13 @@ msa_status msa_pool_block_keys(const msa_kv_desc* kv /* host */, int64_t first_b
  * k_total >= min(k_scored, max_blocks) + force_local.
  * scores_out (nullable): [units, max_blocks] fp32 raw scores of the candidate
  * blocks (max_blocks = max_tokens/64 or max_pages_per_seq); other entries are
- * left unspecified. */
+ * left unspecified.
+ * cfg->mode == MSA_SCORE_TOKEN_MAX (decode, bf16, Hkv <= 8; else
+ *   MSA_ERR_UNSUPPORTED): `pooled` is the index-key cache instead, one shared
+ *   head laid out like one KV head of the cache -- contiguous
+ *   [batch, max_tokens, 128], paged [num_pages, 64, 128] on the cache's pages
+ *   -- and the score of block b is max_{t in b} q_idx . K_idx[t] (fp32). The
+ *   index keys of a sequence are read once for all of its KV heads. */
 msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_q_tokens,
                                   const void* pooled, const msa_kv_desc* kv /* host */,
                                   const msa_select_cfg* cfg /* host */, int32_t* idx_out, int32_t k_total,

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libmsa.so")
-SOURCES = ["api.cu", "pool.cu", "select.cu", "decode.cu", "prefill.cu", "prefill_tc.cu", "step.cu"]
+SOURCES = ["api.cu", "pool.cu", "select.cu", "decode.cu", "prefill.cu", "prefill_tc.cu", "step.cu", "token_max.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]

@@ -35,6 +35,7 @@ msa_status device_info(DeviceInfo** out) {
     if (set_prefill_smem() != cudaSuccess) return MSA_ERR_CUDA;
     if (set_prefill_tc_smem() != cudaSuccess) return MSA_ERR_CUDA;
     if (set_step_smem() != cudaSuccess) return MSA_ERR_CUDA;
+    if (set_token_max_smem() != cudaSuccess) return MSA_ERR_CUDA;
     for (int i = 0; i < 5; ++i) d.step_clusters[i] = step_max_clusters(1 << i);
     d.topk_smem = (kMaxTopkCandidates + kTopkCandCap) * sizeof(uint32_t);
     if (set_topk_smem(d.topk_smem) != cudaSuccess) return MSA_ERR_CUDA;
@@ -351,7 +352,7 @@ msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_
   if (st != MSA_OK) return st;
   if (cfg == nullptr || q == nullptr || pooled == nullptr || idx_out == nullptr) return MSA_ERR_INVALID_ARG;
   if ((st = check_q_heads(kv, num_q_heads)) != MSA_OK) return st;
-  if (cfg->mode != MSA_SCORE_MEAN_POOLED_KEYS) return MSA_ERR_UNSUPPORTED;
+  if (cfg->mode != MSA_SCORE_MEAN_POOLED_KEYS && cfg->mode != MSA_SCORE_TOKEN_MAX) return MSA_ERR_UNSUPPORTED;
   if (cfg->k_scored < 0 || k_total <= 0) return MSA_ERR_INVALID_ARG;
   if (k_total < std::min<int64_t>(cfg->k_scored, kv_max_blocks(kv)) + (cfg->force_local ? 1 : 0))
     return MSA_ERR_INVALID_ARG;
@@ -381,6 +382,19 @@ msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_
   if (!prefill && !decode_units_fit(kv)) return MSA_ERR_UNSUPPORTED;
   KvView view = view_of(kv);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cfg->mode == MSA_SCORE_TOKEN_MAX) {
+    // `pooled` holds the shared index-key head: [batch, max_tokens, 128] or [num_pages, 64, 128]
+    if (prefill || kv->dtype != MSA_DTYPE_BF16 || kv->num_kv_heads > 8) return MSA_ERR_UNSUPPORTED;
+    const int64_t rows = kv->layout == MSA_KV_CONTIGUOUS ? static_cast<int64_t>(kv->batch) * kv->max_tokens
+                                                         : static_cast<int64_t>(kv->num_pages) * kBlock;
+    if (rows >= (int64_t(1) << 31)) return MSA_ERR_UNSUPPORTED;
+    CUtensorMap tmi;
+    if ((st = make_kv_map(&tmi, pooled, rows)) != MSA_OK) return st;
+    if ((st = cuda_status(launch_token_max_scores(tmi, view, kv->batch, static_cast<const __nv_bfloat16*>(q),
+                                                  num_q_heads, cfg->force_local, scores, ws_status(ws), s))) != MSA_OK)
+      return st;
+    return cuda_status(launch_topk_scores(scores, view, kv->batch, *cfg, idx_out, k_total, ws_status(ws), s));
+  }
   if (kv->dtype == MSA_DTYPE_BF16)
     return cuda_status(launch_select<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(q), num_q_heads, n_q_tokens,
                                                     static_cast<const __nv_bfloat16*>(pooled), view, kv->batch,

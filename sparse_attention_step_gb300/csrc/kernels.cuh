@@ -79,6 +79,13 @@ bool step_shape(int64_t units, int64_t max_blocks, int k_scored, int k_total, in
                 int* C, int* chunk, int* bps);
 int step_max_clusters(int C);
 cudaError_t set_step_smem();
+
+// ---- token-level max-pooled scores (token_max.cu) ----
+cudaError_t set_token_max_smem();
+cudaError_t launch_token_max_scores(const CUtensorMap& tmi, const KvView& kv, int batch, const __nv_bfloat16* q,
+                                    int hq, int force_local, float* scores, int32_t* status, cudaStream_t stream);
+cudaError_t launch_topk_scores(const float* scores, const KvView& kv, int batch, const msa_select_cfg& cfg,
+                               int32_t* idx_out, int k_total, int32_t* status, cudaStream_t stream);
 cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmpool,
                                const KvView& kv, int batch, const __nv_bfloat16* q, int hq, const msa_select_cfg& cfg, int k_total, int C, int chunk, int bps, float scale_log2,
                                int32_t* idx_out, __nv_bfloat16* out, float* lse, int32_t* status,

@@ -759,6 +759,16 @@ cudaError_t launch_select(const T* q, int hq, int n_q_tokens, const T* pooled, c
   return cudaGetLastError();
 }
 
+// Top-k over decode scores already in `scores` ([batch, hkv, max_blocks]).
+cudaError_t launch_topk_scores(const float* scores, const KvView& kv, int batch, const msa_select_cfg& cfg,
+                               int32_t* idx_out, int k_total, int32_t* status, cudaStream_t stream) {
+  const int64_t max_blocks = kv.max_blocks();
+  TopkArgs ta{kv.hkv, 0, cfg.force_local, cfg.k_scored, k_total, 0, max_blocks};
+  const size_t smem = static_cast<size_t>(max_blocks + kCandCap) * sizeof(uint32_t);
+  topk_kernel<<<dim3(kv.hkv, batch), kTopkThreads, smem, stream>>>(scores, kv, ta, idx_out, status);
+  return cudaGetLastError();
+}
+
 cudaError_t set_select_decode_smem(size_t bytes) {
   // the decode step's kernels all ask for the largest shared-memory carve-out,
   // so consecutive launches need no L1/shared reconfiguration

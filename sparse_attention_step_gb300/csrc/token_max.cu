@@ -1,0 +1,183 @@
+// Step 1 as the guide draws it ("MiniMax goes sparse", §1 Step 1): token-level
+// index scores q_idx . K_idx[t] against a single index-key head shared by every
+// GQA group of the layer, then a max pool over the 64 tokens of each block.
+//
+// One CTA scores a chunk of a sequence's candidate blocks for all of its KV
+// heads at once (the index keys are shared, so each is read once per step):
+// a producer warp streams each 64-token block of index keys with two 2-D TMA
+// boxes (128-byte swizzle) into a 4-stage ring; four warps take 16 tokens each
+// and compute S[token, group] = K_idx q_idx^T with mma.sync, the fp32 index
+// queries of up to 8 groups split into a bf16 head (one n-tile) and a bf16
+// remainder (a second n-tile), then reduce the max over their tokens. The
+// block maxima go to the score buffer that the top-k kernel reads.
+#include <float.h>
+
+#include "kernels.cuh"
+
+namespace msa {
+
+namespace {
+
+constexpr int kTmWarps = 4;
+constexpr int kTmThreads = 32 * (kTmWarps + 1);
+constexpr int kTmStages = 4;
+constexpr int kTmStage = kBlock * kHeadDim * 2;  // 16 KB: one block of index keys
+constexpr int kTmChunk = 32;                     // candidate blocks per CTA
+constexpr int kTmMaxHeads = 8;
+
+}  // namespace
+
+struct TokenMaxArgs {
+  const __nv_bfloat16* q;  // [batch, hq, 128]
+  int hq, hkv, grp;
+  int force_local;
+  int64_t max_blocks;
+  float* scores;  // [batch, hkv, max_blocks]
+  int32_t* status;
+};
+
+// grid (chunks, batch)
+__global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __grid_constant__ CUtensorMap tmi,
+                                                                     KvView kv, TokenMaxArgs a) {
+  extern __shared__ __align__(1024) uint8_t tm_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tm_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t full[kTmStages], empty[kTmStages];
+  __shared__ float qsum[kTmMaxHeads][kHeadDim];
+  __shared__ int32_t rowid[kTmChunk];                      // first index-key row of each block, -1 = bad page
+  __shared__ float part[kTmChunk][kTmWarps][kTmMaxHeads];  // per-warp block maxima
+
+  const int s = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();
+  const int64_t len = kv.seq_len(s, a.status, kIdScore);
+  const int64_t nb = (len + kBlock - 1) / kBlock;
+  const int64_t nbf = len / kBlock;
+  int64_t n_cand = a.force_local ? min(nbf, nb - 1) : nbf;
+  if (n_cand < 0) n_cand = 0;
+  const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kTmChunk;
+  if (b0 >= n_cand) return;
+  const int nblk = static_cast<int>(min(static_cast<int64_t>(kTmChunk), n_cand - b0));
+
+  if (tid == 0) {
+    for (int i = 0; i < kTmStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kTmWarps);
+    }
+    fence_mbar_init();
+  }
+  if (tid < kTmChunk) {
+    int32_t r = -1;
+    if (tid < nblk) {
+      const int64_t b = b0 + tid;
+      if (kv.layout == MSA_KV_CONTIGUOUS) {
+        r = static_cast<int32_t>(static_cast<int64_t>(s) * kv.max_tokens + b * kBlock);
+      } else {
+        const int32_t p = kv.page(s, b, a.status, kIdScore);
+        r = p < 0 ? -1 : p * kBlock;
+      }
+    }
+    rowid[tid] = r;
+  }
+  for (int i = tid; i < kTmMaxHeads * kHeadDim; i += blockDim.x) {
+    const int h = i / kHeadDim, d = i % kHeadDim;
+    float acc = 0.f;
+    if (h < a.hkv) {
+      const __nv_bfloat16* qg = a.q + (static_cast<int64_t>(s) * a.hq + h * a.grp) * kHeadDim + d;
+      for (int g = 0; g < a.grp; ++g) acc += __bfloat162float(qg[g * kHeadDim]);
+    }
+    qsum[h][d] = acc;
+  }
+  __syncthreads();
+
+  if (warp == kTmWarps) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmi);
+      for (int j = 0; j < nblk; ++j) {
+        const int slot = j % kTmStages;
+        if (j >= kTmStages && !mbar_wait(&empty[slot], ((j / kTmStages) - 1) & 1, a.status, kIdScore)) break;
+        const int32_t y = rowid[j] < 0 ? 0 : rowid[j];
+        uint8_t* dst = ring + slot * kTmStage;
+        mbar_arrive_expect_tx(&full[slot], kTmStage);
+        tma_load_2d(dst, &tmi, 0, y, &full[slot]);
+        tma_load_2d(dst + kTmStage / 2, &tmi, 64, y, &full[slot]);
+      }
+    }
+  } else {
+    const int g = lane >> 2, c = lane & 3;
+    // B operands: column n = group g; n-tile 0 the bf16 head, n-tile 1 the remainder
+    uint32_t qh[8][2], ql[8][2];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int d = 16 * kk + 2 * c + 8 * hlf;
+        const float x0 = qsum[g][d], x1 = qsum[g][d + 1];
+        const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
+        const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
+        qh[kk][hlf] = pack_bf16(h0, h1);
+        ql[kk][hlf] = pack_bf16(x0 - h0, x1 - h1);
+      }
+    }
+    const int krow = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int kchunk = lane >> 4;
+    for (int j = 0; j < nblk; ++j) {
+      const int slot = j % kTmStages;
+      if (!mbar_wait_warp(&full[slot], (j / kTmStages) & 1, a.status, kIdScore)) break;
+      const uint32_t sbase = smem_u32(ring + slot * kTmStage);
+      float hi[4] = {0.f, 0.f, 0.f, 0.f}, lo[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(sbase + (kk >> 2) * (kTmStage / 2) + swz128(krow, (kk & 3) * 2 + kchunk), a0, a1, a2, a3);
+        mma_bf16(hi, a0, a1, a2, a3, qh[kk][0], qh[kk][1]);
+        mma_bf16(lo, a0, a1, a2, a3, ql[kk][0], ql[kk][1]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+      // tokens g and g + 8 of this warp's 16, groups 2c and 2c + 1
+      float m0 = fmaxf(hi[0] + lo[0], hi[2] + lo[2]);
+      float m1 = fmaxf(hi[1] + lo[1], hi[3] + lo[3]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
+      }
+      if (g == 0) {
+        part[j][warp][2 * c] = m0;
+        part[j][warp][2 * c + 1] = m1;
+      }
+    }
+  }
+  pdl_trigger();
+  __syncthreads();
+  for (int i = tid; i < nblk * a.hkv; i += blockDim.x) {
+    const int j = i / a.hkv, h = i % a.hkv;
+    float m = fmaxf(fmaxf(part[j][0][h], part[j][1][h]), fmaxf(part[j][2][h], part[j][3][h]));
+    if (rowid[j] < 0) m = -INFINITY;  // bad page: never selected
+    a.scores[(static_cast<int64_t>(s) * a.hkv + h) * a.max_blocks + b0 + j] = m;
+  }
+}
+
+size_t token_max_smem_bytes() { return 1024 + static_cast<size_t>(kTmStages) * kTmStage; }
+
+cudaError_t set_token_max_smem() {
+  return cudaFuncSetAttribute(token_max_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(token_max_smem_bytes()));
+}
+
+cudaError_t launch_token_max_scores(const CUtensorMap& tmi, const KvView& kv, int batch, const __nv_bfloat16* q,
+                                    int hq, int force_local, float* scores, int32_t* status, cudaStream_t stream) {
+  TokenMaxArgs a;
+  a.q = q;
+  a.hq = hq;
+  a.hkv = kv.hkv;
+  a.grp = hq / kv.hkv;
+  a.force_local = force_local;
+  a.max_blocks = kv.max_blocks();
+  a.scores = scores;
+  a.status = status;
+  const unsigned chunks = static_cast<unsigned>((a.max_blocks + kTmChunk - 1) / kTmChunk);
+  token_max_score_kernel<<<dim3(chunks, batch), kTmThreads, token_max_smem_bytes(), stream>>>(tmi, kv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -22,7 +22,7 @@ MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_WORKSPACE, MSA_ERR_CUD
     MSA_ERR_DEVICE_BOUNDS, MSA_ERR_TIMEOUT = range(7)
 MSA_DTYPE_F32, MSA_DTYPE_BF16 = 0, 1
 MSA_KV_CONTIGUOUS, MSA_KV_PAGED = 0, 1
-MSA_SCORE_MEAN_POOLED_KEYS = 0
+MSA_SCORE_MEAN_POOLED_KEYS, MSA_SCORE_TOKEN_MAX = 0, 1
 (MSA_OP_POOL, MSA_OP_SELECT, MSA_OP_DECODE, MSA_OP_PREFILL, MSA_OP_DENSE_DECODE, MSA_OP_DENSE_PREFILL,
  MSA_OP_SELECT_PREFILL, MSA_OP_DECODE_STEP) = range(8)
 
@@ -154,9 +154,10 @@ def kv_desc(k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor, page_table
     return d
 
 
-def select_cfg(k_scored: int, force_local: bool = True, q_tile: int = 1, q_start: int = 0) -> SelectCfg:
-    return SelectCfg(int(k_scored), 1 if force_local else 0, int(q_tile), MSA_SCORE_MEAN_POOLED_KEYS,
-                     int(q_start))
+def select_cfg(k_scored: int, force_local: bool = True, q_tile: int = 1, q_start: int = 0,
+               mode: int = None) -> SelectCfg:
+    return SelectCfg(int(k_scored), 1 if force_local else 0, int(q_tile),
+                     MSA_SCORE_MEAN_POOLED_KEYS if mode is None else int(mode), int(q_start))
 
 
 # --------------------------------------------------------------------------- entry points

@@ -1,0 +1,105 @@
+"""GPU parity of the guide-literal Step 1 (token-level index scores against a
+shared index-key head, block max pool) against the CPU oracle, through the C
+ABI: msa_select_topk_blocks with MSA_SCORE_TOKEN_MAX, and the whole decode step
+(msa_sparse_decode_step) in that mode. Small cases on every unit, a
+128K-token x 8 batch on sampled units.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import msa_oracle as O
+from synth import make_decode_inputs, make_index_keys
+from tests.parity import SCALE, SelectionStats, check_lse, check_output, check_selection, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev(lib):
+    assert torch.cuda.is_available()
+    return torch.device("cuda:0")
+
+
+def run_token_max(inp, ik, k_scored, k_total, step=False):
+    from sparse_attention_step_gb300 import msa
+    dev = inp.q.device
+    desc = msa.kv_desc(inp.k, inp.v, inp.seq_lens, inp.page_table)
+    hq = inp.num_q_heads
+    ops = [msa.MSA_OP_SELECT, msa.MSA_OP_DECODE, msa.MSA_OP_DECODE_STEP]
+    ws = msa.Workspace(max(msa.msa_workspace_size(op, desc, hq, 1, k_total) for op in ops), dev)
+    b, hkv = inp.batch, inp.num_kv_heads
+    max_blocks = desc.max_tokens // 64 if desc.layout == 0 else desc.max_pages_per_seq
+    idx = torch.full((b, hkv, k_total), -7, dtype=torch.int32, device=dev)
+    scores = torch.full((b * hkv, max_blocks), float("nan"), dtype=torch.float32, device=dev)
+    out = torch.full_like(inp.q, float("nan"))
+    lse = torch.full((b, hq), float("nan"), dtype=torch.float32, device=dev)
+    cfg = msa.select_cfg(k_scored, mode=msa.MSA_SCORE_TOKEN_MAX)
+    if step:
+        msa.msa_sparse_decode_step(inp.q, hq, ik.kidx, desc, cfg, idx, k_total, SCALE, out, lse, ws.buf, ws.nbytes)
+        scores = None
+    else:
+        msa.msa_select_topk_blocks(inp.q, hq, 1, ik.kidx, desc, cfg, idx, k_total, scores, ws.buf, ws.nbytes)
+        msa.msa_sparse_attn_decode(inp.q, hq, desc, idx, k_total, SCALE, out, lse, ws.buf, ws.nbytes)
+    torch.cuda.synchronize()
+    return dict(idx=idx, scores=scores, out=out, lse=lse, status=msa.msa_read_device_status(ws.buf))
+
+
+def verify(inp, ik, res, units, k_scored, k_total, stats=None):
+    grp = inp.num_q_heads // inp.num_kv_heads
+    for s, h in units:
+        n = inp.lens[s]
+        qg = to64(inp.q[s, h * grp:(h + 1) * grp])
+        kidx = to64(ik.rows(inp, s))
+        ref = O.select_token_max(qg, kidx, n, k_scored, k_total)
+        if res["scores"] is not None and ref["n_cand"] > 0:
+            got = to64(res["scores"][s * inp.num_kv_heads + h, :ref["n_cand"]])
+            # fp32 dot products (bf16 head + remainder of the index query) vs fp64
+            lim = 1e-5 * np.maximum(1.0, np.abs(ref["scores"])) + 1e-5 * np.abs(ref["q_idx"]).sum()
+            assert (np.abs(got - ref["scores"]) <= lim).all(), f"token-max scores differ at unit {(s, h)}"
+        got_idx = res["idx"][s, h].cpu().numpy()
+        check_selection(got_idx, ref["scores"], k_scored, ref["forced"], k_total, stats, ik.needles.get((s, h), []))
+        toks = O.tokens_of_blocks(got_idx, n)
+        o, lse, _ = O.attend(qg, to64(inp.kv_rows(s, h, "k")), to64(inp.kv_rows(s, h, "v")), toks, SCALE)
+        check_output(to64(res["out"][s, h * grp:(h + 1) * grp]), o, inp.dtype, f"unit {(s, h)}")
+        check_lse(to64(res["lse"][s, h * grp:(h + 1) * grp]), lse)
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "paged"])
+@pytest.mark.parametrize("hkv,hq", [(2, 16), (1, 8), (8, 64)])
+def test_token_max_select_and_attend(dev, layout, hkv, hq):
+    inp = make_decode_inputs([64 * 90 + 13, 64 * 33, 64 * 7 + 1], hkv, hq, "bf16", layout, seed=41, device=dev)
+    ik = make_index_keys(inp, needles=2, seed=42)
+    res = run_token_max(inp, ik, 6, 7)
+    assert res["status"] == 0
+    verify(inp, ik, res, [(s, h) for s in range(inp.batch) for h in range(hkv)], 6, 7)
+
+
+def test_token_max_through_the_decode_step(dev):
+    inp = make_decode_inputs([64 * 200 + 5, 64 * 64], 4, 32, "bf16", "contiguous", seed=43, device=dev)
+    ik = make_index_keys(inp, needles=3, seed=44)
+    res = run_token_max(inp, ik, 11, 12, step=True)
+    assert res["status"] == 0
+    verify(inp, ik, res, [(s, h) for s in range(2) for h in range(4)], 11, 12)
+
+
+def test_token_max_short_and_empty_sequences(dev):
+    # no candidates (one partial block), exactly one complete block, and k above the candidates
+    inp = make_decode_inputs([40, 64, 64 * 3 + 2], 2, 16, "bf16", "contiguous", seed=45, device=dev)
+    ik = make_index_keys(inp, seed=46)
+    res = run_token_max(inp, ik, 5, 6)
+    assert res["status"] == 0
+    verify(inp, ik, res, [(s, h) for s in range(3) for h in range(2)], 5, 6)
+
+
+def test_token_max_decode_128k_sampled(dev):
+    """8 sequences x 131072 tokens, 8 KV / 64 query heads, top-31 + newest: the
+    benchmark's shape, units sampled across the batch."""
+    inp = make_decode_inputs([131072] * 8, 8, 64, "bf16", "contiguous", seed=1006, device=dev)
+    ik = make_index_keys(inp, needles=8, seed=1007)
+    res = run_token_max(inp, ik, 31, 32)
+    assert res["status"] == 0
+    stats = SelectionStats()
+    verify(inp, ik, res, [(0, 0), (3, 5), (7, 7)], 31, 32, stats)
+    del inp, ik
+    torch.cuda.empty_cache()
