@@ -354,6 +354,42 @@ def extras_decode(torch, msa, timer, name, steps, warmup, hbm):
     return res
 
 
+def extras_token_max(torch, msa, timer, steps, warmup, hbm):
+    """The decode step with the guide-literal Step 1 (token-level scores
+    against a shared index-key head, block max pool) on the 128K x 8 shape:
+    select (token-max scores + top-k) then sparse attention, one CUDA graph."""
+    from synth import make_decode_inputs, make_index_keys
+    inp = make_decode_inputs([131072] * 8, 8, 64, "bf16", "contiguous", seed=1006, device="cuda")
+    ik = make_index_keys(inp, needles=8, seed=1007)
+    k_scored, k_total = 31, 32
+    st = decode_setup(torch, msa, inp, k_scored, k_total)
+    cfg = msa.select_cfg(k_scored, mode=msa.MSA_SCORE_TOKEN_MAX)
+
+    def step():
+        msa.msa_sparse_decode_step(inp.q, st["hq"], ik.kidx, st["desc"], cfg, st["idx"], k_total, SCALE,
+                                   st["out"], st["lse"], st["ws"].buf, st["ws"].nbytes)
+
+    step_ms = time_op(torch, timer, step, steps, warmup)
+    sel_ms = time_op(torch, timer, lambda: msa.msa_select_topk_blocks(
+        inp.q, st["hq"], 1, ik.kidx, st["desc"], cfg, st["idx"], k_total, None, st["ws"].buf, st["ws"].nbytes),
+        steps, warmup)
+    # index keys of every candidate token (read once for all KV heads) + selected K/V + q/out
+    kidx_b = sum(min(n // 64, (n + 63) // 64 - 1) * 64 for n in inp.lens) * 128 * 2
+    _, sel_b, qo_b = decode_bytes(inp, k_total)
+    total = kidx_b + sel_b + qo_b
+    status = msa.msa_read_device_status(st["ws"].buf)
+    res = {
+        "workload": "decode_128k_token_max: 8 x 131072 tokens, 8 KV / 64 query heads, shared bf16 index-key "
+                    "head, top-31 + newest, 8 needle tokens per (seq, head)",
+        "us_per_step": step_ms * 1e3, "select_us": sel_ms * 1e3,
+        "step_GBps": total / (step_ms * 1e-3) / 1e9, "step_roofline_frac": total / (step_ms * 1e-3) / 1e9 / hbm,
+        "select_GBps": kidx_b / (sel_ms * 1e-3) / 1e9, "bytes_per_step": total, "device_status": status,
+    }
+    del inp, ik, st
+    torch.cuda.empty_cache()
+    return res
+
+
 def extras_prefill(torch, msa, timer, steps, warmup, tflops_peak):
     from synth import make_workload, WORKLOADS
     w = WORKLOADS["prefill_8k_on_128k"]
@@ -454,6 +490,7 @@ def run_ours(args):
         extras["ragged_paged_decode"] = extras_decode(torch, msa, timer, "ragged_paged_decode",
                                                       max(10, args.steps // 2), 3, hbm)
         extras["prefill_8k_on_128k"] = extras_prefill(torch, msa, timer, max(5, args.steps // 5), 2, tf_burst)
+        extras["decode_128k_token_max"] = extras_token_max(torch, msa, timer, max(10, args.steps // 2), 3, hbm)
 
     cpu = None
     if rank == 0 and not args.no_cpu:

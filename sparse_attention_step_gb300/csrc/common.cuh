@@ -13,6 +13,7 @@ namespace msa {
 
 constexpr int kHeadDim = 128;
 constexpr int kBlock = 64;
+constexpr int kMaxGroupHeads = 8;  // query heads per KV head (GQA group size) the kernels accept
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

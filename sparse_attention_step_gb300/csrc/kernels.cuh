@@ -76,8 +76,8 @@ cudaError_t launch_prefill_bf16(const CUtensorMap& tmk, const CUtensorMap& tmv, 
 
 // ---- fused decode step (step.cu) ----
 bool step_shape(int64_t units, int64_t max_blocks, int k_scored, int k_total, int num_sms, const int* max_clusters,
-                int* C, int* chunk, int* bps);
-int step_max_clusters(int C);
+                const int* max_clusters_wide, int* C, int* chunk, int* bps, bool* wide);
+int step_max_clusters(int C, bool wide);
 cudaError_t set_step_smem();
 
 // ---- token-level max-pooled scores (token_max.cu) ----
@@ -87,7 +87,8 @@ cudaError_t launch_token_max_scores(const CUtensorMap& tmi, const KvView& kv, in
 cudaError_t launch_topk_scores(const float* scores, const KvView& kv, int batch, const msa_select_cfg& cfg,
                                int32_t* idx_out, int k_total, int32_t* status, cudaStream_t stream);
 cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmpool,
-                               const KvView& kv, int batch, const __nv_bfloat16* q, int hq, const msa_select_cfg& cfg, int k_total, int C, int chunk, int bps, float scale_log2,
+                               const KvView& kv, int batch, const __nv_bfloat16* q, int hq, const msa_select_cfg& cfg,
+                               int k_total, int C, int chunk, int bps, bool wide, float scale_log2,
                                int32_t* idx_out, __nv_bfloat16* out, float* lse, int32_t* status,
                                cudaStream_t stream);
 

@@ -494,8 +494,12 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
     __shared__ float qsum[kHeadDim];
     if (tid < kHeadDim) {
       const T* qg = q + (static_cast<int64_t>(s) * a.hq + h * grp) * kHeadDim + tid;
+      float x[kMaxGroupHeads];
+#pragma unroll
+      for (int g = 0; g < kMaxGroupHeads; ++g) x[g] = g < grp ? __bfloat162float(qg[g * kHeadDim]) : 0.f;
       float acc = 0.f;
-      for (int g = 0; g < grp; ++g) acc += __bfloat162float(qg[g * kHeadDim]);
+#pragma unroll
+      for (int g = 0; g < kMaxGroupHeads; ++g) acc += x[g];
       qsum[tid] = acc;
     }
     __syncthreads();

@@ -36,7 +36,8 @@ namespace {
 constexpr int kStWarps = 8;                     // compute warps
 constexpr int kStAttnWarps = 4;                 // warps that consume attention blocks
 constexpr int kStThreads = 32 * (kStWarps + 1);  // + producer warp
-constexpr int kStStages = 3;
+constexpr int kStStages = 3;                    // ring depth with two CTAs per SM
+constexpr int kStStagesWide = 6;                // ring depth when the grid fits one CTA per SM
 constexpr int kStStage = 32768;
 constexpr int kStRowsPerStage = kStStage / (kHeadDim * 2);  // 128 bf16 summary rows
 constexpr int kStMaxChunk = 1024;                           // candidate rows per CTA
@@ -46,7 +47,7 @@ constexpr int kStPrefetchExtra = 0;             // L2 prefetches per CTA beyond 
 constexpr int kStG = 8;                                     // heads per group handled
 constexpr int kStOS = kHeadDim + 4;                         // padded merge rows
 constexpr int kStRecv = 12;                                 // floats per pushed piece: O[8], M, L, pad
-constexpr size_t kStSmem = 1024 + kStStages * kStStage + kStMaxChunk * sizeof(uint64_t);
+constexpr size_t step_smem(int stages) { return 1024 + stages * kStStage + kStMaxChunk * sizeof(uint64_t); }
 
 }  // namespace
 
@@ -63,15 +64,16 @@ struct StepArgs {
   int32_t* status;
 };
 
-// grid (C, Hkv, batch), cluster (C, 1, 1).
+// grid (C, Hkv, batch), cluster (C, 1, 1). kStages: depth of the shared-memory ring.
+template <int kStages>
 __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid_constant__ CUtensorMap tmk,
                                                                    const __grid_constant__ CUtensorMap tmv,
                                                                    const __grid_constant__ CUtensorMap tmpool, KvView kv,
                                                                    StepArgs a) {
   extern __shared__ __align__(1024) uint8_t st_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(st_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* keys = reinterpret_cast<uint64_t*>(ring + kStStages * kStStage);  // [kStMaxChunk]
-  __shared__ uint64_t full[kStStages], empty[kStStages];
+  uint64_t* keys = reinterpret_cast<uint64_t*>(ring + kStages * kStStage);  // [kStMaxChunk]
+  __shared__ uint64_t full[kStages], empty[kStages];
   __shared__ uint64_t xlist[64];  // this CTA's best keys, read by the whole cluster
   __shared__ int32_t blocks[kStMaxList];
   __shared__ int sorted_blocks[64];
@@ -85,7 +87,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   const int64_t max_blocks = kv.max_tokens / kBlock;
 
   if (tid == 0) {
-    for (int i = 0; i < kStStages; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kStWarps);
     }
@@ -107,9 +109,14 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   const int rows = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(a.chunk), n_cand - r0)));
   const int n_st = (rows + kStRowsPerStage - 1) / kStRowsPerStage;
   if (tid < kHeadDim) {
+    // all G loads in flight at once, then summed in head order
     const __nv_bfloat16* qg = a.q + (static_cast<int64_t>(s) * a.hq + h * a.grp) * kHeadDim + tid;
+    float x[kStG];
+#pragma unroll
+    for (int g = 0; g < kStG; ++g) x[g] = g < a.grp ? __bfloat162float(qg[g * kHeadDim]) : 0.f;
     float acc = 0.f;
-    for (int g = 0; g < a.grp; ++g) acc += __bfloat162float(qg[g * kHeadDim]);
+#pragma unroll
+    for (int g = 0; g < kStG; ++g) acc += x[g];
     qsum[tid] = acc;
   }
   if (rank == 0 && warp == kStWarps && lane >= 28 && forced >= 0) {
@@ -126,8 +133,8 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
       // rows past the CTA's chunk are loaded but never scored
       const int32_t y0 = static_cast<int32_t>(unit * max_blocks + r0);
       for (int st = 0; st < n_st; ++st) {
-        const int slot = st % kStStages;
-        if (st >= kStStages && !mbar_wait(&empty[slot], ((st / kStStages) - 1) & 1, a.status, kIdDecode)) break;
+        const int slot = st % kStages;
+        if (st >= kStages && !mbar_wait(&empty[slot], ((st / kStages) - 1) & 1, a.status, kIdDecode)) break;
         uint8_t* dst = ring + slot * kStStage;
         mbar_arrive_expect_tx(&full[slot], kStStage);
         tma_load_2d(dst, &tmpool, 0, y0 + st * kStRowsPerStage, &full[slot]);
@@ -157,8 +164,8 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     const int krow = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
     const int kchunk = lane >> 4;
     for (int st = 0; st < n_st; ++st) {
-      const int slot = st % kStStages;
-      if (!mbar_wait_warp(&full[slot], (st / kStStages) & 1, a.status, kIdDecode)) break;
+      const int slot = st % kStages;
+      if (!mbar_wait_warp(&full[slot], (st / kStages) & 1, a.status, kIdDecode)) break;
       const uint32_t sbase = smem_u32(ring + slot * kStStage);
       const int n = min(kStRowsPerStage, rows - st * kStRowsPerStage);
       float sacc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -179,6 +186,17 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     }
   }
   __syncthreads();  // every stage consumed: the ring is free until the attention phase
+  if (tid == 0) {
+    // the ring's barriers restart for the attention phase (one warp quartet
+    // consumes each block); nothing waits on them until then
+    for (int i = 0; i < kStages; ++i) {
+      mbar_inval(&full[i]);
+      mbar_inval(&empty[i]);
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kStAttnWarps);
+    }
+    fence_mbar_init();
+  }
 
   // ---------------------------------------------------------------- 2. selection
   // (a) this CTA's best 64: each warp bitonic-sorts batches of 64 keys in
@@ -260,15 +278,6 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
       if (tid < kk) sorted_blocks[pos] = b;
     }
   }
-  if (tid == 0) {
-    for (int i = 0; i < kStStages; ++i) {
-      mbar_inval(&full[i]);
-      mbar_inval(&empty[i]);
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kStAttnWarps);  // one warp quartet consumes each block
-    }
-    fence_mbar_init();
-  }
   __syncthreads();
   // (c) the unit's list: kk blocks ascending, then the forced block, then -1.
   // The leader writes it out; every CTA takes its slice.
@@ -304,8 +313,8 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   if (warp == kStWarps) {
     if (lane == 0) {
       for (int i = 0; i < nblk; ++i) {
-        const int slot = i % kStStages;
-        if (i >= kStStages && !mbar_wait(&empty[slot], ((i / kStStages) - 1) & 1, a.status, kIdDecode)) break;
+        const int slot = i % kStages;
+        if (i >= kStages && !mbar_wait(&empty[slot], ((i / kStages) - 1) & 1, a.status, kIdDecode)) break;
         const int64_t row = kv.block_row(s, h, blocks[i], a.status, kIdDecode);
         const int32_t y = static_cast<int32_t>(row < 0 ? 0 : row);
         uint8_t* dst = ring + slot * kStStage;
@@ -332,8 +341,8 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     const int vrow = 16 * wq + (lane & 7) + ((lane >> 4) & 1) * 8;
     const int vchunk = (lane >> 3) & 1;
     for (int i = 0; i < nblk; ++i) {
-      const int slot = i % kStStages;
-      if (!mbar_wait_warp(&full[slot], (i / kStStages) & 1, a.status, kIdDecode)) break;
+      const int slot = i % kStages;
+      if (!mbar_wait_warp(&full[slot], (i / kStages) & 1, a.status, kIdDecode)) break;
       const uint32_t kbase = smem_u32(ring + slot * kStStage);
       const uint32_t vbase = kbase + 16384;
       float sacc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -501,9 +510,11 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
 // units x C within two resident CTAs per SM and, where max_clusters is given
 // (the device's co-resident cluster count for C = 1, 2, 4, 8, 16), every
 // unit's cluster resident at once; chunk = ceil(max_blocks / C) rounded up to
-// 128 rows (<= 1024), and ceil(k_total / C) <= 64 list entries.
+// 128 rows (<= 1024), and ceil(k_total / C) <= 64 list entries. *wide: the
+// grid fits one CTA per SM (and, per max_clusters_wide, every cluster of the
+// deeper-ring kernel is resident), so the 6-stage ring is used.
 bool step_shape(int64_t units, int64_t max_blocks, int k_scored, int k_total, int num_sms, const int* max_clusters,
-                int* C, int* chunk, int* bps) {
+                const int* max_clusters_wide, int* C, int* chunk, int* bps, bool* wide) {
   if (k_scored > 64) return false;
   const int64_t slots = 2LL * num_sms;
   int c = 1, lg = 0;
@@ -511,23 +522,28 @@ bool step_shape(int64_t units, int64_t max_blocks, int k_scored, int k_total, in
     c *= 2;
     ++lg;
   }
-  while (c < kStMaxCluster && ((max_blocks + c - 1) / c > kStMaxChunk || (k_total + c - 1) / c > kStMaxList)) c *= 2;
+  while (c < kStMaxCluster && ((max_blocks + c - 1) / c > kStMaxChunk || (k_total + c - 1) / c > kStMaxList)) {
+    c *= 2;
+    ++lg;
+  }
   int64_t ch = (max_blocks + c - 1) / c;
   ch = (ch + kStRowsPerStage - 1) / kStRowsPerStage * kStRowsPerStage;
   if (ch > kStMaxChunk || (k_total + c - 1) / c > kStMaxList) return false;
   *C = c;
   *chunk = static_cast<int>(ch);
   *bps = (k_total + c - 1) / c;
+  *wide = units * c <= num_sms && (max_clusters_wide == nullptr || units <= max_clusters_wide[lg]);
   return true;
 }
 
-// How many clusters of C fused-step CTAs the current device keeps resident
-// at once (0 if the query fails). Needs set_step_smem() first.
-int step_max_clusters(int C) {
+namespace {
+
+template <int kStages>
+int max_clusters_of(int C) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, 1, 1);
   cfg.blockDim = dim3(kStThreads, 1, 1);
-  cfg.dynamicSmemBytes = kStSmem;
+  cfg.dynamicSmemBytes = step_smem(kStages);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
@@ -536,25 +552,42 @@ int step_max_clusters(int C) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_step_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, decode_step_kernel<kStages>, &cfg) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
   }
   return n;
 }
 
-cudaError_t set_step_smem() {
-  cudaError_t e = cudaFuncSetAttribute(decode_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kStSmem));
+template <int kStages>
+cudaError_t set_smem_of() {
+  cudaError_t e = cudaFuncSetAttribute(decode_step_kernel<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(step_smem(kStages)));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_step_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(decode_step_kernel<kStages>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(decode_step_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return cudaFuncSetAttribute(decode_step_kernel<kStages>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
+}  // namespace
+
+// How many clusters of C fused-step CTAs the current device keeps resident
+// at once, for the 3-stage (wide = false) or 6-stage kernel (0 if the query
+// fails). Needs set_step_smem() first.
+int step_max_clusters(int C, bool wide) {
+  return wide ? max_clusters_of<kStStagesWide>(C) : max_clusters_of<kStStages>(C);
+}
+
+cudaError_t set_step_smem() {
+  cudaError_t e = set_smem_of<kStStages>();
+  if (e != cudaSuccess) return e;
+  return set_smem_of<kStStagesWide>();
 }
 
 cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmpool,
-                               const KvView& kv, int batch, const __nv_bfloat16* q, int hq, const msa_select_cfg& cfg, int k_total, int C, int chunk, int bps, float scale_log2,
+                               const KvView& kv, int batch, const __nv_bfloat16* q, int hq, const msa_select_cfg& cfg,
+                               int k_total, int C, int chunk, int bps, bool wide, float scale_log2,
                                int32_t* idx_out, __nv_bfloat16* out, float* lse, int32_t* status,
                                cudaStream_t stream) {
   StepArgs a;
@@ -575,7 +608,7 @@ cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, c
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(C, kv.hkv, batch);
   lc.blockDim = dim3(kStThreads, 1, 1);
-  lc.dynamicSmemBytes = kStSmem;
+  lc.dynamicSmemBytes = step_smem(wide ? kStStagesWide : kStStages);
   lc.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -586,7 +619,8 @@ cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, c
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 2;
-  return cudaLaunchKernelEx(&lc, decode_step_kernel, tmk, tmv, tmpool, kv, a);
+  if (wide) return cudaLaunchKernelEx(&lc, decode_step_kernel<kStStagesWide>, tmk, tmv, tmpool, kv, a);
+  return cudaLaunchKernelEx(&lc, decode_step_kernel<kStStages>, tmk, tmv, tmpool, kv, a);
 }
 
 }  // namespace msa

@@ -22,7 +22,8 @@ constexpr int kTmWarps = 4;
 constexpr int kTmThreads = 32 * (kTmWarps + 1);
 constexpr int kTmStages = 4;
 constexpr int kTmStage = kBlock * kHeadDim * 2;  // 16 KB: one block of index keys
-constexpr int kTmChunk = 32;                     // candidate blocks per CTA
+constexpr int kTmMaxChunk = 64;                  // candidate blocks per CTA, at most
+constexpr int kTmCtasPerSm = 3;                  // resident CTAs per SM (65 KB of shared memory each)
 constexpr int kTmMaxHeads = 8;
 
 }  // namespace
@@ -31,6 +32,7 @@ struct TokenMaxArgs {
   const __nv_bfloat16* q;  // [batch, hq, 128]
   int hq, hkv, grp;
   int force_local;
+  int chunk;  // candidate blocks per CTA, <= kTmMaxChunk
   int64_t max_blocks;
   float* scores;  // [batch, hkv, max_blocks]
   int32_t* status;
@@ -43,8 +45,8 @@ __global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __gri
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tm_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t full[kTmStages], empty[kTmStages];
   __shared__ float qsum[kTmMaxHeads][kHeadDim];
-  __shared__ int32_t rowid[kTmChunk];                      // first index-key row of each block, -1 = bad page
-  __shared__ float part[kTmChunk][kTmWarps][kTmMaxHeads];  // per-warp block maxima
+  __shared__ int32_t rowid[kTmMaxChunk];                      // first index-key row of each block, -1 = bad page
+  __shared__ float part[kTmMaxChunk][kTmWarps][kTmMaxHeads];  // per-warp block maxima
 
   const int s = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_wait();
@@ -53,9 +55,9 @@ __global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __gri
   const int64_t nbf = len / kBlock;
   int64_t n_cand = a.force_local ? min(nbf, nb - 1) : nbf;
   if (n_cand < 0) n_cand = 0;
-  const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kTmChunk;
+  const int64_t b0 = static_cast<int64_t>(blockIdx.x) * a.chunk;
   if (b0 >= n_cand) return;
-  const int nblk = static_cast<int>(min(static_cast<int64_t>(kTmChunk), n_cand - b0));
+  const int nblk = static_cast<int>(min(static_cast<int64_t>(a.chunk), n_cand - b0));
 
   if (tid == 0) {
     for (int i = 0; i < kTmStages; ++i) {
@@ -64,7 +66,7 @@ __global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __gri
     }
     fence_mbar_init();
   }
-  if (tid < kTmChunk) {
+  if (tid < kTmMaxChunk) {
     int32_t r = -1;
     if (tid < nblk) {
       const int64_t b = b0 + tid;
@@ -82,7 +84,11 @@ __global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __gri
     float acc = 0.f;
     if (h < a.hkv) {
       const __nv_bfloat16* qg = a.q + (static_cast<int64_t>(s) * a.hq + h * a.grp) * kHeadDim + d;
-      for (int g = 0; g < a.grp; ++g) acc += __bfloat162float(qg[g * kHeadDim]);
+      float x[kMaxGroupHeads];
+#pragma unroll
+      for (int g = 0; g < kMaxGroupHeads; ++g) x[g] = g < a.grp ? __bfloat162float(qg[g * kHeadDim]) : 0.f;
+#pragma unroll
+      for (int g = 0; g < kMaxGroupHeads; ++g) acc += x[g];
     }
     qsum[h][d] = acc;
   }
@@ -175,7 +181,15 @@ cudaError_t launch_token_max_scores(const CUtensorMap& tmi, const KvView& kv, in
   a.max_blocks = kv.max_blocks();
   a.scores = scores;
   a.status = status;
-  const unsigned chunks = static_cast<unsigned>((a.max_blocks + kTmChunk - 1) / kTmChunk);
+  // one wave: the batch's blocks spread evenly over the resident CTAs
+  int num_sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t slots = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * kTmCtasPerSm;
+  int64_t chunk = (static_cast<int64_t>(batch) * a.max_blocks + slots - 1) / slots;
+  chunk = chunk < 8 ? 8 : chunk > kTmMaxChunk ? kTmMaxChunk : chunk;
+  a.chunk = static_cast<int>(chunk);
+  const unsigned chunks = static_cast<unsigned>((a.max_blocks + chunk - 1) / chunk);
   token_max_score_kernel<<<dim3(chunks, batch), kTmThreads, token_max_smem_bytes(), stream>>>(tmi, kv, a);
   return cudaGetLastError();
 }
