@@ -3,21 +3,21 @@
 // scores, TopK keeps the best KV blocks per layer and group; §3: in prefill
 // the index branch still scans the whole input).
 //
-// Three kernels:
+// Kernels:
 //   qidx_prefill_kernel  q_idx of a 64-token prefill tile = sum over its tokens
-//                        and the group's heads (fp32, token-major order).
-//   score_kernel         streams the summary keys of each unit once (bandwidth
-//                        bound, 16-byte loads, one half-warp per block row, 16
-//                        rows in flight per thread), writes fp32 scores and
-//                        adds each score to a per-unit histogram of the top 12
-//                        bits of its order-preserving key; for decode it forms
-//                        q_idx inline from the G query heads.
-//   topk_kernel          per unit: the histogram gives the 12-bit bin that
-//                        holds the k-th largest score; the few scores in that
+//                        and the group's heads (fp32).
+//   score_kernel         streams the summary keys of each unit once (16-byte
+//                        loads, one half-warp per block row) and writes fp32
+//                        scores; for decode it forms q_idx inline from the G
+//                        query heads. bf16 prefill uses score_prefill_mma_kernel
+//                        (tensor cores, 8 tiles per summary row read).
+//   topk_kernel          per unit: a shared-memory histogram of the top 12
+//                        bits of the order-preserving score keys gives the bin
+//                        that holds the k-th largest score; the scores in that
 //                        bin are refined by two 10-bit radix passes, ties go
 //                        to the lower block, and an ordered compaction emits
-//                        the kept blocks ascending, then the forced block. It
-//                        clears the histogram it read for the next call.
+//                        the kept blocks ascending, then the forced block.
+// The decode selection for k <= 64 is select_decode_kernel (below).
 #include <float.h>
 
 #include "kernels.cuh"
@@ -27,23 +27,51 @@
 namespace msa {
 
 // ---------------------------------------------------------------------------
-// q_idx for prefill tiles. grid (Hkv, n_tiles), 128 threads (one per dim).
+// q_idx for prefill tiles. grid (Hkv, n_tiles), 256 threads: the tile's
+// 64 tokens x G heads rows are split over 16 row slots (16 lanes each reading
+// one 256-byte row with 16-byte loads, 8 rows in flight per thread), and the
+// 16 partial sums of each dim are added in slot order through shared memory.
 // ---------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(128) qidx_prefill_kernel(const T* __restrict__ q, int hq, int hkv,
+__global__ void __launch_bounds__(256) qidx_prefill_kernel(const T* __restrict__ q, int hq, int hkv,
                                                           int n_q_tokens, float* __restrict__ qidx) {
+  __shared__ float part[16][kHeadDim + 4];
   const int h = blockIdx.x;
   const int tile = blockIdx.y;
-  const int d = threadIdx.x;
+  const int e = threadIdx.x & 15, slot = threadIdx.x >> 4;
   const int grp = hq / hkv;
   const int r0 = tile * kBlock;
-  const int r1 = min(n_q_tokens, r0 + kBlock);
-  float acc = 0.f;
-  for (int r = r0; r < r1; ++r) {
-    const T* row = q + (static_cast<int64_t>(r) * hq + h * grp) * kHeadDim + d;
-    for (int g = 0; g < grp; ++g) acc += static_cast<float>(row[g * kHeadDim]);
+  const int n_rows = (min(n_q_tokens, r0 + kBlock) - r0) * grp;  // token-major, head-minor
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int i0 = slot; i0 < n_rows; i0 += 16 * 8) {
+    float x[8][8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + 16 * u;
+      if (i < n_rows) {
+        const T* row = q + (static_cast<int64_t>(r0 + i / grp) * hq + h * grp + i % grp) * kHeadDim + 8 * e;
+        load8<T>(row, x[u]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[u][j] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] += x[u][j];
   }
-  qidx[(static_cast<int64_t>(tile) * hkv + h) * kHeadDim + d] = acc;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) part[slot][8 * e + j] = acc[j];
+  __syncthreads();
+  if (threadIdx.x < kHeadDim) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) t += part[k][threadIdx.x];
+    qidx[(static_cast<int64_t>(tile) * hkv + h) * kHeadDim + threadIdx.x] = t;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -155,6 +183,84 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const T* __restric
           scores[unit[t] * a.max_blocks + b] = (b < n_cand[t] && have[u]) ? part : -INFINITY;
         }
       }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Prefill block scores on the tensor cores (bf16 summaries).
+// grid (ceil(rows / 128), Hkv, ceil(n_tiles / 8)), 256 threads. The CTA copies
+// 128 summary rows into shared memory with cp.async (128-byte swizzle, two
+// 64-dim halves) and each warp scores 16 of them against the index queries of
+// 8 tiles at once: mma.sync with the 8 tiles as the N columns, the fp32 index
+// queries split into a bf16 head and a bf16 remainder (two n-tiles).
+// ---------------------------------------------------------------------------
+constexpr int kPsRows = 128;
+constexpr int kPsTiles = 8;
+
+__global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __restrict__ qidx_ws,
+                                                                const __nv_bfloat16* __restrict__ pooled,
+                                                                KvView kv, ScoreArgs a, float* __restrict__ scores,
+                                                                int32_t* status) {
+  __shared__ __align__(1024) uint8_t rows_s[kPsRows * kHeadDim * 2];
+  const int h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = blockIdx.z * kPsTiles;
+  const int64_t chunk0 = static_cast<int64_t>(blockIdx.x) * kPsRows;
+  int64_t n_max = 0;
+  for (int t = 0; t < kPsTiles; ++t)
+    if (t0 + t < a.n_tiles) n_max = max(n_max, a.q_start / kBlock + t0 + t);
+  const int64_t row_end = min(chunk0 + kPsRows, a.max_blocks);
+  // cp.async: 128 rows x 16 pieces of 16 bytes, 8 per thread
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int j = tid + 256 * u;
+    const int row = j >> 4, pc = j & 15;
+    const int64_t b = chunk0 + row;
+    if (b < n_max && b < row_end) {
+      const int64_t prow = kv.pooled_row(0, h, b, status, kIdScore);
+      cp_async16(rows_s + (pc >> 3) * (kPsRows * 128) + row * 128 + (((pc & 7) ^ (row & 7)) << 4),
+                 pooled + prow * kHeadDim + 8 * pc);
+    }
+  }
+  cp_async_commit();
+  // B operands: column g = tile t0 + g
+  const int g = lane >> 2, c = lane & 3;
+  const bool live = t0 + g < a.n_tiles;
+  const float* qg = qidx_ws + (static_cast<int64_t>(live ? t0 + g : 0) * a.hkv + h) * kHeadDim;
+  uint32_t qh[8][2], ql[8][2];
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      const int d = 16 * kk + 2 * c + 8 * hlf;
+      const float x0 = live ? qg[d] : 0.f, x1 = live ? qg[d + 1] : 0.f;
+      const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
+      const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
+      qh[kk][hlf] = pack_bf16(h0, h1);
+      ql[kk][hlf] = pack_bf16(x0 - h0, x1 - h1);
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  const uint32_t sbase = smem_u32(rows_s);
+  const int krow = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int kchunk = lane >> 4;
+  float hi[4] = {0.f, 0.f, 0.f, 0.f}, lo[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4(sbase + (kk >> 2) * (kPsRows * 128) + swz128(krow, (kk & 3) * 2 + kchunk), a0, a1, a2, a3);
+    mma_bf16(hi, a0, a1, a2, a3, qh[kk][0], qh[kk][1]);
+    mma_bf16(lo, a0, a1, a2, a3, ql[kk][0], ql[kk][1]);
+  }
+  // lane: rows 16 warp + g (+8), tiles 2c and 2c + 1
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int64_t b = chunk0 + 16 * warp + g + 8 * (k >> 1);
+    const int tile = t0 + 2 * c + (k & 1);
+    if (b < row_end && tile < a.n_tiles) {
+      const int64_t n_cand = a.q_start / kBlock + tile;
+      scores[(static_cast<int64_t>(tile) * a.hkv + h) * a.max_blocks + b] = b < n_cand ? hi[k] + lo[k] : -INFINITY;
     }
   }
 }
@@ -747,13 +853,19 @@ cudaError_t launch_select(const T* q, int hq, int n_q_tokens, const T* pooled, c
     const int n_tiles = (n_q_tokens + kBlock - 1) / kBlock;
     outer = n_tiles;
     sa.n_tiles = n_tiles;
-    qidx_prefill_kernel<T><<<dim3(kv.hkv, n_tiles), 128, 0, stream>>>(q, hq, kv.hkv, n_q_tokens, qidx_ws);
+    qidx_prefill_kernel<T><<<dim3(kv.hkv, n_tiles), 256, 0, stream>>>(q, hq, kv.hkv, n_q_tokens, qidx_ws);
     constexpr int kT = 8;
     // only the chunks below the last tile's diagonal hold candidates
     const int64_t last = cfg.q_start / kBlock + n_tiles;
-    const unsigned pchunks = static_cast<unsigned>((min(last, max_blocks) + kScoreChunk - 1) / kScoreChunk);
-    score_kernel<T, kT><<<dim3(pchunks, kv.hkv, (n_tiles + kT - 1) / kT), kScoreThreads, 0, stream>>>(
-        q, qidx_ws, pooled, kv, sa, scores, status);
+    if constexpr (sizeof(T) == 2) {
+      const unsigned pchunks = static_cast<unsigned>((min(last, max_blocks) + kPsRows - 1) / kPsRows);
+      score_prefill_mma_kernel<<<dim3(pchunks, kv.hkv, (n_tiles + kPsTiles - 1) / kPsTiles), 256, 0, stream>>>(
+          qidx_ws, pooled, kv, sa, scores, status);
+    } else {
+      const unsigned pchunks = static_cast<unsigned>((min(last, max_blocks) + kScoreChunk - 1) / kScoreChunk);
+      score_kernel<T, kT><<<dim3(pchunks, kv.hkv, (n_tiles + kT - 1) / kT), kScoreThreads, 0, stream>>>(
+          q, qidx_ws, pooled, kv, sa, scores, status);
+    }
   }
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
