@@ -212,6 +212,22 @@ msa_status msa_sparse_decode_step(const void* q, int32_t num_q_heads, const void
                                   int32_t* idx_out, int32_t k_total, float scale, void* out, float* lse, void* ws,
                                   size_t ws_bytes, msa_stream_t stream);
 
+/* The decode step of a generation loop (guide, introduction: decode writes the
+ * output token by token, each new token checked against everything before
+ * it; the summaries of Step 1 must keep up as blocks fill). Same as
+ * msa_sparse_decode_step
+ * (cfg->mode must be MSA_SCORE_MEAN_POOLED_KEYS), and `pooled` is also
+ * written: for every (sequence, KV head) whose seq_len is a multiple of 64 --
+ * its newest block has just filled with the current token -- the summary of
+ * that block is written exactly as msa_pool_block_keys would, so the next step
+ * (one token longer) can score it. In the fused kernel an otherwise idle warp
+ * of the unit's first CTA does this while the attention runs; otherwise one
+ * small pooling launch follows the step. No other summary is touched. */
+msa_status msa_sparse_decode_step_pool(const void* q, int32_t num_q_heads, void* pooled,
+                                       const msa_kv_desc* kv /* host */, const msa_select_cfg* cfg /* host */,
+                                       int32_t* idx_out, int32_t k_total, float scale, void* out, float* lse,
+                                       void* ws, size_t ws_bytes, msa_stream_t stream);
+
 /* Dense causal GQA decode: the full-attention comparator (guide §3 quotes
  * the sparse speed-ups against full attention). Same as msa_sparse_attn_decode
  * with every block 0..ceil(seq_len/64)-1 selected. */

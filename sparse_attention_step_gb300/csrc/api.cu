@@ -437,9 +437,14 @@ msa_status msa_dense_gqa_prefill(const void* q, int32_t num_q_heads, int32_t n_q
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
-msa_status msa_sparse_decode_step(const void* q, int32_t num_q_heads, const void* pooled, const msa_kv_desc* kv,
-                                  const msa_select_cfg* cfg, int32_t* idx_out, int32_t k_total, float scale,
-                                  void* out, float* lse, void* ws, size_t ws_bytes, msa_stream_t stream) {
+namespace {
+
+// The decode step; pooled_update (nullable, the same array as pooled) also
+// gets the summary of every (sequence, head) whose newest block has just
+// filled.
+msa_status decode_step_common(const void* q, int32_t num_q_heads, const void* pooled, void* pooled_update,
+                              const msa_kv_desc* kv, const msa_select_cfg* cfg, int32_t* idx_out, int32_t k_total,
+                              float scale, void* out, float* lse, void* ws, size_t ws_bytes, msa_stream_t stream) {
   msa_status st = validate_kv(kv);
   if (st != MSA_OK) return st;
   if (cfg == nullptr || q == nullptr || pooled == nullptr || idx_out == nullptr || out == nullptr)
@@ -458,10 +463,17 @@ msa_status msa_sparse_decode_step(const void* q, int32_t num_q_heads, const void
                      step_shape(units, kv_max_blocks(kv), cfg->k_scored, k_total, dev->num_sms, dev->step_clusters,
                                 dev->step_clusters_wide, &C, &chunk, &bps, &wide);
   if (!fused) {
-    // the same step as two launches
+    // the same step as two launches (plus the pooling of just-filled blocks)
     st = msa_select_topk_blocks(q, num_q_heads, 1, pooled, kv, cfg, idx_out, k_total, nullptr, ws, ws_bytes, stream);
     if (st != MSA_OK) return st;
-    return msa_sparse_attn_decode(q, num_q_heads, kv, idx_out, k_total, scale, out, lse, ws, ws_bytes, stream);
+    st = msa_sparse_attn_decode(q, num_q_heads, kv, idx_out, k_total, scale, out, lse, ws, ws_bytes, stream);
+    if (st != MSA_OK || pooled_update == nullptr) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (kv->dtype == MSA_DTYPE_BF16)
+      return cuda_status(launch_pool_newest(static_cast<const __nv_bfloat16*>(kv->k), view_of(kv), kv->batch,
+                                            static_cast<__nv_bfloat16*>(pooled_update), ws_status(ws), s));
+    return cuda_status(launch_pool_newest(static_cast<const float*>(kv->k), view_of(kv), kv->batch,
+                                          static_cast<float*>(pooled_update), ws_status(ws), s));
   }
   if ((st = check_ws(ws, ws_bytes, kWsHeader)) != MSA_OK) return st;
   const int64_t rows = kv_rows(kv);
@@ -474,7 +486,26 @@ msa_status msa_sparse_decode_step(const void* q, int32_t num_q_heads, const void
   return cuda_status(launch_decode_step(tmk, tmv, tmp, view_of(kv), kv->batch, static_cast<const __nv_bfloat16*>(q),
                                         num_q_heads, *cfg, k_total, C, chunk, bps, wide, scale * kLog2e, idx_out,
                                         static_cast<__nv_bfloat16*>(out), lse, ws_status(ws),
+                                        static_cast<const __nv_bfloat16*>(kv->k),
+                                        static_cast<__nv_bfloat16*>(pooled_update),
                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+msa_status msa_sparse_decode_step(const void* q, int32_t num_q_heads, const void* pooled, const msa_kv_desc* kv,
+                                  const msa_select_cfg* cfg, int32_t* idx_out, int32_t k_total, float scale,
+                                  void* out, float* lse, void* ws, size_t ws_bytes, msa_stream_t stream) {
+  return decode_step_common(q, num_q_heads, pooled, nullptr, kv, cfg, idx_out, k_total, scale, out, lse, ws, ws_bytes,
+                            stream);
+}
+
+msa_status msa_sparse_decode_step_pool(const void* q, int32_t num_q_heads, void* pooled, const msa_kv_desc* kv,
+                                       const msa_select_cfg* cfg, int32_t* idx_out, int32_t k_total, float scale,
+                                       void* out, float* lse, void* ws, size_t ws_bytes, msa_stream_t stream) {
+  if (cfg != nullptr && cfg->mode != MSA_SCORE_MEAN_POOLED_KEYS) return MSA_ERR_UNSUPPORTED;
+  return decode_step_common(q, num_q_heads, pooled, pooled, kv, cfg, idx_out, k_total, scale, out, lse, ws, ws_bytes,
+                            stream);
 }
 
 msa_status msa_read_device_status(const void* ws, msa_stream_t stream, int32_t* status_out) {

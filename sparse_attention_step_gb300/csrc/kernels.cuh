@@ -10,6 +10,9 @@ namespace msa {
 template <typename T>
 cudaError_t launch_pool(const T* k, const KvView& kv, int batch, int64_t first_block, int64_t n_blocks, T* pooled,
                         int32_t* status, cudaStream_t stream);
+template <typename T>
+cudaError_t launch_pool_newest(const T* k, const KvView& kv, int batch, T* pooled, int32_t* status,
+                               cudaStream_t stream);
 
 // ---- Step 1b/1c: index query, scores, top-k (select.cu) ----
 // Scratch of the fused decode selection (k_scored <= 64).
@@ -90,6 +93,6 @@ cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, c
                                const KvView& kv, int batch, const __nv_bfloat16* q, int hq, const msa_select_cfg& cfg,
                                int k_total, int C, int chunk, int bps, bool wide, float scale_log2,
                                int32_t* idx_out, __nv_bfloat16* out, float* lse, int32_t* status,
-                               cudaStream_t stream);
+                               const __nv_bfloat16* k, __nv_bfloat16* pooled_out, cudaStream_t stream);
 
 }  // namespace msa

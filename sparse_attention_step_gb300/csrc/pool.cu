@@ -56,17 +56,25 @@ struct Vec8<float> {
   }
 };
 
-// grid: (ceil(block range / 16), Hkv, batch)
+// grid: (ceil(block range / 16), Hkv, batch). newest_only: grid (1, Hkv,
+// batch) and each sequence pools only its newest block, when that block has
+// just filled (seq_len a multiple of 64).
 template <typename T>
 __global__ void __launch_bounds__(kPoolThreads) pool_block_keys_kernel(const T* __restrict__ k, KvView kv,
                                                                       int64_t first_block, int64_t n_blocks,
-                                                                      T* __restrict__ pooled, int32_t* status) {
+                                                                      int newest_only, T* __restrict__ pooled,
+                                                                      int32_t* status) {
   const int s = blockIdx.z;
   const int h = blockIdx.y;
   const int e = threadIdx.x & 15;
-  const int64_t b = first_block + static_cast<int64_t>(blockIdx.x) * kPoolBlocksPerCta + (threadIdx.x >> 4);
   const int64_t len = kv.seq_len(s, status, kIdPool);
-  if (n_blocks >= 0 && b >= first_block + n_blocks) return;
+  int64_t b = first_block + static_cast<int64_t>(blockIdx.x) * kPoolBlocksPerCta + (threadIdx.x >> 4);
+  if (newest_only) {
+    if (threadIdx.x >= 16 || len == 0 || len % kBlock != 0) return;
+    b = len / kBlock - 1;
+  } else if (n_blocks >= 0 && b >= first_block + n_blocks) {
+    return;
+  }
   if ((b + 1) * kBlock > len) return;  // partial or absent block: not pooled
   const int64_t row = kv.block_row(s, h, b, status, kIdPool);
   const int64_t prow = kv.pooled_row(s, h, b, status, kIdPool);
@@ -96,7 +104,14 @@ cudaError_t launch_pool(const T* k, const KvView& kv, int batch, int64_t first_b
   if (n_blocks >= 0 && n_blocks < span) span = n_blocks;
   if (span <= 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>((span + kPoolBlocksPerCta - 1) / kPoolBlocksPerCta), kv.hkv, batch);
-  pool_block_keys_kernel<T><<<grid, kPoolThreads, 0, stream>>>(k, kv, first_block, n_blocks, pooled, status);
+  pool_block_keys_kernel<T><<<grid, kPoolThreads, 0, stream>>>(k, kv, first_block, n_blocks, 0, pooled, status);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_pool_newest(const T* k, const KvView& kv, int batch, T* pooled, int32_t* status,
+                               cudaStream_t stream) {
+  pool_block_keys_kernel<T><<<dim3(1, kv.hkv, batch), kPoolThreads, 0, stream>>>(k, kv, 0, -1, 1, pooled, status);
   return cudaGetLastError();
 }
 
@@ -104,5 +119,8 @@ template cudaError_t launch_pool<__nv_bfloat16>(const __nv_bfloat16*, const KvVi
                                                 __nv_bfloat16*, int32_t*, cudaStream_t);
 template cudaError_t launch_pool<float>(const float*, const KvView&, int, int64_t, int64_t, float*, int32_t*,
                                         cudaStream_t);
+template cudaError_t launch_pool_newest<__nv_bfloat16>(const __nv_bfloat16*, const KvView&, int, __nv_bfloat16*,
+                                                       int32_t*, cudaStream_t);
+template cudaError_t launch_pool_newest<float>(const float*, const KvView&, int, float*, int32_t*, cudaStream_t);
 
 }  // namespace msa

@@ -62,6 +62,8 @@ struct StepArgs {
   __nv_bfloat16* out;
   float* lse;
   int32_t* status;
+  const __nv_bfloat16* k;        // keys (for pooling the newest block)
+  __nv_bfloat16* pooled_out;     // nullable: summary of the newest block when it has just filled
 };
 
 // grid (C, Hkv, batch), cluster (C, 1, 1). kStages: depth of the shared-memory ring.
@@ -394,6 +396,41 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
       l0 += __shfl_xor_sync(0xffffffffu, l0, off);
       l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
+  } else if (warp == kStAttnWarps && lane < 16 && rank == 0 && a.pooled_out != nullptr && forced >= 0 &&
+             len % kBlock == 0) {
+    // While warps 0-3 attend, the leader's first idle half-warp writes the
+    // summary of the newest block, which has just filled: the next step scores
+    // it. Same arithmetic as the pooling kernel (fp32 sum of the 64 rows in
+    // order, one multiply by 1/64, round to nearest even); lane e owns dims
+    // [8e, 8e + 8). The rows are in L2 (prefetched at the start).
+    const int64_t row = kv.block_row(s, h, forced, a.status, kIdDecode);
+    if (row >= 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.k + row * kHeadDim) + lane;
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll 1
+      for (int t0 = 0; t0 < kBlock; t0 += 16) {
+        uint4 v[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) v[t] = __ldg(src + (t0 + t) * (kHeadDim / 8));
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const uint32_t w[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[2 * i] += __uint_as_float(w[i] << 16);
+            acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+          }
+        }
+      }
+      uint4 o;
+      o.x = pack_bf16(acc[0] * (1.0f / kBlock), acc[1] * (1.0f / kBlock));
+      o.y = pack_bf16(acc[2] * (1.0f / kBlock), acc[3] * (1.0f / kBlock));
+      o.z = pack_bf16(acc[4] * (1.0f / kBlock), acc[5] * (1.0f / kBlock));
+      o.w = pack_bf16(acc[6] * (1.0f / kBlock), acc[7] * (1.0f / kBlock));
+      *reinterpret_cast<uint4*>(a.pooled_out + (unit * max_blocks + forced) * kHeadDim + 8 * lane) = o;
+    }
   }
   pdl_trigger();
   __syncthreads();  // the ring is free again: warp states go there
@@ -589,7 +626,7 @@ cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, c
                                const KvView& kv, int batch, const __nv_bfloat16* q, int hq, const msa_select_cfg& cfg,
                                int k_total, int C, int chunk, int bps, bool wide, float scale_log2,
                                int32_t* idx_out, __nv_bfloat16* out, float* lse, int32_t* status,
-                               cudaStream_t stream) {
+                               const __nv_bfloat16* k, __nv_bfloat16* pooled_out, cudaStream_t stream) {
   StepArgs a;
   a.q = q;
   a.hq = hq;
@@ -605,6 +642,8 @@ cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, c
   a.out = out;
   a.lse = lse;
   a.status = status;
+  a.k = k;
+  a.pooled_out = pooled_out;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(C, kv.hkv, batch);
   lc.blockDim = dim3(kStThreads, 1, 1);

@@ -30,7 +30,7 @@ MSA_SCORE_MEAN_POOLED_KEYS, MSA_SCORE_TOKEN_MAX = 0, 1
 EXPORTS = ["msa_workspace_size", "msa_workspace_init", "msa_pool_block_keys", "msa_select_topk_blocks",
            "msa_sparse_attn_decode", "msa_sparse_attn_prefill", "msa_dense_gqa_decode", "msa_dense_gqa_prefill",
            "msa_read_device_status", "msa_status_string", "msa_version", "msa_sparse_attn_decode_noalloc",
-           "msa_sparse_decode_step"]
+           "msa_sparse_decode_step", "msa_sparse_decode_step_pool"]
 
 
 class MsaError(RuntimeError):
@@ -72,6 +72,8 @@ _SIGS = {
     "msa_sparse_attn_decode_noalloc": (_I32, [_P, _I32, _DESC, _P, _I32, ctypes.c_float, _P, _P, _P]),
     "msa_sparse_decode_step": (_I32, [_P, _I32, _P, _DESC, ctypes.POINTER(SelectCfg), _P, _I32, ctypes.c_float, _P,
                                       _P, _P, _SZ, _P]),
+    "msa_sparse_decode_step_pool": (_I32, [_P, _I32, _P, _DESC, ctypes.POINTER(SelectCfg), _P, _I32, ctypes.c_float,
+                                           _P, _P, _P, _SZ, _P]),
     "msa_status_string": (ctypes.c_char_p, [_I32]),
     "msa_version": (_I32, []),
 }
@@ -202,6 +204,13 @@ def msa_sparse_decode_step(q, num_q_heads: int, pooled, desc: KvDesc, cfg: Selec
     _check(load().msa_sparse_decode_step(_ptr(q), num_q_heads, _ptr(pooled), ctypes.byref(desc), ctypes.byref(cfg),
                                          _ptr(idx_out), k_total, scale, _ptr(out), _ptr(lse), _ptr(ws), ws_bytes,
                                          _stream(stream)), "msa_sparse_decode_step")
+
+
+def msa_sparse_decode_step_pool(q, num_q_heads: int, pooled, desc: KvDesc, cfg: SelectCfg, idx_out, k_total: int,
+                                scale: float, out, lse, ws, ws_bytes: int, stream=None) -> None:
+    _check(load().msa_sparse_decode_step_pool(_ptr(q), num_q_heads, _ptr(pooled), ctypes.byref(desc),
+                                              ctypes.byref(cfg), _ptr(idx_out), k_total, scale, _ptr(out), _ptr(lse),
+                                              _ptr(ws), ws_bytes, _stream(stream)), "msa_sparse_decode_step_pool")
 
 
 def msa_dense_gqa_decode(q, num_q_heads: int, desc: KvDesc, scale: float, out, lse, ws, ws_bytes: int,
