@@ -150,6 +150,29 @@ def select_blocks(scores: np.ndarray, k_scored: int, forced: int | None, k_total
     return np.array(chosen + [-1] * (k_total - len(chosen)), dtype=np.int64)
 
 
+def select_blocks_sink(scores: np.ndarray, k_scored: int, forced: int | None, k_total: int,
+                       has_block0: bool) -> np.ndarray:
+    """Selection with an attention sink: block 0 is always kept and never
+    scored (the guide, §2, names a sink as one likely replacement for the
+    dropped sliding window). ``scores`` holds candidate blocks 0..n-1; block 0
+    is taken out of the ranking, the best ``min(k_scored, n - 1)`` of blocks
+    1..n-1 are kept, then block 0 (when the sequence has it) and the forced
+    block, ascending, padded with -1."""
+    scores = np.asarray(scores, dtype=np.float64)
+    n = scores.shape[0]
+    rest = np.arange(1, n)
+    order = rest[np.lexsort((rest, -scores[1:]))] if n > 1 else rest
+    chosen = [int(b) for b in order[: min(int(k_scored), max(n - 1, 0))]]
+    if has_block0:
+        chosen.append(0)
+    if forced is not None and int(forced) not in chosen:
+        chosen.append(int(forced))
+    chosen.sort()
+    if len(chosen) > k_total:
+        raise ValueError("k_total too small for the selection")
+    return np.array(chosen + [-1] * (k_total - len(chosen)), dtype=np.int64)
+
+
 def boundary_gap(scores: np.ndarray, k_scored: int):
     """(s_k, s_{k+1}) of the ranked candidate scores, or None when all are kept."""
     s = np.sort(np.asarray(scores, dtype=np.float64))[::-1]

@@ -379,3 +379,33 @@ def test_index_key_needles_are_selected_by_token_max():
         q = inp.q[0, 4 * h:4 * h + 4].double().numpy()
         res = O.select_token_max(q, kidx, inp.lens[0], 3, 4)
         assert sorted(ik.needles[(0, h)]) == [b for b in res["selected"] if b != 40]
+
+
+# --------------------------------------------------------------------------- attention sink
+
+@pytest.mark.parametrize("trial", range(30))
+def test_sink_selection_matches_brute_force(trial):
+    rng = np.random.default_rng(100 + trial)
+    n = int(rng.integers(1, 10))
+    k = int(rng.integers(1, 5))
+    scores = rng.integers(-2, 3, size=n).astype(np.float64) if trial % 3 == 0 else rng.standard_normal(n)
+    forced = n
+    sel = O.select_blocks_sink(scores, k, forced, k + 2, True)
+    # the best k of blocks 1..n-1 by (score, lower index), found by subset search
+    rest = list(range(1, n))
+    want = []
+    if rest:
+        best = _brute_force_topk([scores[b] for b in rest], k)
+        want = [rest[i] for i in best]
+    want = sorted(want + [0, forced])
+    assert list(sel) == want + [-1] * (k + 2 - len(want))
+
+
+def test_sink_selection_edge_cases():
+    # one block that is both the sink and the newest: kept once
+    assert list(O.select_blocks_sink(np.zeros(0), 3, 0, 5, True)) == [0, -1, -1, -1, -1]
+    # block 0 a high scorer: never counted among the k scored blocks
+    sel = O.select_blocks_sink(np.array([9.0, 1.0, 3.0, 2.0]), 2, 4, 4, True)
+    assert list(sel) == [0, 2, 3, 4]
+    # without the sink flag on the block the same scores select block 0 as a scored block
+    assert list(O.select_blocks(np.array([9.0, 1.0, 3.0, 2.0]), 2, 4, 4)) == [0, 2, 4, -1]
