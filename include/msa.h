@@ -103,7 +103,9 @@ typedef struct msa_kv_desc {
 /* Step-1 selection parameters. */
 typedef struct msa_select_cfg {
   int32_t k_scored;    /* number of scored blocks to keep per unit, >= 0 */
-  int32_t force_local; /* 1: always keep the newest / diagonal block (not scored) */
+  int32_t force_local; /* bit 0 (1): always keep the newest / diagonal block; bit 1 (2): always keep
+                          block 0, an attention sink (guide §2 names a sink among the likely
+                          replacements of the sliding window). Kept blocks are not scored. */
   int32_t q_tile;      /* 1: decode (one token per sequence); 64: prefill tiles */
   int32_t mode;        /* msa_score_mode */
   int64_t q_start;     /* prefill: absolute position of the first query token, a multiple of 64 */
@@ -158,7 +160,9 @@ msa_status msa_pool_block_keys(const msa_kv_desc* kv /* host */, int64_t first_b
  * Scores are q_idx . pooled[b] in fp32 (unscaled). The top min(k_scored, n)
  * candidates by (score descending, block ascending) plus the forced block are
  * written sorted ascending, padded with -1;
- * k_total >= min(k_scored, max_blocks) + force_local.
+ * k_total >= min(k_scored, max_blocks) + the number of kept blocks (bits of
+ * force_local). With the sink bit, block 0 leads the list and the candidates
+ * start at block 1.
  * scores_out (nullable): [units, max_blocks] fp32 raw scores of the candidate
  * blocks (max_blocks = max_tokens/64 or max_pages_per_seq); other entries are
  * left unspecified.

@@ -195,6 +195,11 @@ msa_status check_ws(void* ws, size_t have, size_t need) {
 
 msa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
 
+// Blocks kept without scoring: the newest / diagonal one and the attention sink.
+int forced_count(const msa_select_cfg* cfg) {
+  return ((cfg->force_local & kForceLocal) ? 1 : 0) + ((cfg->force_local & kForceSink) ? 1 : 0);
+}
+
 msa_status check_q_heads(const msa_kv_desc* kv, int hq) {
   if (hq <= 0 || hq % kv->num_kv_heads != 0) return MSA_ERR_INVALID_ARG;
   if (hq / kv->num_kv_heads > 8) return MSA_ERR_UNSUPPORTED;
@@ -358,9 +363,9 @@ msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_
   if ((st = check_q_heads(kv, num_q_heads)) != MSA_OK) return st;
   if (cfg->mode != MSA_SCORE_MEAN_POOLED_KEYS && cfg->mode != MSA_SCORE_TOKEN_MAX) return MSA_ERR_UNSUPPORTED;
   if (cfg->k_scored < 0 || k_total <= 0) return MSA_ERR_INVALID_ARG;
-  if (k_total < std::min<int64_t>(cfg->k_scored, kv_max_blocks(kv)) + (cfg->force_local ? 1 : 0))
+  if (k_total < std::min<int64_t>(cfg->k_scored, kv_max_blocks(kv)) + forced_count(cfg))
     return MSA_ERR_INVALID_ARG;
-  if (cfg->force_local != 0 && cfg->force_local != 1) return MSA_ERR_INVALID_ARG;
+  if (cfg->force_local < 0 || cfg->force_local > (kForceLocal | kForceSink)) return MSA_ERR_INVALID_ARG;
   const int prefill = cfg->q_tile == kBlock;
   if (!prefill && cfg->q_tile != 1) return MSA_ERR_UNSUPPORTED;
   if (prefill) {
@@ -459,7 +464,7 @@ msa_status decode_step_common(const void* q, int32_t num_q_heads, const void* po
   const int64_t units = static_cast<int64_t>(kv->batch) * kv->num_kv_heads;
   const bool fused = kv->dtype == MSA_DTYPE_BF16 && kv->layout == MSA_KV_CONTIGUOUS &&
                      cfg->mode == MSA_SCORE_MEAN_POOLED_KEYS && cfg->k_scored >= 0 &&
-                     k_total >= std::min<int64_t>(cfg->k_scored, kv_max_blocks(kv)) + (cfg->force_local ? 1 : 0) &&
+                     k_total >= std::min<int64_t>(cfg->k_scored, kv_max_blocks(kv)) + forced_count(cfg) &&
                      step_shape(units, kv_max_blocks(kv), cfg->k_scored, k_total, dev->num_sms, dev->step_clusters,
                                 dev->step_clusters_wide, &C, &chunk, &bps, &wide);
   if (!fused) {

@@ -14,6 +14,9 @@ namespace msa {
 constexpr int kHeadDim = 128;
 constexpr int kBlock = 64;
 constexpr int kMaxGroupHeads = 8;  // query heads per KV head (GQA group size) the kernels accept
+// msa_select_cfg.force_local bits
+constexpr int kForceLocal = 1;  // keep the newest (decode) / diagonal (prefill) block
+constexpr int kForceSink = 2;   // keep block 0 (attention sink)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

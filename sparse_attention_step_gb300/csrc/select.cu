@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const T* __restric
     const int64_t len = kv.seq_len(seq, status, kIdScore);
     const int64_t nb = (len + kBlock - 1) / kBlock;
     const int64_t nbf = len / kBlock;
-    n_cand[0] = a.force_local ? min(nbf, nb - 1) : nbf;
+    n_cand[0] = (a.force_local & kForceLocal) ? min(nbf, nb - 1) : nbf;
     if (n_cand[0] < 0) n_cand[0] = 0;
     unit[0] = static_cast<int64_t>(seq) * a.hkv + h;
 #pragma unroll
@@ -369,21 +369,27 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   const int tid = threadIdx.x;
   const int64_t unit = static_cast<int64_t>(outer) * a.hkv + h;
 
-  int64_t n64, forced;
+  const bool local = (a.force_local & kForceLocal) != 0, sink = (a.force_local & kForceSink) != 0;
+  int64_t n64, forced, nb;
   if (!a.prefill) {
     const int64_t len = kv.seq_len(outer, status, kIdTopk);
-    const int64_t nb = (len + kBlock - 1) / kBlock;
+    nb = (len + kBlock - 1) / kBlock;
     const int64_t nbf = len / kBlock;
-    n64 = a.force_local ? min(nbf, nb - 1) : nbf;
-    forced = (a.force_local && nb > 0) ? nb - 1 : -1;
+    n64 = local ? min(nbf, nb - 1) : nbf;
+    forced = (local && nb > 0) ? nb - 1 : -1;
   } else {
     n64 = a.q_start / kBlock + outer;
-    forced = a.force_local ? n64 : -1;
+    nb = n64 + 1;
+    forced = local ? n64 : -1;
   }
-  const int n = static_cast<int>(n64 < 0 ? 0 : n64);
+  if (n64 < 0) n64 = 0;
+  // attention sink: block 0 is kept and not scored; the candidates start at 1
+  const int skip = (sink && n64 > 0) ? 1 : 0;
+  const bool keep0 = sink && nb > 0 && forced != 0;
+  const int n = static_cast<int>(n64) - skip;
   const int k = min(a.k_scored, n);
-  const float* sc = scores + unit * a.max_blocks;
-  int32_t* out = idx_out + unit * a.k_total;
+  const float* sc = scores + unit * a.max_blocks + skip;
+  int32_t* out = idx_out + unit * a.k_total + (keep0 ? 1 : 0);
   uint32_t* cand = keys + a.max_blocks;
 
   for (int i = tid; i < n; i += blockDim.x) keys[i] = float_to_key(sc[i]);
@@ -469,15 +475,16 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
           const uint32_t key = keys[i];
           keep = key > thresh || (key == thresh && eq++ < take_equal);
         }
-        if (keep) out[pos++] = static_cast<int32_t>(i);
+        if (keep) out[pos++] = static_cast<int32_t>(i + skip);
       }
     }
     written = tot;
   }
   if (tid == 0) {
+    if (keep0) out[-1] = 0;
     int w = written;
     if (forced >= 0) out[w++] = static_cast<int32_t>(forced);
-    for (; w < a.k_total; ++w) out[w] = -1;
+    for (; w + (keep0 ? 1 : 0) < a.k_total; ++w) out[w] = -1;
   }
 }
 
@@ -519,14 +526,17 @@ __device__ inline int pow2_at_least(int x) {
 
 // Writes the final list of a unit: the blocks of the kk best keys ascending,
 // the forced block, then -1 padding. Called by every thread.
-__device__ inline void write_selection(const uint64_t* top, int kk, int64_t forced, int k_total, int32_t* out,
-                                       int* sorted_tmp) {
+__device__ inline void write_selection(const uint64_t* top, int kk, int64_t forced, bool keep0, int k_total,
+                                       int32_t* out, int* sorted_tmp) {
   if (threadIdx.x < 32) warp_sort64_blocks_asc(top, kk, sorted_tmp);
   __syncthreads();
+  const int o = keep0 ? 1 : 0;  // block 0 (attention sink) leads the list
   for (int i = threadIdx.x; i < k_total; i += blockDim.x) {
+    const int j = i - o;
     int v;
-    if (i < kk) v = sorted_tmp[i];
-    else if (i == kk && forced >= 0) v = static_cast<int>(forced);
+    if (j < 0) v = 0;
+    else if (j < kk) v = sorted_tmp[j];
+    else if (j == kk && forced >= 0) v = static_cast<int>(forced);
     else v = -1;
     out[i] = v;
   }
@@ -566,9 +576,12 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
   const int64_t len = kv.seq_len(s, status, kIdScore);
   const int64_t nb = (len + kBlock - 1) / kBlock;
   const int64_t nbf = len / kBlock;
-  int64_t n_cand = a.force_local ? min(nbf, nb - 1) : nbf;
+  const bool local = (a.force_local & kForceLocal) != 0, sink = (a.force_local & kForceSink) != 0;
+  int64_t n_cand = local ? min(nbf, nb - 1) : nbf;
   if (n_cand < 0) n_cand = 0;
-  const int64_t forced = (a.force_local && nb > 0) ? nb - 1 : -1;
+  const int64_t forced = (local && nb > 0) ? nb - 1 : -1;
+  const int skip = (sink && n_cand > 0) ? 1 : 0;     // attention sink: block 0 kept, not scored
+  const bool keep0 = sink && nb > 0 && forced != 0;
   const int my_chunks = n_cand > 0 ? static_cast<int>((n_cand + a.chunk - 1) / a.chunk) : 1;
   if (c >= my_chunks) return;  // past this sequence's candidates
   const int64_t r0 = static_cast<int64_t>(c) * a.chunk;
@@ -588,6 +601,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
 
   auto emit = [&](int i, float part, bool ok) {  // row i of the chunk
     const int64_t b = r0 + i;
+    ok = ok && !(skip && b == 0);
     keys[i] = ok ? sel_key(part, static_cast<int>(b)) : 0ull;
     if (a.scores_out != nullptr) a.scores_out[unit * a.max_blocks + b] = ok ? part : -INFINITY;
   };
@@ -757,12 +771,12 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
   }  // fp32 rows
   __syncthreads();
   pdl_trigger();  // the attention kernel may start its set-up
-  const int kk = static_cast<int>(n_cand < a.k_scored ? n_cand : static_cast<int64_t>(a.k_scored));
+  const int kk = static_cast<int>(n_cand - skip < a.k_scored ? n_cand - skip : static_cast<int64_t>(a.k_scored));
   int32_t* out = idx_out + unit * a.k_total;
-  const int kk_local = min(kk, rows);
+  const int kk_local = min(kk, rows - (c == 0 ? skip : 0));
   if (kk_local > 0) choose_top(keys, rows, kk_local, ring, top, scr, &count);
   if (my_chunks == 1) {
-    write_selection(top, kk, forced, a.k_total, out, sorted_blocks);
+    write_selection(top, kk, forced, keep0, a.k_total, out, sorted_blocks);
     return;
   }
   // post this chunk's list; the unit's last CTA selects among them
@@ -779,7 +793,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
   for (int i = tid; i < n_all; i += blockDim.x) keys[i] = __ldcg(all + i);
   __syncthreads();
   if (kk > 0) choose_top(keys, n_all, kk, ring, top, scr, &count);
-  write_selection(top, kk, forced, a.k_total, out, sorted_blocks);
+  write_selection(top, kk, forced, keep0, a.k_total, out, sorted_blocks);
   if (tid == 0) a.tickets[unit] = 0;  // ready for the next call
 }
 

@@ -104,9 +104,12 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   const int64_t len = kv.seq_len(s, a.status, kIdDecode);
   const int64_t nb = (len + kBlock - 1) / kBlock;
   const int64_t nbf = len / kBlock;
-  int64_t n_cand = a.force_local ? min(nbf, nb - 1) : nbf;
+  const bool local = (a.force_local & kForceLocal) != 0, sink = (a.force_local & kForceSink) != 0;
+  int64_t n_cand = local ? min(nbf, nb - 1) : nbf;
   if (n_cand < 0) n_cand = 0;
-  const int64_t forced = (a.force_local && nb > 0) ? nb - 1 : -1;
+  const int64_t forced = (local && nb > 0) ? nb - 1 : -1;
+  const int skip = (sink && n_cand > 0) ? 1 : 0;  // attention sink: block 0 kept, not scored
+  const int keep0 = (sink && nb > 0 && forced != 0) ? 1 : 0;
   const int64_t r0 = static_cast<int64_t>(rank) * a.chunk;
   const int rows = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(a.chunk), n_cand - r0)));
   const int n_st = (rows + kStRowsPerStage - 1) / kStRowsPerStage;
@@ -180,7 +183,8 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
       if (c == 0) {
         const int i0 = 16 * warp + g, i1 = i0 + 8;
         const int base = st * kStRowsPerStage;
-        if (i0 < n) keys[base + i0] = sel_key(sacc[0] + sacc[1], static_cast<int>(r0 + base + i0));
+        if (i0 < n)
+          keys[base + i0] = (skip && r0 + base + i0 == 0) ? 0ull : sel_key(sacc[0] + sacc[1], static_cast<int>(r0 + base + i0));
         if (i1 < n) keys[base + i1] = sel_key(sacc[2] + sacc[3], static_cast<int>(r0 + base + i1));
       }
       __syncwarp();
@@ -230,7 +234,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   __syncthreads();
   const uint64_t* mine = block_merge_lists(lists, tmp, kStWarps);
   if (tid < 64) xlist[tid] = mine[tid];
-  const int kk = static_cast<int>(n_cand < a.k_scored ? n_cand : static_cast<int64_t>(a.k_scored));
+  const int kk = static_cast<int>(n_cand - skip < a.k_scored ? n_cand - skip : static_cast<int64_t>(a.k_scored));
   // (b) every CTA of the cluster gathers the C lists through distributed
   // shared memory and merges them the same way, so each one holds the same
   // top 64 of the unit without a second cluster barrier. xlist is never
@@ -283,17 +287,21 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   __syncthreads();
   // (c) the unit's list: kk blocks ascending, then the forced block, then -1.
   // The leader writes it out; every CTA takes its slice.
+  // (block 0 leads when it is kept as the attention sink)
+  auto list_at = [&](int i) -> int32_t {
+    const int j = i - keep0;
+    return j < 0 ? 0 : j < kk ? sorted_blocks[j] : (j == kk && forced >= 0 ? static_cast<int32_t>(forced) : -1);
+  };
   if (rank == 0) {
     int32_t* out = a.idx_out + unit * a.k_total;
-    for (int i = tid; i < a.k_total; i += blockDim.x)
-      out[i] = i < kk ? sorted_blocks[i] : (i == kk && forced >= 0 ? static_cast<int>(forced) : -1);
+    for (int i = tid; i < a.k_total; i += blockDim.x) out[i] = list_at(i);
   }
   if (warp == 0) {
     const int lo = rank * a.bps, hi = min(a.k_total, lo + a.bps);
     int n = 0;
     for (int b0 = lo; b0 < hi; b0 += 32) {
       const int i = b0 + lane;
-      const int32_t b = i >= hi ? -1 : i < kk ? sorted_blocks[i] : (i == kk && forced >= 0 ? static_cast<int>(forced) : -1);
+      const int32_t b = i >= hi ? -1 : list_at(i);
       if (b >= nb) set_status(a.status, MSA_ERR_DEVICE_BOUNDS, kIdDecode);
       const bool ok = b >= 0 && b < nb;
       const unsigned m = __ballot_sync(0xffffffffu, ok);

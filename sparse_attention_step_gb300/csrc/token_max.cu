@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __gri
   const int64_t len = kv.seq_len(s, a.status, kIdScore);
   const int64_t nb = (len + kBlock - 1) / kBlock;
   const int64_t nbf = len / kBlock;
-  int64_t n_cand = a.force_local ? min(nbf, nb - 1) : nbf;
+  int64_t n_cand = (a.force_local & kForceLocal) ? min(nbf, nb - 1) : nbf;
   if (n_cand < 0) n_cand = 0;
   const int64_t b0 = static_cast<int64_t>(blockIdx.x) * a.chunk;
   if (b0 >= n_cand) return;

@@ -157,8 +157,8 @@ def kv_desc(k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor, page_table
 
 
 def select_cfg(k_scored: int, force_local: bool = True, q_tile: int = 1, q_start: int = 0,
-               mode: int = None) -> SelectCfg:
-    return SelectCfg(int(k_scored), 1 if force_local else 0, int(q_tile),
+               mode: int = None, sink: bool = False) -> SelectCfg:
+    return SelectCfg(int(k_scored), (1 if force_local else 0) | (2 if sink else 0), int(q_tile),
                      MSA_SCORE_MEAN_POOLED_KEYS if mode is None else int(mode), int(q_start))
 
 
