@@ -153,7 +153,7 @@ msa_status msa_pool_block_keys(const msa_kv_desc* kv /* host */, int64_t first_b
  *   q_idx = sum of the group's G query heads (fp32); candidates are the
  *   complete blocks, minus the newest block nb-1 (nb = ceil(seq_len/64)) when
  *   force_local. Output idx_out [batch, Hkv, k_total].
- * Prefill (cfg->q_tile == 64, batch 1): q [n_q_tokens, Hq, 128]; unit =
+ * Prefill (cfg->q_tile == 64, batch 1, contiguous or paged cache): q [n_q_tokens, Hq, 128]; unit =
  *   (tile j, KV head); q_idx = sum over the tile's tokens and the group's
  *   heads; candidates are the blocks before the diagonal block
  *   q_start/64 + j. Output idx_out [ceil(n_q_tokens/64), Hkv, k_total].
@@ -191,7 +191,8 @@ msa_status msa_sparse_attn_decode(const void* q, int32_t num_q_heads, const msa_
                                   float* lse, void* ws, size_t ws_bytes, msa_stream_t stream);
 
 /* Step 2, chunked prefill (guide §1, Step 2, and §3: during prefill the
- * savings fall on the main attention). Batch 1; query token r sits at
+ * savings fall on the main attention). Batch 1, bf16, contiguous or paged
+ * cache (q_start + n_q_tokens within its capacity); query token r sits at
  * absolute position p = q_start + r and attends to the tokens t <= p of the
  * blocks idx[r / 64, h, :] (idx from msa_select_topk_blocks with q_tile 64).
  * At most 512 entries of a list may be valid blocks (-1 padding is free); a

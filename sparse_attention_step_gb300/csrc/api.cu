@@ -257,9 +257,9 @@ msa_status prefill_common(const void* q, int hq, int n_q_tokens, int64_t q_start
   if (q == nullptr || out == nullptr || n_q_tokens <= 0 || q_start < 0) return MSA_ERR_INVALID_ARG;
   if (idx != nullptr && k_total <= 0) return MSA_ERR_INVALID_ARG;
   if (!(scale > 0.f)) return MSA_ERR_INVALID_ARG;
-  if (kv->batch != 1 || kv->layout != MSA_KV_CONTIGUOUS || kv->dtype != MSA_DTYPE_BF16) return MSA_ERR_UNSUPPORTED;
+  if (kv->batch != 1 || kv->dtype != MSA_DTYPE_BF16) return MSA_ERR_UNSUPPORTED;
   if (q_start % kBlock != 0) return MSA_ERR_UNSUPPORTED;
-  if (q_start + n_q_tokens > kv->max_tokens) return MSA_ERR_INVALID_ARG;
+  if (q_start + n_q_tokens > kv_max_blocks(kv) * kBlock) return MSA_ERR_INVALID_ARG;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != MSA_OK) return st;
   if ((st = check_ws(ws, ws_bytes, kWsHeader)) != MSA_OK) return st;
@@ -371,8 +371,7 @@ msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_
   if (prefill) {
     if (kv->batch != 1 || n_q_tokens <= 0 || cfg->q_start < 0) return MSA_ERR_INVALID_ARG;
     if (cfg->q_start % kBlock != 0) return MSA_ERR_UNSUPPORTED;
-    if (kv->layout != MSA_KV_CONTIGUOUS) return MSA_ERR_UNSUPPORTED;
-    if (cfg->q_start + n_q_tokens > kv->max_tokens) return MSA_ERR_INVALID_ARG;
+    if (cfg->q_start + n_q_tokens > kv_max_blocks(kv) * kBlock) return MSA_ERR_INVALID_ARG;
   } else if (n_q_tokens != 1 && n_q_tokens != kv->batch) {
     return MSA_ERR_INVALID_ARG;
   }

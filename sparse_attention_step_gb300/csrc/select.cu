@@ -203,6 +203,7 @@ __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __r
                                                                 KvView kv, ScoreArgs a, float* __restrict__ scores,
                                                                 int32_t* status) {
   __shared__ __align__(1024) uint8_t rows_s[kPsRows * kHeadDim * 2];
+  __shared__ uint8_t bad[kPsRows];  // rows whose page id is out of range
   const int h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.z * kPsTiles;
   const int64_t chunk0 = static_cast<int64_t>(blockIdx.x) * kPsRows;
@@ -216,11 +217,15 @@ __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __r
     const int j = tid + 256 * u;
     const int row = j >> 4, pc = j & 15;
     const int64_t b = chunk0 + row;
+    bool miss = false;
     if (b < n_max && b < row_end) {
-      const int64_t prow = kv.pooled_row(0, h, b, status, kIdScore);
-      cp_async16(rows_s + (pc >> 3) * (kPsRows * 128) + row * 128 + (((pc & 7) ^ (row & 7)) << 4),
-                 pooled + prow * kHeadDim + 8 * pc);
+      const int64_t prow = kv.pooled_row(0, h, b, pc == 0 ? status : nullptr, kIdScore);
+      miss = prow < 0;
+      if (!miss)
+        cp_async16(rows_s + (pc >> 3) * (kPsRows * 128) + row * 128 + (((pc & 7) ^ (row & 7)) << 4),
+                   pooled + prow * kHeadDim + 8 * pc);
     }
+    if (pc == 0) bad[row] = miss ? 1 : 0;
   }
   cp_async_commit();
   // B operands: column g = tile t0 + g
@@ -260,7 +265,8 @@ __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __r
     const int tile = t0 + 2 * c + (k & 1);
     if (b < row_end && tile < a.n_tiles) {
       const int64_t n_cand = a.q_start / kBlock + tile;
-      scores[(static_cast<int64_t>(tile) * a.hkv + h) * a.max_blocks + b] = b < n_cand ? hi[k] + lo[k] : -INFINITY;
+      const bool ok = b < n_cand && !bad[b - chunk0];
+      scores[(static_cast<int64_t>(tile) * a.hkv + h) * a.max_blocks + b] = ok ? hi[k] + lo[k] : -INFINITY;
     }
   }
 }

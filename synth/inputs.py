@@ -217,7 +217,7 @@ def make_index_keys(inp: DecodeInputs, needles: int = 0, seed: int = 0) -> Index
 @dataclasses.dataclass
 class PrefillInputs:
     q: torch.Tensor        # [N, Hq, D] new query tokens
-    k: torch.Tensor        # [1, Hkv, T, D] contiguous cache holding prefix + new tokens
+    k: torch.Tensor        # contiguous [1, Hkv, T, D] or paged [P, Hkv, 64, D]: prefix + new tokens
     v: torch.Tensor
     seq_lens: torch.Tensor  # int32 [1] = q_start + N
     q_start: int
@@ -225,24 +225,44 @@ class PrefillInputs:
     num_kv_heads: int
     num_q_heads: int
     dtype: str
+    layout: str = "contiguous"
+    page_table: torch.Tensor | None = None  # int32 [1, pages] (paged)
+
+    def kv_rows(self, h: int, which: str = "k") -> torch.Tensor:
+        """[capacity, D] rows of KV head h in logical token order."""
+        t = self.k if which == "k" else self.v
+        if self.layout == "contiguous":
+            return t[0, h]
+        pages = self.page_table[0].long()
+        return t[pages, h].reshape(pages.numel() * BLOCK, t.shape[-1])
 
 
 def make_prefill_inputs(prefix: int, n_new: int, num_kv_heads: int, num_q_heads: int,
                         dtype: str = "bf16", seed: int = 0, device="cpu",
-                        max_tokens: int | None = None) -> PrefillInputs:
-    """A chunk of ``n_new`` query tokens appended to a ``prefix``-token cache."""
+                        max_tokens: int | None = None, layout: str = "contiguous") -> PrefillInputs:
+    """A chunk of ``n_new`` query tokens appended to a ``prefix``-token cache
+    (contiguous, or paged with a shuffled page table)."""
     total = prefix + n_new
     cap = max_tokens if max_tokens is not None else -(-total // BLOCK) * BLOCK
     tdt = torch_dtype(dtype)
     q = torch.empty(n_new, num_q_heads, HEAD_DIM, dtype=tdt, device=device)
-    k = torch.empty(1, num_kv_heads, cap, HEAD_DIM, dtype=tdt, device=device)
+    page_table = None
+    if layout == "contiguous":
+        k = torch.empty(1, num_kv_heads, cap, HEAD_DIM, dtype=tdt, device=device)
+    elif layout == "paged":
+        pages = cap // BLOCK
+        perm = np.random.default_rng([int(seed), _S_PAGES]).permutation(pages).astype(np.int32)
+        page_table = torch.from_numpy(perm.reshape(1, pages)).to(device)
+        k = torch.empty(pages, num_kv_heads, BLOCK, HEAD_DIM, dtype=tdt, device=device)
+    else:
+        raise ValueError(layout)
     v = torch.empty_like(k)
     _randn_into(q, _gen(seed, _S_Q, device))
     _randn_into(k, _gen(seed, _S_K, device))
     _randn_into(v, _gen(seed, _S_V, device))
     return PrefillInputs(q=q, k=k, v=v, seq_lens=torch.tensor([total], dtype=torch.int32, device=device),
                          q_start=prefix, n_new=n_new, num_kv_heads=num_kv_heads,
-                         num_q_heads=num_q_heads, dtype=dtype)
+                         num_q_heads=num_q_heads, dtype=dtype, layout=layout, page_table=page_table)
 
 
 # ---------------------------------------------------------------------------

@@ -20,7 +20,7 @@ def dev(lib):
 def run_prefill(inp, k_scored, k_total, dense=False, sparse=True):
     from sparse_attention_step_gb300 import msa
     dev = inp.q.device
-    desc = msa.kv_desc(inp.k, inp.v, inp.seq_lens)
+    desc = msa.kv_desc(inp.k, inp.v, inp.seq_lens, inp.page_table)
     hq, n = inp.num_q_heads, inp.n_new
     n_tiles = (n + 63) // 64
     need = max(msa.msa_workspace_size(msa.MSA_OP_SELECT_PREFILL, desc, hq, n, k_total),
@@ -28,7 +28,8 @@ def run_prefill(inp, k_scored, k_total, dense=False, sparse=True):
     ws = msa.Workspace(need, dev)
     pooled = torch.full(msa.pooled_shape(desc), float("nan"), dtype=inp.k.dtype, device=dev)
     idx = torch.full((n_tiles, inp.num_kv_heads, k_total), -7, dtype=torch.int32, device=dev)
-    scores = torch.empty(n_tiles * inp.num_kv_heads, desc.max_tokens // 64, dtype=torch.float32, device=dev)
+    max_blocks = desc.max_tokens // 64 if desc.layout == 0 else desc.max_pages_per_seq
+    scores = torch.empty(n_tiles * inp.num_kv_heads, max_blocks, dtype=torch.float32, device=dev)
     out = torch.full_like(inp.q, float("nan"))
     lse = torch.full((n, hq), float("nan"), dtype=torch.float32, device=dev)
     msa.msa_pool_block_keys(desc, 0, -1, pooled, ws.buf, ws.nbytes)
@@ -53,10 +54,14 @@ def verify_tiles(inp, res, tiles, heads, k_scored, k_total, rows_per_tile=None, 
     grp = inp.num_q_heads // inp.num_kv_heads
     total = inp.q_start + inp.n_new
     for h in heads:
-        kr = to64(inp.k[0, h])
-        vr = to64(inp.v[0, h])
+        kr = to64(inp.kv_rows(h, "k"))
+        vr = to64(inp.kv_rows(h, "v"))
         pooled, _ = O.pool_block_keys(kr, total, inp.dtype)
-        assert np.array_equal(to64(res["pooled"][0, h, :total // 64]), pooled), f"pooled keys differ, head {h}"
+        if inp.layout == "contiguous":
+            got_pool = res["pooled"][0, h, :total // 64]
+        else:
+            got_pool = res["pooled"][inp.page_table[0, :total // 64].long(), h]
+        assert np.array_equal(to64(got_pool), pooled), f"pooled keys differ, head {h}"
         for j in tiles:
             r0, r1 = 64 * j, min(inp.n_new, 64 * j + 64)
             q_tile = to64(inp.q[r0:r1, h * grp:(h + 1) * grp])
@@ -86,6 +91,16 @@ def test_prefill_small(dev, hq, hkv):
     assert res["status"] == 0
     n_tiles = (inp.n_new + 63) // 64
     verify_tiles(inp, res, range(n_tiles), range(hkv), 4, 5, check_dense=True)
+
+
+@pytest.mark.parametrize("hq,hkv", [(64, 8), (16, 4)])
+def test_prefill_paged_cache(dev, hq, hkv):
+    # the same chunked prefill over a paged cache (shuffled pages), tcgen05 and mma.sync kernels
+    inp = make_prefill_inputs(64 * 37, 64 * 3 + 21, hkv, hq, "bf16", seed=71, device=dev, layout="paged")
+    res = run_prefill(inp, 6, 7, dense=True)
+    assert res["status"] == 0
+    n_tiles = (inp.n_new + 63) // 64
+    verify_tiles(inp, res, range(n_tiles), range(hkv), 6, 7, rows_per_tile=9, check_dense=True)
 
 
 def test_prefill_all_blocks_equals_dense(dev):
