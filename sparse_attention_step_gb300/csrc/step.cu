@@ -88,19 +88,41 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   const int64_t unit = static_cast<int64_t>(s) * a.hkv + h;
   const int64_t max_blocks = kv.max_tokens / kBlock;
 
-  if (tid == 0) {
+  // The producer sets up the ring and, as soon as the inputs are ready, starts
+  // streaming the first stages of its chunk: their rows do not depend on the
+  // sequence length, which is read meanwhile (stages past the candidates are
+  // drained unread).
+  const int n_pre = min(kStages, (a.chunk + kStRowsPerStage - 1) / kStRowsPerStage);
+  const int32_t y0 = static_cast<int32_t>(unit * max_blocks + static_cast<int64_t>(rank) * a.chunk);
+  if (warp == kStWarps && lane == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kStWarps);
     }
     fence_mbar_init();
-  }
-  if (warp == kStWarps && lane == 0) {
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
     tma_prefetch_desc(&tmpool);
+    pdl_wait();
+    for (int st = 0; st < n_pre; ++st) {
+      uint8_t* dst = ring + st * kStStage;
+      mbar_arrive_expect_tx(&full[st], kStStage);
+      tma_load_2d(dst, &tmpool, 0, y0 + st * kStRowsPerStage, &full[st]);
+      tma_load_2d(dst + kStStage / 2, &tmpool, 64, y0 + st * kStRowsPerStage, &full[st]);
+    }
   }
   pdl_wait();
+  if (tid < kHeadDim) {
+    // all G loads in flight at once, then summed in head order
+    const __nv_bfloat16* qg = a.q + (static_cast<int64_t>(s) * a.hq + h * a.grp) * kHeadDim + tid;
+    float x[kStG];
+#pragma unroll
+    for (int g = 0; g < kStG; ++g) x[g] = g < a.grp ? __bfloat162float(qg[g * kHeadDim]) : 0.f;
+    float acc = 0.f;
+#pragma unroll
+    for (int g = 0; g < kStG; ++g) acc += x[g];
+    qsum[tid] = acc;
+  }
   const int64_t len = kv.seq_len(s, a.status, kIdDecode);
   const int64_t nb = (len + kBlock - 1) / kBlock;
   const int64_t nbf = len / kBlock;
@@ -113,17 +135,6 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   const int64_t r0 = static_cast<int64_t>(rank) * a.chunk;
   const int rows = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(a.chunk), n_cand - r0)));
   const int n_st = (rows + kStRowsPerStage - 1) / kStRowsPerStage;
-  if (tid < kHeadDim) {
-    // all G loads in flight at once, then summed in head order
-    const __nv_bfloat16* qg = a.q + (static_cast<int64_t>(s) * a.hq + h * a.grp) * kHeadDim + tid;
-    float x[kStG];
-#pragma unroll
-    for (int g = 0; g < kStG; ++g) x[g] = g < a.grp ? __bfloat162float(qg[g * kHeadDim]) : 0.f;
-    float acc = 0.f;
-#pragma unroll
-    for (int g = 0; g < kStG; ++g) acc += x[g];
-    qsum[tid] = acc;
-  }
   if (rank == 0 && warp == kStWarps && lane >= 28 && forced >= 0) {
     // the newest block is always attended: pull it into L2 during scoring
     const int64_t row = kv.block_row(s, h, forced, a.status, kIdDecode);
@@ -136,8 +147,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     if (lane == 0) {
       // 128 summary rows per stage as two 64-column boxes (128-byte swizzle);
       // rows past the CTA's chunk are loaded but never scored
-      const int32_t y0 = static_cast<int32_t>(unit * max_blocks + r0);
-      for (int st = 0; st < n_st; ++st) {
+      for (int st = n_pre; st < n_st; ++st) {
         const int slot = st % kStages;
         if (st >= kStages && !mbar_wait(&empty[slot], ((st / kStages) - 1) & 1, a.status, kIdDecode)) break;
         uint8_t* dst = ring + slot * kStStage;
@@ -145,6 +155,8 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
         tma_load_2d(dst, &tmpool, 0, y0 + st * kStRowsPerStage, &full[slot]);
         tma_load_2d(dst + kStStage / 2, &tmpool, 64, y0 + st * kStRowsPerStage, &full[slot]);
       }
+      // early stages beyond this chunk's candidates: wait until they land
+      for (int st = n_st; st < n_pre; ++st) mbar_wait(&full[st], 0, a.status, kIdDecode);
     }
   } else {
     // S = K_pool q_idx on the tensor cores, warp w taking rows 16w..16w+15 of
