@@ -18,8 +18,7 @@ struct DeviceInfo {
   bool ready = false;
   int num_sms = 0;
   size_t topk_smem = 0;
-  int step_clusters[5] = {0, 0, 0, 0, 0};       // co-resident fused-step clusters of 1, 2, 4, 8, 16 CTAs
-  int step_clusters_wide[5] = {0, 0, 0, 0, 0};  // the same for the 6-stage (one CTA per SM) kernel
+  int step_clusters[5] = {0, 0, 0, 0, 0};  // co-resident fused-step clusters of 1, 2, 4, 8, 16 CTAs
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -37,10 +36,7 @@ msa_status device_info(DeviceInfo** out) {
     if (set_prefill_tc_smem() != cudaSuccess) return MSA_ERR_CUDA;
     if (set_step_smem() != cudaSuccess) return MSA_ERR_CUDA;
     if (set_token_max_smem() != cudaSuccess) return MSA_ERR_CUDA;
-    for (int i = 0; i < 5; ++i) {
-      d.step_clusters[i] = step_max_clusters(1 << i, false);
-      d.step_clusters_wide[i] = step_max_clusters(1 << i, true);
-    }
+    for (int i = 0; i < 5; ++i) d.step_clusters[i] = step_max_clusters(1 << i);
     d.topk_smem = (kMaxTopkCandidates + kTopkCandCap) * sizeof(uint32_t);
     if (set_topk_smem(d.topk_smem) != cudaSuccess) return MSA_ERR_CUDA;
     if (set_select_decode_smem(select_decode_smem(4096)) != cudaSuccess) return MSA_ERR_CUDA;
@@ -459,13 +455,12 @@ msa_status decode_step_common(const void* q, int32_t num_q_heads, const void* po
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != MSA_OK) return st;
   int C = 0, chunk = 0, bps = 0;
-  bool wide = false;
   const int64_t units = static_cast<int64_t>(kv->batch) * kv->num_kv_heads;
   const bool fused = kv->dtype == MSA_DTYPE_BF16 && kv->layout == MSA_KV_CONTIGUOUS &&
                      cfg->mode == MSA_SCORE_MEAN_POOLED_KEYS && cfg->k_scored >= 0 &&
                      k_total >= std::min<int64_t>(cfg->k_scored, kv_max_blocks(kv)) + forced_count(cfg) &&
-                     step_shape(units, kv_max_blocks(kv), cfg->k_scored, k_total, dev->num_sms, dev->step_clusters,
-                                dev->step_clusters_wide, &C, &chunk, &bps, &wide);
+                     step_shape(units, kv_max_blocks(kv), cfg->k_scored, k_total, dev->num_sms, dev->step_clusters, &C,
+                                &chunk, &bps);
   if (!fused) {
     // the same step as two launches (plus the pooling of just-filled blocks)
     st = msa_select_topk_blocks(q, num_q_heads, 1, pooled, kv, cfg, idx_out, k_total, nullptr, ws, ws_bytes, stream);
@@ -488,7 +483,7 @@ msa_status decode_step_common(const void* q, int32_t num_q_heads, const void* po
   if ((st = make_kv_map(&tmv, kv->v, rows)) != MSA_OK) return st;
   if ((st = make_kv_map(&tmp, pooled, units * kv_max_blocks(kv), 128)) != MSA_OK) return st;
   return cuda_status(launch_decode_step(tmk, tmv, tmp, view_of(kv), kv->batch, static_cast<const __nv_bfloat16*>(q),
-                                        num_q_heads, *cfg, k_total, C, chunk, bps, wide, scale * kLog2e, idx_out,
+                                        num_q_heads, *cfg, k_total, C, chunk, bps, scale * kLog2e, idx_out,
                                         static_cast<__nv_bfloat16*>(out), lse, ws_status(ws),
                                         static_cast<const __nv_bfloat16*>(kv->k),
                                         static_cast<__nv_bfloat16*>(pooled_update),

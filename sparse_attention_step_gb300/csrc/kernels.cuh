@@ -79,8 +79,8 @@ cudaError_t launch_prefill_bf16(const CUtensorMap& tmk, const CUtensorMap& tmv, 
 
 // ---- fused decode step (step.cu) ----
 bool step_shape(int64_t units, int64_t max_blocks, int k_scored, int k_total, int num_sms, const int* max_clusters,
-                const int* max_clusters_wide, int* C, int* chunk, int* bps, bool* wide);
-int step_max_clusters(int C, bool wide);
+                int* C, int* chunk, int* bps);
+int step_max_clusters(int C);
 cudaError_t set_step_smem();
 
 // ---- token-level max-pooled scores (token_max.cu) ----
@@ -91,7 +91,7 @@ cudaError_t launch_topk_scores(const float* scores, const KvView& kv, int batch,
                                int32_t* idx_out, int k_total, int32_t* status, cudaStream_t stream);
 cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmpool,
                                const KvView& kv, int batch, const __nv_bfloat16* q, int hq, const msa_select_cfg& cfg,
-                               int k_total, int C, int chunk, int bps, bool wide, float scale_log2,
+                               int k_total, int C, int chunk, int bps, float scale_log2,
                                int32_t* idx_out, __nv_bfloat16* out, float* lse, int32_t* status,
                                const __nv_bfloat16* k, __nv_bfloat16* pooled_out, cudaStream_t stream);
 

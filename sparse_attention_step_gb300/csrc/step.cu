@@ -36,8 +36,7 @@ namespace {
 constexpr int kStWarps = 8;                     // compute warps
 constexpr int kStAttnWarps = 4;                 // warps that consume attention blocks
 constexpr int kStThreads = 32 * (kStWarps + 1);  // + producer warp
-constexpr int kStStages = 3;                    // ring depth with two CTAs per SM
-constexpr int kStStagesWide = 6;                // ring depth when the grid fits one CTA per SM
+constexpr int kStStages = 3;                    // ring depth (two CTAs per SM)
 constexpr int kStStage = 32768;
 constexpr int kStRowsPerStage = kStStage / (kHeadDim * 2);  // 128 bf16 summary rows
 constexpr int kStMaxChunk = 1024;                           // candidate rows per CTA
@@ -567,11 +566,9 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
 // units x C within two resident CTAs per SM and, where max_clusters is given
 // (the device's co-resident cluster count for C = 1, 2, 4, 8, 16), every
 // unit's cluster resident at once; chunk = ceil(max_blocks / C) rounded up to
-// 128 rows (<= 1024), and ceil(k_total / C) <= 64 list entries. *wide: the
-// grid fits one CTA per SM (and, per max_clusters_wide, every cluster of the
-// deeper-ring kernel is resident), so the 6-stage ring is used.
+// 128 rows (<= 1024), and ceil(k_total / C) <= 64 list entries.
 bool step_shape(int64_t units, int64_t max_blocks, int k_scored, int k_total, int num_sms, const int* max_clusters,
-                const int* max_clusters_wide, int* C, int* chunk, int* bps, bool* wide) {
+                int* C, int* chunk, int* bps) {
   if (k_scored > 64) return false;
   const int64_t slots = 2LL * num_sms;
   int c = 1, lg = 0;
@@ -589,7 +586,6 @@ bool step_shape(int64_t units, int64_t max_blocks, int k_scored, int k_total, in
   *C = c;
   *chunk = static_cast<int>(ch);
   *bps = (k_total + c - 1) / c;
-  *wide = units * c <= num_sms && (max_clusters_wide == nullptr || units <= max_clusters_wide[lg]);
   return true;
 }
 
@@ -630,21 +626,14 @@ cudaError_t set_smem_of() {
 }  // namespace
 
 // How many clusters of C fused-step CTAs the current device keeps resident
-// at once, for the 3-stage (wide = false) or 6-stage kernel (0 if the query
-// fails). Needs set_step_smem() first.
-int step_max_clusters(int C, bool wide) {
-  return wide ? max_clusters_of<kStStagesWide>(C) : max_clusters_of<kStStages>(C);
-}
+// at once (0 if the query fails). Needs set_step_smem() first.
+int step_max_clusters(int C) { return max_clusters_of<kStStages>(C); }
 
-cudaError_t set_step_smem() {
-  cudaError_t e = set_smem_of<kStStages>();
-  if (e != cudaSuccess) return e;
-  return set_smem_of<kStStagesWide>();
-}
+cudaError_t set_step_smem() { return set_smem_of<kStStages>(); }
 
 cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmpool,
                                const KvView& kv, int batch, const __nv_bfloat16* q, int hq, const msa_select_cfg& cfg,
-                               int k_total, int C, int chunk, int bps, bool wide, float scale_log2,
+                               int k_total, int C, int chunk, int bps, float scale_log2,
                                int32_t* idx_out, __nv_bfloat16* out, float* lse, int32_t* status,
                                const __nv_bfloat16* k, __nv_bfloat16* pooled_out, cudaStream_t stream) {
   StepArgs a;
@@ -667,7 +656,7 @@ cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, c
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(C, kv.hkv, batch);
   lc.blockDim = dim3(kStThreads, 1, 1);
-  lc.dynamicSmemBytes = step_smem(wide ? kStStagesWide : kStStages);
+  lc.dynamicSmemBytes = step_smem(kStStages);
   lc.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -678,7 +667,6 @@ cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, c
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 2;
-  if (wide) return cudaLaunchKernelEx(&lc, decode_step_kernel<kStStagesWide>, tmk, tmv, tmpool, kv, a);
   return cudaLaunchKernelEx(&lc, decode_step_kernel<kStStages>, tmk, tmv, tmpool, kv, a);
 }
 
