@@ -23,6 +23,14 @@ struct RawRow<__nv_bfloat16> {
     }
     return acc;
   }
+  __device__ void add_to(float (&acc)[8]) const {
+    const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] += __uint_as_float(v[i] << 16);
+      acc[2 * i + 1] += __uint_as_float(v[i] & 0xFFFF0000u);
+    }
+  }
 };
 template <>
 struct RawRow<float> {
@@ -36,6 +44,10 @@ struct RawRow<float> {
     acc = fmaf(qi[0], a.x, acc); acc = fmaf(qi[1], a.y, acc); acc = fmaf(qi[2], a.z, acc); acc = fmaf(qi[3], a.w, acc);
     acc = fmaf(qi[4], b.x, acc); acc = fmaf(qi[5], b.y, acc); acc = fmaf(qi[6], b.z, acc); acc = fmaf(qi[7], b.w, acc);
     return acc;
+  }
+  __device__ void add_to(float (&acc)[8]) const {
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
   }
 };
 

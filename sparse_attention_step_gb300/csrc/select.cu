@@ -46,22 +46,17 @@ __global__ void __launch_bounds__(256) qidx_prefill_kernel(const T* __restrict__
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   for (int i0 = slot; i0 < n_rows; i0 += 16 * 8) {
-    float x[8][8];
+    RawRow<T> x[8];  // raw 16-byte pieces: few registers per row in flight
+    bool have[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int i = i0 + 16 * u;
-      if (i < n_rows) {
-        const T* row = q + (static_cast<int64_t>(r0 + i / grp) * hq + h * grp + i % grp) * kHeadDim + 8 * e;
-        load8<T>(row, x[u]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) x[u][j] = 0.f;
-      }
+      have[u] = i < n_rows;
+      if (have[u]) x[u].load(q + (static_cast<int64_t>(r0 + i / grp) * hq + h * grp + i % grp) * kHeadDim + 8 * e);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] += x[u][j];
+      if (have[u]) x[u].add_to(acc);
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) part[slot][8 * e + j] = acc[j];
