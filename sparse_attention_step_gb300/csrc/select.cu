@@ -270,6 +270,9 @@ __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __r
 // Top-k. grid (Hkv, outer) with outer = batch (decode) or n_tiles (prefill).
 // ---------------------------------------------------------------------------
 constexpr int kTopkThreads = 1024;
+// Threads per top-k CTA: a quarter CTA while a unit has at most 4096
+// candidates (fewer, cheaper barriers; four CTAs share an SM), else 1024.
+inline int topk_threads(int64_t max_blocks) { return max_blocks <= 4096 ? 256 : kTopkThreads; }
 
 // Inclusive block-wide scan of one int per thread; returns the inclusive
 // value; *total gets the block sum. Uses `tmp` (>= 33 ints of shared memory).
@@ -315,9 +318,9 @@ constexpr int kCandCap = 8192;  // keys of the threshold bin refined in shared m
 
 // Finds, among `nbins` counts in shared memory (bin index increasing with the
 // key), the bin holding the k-th largest element: *bin and *above (the count
-// in higher bins). Each of the 1024 threads owns nbins/1024 consecutive bins.
+// in higher bins). Each thread owns nbins / blockDim.x consecutive bins.
 __device__ inline void find_kth_bin(const int* cnt, int nbins, int k, int* scan_tmp, int* out_bin, int* out_above) {
-  const int per = nbins / kTopkThreads;
+  const int per = nbins / blockDim.x;
   const int lo = threadIdx.x * per;
   int own = 0;
   for (int j = 0; j < per; ++j) own += cnt[lo + j];
@@ -886,7 +889,7 @@ cudaError_t launch_select(const T* q, int hq, int n_q_tokens, const T* pooled, c
   if (err != cudaSuccess) return err;
   TopkArgs ta{kv.hkv, prefill, cfg.force_local, cfg.k_scored, k_total, cfg.q_start, max_blocks};
   const size_t smem = static_cast<size_t>(max_blocks + kCandCap) * sizeof(uint32_t);
-  topk_kernel<<<dim3(kv.hkv, outer), kTopkThreads, smem, stream>>>(scores, kv, ta, idx_out, status);
+  topk_kernel<<<dim3(kv.hkv, outer), topk_threads(max_blocks), smem, stream>>>(scores, kv, ta, idx_out, status);
   return cudaGetLastError();
 }
 
@@ -896,7 +899,7 @@ cudaError_t launch_topk_scores(const float* scores, const KvView& kv, int batch,
   const int64_t max_blocks = kv.max_blocks();
   TopkArgs ta{kv.hkv, 0, cfg.force_local, cfg.k_scored, k_total, 0, max_blocks};
   const size_t smem = static_cast<size_t>(max_blocks + kCandCap) * sizeof(uint32_t);
-  topk_kernel<<<dim3(kv.hkv, batch), kTopkThreads, smem, stream>>>(scores, kv, ta, idx_out, status);
+  topk_kernel<<<dim3(kv.hkv, batch), topk_threads(max_blocks), smem, stream>>>(scores, kv, ta, idx_out, status);
   return cudaGetLastError();
 }
 
