@@ -6,22 +6,24 @@
 // the 8 heads of the group, as two M = 128 tiles (rows token-major,
 // head-minor). For every selected 64-key block:
 //   S_t = Q_t K^T      tcgen05.mma M128 N64 K16 x 8, bf16 -> fp32 in TMEM
-//   softmax            one thread per row: tcgen05.ld of its 64 scores, causal
-//                      mask on the diagonal block, online max with lazy
-//                      rescaling (O is rescaled in TMEM only when the running
-//                      max grows by more than 2^8), exp2, P (bf16) written to
-//                      shared memory in the 128-byte-swizzled K-major layout
-//   O_t += P_t V       tcgen05.mma M128 N128 K16 x 4, V read MN-major
+//   softmax            tcgen05.ld of the scores, causal mask on the diagonal
+//                      block, online max with lazy rescaling (O is rescaled
+//                      in TMEM only when the running max grows by more than
+//                      2^8), exp2; P (bf16, two per 32-bit column) is stored
+//                      back over the scores it came from
+//   O_t += P_t V       tcgen05.mma M128 N128 K16 x 4 with A = P read from
+//                      TMEM and V read MN-major from shared memory
 // Warp roles: warps 0-7 softmax of tile 0 and warps 8-15 of tile 1; within a
 // tile, warps 0-3 take score columns 0-31 and warps 4-7 columns 32-63 of the
 // rows in TMEM lanes 32 (w mod 4) .. (a warp reaches only those lanes); the
 // two halves of a row exchange their maxima and sums through shared memory
 // (a named barrier per tile). Warp 16 is the TMA producer (Q once, then a
-// 3-stage K/V ring), warp 17 the TMEM allocator and MMA issuer. The two tiles
+// 4-stage K/V ring), warp 17 the TMEM allocator and MMA issuer. The two tiles
 // ping-pong: the tensor core runs one tile's MMAs while the other tile's
 // softmax runs, and S is double-buffered so S of the next block is computed
-// while the softmax of this one runs. TMEM: S of tile t in [128 t, 128 t +
-// 128) (two 64-column buffers), O_t in [256 + 128 t, 384 + 128 t).
+// while the softmax of this one runs (it is issued after O += P V of the block
+// two back, whose P shares its buffer). TMEM: S / P of tile t in
+// [128 t, 128 t + 128) (two 64-column buffers), O_t in [256 + 128 t, 384 + 128 t).
 #include <float.h>
 
 #include "kernels.cuh"
@@ -32,7 +34,7 @@ namespace msa {
 namespace {
 
 constexpr int kTcTiles = 2;
-constexpr int kTcStages = 3;
+constexpr int kTcStages = 4;
 constexpr int kSoftmaxWarps = 16;
 constexpr int kTcThreads = 32 * (kSoftmaxWarps + 2);
 constexpr int kProducerWarp = kSoftmaxWarps;
@@ -40,7 +42,6 @@ constexpr int kMmaWarp = kSoftmaxWarps + 1;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kQBytes = kTcTiles * 2 * 16384;   // two tiles x two 64-dim halves
 constexpr int kKVBytes = kTcStages * 32768;
-constexpr int kPBytes = kTcTiles * 16384;
 constexpr int kMaxList = 512;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 
@@ -59,7 +60,7 @@ struct TcTail {
   int32_t blocks[kMaxList];
 };
 
-constexpr size_t kTcSmem = 1024 + kQBytes + kKVBytes + kPBytes + sizeof(TcTail);
+constexpr size_t kTcSmem = 1024 + kQBytes + kKVBytes + sizeof(TcTail);
 
 __device__ inline float ex2_approx(float x) {
   float y;
@@ -107,8 +108,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qs = base;
   uint8_t* kvs = base + kQBytes;
-  uint8_t* ps = kvs + kKVBytes;
-  TcTail& st = *reinterpret_cast<TcTail*>(ps + kPBytes);
+  TcTail& st = *reinterpret_cast<TcTail*>(kvs + kKVBytes);
 
   const int rh = blockIdx.x, h = blockIdx.y, tile = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     if (lane == 0) {
       constexpr uint32_t kIdS = tc::idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t kIdO = tc::idesc_bf16(128, 128, 0, 1);
-      const uint32_t q_addr = smem_u32(qs), kv_addr = smem_u32(kvs), p_addr = smem_u32(ps);
+      const uint32_t q_addr = smem_u32(qs), kv_addr = smem_u32(kvs);
       auto issue_s = [&](int t, int buf, int stg) {
         const uint32_t d = tmem + t * 128 + buf * 64;
 #pragma unroll
@@ -210,13 +210,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
           tc::mma_ss(d, ad, bd, kIdS, kk > 0);
         }
       };
-      auto issue_pv = [&](int t, int stg, bool acc) {
+      // O_t += P V with P (bf16, packed in pairs) in the S buffer of its block
+      auto issue_pv = [&](int t, int buf, int stg, bool acc) {
         const uint32_t d = tmem + 256 + t * 128;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t ad = tc::sdesc_sw128(p_addr + t * 16384 + ks * 32, 16, 1024);
           const uint64_t bd = tc::sdesc_sw128(kv_addr + stg * 32768 + 16384 + ks * 2048, 8192, 1024);
-          tc::mma_ss(d, ad, bd, kIdO, (acc || ks > 0) ? 1u : 0u);
+          tc::mma_ts(d, tmem + t * 128 + buf * 64 + 8 * ks, bd, kIdO, (acc || ks > 0) ? 1u : 0u);
         }
       };
       // S_{i+1} of both tiles is issued before O += P_i V_i, into the other S
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         for (int t = 0; t < kTcTiles; ++t) {
           if (!(ok = wait_or_abort(&st.p_full[t], i & 1, abort, a.status))) break;
           tc::fence_after();
-          issue_pv(t, i % kTcStages, i > 0);
+          issue_pv(t, i & 1, i % kTcStages, i > 0);
           tc::commit(&st.pv_done[t]);
         }
         if (!ok) break;
@@ -267,7 +267,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     const int64_t tq = static_cast<int64_t>(tile) * kBlock + tt;  // token within the chunk
     const bool live = tq < a.n_q_tokens;
     float m = -INFINITY, l = 0.f;  // running max (log2 units) and this half's running sum
-    uint8_t* prow = ps + t * 16384 + r * 128;
     bool ok = true;
     // Every warp of the tile runs every iteration and every named barrier, even
     // after a wait gave up (then it skips the work), so no partner warp can be
@@ -348,18 +347,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       }
       const float2 acc = fadd2(acc0, acc1);
       const float sum = acc.x + acc.y;
-      wait_pv();
-#pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        uint4 v;
-        v.x = pk[4 * c8];
-        v.y = pk[4 * c8 + 1];
-        v.z = pk[4 * c8 + 2];
-        v.w = pk[4 * c8 + 3];
-        *reinterpret_cast<uint4*>(prow + (((4 * hf + c8) ^ (r & 7)) << 4)) = v;
+      // P replaces the scores it came from: columns [16 hf, 16 hf + 16) of
+      // this block's S buffer hold keys [32 hf, 32 hf + 32) in pairs. The
+      // next S into this buffer is issued after O += P V of this block.
+      if (ok) {
+        tc::st16(tmem + lane_base + t * 128 + (i & 1) * 64 + 16 * hf, pk);
+        tc::wait_st();
       }
       l += sum;
-      fence_proxy_async();  // P is read by the tensor core (async proxy)
       tc::fence_before();
       __syncwarp();
       if (lane == 0 && ok) mbar_arrive(&st.p_full[t]);
