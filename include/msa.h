@@ -119,7 +119,9 @@ typedef enum msa_op {
   MSA_OP_PREFILL = 3,
   MSA_OP_DENSE_DECODE = 4,
   MSA_OP_DENSE_PREFILL = 5,
-  MSA_OP_SELECT_PREFILL = 6, /* msa_select_topk_blocks with q_tile 64 */
+  MSA_OP_SELECT_PREFILL = 6, /* msa_select_topk_blocks with q_tile 64, and
+                                msa_select_topk_blocks_varlen with n_q_tokens =
+                                64 * sum over s of ceil(q_counts[s] / 64) */
   MSA_OP_DECODE_STEP = 7     /* msa_sparse_decode_step */
 } msa_op;
 
@@ -177,6 +179,27 @@ msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_
                                   const msa_select_cfg* cfg /* host */, int32_t* idx_out, int32_t k_total,
                                   float* scores_out, void* ws, size_t ws_bytes, msa_stream_t stream);
 
+/* Step 1b/1c for a batch of chunks (guide §1, Step 1, applied to the prefill
+ * chunk of every sequence of a batch at once): sequence s (n_seqs ==
+ * kv->batch, at most 64) has q_counts[s] >= 0 new tokens at absolute positions
+ * q_starts[s] + r (q_starts[s] a multiple of 64, q_starts[s] + q_counts[s]
+ * within the sequence's capacity; both arrays on the host). q holds the
+ * sequences' tokens back to back: [sum q_counts, Hq, 128], sequence s from row
+ * q_off[s] = q_counts[0] + ... + q_counts[s-1]. Its tiles j = 0 ..
+ * ceil(q_counts[s]/64) - 1 are numbered globally in the same order (tile_off[s]
+ * + j), and idx_out [total tiles, Hkv, k_total] gets, for global tile
+ * tile_off[s] + j, exactly what msa_select_topk_blocks (q_tile 64, q_start =
+ * q_starts[s]) gives for tile j of sequence s alone, scored against sequence
+ * s's summaries (pooled [batch, Hkv, max_blocks, 128] contiguous, or the
+ * cache's pages). cfg->q_tile must be 64 (cfg->q_start is ignored); fp32
+ * caches take one sequence only (MSA_ERR_UNSUPPORTED above), token-max mode is
+ * not supported. A batch with no new tokens queues nothing. */
+msa_status msa_select_topk_blocks_varlen(const void* q, int32_t num_q_heads, int32_t n_seqs,
+                                         const int64_t* q_starts /* host */, const int32_t* q_counts /* host */,
+                                         const void* pooled, const msa_kv_desc* kv /* host */,
+                                         const msa_select_cfg* cfg /* host */, int32_t* idx_out, int32_t k_total,
+                                         float* scores_out, void* ws, size_t ws_bytes, msa_stream_t stream);
+
 /* Step 2, decode (guide §1, Step 2: attention over the gathered selected
  * blocks; all heads of a group share the group's list).
  * For each sequence s and query head j (KV head h = j / G):
@@ -202,6 +225,20 @@ msa_status msa_sparse_attn_prefill(const void* q, int32_t num_q_heads, int32_t n
                                    const msa_kv_desc* kv /* host */, const int32_t* idx, int32_t k_total,
                                    float scale, void* out, float* lse, void* ws, size_t ws_bytes,
                                    msa_stream_t stream);
+
+/* Step 2 for a batch of chunks: msa_sparse_attn_prefill for every sequence s
+ * of the cache (n_seqs == kv->batch, at most 64) at once, in one launch. The
+ * sequences, q, out and lse are laid out as for msa_select_topk_blocks_varlen:
+ * tokens back to back (out [sum q_counts, Hq, 128], lse [sum q_counts, Hq]),
+ * idx [total tiles, Hkv, k_total] with global tile numbers; token r of
+ * sequence s sits at absolute position q_starts[s] + r and attends to the
+ * tokens t <= that position of sequence s's listed blocks. Results equal those
+ * of msa_sparse_attn_prefill on each sequence alone. */
+msa_status msa_sparse_attn_prefill_varlen(const void* q, int32_t num_q_heads, int32_t n_seqs,
+                                          const int64_t* q_starts /* host */, const int32_t* q_counts /* host */,
+                                          const msa_kv_desc* kv /* host */, const int32_t* idx, int32_t k_total,
+                                          float scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                                          msa_stream_t stream);
 
 /* One whole decode step (guide §1, Step 1 then Step 2): the index lists of
  * msa_select_topk_blocks (decode, cfg->q_tile == 1) written to idx_out, and

@@ -244,28 +244,47 @@ msa_status decode_common(const void* q, int hq, const msa_kv_desc* kv, const int
                                        kv->batch, a, stream));
 }
 
-msa_status prefill_common(const void* q, int hq, int n_q_tokens, int64_t q_start, const msa_kv_desc* kv,
+// Host checks of a chunk batch against the cache: sequence s's new tokens
+// [q_starts[s], q_starts[s] + q_counts[s]) start on a block boundary and fit
+// in its capacity. Fills *pb; *n_tokens gets the rows of q and out.
+msa_status build_batch(const msa_kv_desc* kv, int n_seqs, const int64_t* q_starts, const int32_t* q_counts,
+                       PrefillBatch* pb, int64_t* n_tokens) {
+  if (n_seqs != kv->batch || q_starts == nullptr || q_counts == nullptr) return MSA_ERR_INVALID_ARG;
+  if (n_seqs > kMaxPrefillSeqs) return MSA_ERR_UNSUPPORTED;
+  int64_t total = 0, tiles = 0;
+  const int64_t cap = kv_max_blocks(kv) * kBlock;
+  for (int s = 0; s < n_seqs; ++s) {
+    if (q_counts[s] < 0 || q_starts[s] < 0) return MSA_ERR_INVALID_ARG;
+    if (q_starts[s] % kBlock != 0) return MSA_ERR_UNSUPPORTED;
+    if (q_starts[s] + q_counts[s] > cap) return MSA_ERR_INVALID_ARG;
+    total += q_counts[s];
+    tiles += (q_counts[s] + kBlock - 1) / kBlock;
+  }
+  if (total >= (int64_t(1) << 31) || tiles > 65535) return MSA_ERR_UNSUPPORTED;
+  if (!make_prefill_batch(n_seqs, q_starts, q_counts, pb)) return MSA_ERR_INVALID_ARG;
+  *n_tokens = total;
+  return MSA_OK;
+}
+
+msa_status prefill_common(const void* q, int hq, const PrefillBatch& pb, int64_t n_tokens, const msa_kv_desc* kv,
                           const int32_t* idx, int k_total, float scale, void* out, float* lse, void* ws,
                           size_t ws_bytes, cudaStream_t stream) {
-  msa_status st = validate_kv(kv);
-  if (st != MSA_OK) return st;
+  msa_status st = MSA_OK;
   if ((st = check_q_heads(kv, hq)) != MSA_OK) return st;
-  if (q == nullptr || out == nullptr || n_q_tokens <= 0 || q_start < 0) return MSA_ERR_INVALID_ARG;
+  if (q == nullptr || out == nullptr) return MSA_ERR_INVALID_ARG;
   if (idx != nullptr && k_total <= 0) return MSA_ERR_INVALID_ARG;
   if (!(scale > 0.f)) return MSA_ERR_INVALID_ARG;
-  if (kv->batch != 1 || kv->dtype != MSA_DTYPE_BF16) return MSA_ERR_UNSUPPORTED;
-  if (q_start % kBlock != 0) return MSA_ERR_UNSUPPORTED;
-  if (q_start + n_q_tokens > kv_max_blocks(kv) * kBlock) return MSA_ERR_INVALID_ARG;
+  if (kv->dtype != MSA_DTYPE_BF16) return MSA_ERR_UNSUPPORTED;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != MSA_OK) return st;
   if ((st = check_ws(ws, ws_bytes, kWsHeader)) != MSA_OK) return st;
+  if (pb.total_tiles() == 0) return MSA_OK;  // no new tokens
   PrefillArgs a;
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.hq = hq;
   a.hkv = kv->num_kv_heads;
   a.grp = hq / kv->num_kv_heads;
-  a.n_q_tokens = n_q_tokens;
-  a.q_start = q_start;
+  a.batch = pb;
   a.idx = idx;
   a.k_total = idx != nullptr ? k_total : 0;
   a.scale_log2 = scale * kLog2e;
@@ -279,12 +298,89 @@ msa_status prefill_common(const void* q, int hq, int n_q_tokens, int64_t q_start
   if ((st = make_kv_map(&tmv, kv->v, rows)) != MSA_OK) return st;
   if (a.grp == 8) {
     CUtensorMap tmq;
-    if ((st = make_q_map(&tmq, q, n_q_tokens, hq)) != MSA_OK) return st;
+    if ((st = make_q_map(&tmq, q, n_tokens, hq)) != MSA_OK) return st;
     return cuda_status(launch_prefill_tc(tmq, tmk, tmv, view_of(kv), a, stream));
   }
   return cuda_status(launch_prefill_bf16(tmk, tmv, view_of(kv), a, stream));
 }
 
+// One sequence (kv->batch == 1) with n_q_tokens new tokens from q_start.
+msa_status prefill_one(const void* q, int hq, int n_q_tokens, int64_t q_start, const msa_kv_desc* kv,
+                       const int32_t* idx, int k_total, float scale, void* out, float* lse, void* ws,
+                       size_t ws_bytes, cudaStream_t stream) {
+  msa_status st = validate_kv(kv);
+  if (st != MSA_OK) return st;
+  if (n_q_tokens <= 0) return MSA_ERR_INVALID_ARG;
+  if (kv->batch != 1) return MSA_ERR_UNSUPPORTED;
+  PrefillBatch pb;
+  int64_t n_tokens = 0;
+  const int32_t cnt = n_q_tokens;
+  if ((st = build_batch(kv, 1, &q_start, &cnt, &pb, &n_tokens)) != MSA_OK) return st;
+  return prefill_common(q, hq, pb, n_tokens, kv, idx, k_total, scale, out, lse, ws, ws_bytes, stream);
+}
+
+// Selection for decode (pb == nullptr: one query token per sequence) or for
+// the 64-token tiles of a chunk batch.
+msa_status select_common(const void* q, int32_t num_q_heads, int32_t n_q_tokens, const PrefillBatch* pb,
+                         const void* pooled, const msa_kv_desc* kv, const msa_select_cfg* cfg, int32_t* idx_out,
+                         int32_t k_total, float* scores_out, void* ws, size_t ws_bytes, msa_stream_t stream) {
+  msa_status st = MSA_OK;
+  const int prefill = pb != nullptr;
+  if (!prefill && n_q_tokens != 1 && n_q_tokens != kv->batch) return MSA_ERR_INVALID_ARG;
+  if (prefill && kv->dtype != MSA_DTYPE_BF16 && pb->n_seqs != 1) return MSA_ERR_UNSUPPORTED;
+  if (kv_max_blocks(kv) > kMaxTopkCandidates) return MSA_ERR_UNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != MSA_OK) return st;
+  SelectLayout L = select_layout(kv, prefill ? kBlock * pb->total_tiles() : 1, prefill);
+  if ((st = check_ws(ws, ws_bytes, L.total)) != MSA_OK) return st;
+  if (prefill && pb->total_tiles() == 0) return MSA_OK;  // no new tokens
+  float* scores = scores_out != nullptr ? scores_out : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.scores);
+  float* qidx = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.qidx);
+  FusedSelect fused;
+  fused.scores_out = scores_out;
+  fused.cand = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + L.cand);
+  fused.tickets = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + kWsHeader);
+  fused.num_sms = dev->num_sms;
+  if (!prefill && !decode_units_fit(kv)) return MSA_ERR_UNSUPPORTED;
+  KvView view = view_of(kv);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cfg->mode == MSA_SCORE_TOKEN_MAX) {
+    // `pooled` holds the shared index-key head: [batch, max_tokens, 128] or [num_pages, 64, 128]
+    if (prefill || kv->dtype != MSA_DTYPE_BF16 || kv->num_kv_heads > 8) return MSA_ERR_UNSUPPORTED;
+    const int64_t rows = kv->layout == MSA_KV_CONTIGUOUS ? static_cast<int64_t>(kv->batch) * kv->max_tokens
+                                                         : static_cast<int64_t>(kv->num_pages) * kBlock;
+    if (rows >= (int64_t(1) << 31)) return MSA_ERR_UNSUPPORTED;
+    CUtensorMap tmi;
+    if ((st = make_kv_map(&tmi, pooled, rows)) != MSA_OK) return st;
+    if ((st = cuda_status(launch_token_max_scores(tmi, view, kv->batch, static_cast<const __nv_bfloat16*>(q),
+                                                  num_q_heads, cfg->force_local, scores, ws_status(ws), s))) != MSA_OK)
+      return st;
+    return cuda_status(launch_topk_scores(scores, view, kv->batch, *cfg, idx_out, k_total, ws_status(ws), s));
+  }
+  if (kv->dtype == MSA_DTYPE_BF16)
+    return cuda_status(launch_select<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(q), num_q_heads, pb,
+                                                    static_cast<const __nv_bfloat16*>(pooled), view, kv->batch,
+                                                    *cfg, idx_out, k_total, scores, qidx, &fused, ws_status(ws), s));
+  return cuda_status(launch_select<float>(static_cast<const float*>(q), num_q_heads, pb,
+                                          static_cast<const float*>(pooled), view, kv->batch, *cfg, idx_out,
+                                          k_total, scores, qidx, &fused, ws_status(ws), s));
+}
+
+// Checks shared by both selection entries.
+msa_status check_select(const void* q, int32_t num_q_heads, const void* pooled, const msa_kv_desc* kv,
+                        const msa_select_cfg* cfg, const int32_t* idx_out, int32_t k_total) {
+  msa_status st = validate_kv(kv);
+  if (st != MSA_OK) return st;
+  if (cfg == nullptr || q == nullptr || pooled == nullptr || idx_out == nullptr) return MSA_ERR_INVALID_ARG;
+  if ((st = check_q_heads(kv, num_q_heads)) != MSA_OK) return st;
+  if (cfg->mode != MSA_SCORE_MEAN_POOLED_KEYS && cfg->mode != MSA_SCORE_TOKEN_MAX) return MSA_ERR_UNSUPPORTED;
+  if (cfg->k_scored < 0 || k_total <= 0) return MSA_ERR_INVALID_ARG;
+  if (k_total < std::min<int64_t>(cfg->k_scored, kv_max_blocks(kv)) + forced_count(cfg))
+    return MSA_ERR_INVALID_ARG;
+  if (cfg->force_local < 0 || cfg->force_local > (kForceLocal | kForceSink)) return MSA_ERR_INVALID_ARG;
+  if (cfg->q_tile != 1 && cfg->q_tile != kBlock) return MSA_ERR_UNSUPPORTED;
+  return MSA_OK;
+}
 }  // namespace
 }  // namespace msa
 
@@ -353,59 +449,32 @@ msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_
                                   const msa_kv_desc* kv, const msa_select_cfg* cfg, int32_t* idx_out,
                                   int32_t k_total, float* scores_out, void* ws, size_t ws_bytes,
                                   msa_stream_t stream) {
-  msa_status st = validate_kv(kv);
+  msa_status st = check_select(q, num_q_heads, pooled, kv, cfg, idx_out, k_total);
   if (st != MSA_OK) return st;
-  if (cfg == nullptr || q == nullptr || pooled == nullptr || idx_out == nullptr) return MSA_ERR_INVALID_ARG;
-  if ((st = check_q_heads(kv, num_q_heads)) != MSA_OK) return st;
-  if (cfg->mode != MSA_SCORE_MEAN_POOLED_KEYS && cfg->mode != MSA_SCORE_TOKEN_MAX) return MSA_ERR_UNSUPPORTED;
-  if (cfg->k_scored < 0 || k_total <= 0) return MSA_ERR_INVALID_ARG;
-  if (k_total < std::min<int64_t>(cfg->k_scored, kv_max_blocks(kv)) + forced_count(cfg))
-    return MSA_ERR_INVALID_ARG;
-  if (cfg->force_local < 0 || cfg->force_local > (kForceLocal | kForceSink)) return MSA_ERR_INVALID_ARG;
-  const int prefill = cfg->q_tile == kBlock;
-  if (!prefill && cfg->q_tile != 1) return MSA_ERR_UNSUPPORTED;
-  if (prefill) {
-    if (kv->batch != 1 || n_q_tokens <= 0 || cfg->q_start < 0) return MSA_ERR_INVALID_ARG;
-    if (cfg->q_start % kBlock != 0) return MSA_ERR_UNSUPPORTED;
-    if (cfg->q_start + n_q_tokens > kv_max_blocks(kv) * kBlock) return MSA_ERR_INVALID_ARG;
-  } else if (n_q_tokens != 1 && n_q_tokens != kv->batch) {
-    return MSA_ERR_INVALID_ARG;
-  }
-  if (kv_max_blocks(kv) > kMaxTopkCandidates) return MSA_ERR_UNSUPPORTED;
-  DeviceInfo* dev = nullptr;
-  if ((st = device_info(&dev)) != MSA_OK) return st;
-  SelectLayout L = select_layout(kv, prefill ? n_q_tokens : 1, prefill);
-  if ((st = check_ws(ws, ws_bytes, L.total)) != MSA_OK) return st;
-  float* scores = scores_out != nullptr ? scores_out : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.scores);
-  float* qidx = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.qidx);
-  FusedSelect fused;
-  fused.scores_out = scores_out;
-  fused.cand = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + L.cand);
-  fused.tickets = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + kWsHeader);
-  fused.num_sms = dev->num_sms;
-  if (!prefill && !decode_units_fit(kv)) return MSA_ERR_UNSUPPORTED;
-  KvView view = view_of(kv);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cfg->mode == MSA_SCORE_TOKEN_MAX) {
-    // `pooled` holds the shared index-key head: [batch, max_tokens, 128] or [num_pages, 64, 128]
-    if (prefill || kv->dtype != MSA_DTYPE_BF16 || kv->num_kv_heads > 8) return MSA_ERR_UNSUPPORTED;
-    const int64_t rows = kv->layout == MSA_KV_CONTIGUOUS ? static_cast<int64_t>(kv->batch) * kv->max_tokens
-                                                         : static_cast<int64_t>(kv->num_pages) * kBlock;
-    if (rows >= (int64_t(1) << 31)) return MSA_ERR_UNSUPPORTED;
-    CUtensorMap tmi;
-    if ((st = make_kv_map(&tmi, pooled, rows)) != MSA_OK) return st;
-    if ((st = cuda_status(launch_token_max_scores(tmi, view, kv->batch, static_cast<const __nv_bfloat16*>(q),
-                                                  num_q_heads, cfg->force_local, scores, ws_status(ws), s))) != MSA_OK)
-      return st;
-    return cuda_status(launch_topk_scores(scores, view, kv->batch, *cfg, idx_out, k_total, ws_status(ws), s));
-  }
-  if (kv->dtype == MSA_DTYPE_BF16)
-    return cuda_status(launch_select<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(q), num_q_heads, n_q_tokens,
-                                                    static_cast<const __nv_bfloat16*>(pooled), view, kv->batch,
-                                                    *cfg, idx_out, k_total, scores, qidx, &fused, ws_status(ws), s));
-  return cuda_status(launch_select<float>(static_cast<const float*>(q), num_q_heads, n_q_tokens,
-                                          static_cast<const float*>(pooled), view, kv->batch, *cfg, idx_out,
-                                          k_total, scores, qidx, &fused, ws_status(ws), s));
+  if (cfg->q_tile == 1)
+    return select_common(q, num_q_heads, n_q_tokens, nullptr, pooled, kv, cfg, idx_out, k_total, scores_out, ws,
+                         ws_bytes, stream);
+  if (kv->batch != 1 || n_q_tokens <= 0 || cfg->q_start < 0) return MSA_ERR_INVALID_ARG;
+  PrefillBatch pb;
+  int64_t n_tokens = 0;
+  const int64_t q_start = cfg->q_start;
+  if ((st = build_batch(kv, 1, &q_start, &n_q_tokens, &pb, &n_tokens)) != MSA_OK) return st;
+  return select_common(q, num_q_heads, n_q_tokens, &pb, pooled, kv, cfg, idx_out, k_total, scores_out, ws, ws_bytes,
+                       stream);
+}
+
+msa_status msa_select_topk_blocks_varlen(const void* q, int32_t num_q_heads, int32_t n_seqs, const int64_t* q_starts,
+                                         const int32_t* q_counts, const void* pooled, const msa_kv_desc* kv,
+                                         const msa_select_cfg* cfg, int32_t* idx_out, int32_t k_total,
+                                         float* scores_out, void* ws, size_t ws_bytes, msa_stream_t stream) {
+  msa_status st = check_select(q, num_q_heads, pooled, kv, cfg, idx_out, k_total);
+  if (st != MSA_OK) return st;
+  if (cfg->q_tile != kBlock) return MSA_ERR_INVALID_ARG;
+  PrefillBatch pb;
+  int64_t n_tokens = 0;
+  if ((st = build_batch(kv, n_seqs, q_starts, q_counts, &pb, &n_tokens)) != MSA_OK) return st;
+  return select_common(q, num_q_heads, static_cast<int32_t>(n_tokens), &pb, pooled, kv, cfg, idx_out, k_total,
+                       scores_out, ws, ws_bytes, stream);
 }
 
 msa_status msa_sparse_attn_decode(const void* q, int32_t num_q_heads, const msa_kv_desc* kv, const int32_t* idx,
@@ -426,15 +495,29 @@ msa_status msa_sparse_attn_prefill(const void* q, int32_t num_q_heads, int32_t n
                                    const msa_kv_desc* kv, const int32_t* idx, int32_t k_total, float scale,
                                    void* out, float* lse, void* ws, size_t ws_bytes, msa_stream_t stream) {
   if (idx == nullptr) return MSA_ERR_INVALID_ARG;
-  return prefill_common(q, num_q_heads, n_q_tokens, q_start, kv, idx, k_total, scale, out, lse, ws, ws_bytes,
+  return prefill_one(q, num_q_heads, n_q_tokens, q_start, kv, idx, k_total, scale, out, lse, ws, ws_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_sparse_attn_prefill_varlen(const void* q, int32_t num_q_heads, int32_t n_seqs,
+                                          const int64_t* q_starts, const int32_t* q_counts, const msa_kv_desc* kv,
+                                          const int32_t* idx, int32_t k_total, float scale, void* out, float* lse,
+                                          void* ws, size_t ws_bytes, msa_stream_t stream) {
+  if (idx == nullptr) return MSA_ERR_INVALID_ARG;
+  msa_status st = validate_kv(kv);
+  if (st != MSA_OK) return st;
+  PrefillBatch pb;
+  int64_t n_tokens = 0;
+  if ((st = build_batch(kv, n_seqs, q_starts, q_counts, &pb, &n_tokens)) != MSA_OK) return st;
+  return prefill_common(q, num_q_heads, pb, n_tokens, kv, idx, k_total, scale, out, lse, ws, ws_bytes,
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 msa_status msa_dense_gqa_prefill(const void* q, int32_t num_q_heads, int32_t n_q_tokens, int64_t q_start,
                                  const msa_kv_desc* kv, float scale, void* out, float* lse, void* ws,
                                  size_t ws_bytes, msa_stream_t stream) {
-  return prefill_common(q, num_q_heads, n_q_tokens, q_start, kv, nullptr, 0, scale, out, lse, ws, ws_bytes,
-                        reinterpret_cast<cudaStream_t>(stream));
+  return prefill_one(q, num_q_heads, n_q_tokens, q_start, kv, nullptr, 0, scale, out, lse, ws, ws_bytes,
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 namespace {

@@ -6,6 +6,36 @@
 
 namespace msa {
 
+// Sequences of a (batched) chunked prefill: sequence s has q_cnt[s] new
+// tokens at absolute positions q_start[s] + r (q_start[s] a multiple of 64),
+// stored in rows q_off[s] + r of q and out; its 64-token tiles are global
+// tiles tile_off[s] .. tile_off[s + 1] - 1, and the prefill scorer takes them
+// in groups of 8 (global groups grp_off[s] .. grp_off[s + 1] - 1).
+constexpr int kMaxPrefillSeqs = 64;
+struct PrefillBatch {
+  int n_seqs;
+  int64_t q_start[kMaxPrefillSeqs];
+  int32_t q_off[kMaxPrefillSeqs];
+  int32_t q_cnt[kMaxPrefillSeqs];
+  int32_t tile_off[kMaxPrefillSeqs + 1];
+  int32_t grp_off[kMaxPrefillSeqs + 1];
+  __host__ __device__ int seq_of_tile(int tile) const {
+    int s = 0;
+    while (s + 1 < n_seqs && tile_off[s + 1] <= tile) ++s;
+    return s;
+  }
+  __host__ __device__ int seq_of_group(int g) const {
+    int s = 0;
+    while (s + 1 < n_seqs && grp_off[s + 1] <= g) ++s;
+    return s;
+  }
+  __host__ __device__ int total_tiles() const { return tile_off[n_seqs]; }
+};
+// Fills b from host arrays; false when n_seqs is out of [1, kMaxPrefillSeqs]
+// or a count is negative.
+bool make_prefill_batch(int n_seqs, const int64_t* q_starts, const int32_t* q_counts, PrefillBatch* b);
+
+
 // ---- Step 1a: pooling (pool.cu) ----
 template <typename T>
 cudaError_t launch_pool(const T* k, const KvView& kv, int batch, int64_t first_block, int64_t n_blocks, T* pooled,
@@ -23,7 +53,7 @@ struct FusedSelect {
   int num_sms;
 };
 template <typename T>
-cudaError_t launch_select(const T* q, int hq, int n_q_tokens, const T* pooled, const KvView& kv, int batch,
+cudaError_t launch_select(const T* q, int hq, const PrefillBatch* pb, const T* pooled, const KvView& kv, int batch,
                           const msa_select_cfg& cfg, int32_t* idx_out, int k_total, float* scores, float* qidx_ws,
                           const FusedSelect* fused, int32_t* status, cudaStream_t stream);
 void select_decode_shape(int64_t max_blocks, int64_t units, int num_sms, int* chunk, int* n_chunks);
@@ -58,11 +88,10 @@ cudaError_t launch_decode_f32(const float* k, const float* v, const KvView& kv, 
 
 // ---- Step 2, prefill (prefill.cu) ----
 struct PrefillArgs {
-  const __nv_bfloat16* q;  // [n_q_tokens, hq, 128]
+  const __nv_bfloat16* q;  // [total new tokens, hq, 128]
   int hq, hkv, grp;
-  int n_q_tokens;
-  int64_t q_start;
-  const int32_t* idx;  // [n_tiles, hkv, k_total] or nullptr (dense)
+  PrefillBatch batch;
+  const int32_t* idx;  // [total tiles, hkv, k_total] or nullptr (dense)
   int k_total;
   float scale_log2;
   __nv_bfloat16* out;

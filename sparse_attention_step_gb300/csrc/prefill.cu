@@ -39,10 +39,13 @@ __global__ void __launch_bounds__(kPfThreads) prefill_bf16_kernel(const __grid_c
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   PrefillSmemTail& st = *reinterpret_cast<PrefillSmemTail*>(ring + kPfStages * kPfStageBytes);
 
-  const int rg = blockIdx.x, h = blockIdx.y, tile = blockIdx.z;
+  const int rg = blockIdx.x, h = blockIdx.y, tile = blockIdx.z;  // tile: global over the batch
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t len = kv.seq_len(0, a.status, kIdPrefill);
-  const int64_t diag = a.q_start / kBlock + tile;
+  const int seq = a.batch.seq_of_tile(tile);
+  const int jt = tile - a.batch.tile_off[seq];  // tile within its sequence
+  const int64_t q_start = a.batch.q_start[seq];
+  const int64_t len = kv.seq_len(seq, a.status, kIdPrefill);
+  const int64_t diag = q_start / kBlock + jt;
 
   if (tid == 0) {
     int n = 0;
@@ -84,7 +87,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_bf16_kernel(const __grid_c
         const int stg = i % kPfStages;
         if (i >= kPfStages && !mbar_wait(&st.empty[stg], ((i / kPfStages) - 1) & 1, a.status, kIdPrefill)) break;
         const int b = dense ? i : st.blocks[i];
-        const int64_t row = kv.block_row(0, h, b, a.status, kIdPrefill);
+        const int64_t row = kv.block_row(seq, h, b, a.status, kIdPrefill);
         uint8_t* dst = ring + stg * kPfStageBytes;
         mbar_arrive_expect_tx(&st.full[stg], kPfStageBytes);
         const int32_t y = static_cast<int32_t>(row < 0 ? 0 : row);
@@ -106,10 +109,10 @@ __global__ void __launch_bounds__(kPfThreads) prefill_bf16_kernel(const __grid_c
   for (int hr = 0; hr < 2; ++hr) {
     const int r = rg * kPfRows + 16 * warp + g + 8 * hr;
     const int t = r / a.grp, gh = r % a.grp;
-    const int64_t tq = static_cast<int64_t>(tile) * kBlock + t;  // query index within the chunk
-    live[hr] = (t < kBlock) && (tq < a.n_q_tokens);
-    pos[hr] = a.q_start + tq;
-    qrow[hr] = live[hr] ? tq * a.hq + h * a.grp + gh : 0;
+    const int64_t tq = static_cast<int64_t>(jt) * kBlock + t;  // query index within its sequence's chunk
+    live[hr] = (t < kBlock) && (tq < a.batch.q_cnt[seq]);
+    pos[hr] = q_start + tq;
+    qrow[hr] = live[hr] ? (a.batch.q_off[seq] + tq) * a.hq + h * a.grp + gh : 0;
   }
   uint32_t qa[8][4];
 #pragma unroll
@@ -154,7 +157,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_bf16_kernel(const __grid_c
     }
     // mask and scale
     const int64_t key0 = static_cast<int64_t>(b) * kBlock;
-    const bool need_mask = (key0 + kBlock - 1 > a.q_start + static_cast<int64_t>(tile) * kBlock) ||
+    const bool need_mask = (key0 + kBlock - 1 > q_start + static_cast<int64_t>(jt) * kBlock) ||
                            (key0 + kBlock > len);
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -244,9 +247,8 @@ cudaError_t set_prefill_smem() {
 
 cudaError_t launch_prefill_bf16(const CUtensorMap& tmk, const CUtensorMap& tmv, const KvView& kv,
                                 const PrefillArgs& a, cudaStream_t stream) {
-  const int n_tiles = (a.n_q_tokens + kBlock - 1) / kBlock;
   const int row_groups = (kBlock * a.grp + kPfRows - 1) / kPfRows;
-  dim3 grid(row_groups, kv.hkv, n_tiles);
+  dim3 grid(row_groups, kv.hkv, a.batch.total_tiles());
   prefill_bf16_kernel<<<grid, kPfThreads, prefill_smem_bytes(), stream>>>(tmk, tmv, kv, a);
   return cudaGetLastError();
 }

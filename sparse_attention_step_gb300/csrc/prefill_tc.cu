@@ -110,9 +110,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   uint8_t* kvs = base + kQBytes;
   TcTail& st = *reinterpret_cast<TcTail*>(kvs + kKVBytes);
 
-  const int rh = blockIdx.x, h = blockIdx.y, tile = blockIdx.z;
+  const int rh = blockIdx.x, h = blockIdx.y, tile = blockIdx.z;  // tile: global over the batch
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t diag = a.q_start / kBlock + tile;
+  const int seq = a.batch.seq_of_tile(tile);
+  const int jt = tile - a.batch.tile_off[seq];  // tile within its sequence
+  const int64_t diag = a.batch.q_start[seq] / kBlock + jt;
 
   if (tid == 0) {
     int n = 0;
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
       mbar_arrive_expect_tx(&st.q_full, kQBytes);
-      const int32_t tok0 = tile * kBlock + rh * (kTcTiles * 16);
+      const int32_t tok0 = a.batch.q_off[seq] + jt * kBlock + rh * (kTcTiles * 16);
       for (int t = 0; t < kTcTiles; ++t)
         for (int half = 0; half < 2; ++half)
           tma_load_3d(qs + t * 32768 + half * 16384, &tmq, 64 * half, h * 8, tok0 + 16 * t, &st.q_full);
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         const int stg = i % kTcStages;
         if (i >= kTcStages && !wait_or_abort(&st.kv_empty[stg], ((i / kTcStages) - 1) & 1, abort, a.status)) break;
         const int b = dense ? i : st.blocks[i];
-        const int64_t row = kv.block_row(0, h, b, a.status, kIdPrefill);
+        const int64_t row = kv.block_row(seq, h, b, a.status, kIdPrefill);
         const int32_t y = static_cast<int32_t>(row < 0 ? 0 : row);
         uint8_t* dst = kvs + stg * 32768;
         mbar_arrive_expect_tx(&st.kv_full[stg], 32768);
@@ -264,8 +266,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     const int bar_id = 1 + t;               // the tile's 8 softmax warps
     const int tt = rh * (kTcTiles * 16) + 16 * t + (r >> 3);  // token within the 64-token tile
     const int head = h * 8 + (r & 7);
-    const int64_t tq = static_cast<int64_t>(tile) * kBlock + tt;  // token within the chunk
-    const bool live = tq < a.n_q_tokens;
+    const int64_t tl = static_cast<int64_t>(jt) * kBlock + tt;  // token within its sequence's chunk
+    const bool live = tl < a.batch.q_cnt[seq];
+    const int64_t tq = a.batch.q_off[seq] + tl;                 // its row in q and out
     float m = -INFINITY, l = 0.f;  // running max (log2 units) and this half's running sum
     bool ok = true;
     // Every warp of the tile runs every iteration and every named barrier, even
@@ -408,8 +411,7 @@ cudaError_t set_prefill_tc_smem() {
 
 cudaError_t launch_prefill_tc(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                               const KvView& kv, const PrefillArgs& a, cudaStream_t stream) {
-  const int n_tiles = (a.n_q_tokens + kBlock - 1) / kBlock;
-  dim3 grid(2, kv.hkv, n_tiles);
+  dim3 grid(2, kv.hkv, a.batch.total_tiles());
   prefill_tc_kernel<<<grid, kTcThreads, kTcSmem, stream>>>(tmq, tmk, tmv, kv, a);
   return cudaGetLastError();
 }

@@ -34,14 +34,16 @@ namespace msa {
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(256) qidx_prefill_kernel(const T* __restrict__ q, int hq, int hkv,
-                                                          int n_q_tokens, float* __restrict__ qidx) {
+                                                          const PrefillBatch pb, float* __restrict__ qidx) {
   __shared__ float part[16][kHeadDim + 4];
   const int h = blockIdx.x;
-  const int tile = blockIdx.y;
+  const int tile = blockIdx.y;  // global tile
   const int e = threadIdx.x & 15, slot = threadIdx.x >> 4;
   const int grp = hq / hkv;
-  const int r0 = tile * kBlock;
-  const int n_rows = (min(n_q_tokens, r0 + kBlock) - r0) * grp;  // token-major, head-minor
+  const int s = pb.seq_of_tile(tile);
+  const int j0 = (tile - pb.tile_off[s]) * kBlock;  // first token of the tile within its sequence
+  const int r0 = pb.q_off[s] + j0;                  // its row in q
+  const int n_rows = (min(pb.q_cnt[s], j0 + kBlock) - j0) * grp;  // token-major, head-minor
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
@@ -195,16 +197,21 @@ constexpr int kPsTiles = 8;
 
 __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __restrict__ qidx_ws,
                                                                 const __nv_bfloat16* __restrict__ pooled,
-                                                                KvView kv, ScoreArgs a, float* __restrict__ scores,
-                                                                int32_t* status) {
+                                                                KvView kv, ScoreArgs a, const PrefillBatch pb,
+                                                                float* __restrict__ scores, int32_t* status) {
   __shared__ __align__(1024) uint8_t rows_s[kPsRows * kHeadDim * 2];
   __shared__ uint8_t bad[kPsRows];  // rows whose page id is out of range
   const int h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t0 = blockIdx.z * kPsTiles;
+  // 8 tiles of one sequence: global tiles t0 .. t_end - 1, local tiles j0 ..
+  const int seq = pb.seq_of_group(blockIdx.z);
+  const int j0 = (blockIdx.z - pb.grp_off[seq]) * kPsTiles;
+  const int t0 = pb.tile_off[seq] + j0;
+  const int t_end = min(t0 + kPsTiles, pb.tile_off[seq + 1]);
+  const int64_t diag0 = pb.q_start[seq] / kBlock + j0;  // candidates of tile t0 + t: blocks < diag0 + t
   const int64_t chunk0 = static_cast<int64_t>(blockIdx.x) * kPsRows;
   int64_t n_max = 0;
   for (int t = 0; t < kPsTiles; ++t)
-    if (t0 + t < a.n_tiles) n_max = max(n_max, a.q_start / kBlock + t0 + t);
+    if (t0 + t < t_end) n_max = max(n_max, diag0 + t);
   const int64_t row_end = min(chunk0 + kPsRows, a.max_blocks);
   // cp.async: 128 rows x 16 pieces of 16 bytes, 8 per thread
 #pragma unroll
@@ -214,7 +221,7 @@ __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __r
     const int64_t b = chunk0 + row;
     bool miss = false;
     if (b < n_max && b < row_end) {
-      const int64_t prow = kv.pooled_row(0, h, b, pc == 0 ? status : nullptr, kIdScore);
+      const int64_t prow = kv.pooled_row(seq, h, b, pc == 0 ? status : nullptr, kIdScore);
       miss = prow < 0;
       if (!miss)
         cp_async16(rows_s + (pc >> 3) * (kPsRows * 128) + row * 128 + (((pc & 7) ^ (row & 7)) << 4),
@@ -225,7 +232,7 @@ __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __r
   cp_async_commit();
   // B operands: column g = tile t0 + g
   const int g = lane >> 2, c = lane & 3;
-  const bool live = t0 + g < a.n_tiles;
+  const bool live = t0 + g < t_end;
   const float* qg = qidx_ws + (static_cast<int64_t>(live ? t0 + g : 0) * a.hkv + h) * kHeadDim;
   uint32_t qh[8][2], ql[8][2];
 #pragma unroll
@@ -258,8 +265,8 @@ __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __r
   for (int k = 0; k < 4; ++k) {
     const int64_t b = chunk0 + 16 * warp + g + 8 * (k >> 1);
     const int tile = t0 + 2 * c + (k & 1);
-    if (b < row_end && tile < a.n_tiles) {
-      const int64_t n_cand = a.q_start / kBlock + tile;
+    if (b < row_end && tile < t_end) {
+      const int64_t n_cand = diag0 + (tile - t0);
       const bool ok = b < n_cand && !bad[b - chunk0];
       scores[(static_cast<int64_t>(tile) * a.hkv + h) * a.max_blocks + b] = ok ? hi[k] + lo[k] : -INFINITY;
     }
@@ -310,8 +317,8 @@ struct TopkArgs {
   int force_local;
   int k_scored;
   int k_total;
-  int64_t q_start;
   int64_t max_blocks;
+  PrefillBatch pb;  // prefill: the tiles' sequences
 };
 
 constexpr int kCandCap = 8192;  // keys of the threshold bin refined in shared memory
@@ -382,7 +389,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     n64 = local ? min(nbf, nb - 1) : nbf;
     forced = (local && nb > 0) ? nb - 1 : -1;
   } else {
-    n64 = a.q_start / kBlock + outer;
+    const int s = a.pb.seq_of_tile(outer);
+    n64 = a.pb.q_start[s] / kBlock + (outer - a.pb.tile_off[s]);
     nb = n64 + 1;
     forced = local ? n64 : -1;
   }
@@ -831,12 +839,12 @@ size_t select_decode_cand_bytes(int64_t units, int n_chunks) {
 // Host launchers
 // ---------------------------------------------------------------------------
 template <typename T>
-cudaError_t launch_select(const T* q, int hq, int n_q_tokens, const T* pooled, const KvView& kv, int batch,
+cudaError_t launch_select(const T* q, int hq, const PrefillBatch* pb, const T* pooled, const KvView& kv, int batch,
                           const msa_select_cfg& cfg, int32_t* idx_out, int k_total, float* scores, float* qidx_ws,
                           const FusedSelect* fused, int32_t* status, cudaStream_t stream) {
   const int prefill = cfg.q_tile == kBlock;
   const int64_t max_blocks = kv.max_blocks();
-  ScoreArgs sa{hq, kv.hkv, prefill, cfg.force_local, cfg.q_start, 0, max_blocks};
+  ScoreArgs sa{hq, kv.hkv, prefill, cfg.force_local, prefill ? pb->q_start[0] : 0, 0, max_blocks};
   const unsigned chunks = static_cast<unsigned>((max_blocks + kScoreChunk - 1) / kScoreChunk);
   int outer;
   if (!prefill && cfg.k_scored <= 64 && fused != nullptr) {
@@ -868,18 +876,20 @@ cudaError_t launch_select(const T* q, int hq, int n_q_tokens, const T* pooled, c
     score_kernel<T, 1><<<dim3(chunks, kv.hkv, batch), kScoreThreads, 0, stream>>>(q, nullptr, pooled, kv, sa,
                                                                                   scores, status);
   } else {
-    const int n_tiles = (n_q_tokens + kBlock - 1) / kBlock;
+    const int n_tiles = pb->total_tiles();
     outer = n_tiles;
     sa.n_tiles = n_tiles;
-    qidx_prefill_kernel<T><<<dim3(kv.hkv, n_tiles), 256, 0, stream>>>(q, hq, kv.hkv, n_q_tokens, qidx_ws);
+    qidx_prefill_kernel<T><<<dim3(kv.hkv, n_tiles), 256, 0, stream>>>(q, hq, kv.hkv, *pb, qidx_ws);
     constexpr int kT = 8;
     // only the chunks below the last tile's diagonal hold candidates
-    const int64_t last = cfg.q_start / kBlock + n_tiles;
+    int64_t last = 0;
+    for (int s = 0; s < pb->n_seqs; ++s)
+      last = max(last, pb->q_start[s] / kBlock + (pb->tile_off[s + 1] - pb->tile_off[s]));
     if constexpr (sizeof(T) == 2) {
       const unsigned pchunks = static_cast<unsigned>((min(last, max_blocks) + kPsRows - 1) / kPsRows);
-      score_prefill_mma_kernel<<<dim3(pchunks, kv.hkv, (n_tiles + kPsTiles - 1) / kPsTiles), 256, 0, stream>>>(
-          qidx_ws, pooled, kv, sa, scores, status);
-    } else {
+      score_prefill_mma_kernel<<<dim3(pchunks, kv.hkv, pb->grp_off[pb->n_seqs]), 256, 0, stream>>>(
+          qidx_ws, pooled, kv, sa, *pb, scores, status);
+    } else {  // fp32 prefill selection: one sequence
       const unsigned pchunks = static_cast<unsigned>((min(last, max_blocks) + kScoreChunk - 1) / kScoreChunk);
       score_kernel<T, kT><<<dim3(pchunks, kv.hkv, (n_tiles + kT - 1) / kT), kScoreThreads, 0, stream>>>(
           q, qidx_ws, pooled, kv, sa, scores, status);
@@ -887,7 +897,8 @@ cudaError_t launch_select(const T* q, int hq, int n_q_tokens, const T* pooled, c
   }
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  TopkArgs ta{kv.hkv, prefill, cfg.force_local, cfg.k_scored, k_total, cfg.q_start, max_blocks};
+  TopkArgs ta{kv.hkv, prefill, cfg.force_local, cfg.k_scored, k_total, max_blocks, {}};
+  if (prefill) ta.pb = *pb;
   const size_t smem = static_cast<size_t>(max_blocks + kCandCap) * sizeof(uint32_t);
   topk_kernel<<<dim3(kv.hkv, outer), topk_threads(max_blocks), smem, stream>>>(scores, kv, ta, idx_out, status);
   return cudaGetLastError();
@@ -897,7 +908,7 @@ cudaError_t launch_select(const T* q, int hq, int n_q_tokens, const T* pooled, c
 cudaError_t launch_topk_scores(const float* scores, const KvView& kv, int batch, const msa_select_cfg& cfg,
                                int32_t* idx_out, int k_total, int32_t* status, cudaStream_t stream) {
   const int64_t max_blocks = kv.max_blocks();
-  TopkArgs ta{kv.hkv, 0, cfg.force_local, cfg.k_scored, k_total, 0, max_blocks};
+  TopkArgs ta{kv.hkv, 0, cfg.force_local, cfg.k_scored, k_total, max_blocks, {}};
   const size_t smem = static_cast<size_t>(max_blocks + kCandCap) * sizeof(uint32_t);
   topk_kernel<<<dim3(kv.hkv, batch), topk_threads(max_blocks), smem, stream>>>(scores, kv, ta, idx_out, status);
   return cudaGetLastError();
@@ -921,11 +932,34 @@ cudaError_t set_topk_smem(size_t bytes) {
   return cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
 }
 
-template cudaError_t launch_select<__nv_bfloat16>(const __nv_bfloat16*, int, int, const __nv_bfloat16*,
-                                                  const KvView&, int, const msa_select_cfg&, int32_t*, int, float*,
-                                                  float*, const FusedSelect*, int32_t*, cudaStream_t);
-template cudaError_t launch_select<float>(const float*, int, int, const float*, const KvView&, int,
+template cudaError_t launch_select<__nv_bfloat16>(const __nv_bfloat16*, int, const PrefillBatch*,
+                                                  const __nv_bfloat16*, const KvView&, int, const msa_select_cfg&,
+                                                  int32_t*, int, float*, float*, const FusedSelect*, int32_t*,
+                                                  cudaStream_t);
+template cudaError_t launch_select<float>(const float*, int, const PrefillBatch*, const float*, const KvView&, int,
                                           const msa_select_cfg&, int32_t*, int, float*, float*, const FusedSelect*,
                                           int32_t*, cudaStream_t);
+
+bool make_prefill_batch(int n_seqs, const int64_t* q_starts, const int32_t* q_counts, PrefillBatch* b) {
+  if (n_seqs < 1 || n_seqs > kMaxPrefillSeqs || q_starts == nullptr || q_counts == nullptr) return false;
+  *b = PrefillBatch{};
+  b->n_seqs = n_seqs;
+  int32_t off = 0, tiles = 0, groups = 0;
+  for (int s = 0; s < n_seqs; ++s) {
+    if (q_counts[s] < 0 || q_starts[s] < 0) return false;
+    b->q_start[s] = q_starts[s];
+    b->q_off[s] = off;
+    b->q_cnt[s] = q_counts[s];
+    b->tile_off[s] = tiles;
+    b->grp_off[s] = groups;
+    const int32_t t = (q_counts[s] + kBlock - 1) / kBlock;
+    off += q_counts[s];
+    tiles += t;
+    groups += (t + kPsTiles - 1) / kPsTiles;
+  }
+  b->tile_off[n_seqs] = tiles;
+  b->grp_off[n_seqs] = groups;
+  return true;
+}
 
 }  // namespace msa

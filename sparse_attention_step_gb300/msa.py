@@ -30,7 +30,8 @@ MSA_SCORE_MEAN_POOLED_KEYS, MSA_SCORE_TOKEN_MAX = 0, 1
 EXPORTS = ["msa_workspace_size", "msa_workspace_init", "msa_pool_block_keys", "msa_select_topk_blocks",
            "msa_sparse_attn_decode", "msa_sparse_attn_prefill", "msa_dense_gqa_decode", "msa_dense_gqa_prefill",
            "msa_read_device_status", "msa_status_string", "msa_version", "msa_sparse_attn_decode_noalloc",
-           "msa_sparse_decode_step", "msa_sparse_decode_step_pool"]
+           "msa_sparse_decode_step", "msa_sparse_decode_step_pool", "msa_select_topk_blocks_varlen",
+           "msa_sparse_attn_prefill_varlen"]
 
 
 class MsaError(RuntimeError):
@@ -74,6 +75,10 @@ _SIGS = {
                                       _P, _P, _SZ, _P]),
     "msa_sparse_decode_step_pool": (_I32, [_P, _I32, _P, _DESC, ctypes.POINTER(SelectCfg), _P, _I32, ctypes.c_float,
                                            _P, _P, _P, _SZ, _P]),
+    "msa_select_topk_blocks_varlen": (_I32, [_P, _I32, _I32, _P, _P, _P, _DESC, ctypes.POINTER(SelectCfg), _P, _I32,
+                                             _P, _P, _SZ, _P]),
+    "msa_sparse_attn_prefill_varlen": (_I32, [_P, _I32, _I32, _P, _P, _DESC, _P, _I32, ctypes.c_float, _P, _P, _P,
+                                              _SZ, _P]),
     "msa_status_string": (ctypes.c_char_p, [_I32]),
     "msa_version": (_I32, []),
 }
@@ -183,6 +188,36 @@ def msa_select_topk_blocks(q, num_q_heads: int, n_q_tokens: int, pooled, desc: K
     _check(load().msa_select_topk_blocks(_ptr(q), num_q_heads, n_q_tokens, _ptr(pooled), ctypes.byref(desc),
                                          ctypes.byref(cfg), _ptr(idx_out), k_total, _ptr(scores_out), _ptr(ws),
                                          ws_bytes, _stream(stream)), "msa_select_topk_blocks")
+
+
+def _host_batch(q_starts, q_counts):
+    """Host arrays of a chunk batch: (n_seqs, int64 starts, int32 counts), kept
+    alive by the caller for the duration of the call."""
+    n = len(q_starts)
+    if len(q_counts) != n:
+        raise ValueError("q_starts and q_counts differ in length")
+    return n, (ctypes.c_int64 * n)(*[int(x) for x in q_starts]), (ctypes.c_int32 * n)(*[int(x) for x in q_counts])
+
+
+def varlen_tiles(q_counts) -> int:
+    """Global 64-token tiles of a chunk batch (rows of the varlen index lists)."""
+    return sum((int(c) + 63) // 64 for c in q_counts)
+
+
+def msa_select_topk_blocks_varlen(q, num_q_heads: int, q_starts, q_counts, pooled, desc: KvDesc, cfg: SelectCfg,
+                                  idx_out, k_total: int, scores_out, ws, ws_bytes: int, stream=None) -> None:
+    n, st, ct = _host_batch(q_starts, q_counts)
+    _check(load().msa_select_topk_blocks_varlen(_ptr(q), num_q_heads, n, st, ct, _ptr(pooled), ctypes.byref(desc),
+                                                ctypes.byref(cfg), _ptr(idx_out), k_total, _ptr(scores_out),
+                                                _ptr(ws), ws_bytes, _stream(stream)), "msa_select_topk_blocks_varlen")
+
+
+def msa_sparse_attn_prefill_varlen(q, num_q_heads: int, q_starts, q_counts, desc: KvDesc, idx, k_total: int,
+                                   scale: float, out, lse, ws, ws_bytes: int, stream=None) -> None:
+    n, st, ct = _host_batch(q_starts, q_counts)
+    _check(load().msa_sparse_attn_prefill_varlen(_ptr(q), num_q_heads, n, st, ct, ctypes.byref(desc), _ptr(idx),
+                                                 k_total, scale, _ptr(out), _ptr(lse), _ptr(ws), ws_bytes,
+                                                 _stream(stream)), "msa_sparse_attn_prefill_varlen")
 
 
 def msa_sparse_attn_decode(q, num_q_heads: int, desc: KvDesc, idx, k_total: int, scale: float, out, lse, ws,

@@ -23,7 +23,8 @@ BLOCK = 64
 HEAD_DIM = 128
 
 # stream ids
-_S_Q, _S_K, _S_V, _S_NEEDLE_POS, _S_NEEDLE_NOISE, _S_LENS, _S_PAGES, _S_KIDX, _S_KIDX_POS, _S_KIDX_NOISE = range(10)
+(_S_Q, _S_K, _S_V, _S_NEEDLE_POS, _S_NEEDLE_NOISE, _S_LENS, _S_PAGES, _S_KIDX, _S_KIDX_POS, _S_KIDX_NOISE,
+ _S_CHUNK_Q) = range(11)
 
 
 def _gen(seed: int, stream: int, device) -> torch.Generator:
@@ -263,6 +264,47 @@ def make_prefill_inputs(prefix: int, n_new: int, num_kv_heads: int, num_q_heads:
     return PrefillInputs(q=q, k=k, v=v, seq_lens=torch.tensor([total], dtype=torch.int32, device=device),
                          q_start=prefix, n_new=n_new, num_kv_heads=num_kv_heads,
                          num_q_heads=num_q_heads, dtype=dtype, layout=layout, page_table=page_table)
+
+
+@dataclasses.dataclass
+class PrefillBatchInputs:
+    """A batch of prefill chunks: sequence s appends q_counts[s] tokens to a
+    q_starts[s]-token prefix. ``cache`` holds every sequence's prefix and new
+    tokens (lengths q_starts[s] + q_counts[s], either layout); ``q`` holds the
+    chunks' query tokens back to back."""
+    cache: DecodeInputs
+    q: torch.Tensor      # [sum q_counts, Hq, D]
+    q_starts: list
+    q_counts: list
+
+    @property
+    def q_off(self) -> list:
+        return [sum(self.q_counts[:s]) for s in range(len(self.q_counts))]
+
+    @property
+    def tile_off(self) -> list:
+        return [sum(-(-c // BLOCK) for c in self.q_counts[:s]) for s in range(len(self.q_counts) + 1)]
+
+    def q_rows(self, s: int) -> torch.Tensor:
+        o = self.q_off[s]
+        return self.q[o:o + self.q_counts[s]]
+
+
+def make_prefill_batch_inputs(q_starts, q_counts, num_kv_heads: int, num_q_heads: int, dtype: str = "bf16",
+                              layout: str = "contiguous", seed: int = 0, device="cpu") -> PrefillBatchInputs:
+    """Chunks of ``q_counts[s]`` new tokens after ``q_starts[s]``-token prefixes
+    (multiples of 64), one per sequence of a shared cache."""
+    q_starts = [int(x) for x in q_starts]
+    q_counts = [int(x) for x in q_counts]
+    assert all(x % BLOCK == 0 for x in q_starts)
+    lens = [a + c for a, c in zip(q_starts, q_counts)]
+    cache = make_decode_inputs([max(n, 1) for n in lens], num_kv_heads, num_q_heads, dtype, layout, seed=seed,
+                               device=device)
+    cache.seq_lens.copy_(torch.tensor(lens, dtype=torch.int32))
+    cache.lens = lens
+    q = torch.empty(sum(q_counts), num_q_heads, HEAD_DIM, dtype=torch_dtype(dtype), device=device)
+    _randn_into(q, _gen(seed, _S_CHUNK_Q, device))
+    return PrefillBatchInputs(cache=cache, q=q, q_starts=q_starts, q_counts=q_counts)
 
 
 # ---------------------------------------------------------------------------
