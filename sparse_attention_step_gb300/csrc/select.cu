@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
 // score them (a half-warp per row) into 64-bit selection keys; block_topk
 // keeps the chunk's best. A unit spread over several chunks posts the chunk
 // lists and its last CTA to finish (atomic ticket) selects among them.
-// grid (n_chunks, Hkv, batch); chunks past a sequence's candidates exit at
+// grid (Hkv, batch, n_chunks); chunks past a sequence's candidates exit at
 // once and take no ticket.
 // ---------------------------------------------------------------------------
 constexpr int kSelWarps = 8;
@@ -579,7 +579,10 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
   __shared__ int sorted_blocks[64];
   __shared__ int count, is_last;
 
-  const int c = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  // chunk pieces are dispatched deepest first (grid z descending): the long
+  // units' full pieces start first and the small ones fill in behind them
+  const int c = static_cast<int>(gridDim.z) - 1 - static_cast<int>(blockIdx.z);
+  const int h = blockIdx.x, s = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t unit = static_cast<int64_t>(s) * a.hkv + h;
   const int grp = a.hq / a.hkv;
@@ -596,8 +599,11 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
   const bool keep0 = sink && nb > 0 && forced != 0;
   const int my_chunks = n_cand > 0 ? static_cast<int>((n_cand + a.chunk - 1) / a.chunk) : 1;
   if (c >= my_chunks) return;  // past this sequence's candidates
-  const int64_t r0 = static_cast<int64_t>(c) * a.chunk;
-  const int rows = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(a.chunk), n_cand - r0)));
+  // piece 0 is the partial one: rows [0, p); piece c >= 1 is rows
+  // [p + (c - 1) chunk, p + c chunk), a full chunk
+  const int64_t p0 = n_cand - static_cast<int64_t>(my_chunks - 1) * a.chunk;
+  const int64_t r0 = c == 0 ? 0 : p0 + static_cast<int64_t>(c - 1) * a.chunk;
+  const int rows = static_cast<int>(max(static_cast<int64_t>(0), c == 0 ? p0 : static_cast<int64_t>(a.chunk)));
   const int n_stages = (rows + kStageRows - 1) / kStageRows;
 
   if (tid == 0) {
@@ -860,7 +866,7 @@ cudaError_t launch_select(const T* q, int hq, const PrefillBatch* pb, const T* p
     da.cand = fused->cand;
     da.tickets = fused->tickets;
     cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(da.n_chunks, kv.hkv, batch);
+    lc.gridDim = dim3(kv.hkv, batch, da.n_chunks);
     lc.blockDim = dim3(kSelThreads, 1, 1);
     lc.dynamicSmemBytes = select_decode_smem(da.chunk);
     lc.stream = stream;

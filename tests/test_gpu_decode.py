@@ -297,6 +297,22 @@ def test_fused_step_without_forced_block(dev):
     verify_units(inp, res, all_units(inp), 6, 6, force_local=False)
 
 
+def test_fused_step_flat_scores(dev):
+    """Every key row equal, so every summary and every score ties: the
+    selection must be the lowest-index candidates (ties go to the lower
+    block). With 512 candidate rows per CTA (one unit, clusters of 16) and
+    k = 63, far more than 128 keys reach each selection threshold, so both the
+    CTA-local and the cluster selection take their sorting-network path."""
+    n_full = 6144
+    inp = make_decode_inputs([64 * n_full + 17], 1, 8, "bf16", "contiguous", seed=5, device=dev)
+    inp.k.copy_(inp.k[:, :, :1, :].expand_as(inp.k))
+    res = run_step(inp, 63, 64)
+    assert res["status"] == 0
+    want = O.select_blocks(np.zeros(n_full), 63, n_full, 64)
+    assert res["idx"][0, 0].cpu().tolist() == [int(b) for b in want]
+    verify_units(inp, res, [(0, 0)], 63, 64, check_needles=False)
+
+
 @pytest.mark.parametrize("name,units", [("decode_128k", [(0, 0), (4, 3), (7, 7)]), ("decode_1m", [(0, 1), (0, 7)])])
 def test_fused_step_full(dev, name, units):
     w = WORKLOADS[name]
