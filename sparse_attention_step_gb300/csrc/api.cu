@@ -39,6 +39,7 @@ msa_status device_info(DeviceInfo** out) {
     for (int i = 0; i < 5; ++i) d.step_clusters[i] = step_max_clusters(1 << i);
     d.topk_smem = (kMaxTopkCandidates + kTopkCandCap) * sizeof(uint32_t);
     if (set_topk_smem(d.topk_smem) != cudaSuccess) return MSA_ERR_CUDA;
+    if (set_qidx_smem() != cudaSuccess) return MSA_ERR_CUDA;
     if (set_select_decode_smem(select_decode_smem(4096)) != cudaSuccess) return MSA_ERR_CUDA;
     d.ready = true;
   }

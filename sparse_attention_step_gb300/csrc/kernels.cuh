@@ -61,6 +61,7 @@ size_t select_decode_smem(int chunk);
 size_t select_decode_cand_bytes(int64_t units, int n_chunks);
 cudaError_t set_select_decode_smem(size_t bytes);
 cudaError_t set_topk_smem(size_t bytes);
+cudaError_t set_qidx_smem();
 
 // ---- Step 2, decode (decode.cu) ----
 struct DecodeArgs {

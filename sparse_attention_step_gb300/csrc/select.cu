@@ -71,6 +71,57 @@ __global__ void __launch_bounds__(256) qidx_prefill_kernel(const T* __restrict__
   }
 }
 
+// bf16 q: the tile's rows (64 tokens x G heads, 256 bytes each; a token's G
+// heads are contiguous) are pulled into shared memory with 16-byte cp.async,
+// every piece in flight at once and no registers held while they travel, then
+// summed like the kernel above: 16 row slots per 16-byte piece of the dims,
+// the slots' partial sums added in slot order. grid (Hkv, n_tiles), 256
+// threads, dynamic shared memory 64 G x 256 bytes.
+constexpr int kQidxThreads = 256;
+__global__ void __launch_bounds__(kQidxThreads) qidx_prefill_bf16_kernel(const __nv_bfloat16* __restrict__ q, int hq,
+                                                                       int hkv, const PrefillBatch pb,
+                                                                       float* __restrict__ qidx) {
+  extern __shared__ __align__(16) uint8_t qrows[];  // [n_rows][256 B]
+  __shared__ float part[16][kHeadDim + 4];
+  const int h = blockIdx.x;
+  const int tile = blockIdx.y;  // global tile
+  const int grp = hq / hkv;
+  const int s = pb.seq_of_tile(tile);
+  const int j0 = (tile - pb.tile_off[s]) * kBlock;
+  const int r0 = pb.q_off[s] + j0;
+  const int n_rows = (min(pb.q_cnt[s], j0 + kBlock) - j0) * grp;  // token-major, head-minor
+  const int tid = threadIdx.x;
+  for (int i = tid; i < n_rows * 16; i += kQidxThreads) {
+    const int row = i >> 4, pc = i & 15;
+    const int t = row / grp, g = row - t * grp;
+    cp_async16(qrows + row * 256 + pc * 16,
+               q + (static_cast<int64_t>(r0 + t) * hq + h * grp + g) * kHeadDim + 8 * pc);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  const int e = tid & 15, slot = tid >> 4;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll 4
+  for (int row = slot; row < n_rows; row += 16) {
+    RawRow<__nv_bfloat16> x;
+    x.w = *reinterpret_cast<const uint4*>(qrows + row * 256 + 16 * e);
+    x.add_to(acc);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) part[slot][8 * e + j] = acc[j];
+  __syncthreads();
+  if (tid < kHeadDim) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) t += part[k][tid];
+    qidx[(static_cast<int64_t>(tile) * hkv + h) * kHeadDim + tid] = t;
+  }
+}
+constexpr size_t kQidxSmemMax = static_cast<size_t>(kBlock) * kMaxGroupHeads * 256;
+
 // ---------------------------------------------------------------------------
 // Block scores.
 // Decode:  grid (chunks, Hkv, batch); unit = s*Hkv + h; q_idx from q inline.
@@ -562,6 +613,47 @@ __device__ inline void choose_top(const uint64_t* keys, int n, int k, uint8_t* r
   block_topk(keys, n, k, reinterpret_cast<uint64_t*>(ring), top, count);
 }
 
+// Top-k of prefill tiles for k_scored <= 64 and at most 4096 candidates:
+// the scores become 64-bit selection keys (score, then lower block first) in
+// shared memory; the binned selection picks the k best, the threshold sort
+// (block_topk) takes the keys that crowd one bin. The list is written as the
+// radix top-k writes it. grid (Hkv, n_tiles), 256 threads; dynamic shared
+// memory topk64_smem(max_blocks).
+constexpr int kTopk64Threads = 256;
+constexpr int kTopk64MaxCand = 4096;
+__host__ __device__ inline int topk64_pad(int64_t n) {
+  int lists = 1;
+  while (static_cast<int64_t>(lists) * 64 < n) lists <<= 1;
+  return lists * 64 > 128 ? lists * 64 : 128;
+}
+size_t topk64_smem(int64_t max_blocks) {
+  return static_cast<size_t>(max_blocks + 2 * topk64_pad(max_blocks) + 64) * sizeof(uint64_t);
+}
+__global__ void __launch_bounds__(kTopk64Threads) topk64_prefill_kernel(const float* __restrict__ scores, TopkArgs a,
+                                                                      int32_t* __restrict__ idx_out) {
+  extern __shared__ __align__(16) uint64_t tk[];  // keys [max_blocks], then the threshold sort's scratch
+  __shared__ uint64_t top[64];
+  __shared__ SelectScratch scr;
+  __shared__ int sorted_blocks[64];
+  __shared__ int count;
+  const int h = blockIdx.x, tile = blockIdx.y;
+  const int64_t unit = static_cast<int64_t>(tile) * a.hkv + h;
+  const bool local = (a.force_local & kForceLocal) != 0, sink = (a.force_local & kForceSink) != 0;
+  const int seq = a.pb.seq_of_tile(tile);
+  const int64_t n64 = a.pb.q_start[seq] / kBlock + (tile - a.pb.tile_off[seq]);  // blocks before the diagonal
+  const int64_t forced = local ? n64 : -1;
+  const int skip = (sink && n64 > 0) ? 1 : 0;  // attention sink: block 0 kept, not scored
+  const bool keep0 = sink && forced != 0;
+  const int n = static_cast<int>(n64) - skip;
+  const int k = min(a.k_scored, n);
+  const float* sc = scores + unit * a.max_blocks;
+  for (int i = threadIdx.x; i < n; i += kTopk64Threads) tk[i] = sel_key(sc[i + skip], i + skip);
+  __syncthreads();
+  if (k > 0 && !block_select(tk, n, k, top, scr))
+    block_topk(tk, n, k, tk + a.max_blocks, top, &count);
+  write_selection(top, max(k, 0), forced, keep0, a.k_total, idx_out + unit * a.k_total, sorted_blocks);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* __restrict__ q,
                                                                    const T* __restrict__ pooled, KvView kv,
@@ -885,7 +977,12 @@ cudaError_t launch_select(const T* q, int hq, const PrefillBatch* pb, const T* p
     const int n_tiles = pb->total_tiles();
     outer = n_tiles;
     sa.n_tiles = n_tiles;
-    qidx_prefill_kernel<T><<<dim3(kv.hkv, n_tiles), 256, 0, stream>>>(q, hq, kv.hkv, *pb, qidx_ws);
+    if constexpr (sizeof(T) == 2) {
+      const size_t smem = static_cast<size_t>(kBlock) * (hq / kv.hkv) * 256;
+      qidx_prefill_bf16_kernel<<<dim3(kv.hkv, n_tiles), kQidxThreads, smem, stream>>>(q, hq, kv.hkv, *pb, qidx_ws);
+    } else {
+      qidx_prefill_kernel<T><<<dim3(kv.hkv, n_tiles), 256, 0, stream>>>(q, hq, kv.hkv, *pb, qidx_ws);
+    }
     constexpr int kT = 8;
     // only the chunks below the last tile's diagonal hold candidates
     int64_t last = 0;
@@ -905,6 +1002,11 @@ cudaError_t launch_select(const T* q, int hq, const PrefillBatch* pb, const T* p
   if (err != cudaSuccess) return err;
   TopkArgs ta{kv.hkv, prefill, cfg.force_local, cfg.k_scored, k_total, max_blocks, {}};
   if (prefill) ta.pb = *pb;
+  if (prefill && cfg.k_scored <= 64 && max_blocks <= kTopk64MaxCand) {
+    topk64_prefill_kernel<<<dim3(kv.hkv, outer), kTopk64Threads, topk64_smem(max_blocks), stream>>>(scores, ta,
+                                                                                                  idx_out);
+    return cudaGetLastError();
+  }
   const size_t smem = static_cast<size_t>(max_blocks + kCandCap) * sizeof(uint32_t);
   topk_kernel<<<dim3(kv.hkv, outer), topk_threads(max_blocks), smem, stream>>>(scores, kv, ta, idx_out, status);
   return cudaGetLastError();
@@ -932,6 +1034,14 @@ cudaError_t set_select_decode_smem(size_t bytes) {
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+cudaError_t set_qidx_smem() {
+  cudaError_t e = cudaFuncSetAttribute(qidx_prefill_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kQidxSmemMax));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(topk64_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(topk64_smem(kTopk64MaxCand)));
 }
 
 cudaError_t set_topk_smem(size_t bytes) {
