@@ -226,6 +226,11 @@ __device__ inline void cluster_sync() {
 __device__ inline void bar_sync_warps(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Arrive at named barrier `id` without waiting (the threads that bar.sync on
+// it see this thread's earlier shared-memory writes).
+__device__ inline void bar_arrive_warps(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 // The two halves of cluster_sync, for work that fits between them.
 __device__ inline void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 __device__ inline void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }

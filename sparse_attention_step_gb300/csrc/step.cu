@@ -43,6 +43,7 @@ constexpr int kStMaxChunk = 1024;                           // candidate rows pe
 constexpr int kStMaxList = 64;                              // selected blocks per CTA
 constexpr int kStMaxCluster = 16;
 constexpr int kStPrefetchExtra = 0;             // L2 prefetches per CTA beyond ceil(kk / C)
+constexpr int kStEarlyPrefetch = 4;             // blocks per CTA prefetched from the warp maxima
 constexpr int kStG = 8;                                     // heads per group handled
 constexpr int kStOS = kHeadDim + 4;                         // padded merge rows
 constexpr int kStRecv = 12;                                 // floats per pushed piece: O[8], M, L, pad
@@ -79,6 +80,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   __shared__ int32_t blocks[kStMaxList];
   __shared__ int sorted_blocks[64];
   __shared__ int n_blocks;
+  __shared__ uint64_t wbest[kStWarps];  // each compute warp's best key (early prefetch)
   __shared__ float qsum[kHeadDim];  // the group's index query (sum of its query heads), fp32
   __shared__ float wm[kStAttnWarps][kStG], wl[kStAttnWarps][kStG];
 
@@ -221,8 +223,25 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   // then merged pairwise. Key 0 pads and sorts last.
   uint64_t* lists = reinterpret_cast<uint64_t*>(ring);  // [kStMaxCluster][64]
   uint64_t* tmp = lists + kStMaxCluster * 64;           // [kStMaxCluster / 2][64]
+  const int kk = static_cast<int>(n_cand - skip < a.k_scored ? n_cand - skip : static_cast<int64_t>(a.k_scored));
   if (warp < kStWarps) {
     __syncwarp();
+    {
+      // The best key of the warp's first 64 rows goes to the producer, which
+      // pulls the K/V blocks of the CTA's leading warp maxima into L2 while
+      // the sort runs (HBM is otherwise idle then): the CTA's few best blocks
+      // are almost always among the unit's selection.
+      const int e0 = warp * 64 + 2 * lane;
+      const uint64_t x0 = e0 < rows ? keys[e0] : 0ull, x1 = e0 + 1 < rows ? keys[e0 + 1] : 0ull;
+      uint64_t m = x0 > x1 ? x0 : x1;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const uint64_t o = shfl_xor_u64(m, off);
+        m = o > m ? o : m;
+      }
+      if (lane == 0) wbest[warp] = m;
+      bar_arrive_warps(2, 32 * (kStWarps + 1));
+    }
     uint64_t run[2] = {0ull, 0ull};
     for (int b = warp * 64; b < rows; b += kStWarps * 64) {
       uint64_t x[2];
@@ -241,11 +260,31 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     }
     lists[warp * 64 + 2 * lane] = run[0];
     lists[warp * 64 + 2 * lane + 1] = run[1];
+  } else {
+    bar_sync_warps(2, 32 * (kStWarps + 1));
+    const uint64_t m = lane < kStWarps ? wbest[lane] : 0ull;
+    int rk = 0;
+#pragma unroll
+    for (int j = 0; j < kStWarps; ++j) {
+      const uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(m), j);
+      const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(m >> 32), j);
+      rk += ((static_cast<uint64_t>(hi) << 32) | lo) > m ? 1 : 0;
+    }
+    const int n_early = min(kStEarlyPrefetch, (kk + C - 1) / C / 2);  // half the CTA's share of the list
+    if (lane < kStWarps && m != 0ull && rk < n_early) {
+      const int64_t row = kv.block_row(s, h, sel_block(m), a.status, kIdDecode);
+      if (row >= 0) {
+        const int32_t y = static_cast<int32_t>(row);
+        tma_prefetch_2d(&tmk, 0, y);
+        tma_prefetch_2d(&tmk, 64, y);
+        tma_prefetch_2d(&tmv, 0, y);
+        tma_prefetch_2d(&tmv, 64, y);
+      }
+    }
   }
   __syncthreads();
   const uint64_t* mine = block_merge_lists(lists, tmp, kStWarps);
   if (tid < 64) xlist[tid] = mine[tid];
-  const int kk = static_cast<int>(n_cand - skip < a.k_scored ? n_cand - skip : static_cast<int64_t>(a.k_scored));
   // (b) every CTA of the cluster gathers the C lists through distributed
   // shared memory and merges them the same way, so each one holds the same
   // top 64 of the unit without a second cluster barrier. xlist is never
