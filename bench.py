@@ -247,8 +247,9 @@ def capture(torch, fn):
     return g
 
 
-def time_graph(torch, timer, g, steps, warmup, dist=None):
-    """Mean device time of one replay, L2 flushed before each timed replay."""
+def time_graph(torch, timer, g, steps, warmup, dist=None, samples=None):
+    """Mean device time of one replay, L2 flushed before each timed replay
+    (each replay's time is appended to ``samples`` when given)."""
     for _ in range(warmup):
         g.replay()
     torch.cuda.synchronize()
@@ -265,7 +266,19 @@ def time_graph(torch, timer, g, steps, warmup, dist=None):
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+    times = [a.elapsed_time(b) for a, b in ev]
+    if samples is not None:
+        samples.extend(times)
+    return statistics.mean(times)
+
+
+def quantiles_us(ms_samples):
+    """p10 / median / p90 of per-step times (ms in, microseconds out), this rank."""
+    xs = sorted(ms_samples)
+    if not xs:
+        return None
+    pick = lambda f: round(xs[min(len(xs) - 1, int(f * len(xs)))] * 1e3, 3)
+    return {"p10": pick(0.1), "p50": round(statistics.median(xs) * 1e3, 3), "p90": pick(0.9)}
 
 
 def decode_step(msa, st, q, out=None):
@@ -275,7 +288,7 @@ def decode_step(msa, st, q, out=None):
                                st["out"] if out is None else out, st["lse"], st["ws"].buf, st["ws"].nbytes)
 
 
-def time_decode(torch, msa, timer, st, inp, steps, warmup, dist):
+def time_decode(torch, msa, timer, st, inp, steps, warmup, dist, samples=None):
     """Times the step (msa_sparse_decode_step) as one CUDA graph replay, and
     the two-kernel form (select, then attend; each its own graph) for the
     per-kernel figures."""
@@ -288,7 +301,7 @@ def time_decode(torch, msa, timer, st, inp, steps, warmup, dist):
     g_step = capture(torch, lambda: decode_step(msa, st, q))
     g_sel = capture(torch, lambda: decode_select(msa, st, q))
     g_att = capture(torch, lambda: decode_attend(msa, st, q))
-    step = time_graph(torch, timer, g_step, steps, warmup, dist)
+    step = time_graph(torch, timer, g_step, steps, warmup, dist, samples)
     sel = time_graph(torch, timer, g_sel, steps, warmup)
     att = time_graph(torch, timer, g_att, steps, warmup)
     return step, sel, att
@@ -468,7 +481,8 @@ def run_ours(args):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.5)
-    step_ms, sel_ms, att_ms = time_decode(torch, msa, timer, st, inp, args.steps, args.warmup, dist)
+    step_samples = []
+    step_ms, sel_ms, att_ms = time_decode(torch, msa, timer, st, inp, args.steps, args.warmup, dist, step_samples)
     clk = clocks.stop()
     step_ms = dist.max(step_ms)
     att_ms = dist.max(att_ms)
@@ -513,6 +527,7 @@ def run_ours(args):
                     "CUDA graph; summary keys pooled beforehand",
         },
         "tokens_per_s": round(args.batch * world / (step_ms * 1e-3), 1),
+        "step_us_quantiles": quantiles_us(step_samples),
         "step_GBps": round(step_gbps, 1),
         "step_bytes": step_bytes,
         "roofline": {"kernel": "decode_step_kernel (fused scores + top-k + sparse flash-decode)", "bound": "hbm",

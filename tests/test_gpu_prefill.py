@@ -112,6 +112,23 @@ def test_prefill_all_blocks_equals_dense(dev):
     verify_tiles(inp, res, range(3), range(2), 1000, 1001, check_dense=True)
 
 
+def test_prefill_flat_scores(dev):
+    """Every key row equal, so every summary score of a tile ties: each tile
+    keeps its lowest-index candidates (ties go to the lower block). All keys
+    fall in one bin of the binned selection and more than 128 reach the
+    threshold, so the top-k runs its full sorting-network path."""
+    inp = make_prefill_inputs(64 * 300, 64 * 2 + 11, 2, 16, "bf16", seed=12, device=dev)
+    inp.k.copy_(inp.k[:, :, :1, :].expand_as(inp.k))
+    res = run_prefill(inp, 32, 33)
+    assert res["status"] == 0
+    for j in range(3):
+        diag = inp.q_start // 64 + j
+        want = [int(b) for b in O.select_blocks(np.zeros(diag), 32, diag, 33)]
+        for h in range(2):
+            assert res["idx"][j, h].cpu().tolist() == want, f"tile {j} head {h}"
+    verify_tiles(inp, res, range(3), range(2), 32, 33, rows_per_tile=5)
+
+
 def test_prefill_from_empty_prefix(dev):
     inp = make_prefill_inputs(0, 64 * 4, 2, 16, "bf16", seed=8, device=dev)
     res = run_prefill(inp, 2, 3, dense=True)
