@@ -55,8 +55,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="time only the headline workload")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--only", choices=["prefill"], default=None,
-                    help="time only the chunked-prefill workload and print its figures (profiling)")
+    ap.add_argument("--only", choices=["prefill", "token_max"], default=None,
+                    help="time only the chunked-prefill or the token-max decode workload and print its figures "
+                         "(profiling)")
     ap.add_argument("--batch", type=int, default=8,
                     help="sequences of the 131072-token decode workload (8 = the benchmark; fewer for profiling)")
     return ap.parse_args()
@@ -662,21 +663,24 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def run_prefill_only(args):
+def run_only(args):
     import torch
     from sparse_attention_step_gb300 import build, msa
     build.build()
     msa.load()
-    _, tf_burst, _, _ = peaks()
+    hbm, tf_burst, _, _ = peaks()
     timer = Timer(torch)
-    res = extras_prefill(torch, msa, timer, args.steps, args.warmup, tf_burst)
+    if args.only == "prefill":
+        res = extras_prefill(torch, msa, timer, args.steps, args.warmup, tf_burst)
+    else:
+        res = extras_token_max(torch, msa, timer, args.steps, args.warmup, hbm)
     print(json.dumps(res), flush=True)
 
 
 def main():
     args = parse()
-    if args.only == "prefill":
-        run_prefill_only(args)
+    if args.only is not None:
+        run_only(args)
         return
     if args.impl == "reference":
         run_reference(args)

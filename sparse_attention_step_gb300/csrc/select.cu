@@ -613,12 +613,13 @@ __device__ inline void choose_top(const uint64_t* keys, int n, int k, uint8_t* r
   block_topk(keys, n, k, reinterpret_cast<uint64_t*>(ring), top, count);
 }
 
-// Top-k of prefill tiles for k_scored <= 64 and at most 4096 candidates:
-// the scores become 64-bit selection keys (score, then lower block first) in
-// shared memory; the binned selection picks the k best, the threshold sort
-// (block_topk) takes the keys that crowd one bin. The list is written as the
-// radix top-k writes it. grid (Hkv, n_tiles), 256 threads; dynamic shared
-// memory topk64_smem(max_blocks).
+// Top-k for k_scored <= 64 and at most 4096 candidates (prefill tiles, and
+// decode scores computed apart, as in token-max mode): the scores become
+// 64-bit selection keys (score, then lower block first) in shared memory;
+// the binned selection picks the k best, the threshold sort (block_topk)
+// takes the keys that crowd one bin. The list is written as the radix top-k
+// writes it. grid (Hkv, outer) with outer = batch (decode) or n_tiles
+// (prefill), 256 threads; dynamic shared memory topk64_smem(max_blocks).
 constexpr int kTopk64Threads = 256;
 constexpr int kTopk64MaxCand = 4096;
 __host__ __device__ inline int topk64_pad(int64_t n) {
@@ -629,21 +630,32 @@ __host__ __device__ inline int topk64_pad(int64_t n) {
 size_t topk64_smem(int64_t max_blocks) {
   return static_cast<size_t>(max_blocks + 2 * topk64_pad(max_blocks) + 64) * sizeof(uint64_t);
 }
-__global__ void __launch_bounds__(kTopk64Threads) topk64_prefill_kernel(const float* __restrict__ scores, TopkArgs a,
-                                                                      int32_t* __restrict__ idx_out) {
+__global__ void __launch_bounds__(kTopk64Threads) topk64_kernel(const float* __restrict__ scores, KvView kv, TopkArgs a,
+                                                              int32_t* __restrict__ idx_out, int32_t* status) {
   extern __shared__ __align__(16) uint64_t tk[];  // keys [max_blocks], then the threshold sort's scratch
   __shared__ uint64_t top[64];
   __shared__ SelectScratch scr;
   __shared__ int sorted_blocks[64];
   __shared__ int count;
-  const int h = blockIdx.x, tile = blockIdx.y;
-  const int64_t unit = static_cast<int64_t>(tile) * a.hkv + h;
+  const int h = blockIdx.x, outer = blockIdx.y;
+  const int64_t unit = static_cast<int64_t>(outer) * a.hkv + h;
   const bool local = (a.force_local & kForceLocal) != 0, sink = (a.force_local & kForceSink) != 0;
-  const int seq = a.pb.seq_of_tile(tile);
-  const int64_t n64 = a.pb.q_start[seq] / kBlock + (tile - a.pb.tile_off[seq]);  // blocks before the diagonal
-  const int64_t forced = local ? n64 : -1;
+  int64_t n64, forced, nb;  // candidates, the kept newest / diagonal block, blocks in view
+  if (!a.prefill) {
+    const int64_t len = kv.seq_len(outer, status, kIdTopk);
+    nb = (len + kBlock - 1) / kBlock;
+    const int64_t nbf = len / kBlock;
+    n64 = local ? min(nbf, nb - 1) : nbf;
+    forced = (local && nb > 0) ? nb - 1 : -1;
+  } else {
+    const int seq = a.pb.seq_of_tile(outer);
+    n64 = a.pb.q_start[seq] / kBlock + (outer - a.pb.tile_off[seq]);  // blocks before the diagonal
+    nb = n64 + 1;
+    forced = local ? n64 : -1;
+  }
+  if (n64 < 0) n64 = 0;
   const int skip = (sink && n64 > 0) ? 1 : 0;  // attention sink: block 0 kept, not scored
-  const bool keep0 = sink && forced != 0;
+  const bool keep0 = sink && nb > 0 && forced != 0;
   const int n = static_cast<int>(n64) - skip;
   const int k = min(a.k_scored, n);
   const float* sc = scores + unit * a.max_blocks;
@@ -1003,8 +1015,8 @@ cudaError_t launch_select(const T* q, int hq, const PrefillBatch* pb, const T* p
   TopkArgs ta{kv.hkv, prefill, cfg.force_local, cfg.k_scored, k_total, max_blocks, {}};
   if (prefill) ta.pb = *pb;
   if (prefill && cfg.k_scored <= 64 && max_blocks <= kTopk64MaxCand) {
-    topk64_prefill_kernel<<<dim3(kv.hkv, outer), kTopk64Threads, topk64_smem(max_blocks), stream>>>(scores, ta,
-                                                                                                  idx_out);
+    topk64_kernel<<<dim3(kv.hkv, outer), kTopk64Threads, topk64_smem(max_blocks), stream>>>(scores, kv, ta, idx_out,
+                                                                                          status);
     return cudaGetLastError();
   }
   const size_t smem = static_cast<size_t>(max_blocks + kCandCap) * sizeof(uint32_t);
@@ -1017,6 +1029,11 @@ cudaError_t launch_topk_scores(const float* scores, const KvView& kv, int batch,
                                int32_t* idx_out, int k_total, int32_t* status, cudaStream_t stream) {
   const int64_t max_blocks = kv.max_blocks();
   TopkArgs ta{kv.hkv, 0, cfg.force_local, cfg.k_scored, k_total, max_blocks, {}};
+  if (cfg.k_scored <= 64 && max_blocks <= kTopk64MaxCand) {
+    topk64_kernel<<<dim3(kv.hkv, batch), kTopk64Threads, topk64_smem(max_blocks), stream>>>(scores, kv, ta, idx_out,
+                                                                                          status);
+    return cudaGetLastError();
+  }
   const size_t smem = static_cast<size_t>(max_blocks + kCandCap) * sizeof(uint32_t);
   topk_kernel<<<dim3(kv.hkv, batch), topk_threads(max_blocks), smem, stream>>>(scores, kv, ta, idx_out, status);
   return cudaGetLastError();
@@ -1040,7 +1057,7 @@ cudaError_t set_qidx_smem() {
   cudaError_t e = cudaFuncSetAttribute(qidx_prefill_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kQidxSmemMax));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(topk64_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(topk64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(topk64_smem(kTopk64MaxCand)));
 }
 
