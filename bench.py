@@ -363,6 +363,21 @@ def extras_decode(torch, msa, timer, name, steps, warmup, hbm):
         "dense_us": dense_ms * 1e3, "dense_GBps": dense_bytes / (dense_ms * 1e-3) / 1e9,
         "dense_over_sparse": dense_ms / step_ms, "device_status": status,
     }
+    if name == "decode_1m":
+        # context point (not the headline): k near the ratio the guide implies
+        # (~6.4% of 16384 blocks); k > 64 runs the selection and attention
+        # kernels in turn
+        k_big = 1050
+        st2 = decode_setup(torch, msa, inp, k_big, k_big + 1)
+        st2["pooled"] = st["pooled"]
+        big_ms = time_op(torch, timer, lambda: decode_step(msa, st2, inp.q), max(5, steps // 2), 2)
+        pb2, sb2, qb2 = decode_bytes(inp, k_big + 1)
+        res["k1050"] = {"k_scored": k_big, "us_per_step": big_ms * 1e3,
+                        "step_GBps": (pb2 + sb2 + qb2) / (big_ms * 1e-3) / 1e9,
+                        "step_roofline_frac": (pb2 + sb2 + qb2) / (big_ms * 1e-3) / 1e9 / hbm,
+                        "bytes_per_step": pb2 + sb2 + qb2, "dense_over_sparse": dense_ms / big_ms,
+                        "device_status": msa.msa_read_device_status(st2["ws"].buf)}
+        del st2
     del inp, st
     torch.cuda.empty_cache()
     return res
