@@ -409,3 +409,34 @@ def test_sink_selection_edge_cases():
     assert list(sel) == [0, 2, 3, 4]
     # without the sink flag on the block the same scores select block 0 as a scored block
     assert list(O.select_blocks(np.array([9.0, 1.0, 3.0, 2.0]), 2, 4, 4)) == [0, 2, 4, -1]
+
+
+# --------------------------------------------------------------------------- small helpers, pinned directly
+
+def test_store_as_matches_torch_storage():
+    # the value a float32 takes once stored: torch's own bf16 / fp32 conversions
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(4096) * np.exp2(rng.integers(-20, 20, 4096))).astype(np.float32)
+    want_bf16 = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.store_as(x, "bf16"), want_bf16)
+    assert np.array_equal(O.store_as(x, "f32"), x.astype(np.float64))
+    with pytest.raises(ValueError):
+        O.store_as(x, "f16")
+
+
+@pytest.mark.parametrize("n,full,total", [(0, 0, 0), (1, 0, 1), (63, 0, 1), (64, 1, 1), (65, 1, 2), (128, 2, 2),
+                                          (131072, 2048, 2048), (131071, 2047, 2048)])
+def test_block_counts_closed_form(n, full, total):
+    assert O.num_full_blocks(n) == full
+    assert O.num_blocks(n) == total
+
+
+def test_boundary_gap_definition():
+    # the k-th and (k+1)-th largest scores; None when every candidate is kept
+    s = np.array([0.5, 3.0, -1.0, 2.0, 2.0, 7.0])
+    assert O.boundary_gap(s, 1) == (7.0, 3.0)
+    assert O.boundary_gap(s, 3) == (2.0, 2.0)   # a tie at the boundary
+    assert O.boundary_gap(s, 5) == (0.5, -1.0)
+    assert O.boundary_gap(s, 6) is None
+    assert O.boundary_gap(s, 0) is None
+    assert O.boundary_gap(np.array([]), 3) is None
