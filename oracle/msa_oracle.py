@@ -299,6 +299,22 @@ def prefill_tile_select(q_tile, tile_index, q_start, pooled, k_scored, k_total):
     return dict(selected=sel, scores=scores, q_idx=q_idx, diag=diag)
 
 
+def prefill_tile_select_token_max(q_tile, tile_index, q_start, kidx_rows, k_scored, k_total):
+    """Selection for one (64-query tile, KV head) of a chunked prefill with the
+    guide-literal block score: the tile's index query (sum over its tokens and
+    the group's heads) against every token of the shared index-key head, max
+    over each block's 64 tokens; candidates are the blocks before the tile's
+    diagonal block q_start/64 + tile_index, which is always kept. Guide §1,
+    Step 1 as drawn, and §3 (in prefill the index branch scans the whole
+    input).
+    """
+    diag = int(q_start) // BLOCK + int(tile_index)
+    q_idx = index_query(q_tile)
+    scores = score_blocks_token_max(q_idx, kidx_rows, diag)
+    sel = select_blocks(scores, k_scored, diag, k_total)
+    return dict(selected=sel, scores=scores, q_idx=q_idx, diag=diag)
+
+
 def prefill_rows(q_rows, positions, k_rows, v_rows, seq_len, blocks, scale):
     """Causal attention of prefill query rows over the selected blocks.
 

@@ -381,6 +381,38 @@ def test_index_key_needles_are_selected_by_token_max():
         assert sorted(ik.needles[(0, h)]) == [b for b in res["selected"] if b != 40]
 
 
+def test_prefill_token_max_one_token_tile_equals_decode():
+    # a prefill tile holding one token at a block start sees exactly what a
+    # decode step with that token as its newest sees: the same index query, the
+    # same candidates (the blocks before it) and the same kept block
+    rng = np.random.default_rng(23)
+    q_start = 64 * 9
+    kidx = rng.standard_normal((q_start + 64, O.HEAD_DIM))
+    q_tok = rng.standard_normal((1, 4, O.HEAD_DIM))
+    for k in (1, 4, 9, 12):
+        pre = O.prefill_tile_select_token_max(q_tok, 0, q_start, kidx, k, k + 1)
+        dec = O.select_token_max(q_tok[0], kidx, q_start + 1, k, k + 1)
+        assert list(pre["selected"]) == list(dec["selected"])
+        np.testing.assert_array_equal(pre["scores"], dec["scores"])
+        assert pre["diag"] == dec["forced"] == 9
+
+
+def test_prefill_token_max_brute_force():
+    # index query = sum over the tile's tokens and heads; score = max token score
+    # of each block before the diagonal; a hot token makes its block win
+    rng = np.random.default_rng(24)
+    q_tile = rng.standard_normal((7, 3, O.HEAD_DIM))
+    kidx = rng.standard_normal((64 * 6, O.HEAD_DIM))
+    q_idx = q_tile.sum(axis=(0, 1))
+    kidx[64 * 2 + 40] = 5.0 * q_idx / np.linalg.norm(q_idx)
+    res = O.prefill_tile_select_token_max(q_tile, 1, 64 * 4, kidx, 1, 3)
+    assert res["diag"] == 5
+    want = [max(math.fsum(float(q_idx[d]) * float(kidx[b * 64 + t, d]) for d in range(O.HEAD_DIM))
+                for t in range(64)) for b in range(5)]
+    np.testing.assert_allclose(res["scores"], want, rtol=1e-12, atol=1e-12)
+    assert list(res["selected"]) == [2, 5, -1]
+
+
 # --------------------------------------------------------------------------- attention sink
 
 @pytest.mark.parametrize("trial", range(30))
