@@ -168,12 +168,14 @@ msa_status msa_pool_block_keys(const msa_kv_desc* kv /* host */, int64_t first_b
  * scores_out (nullable): [units, max_blocks] fp32 raw scores of the candidate
  * blocks (max_blocks = max_tokens/64 or max_pages_per_seq); other entries are
  * left unspecified.
- * cfg->mode == MSA_SCORE_TOKEN_MAX (decode, bf16, Hkv <= 8; else
+ * cfg->mode == MSA_SCORE_TOKEN_MAX (bf16, Hkv <= 8; else
  *   MSA_ERR_UNSUPPORTED): `pooled` is the index-key cache instead, one shared
  *   head laid out like one KV head of the cache -- contiguous
  *   [batch, max_tokens, 128], paged [num_pages, 64, 128] on the cache's pages
- *   -- and the score of block b is max_{t in b} q_idx . K_idx[t] (fp32). The
- *   index keys of a sequence are read once for all of its KV heads. */
+ *   -- and the score of block b is max_{t in b} q_idx . K_idx[t] (fp32), for
+ *   decode and for prefill tiles alike. The index keys of a sequence are read
+ *   once for all of its KV heads (decode) or once per group of 8 tiles
+ *   (prefill). */
 msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_q_tokens,
                                   const void* pooled, const msa_kv_desc* kv /* host */,
                                   const msa_select_cfg* cfg /* host */, int32_t* idx_out, int32_t k_total,
@@ -191,9 +193,9 @@ msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_
  * tile_off[s] + j, exactly what msa_select_topk_blocks (q_tile 64, q_start =
  * q_starts[s]) gives for tile j of sequence s alone, scored against sequence
  * s's summaries (pooled [batch, Hkv, max_blocks, 128] contiguous, or the
- * cache's pages). cfg->q_tile must be 64 (cfg->q_start is ignored); fp32
- * caches take one sequence only (MSA_ERR_UNSUPPORTED above), token-max mode is
- * not supported. A batch with no new tokens queues nothing. */
+ * cache's pages; in token-max mode the index-key cache). cfg->q_tile must be
+ * 64 (cfg->q_start is ignored); fp32 caches take one sequence only
+ * (MSA_ERR_UNSUPPORTED above). A batch with no new tokens queues nothing. */
 msa_status msa_select_topk_blocks_varlen(const void* q, int32_t num_q_heads, int32_t n_seqs,
                                          const int64_t* q_starts /* host */, const int32_t* q_counts /* host */,
                                          const void* pooled, const msa_kv_desc* kv /* host */,

@@ -347,12 +347,16 @@ msa_status select_common(const void* q, int32_t num_q_heads, int32_t n_q_tokens,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cfg->mode == MSA_SCORE_TOKEN_MAX) {
     // `pooled` holds the shared index-key head: [batch, max_tokens, 128] or [num_pages, 64, 128]
-    if (prefill || kv->dtype != MSA_DTYPE_BF16 || kv->num_kv_heads > 8) return MSA_ERR_UNSUPPORTED;
+    if (kv->dtype != MSA_DTYPE_BF16 || kv->num_kv_heads > 8) return MSA_ERR_UNSUPPORTED;
     const int64_t rows = kv->layout == MSA_KV_CONTIGUOUS ? static_cast<int64_t>(kv->batch) * kv->max_tokens
                                                          : static_cast<int64_t>(kv->num_pages) * kBlock;
     if (rows >= (int64_t(1) << 31)) return MSA_ERR_UNSUPPORTED;
     CUtensorMap tmi;
     if ((st = make_kv_map(&tmi, pooled, rows)) != MSA_OK) return st;
+    if (prefill)
+      return cuda_status(launch_select_token_max_prefill(tmi, static_cast<const __nv_bfloat16*>(q), num_q_heads, *pb,
+                                                         view, *cfg, idx_out, k_total, scores, qidx, ws_status(ws),
+                                                         s));
     if ((st = cuda_status(launch_token_max_scores(tmi, view, kv->batch, static_cast<const __nv_bfloat16*>(q),
                                                   num_q_heads, cfg->force_local, scores, ws_status(ws), s))) != MSA_OK)
       return st;

@@ -115,6 +115,12 @@ cudaError_t set_step_smem();
 
 // ---- token-level max-pooled scores (token_max.cu) ----
 cudaError_t set_token_max_smem();
+cudaError_t launch_token_max_prefill_scores(const CUtensorMap& tmi, const KvView& kv, const PrefillBatch& pb,
+                                            const float* qidx, float* scores, int32_t* status, cudaStream_t stream);
+cudaError_t launch_select_token_max_prefill(const CUtensorMap& tmi, const __nv_bfloat16* q, int hq,
+                                            const PrefillBatch& pb, const KvView& kv, const msa_select_cfg& cfg,
+                                            int32_t* idx_out, int k_total, float* scores, float* qidx_ws,
+                                            int32_t* status, cudaStream_t stream);
 cudaError_t launch_token_max_scores(const CUtensorMap& tmi, const KvView& kv, int batch, const __nv_bfloat16* q,
                                     int hq, int force_local, float* scores, int32_t* status, cudaStream_t stream);
 cudaError_t launch_topk_scores(const float* scores, const KvView& kv, int batch, const msa_select_cfg& cfg,

@@ -948,6 +948,20 @@ size_t select_decode_cand_bytes(int64_t units, int n_chunks) {
 // ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
+// The top-k over scores in `scores`: the key-based kernel for k <= 64 of at
+// most 4096 candidates, else the radix select. grid (Hkv, outer).
+static cudaError_t launch_topk(const float* scores, const KvView& kv, const TopkArgs& ta, int outer,
+                               int32_t* idx_out, int32_t* status, cudaStream_t stream) {
+  if (ta.k_scored <= 64 && ta.max_blocks <= kTopk64MaxCand) {
+    topk64_kernel<<<dim3(kv.hkv, outer), kTopk64Threads, topk64_smem(ta.max_blocks), stream>>>(scores, kv, ta,
+                                                                                             idx_out, status);
+    return cudaGetLastError();
+  }
+  const size_t smem = static_cast<size_t>(ta.max_blocks + kCandCap) * sizeof(uint32_t);
+  topk_kernel<<<dim3(kv.hkv, outer), topk_threads(ta.max_blocks), smem, stream>>>(scores, kv, ta, idx_out, status);
+  return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_select(const T* q, int hq, const PrefillBatch* pb, const T* pooled, const KvView& kv, int batch,
                           const msa_select_cfg& cfg, int32_t* idx_out, int k_total, float* scores, float* qidx_ws,
@@ -1014,29 +1028,30 @@ cudaError_t launch_select(const T* q, int hq, const PrefillBatch* pb, const T* p
   if (err != cudaSuccess) return err;
   TopkArgs ta{kv.hkv, prefill, cfg.force_local, cfg.k_scored, k_total, max_blocks, {}};
   if (prefill) ta.pb = *pb;
-  if (prefill && cfg.k_scored <= 64 && max_blocks <= kTopk64MaxCand) {
-    topk64_kernel<<<dim3(kv.hkv, outer), kTopk64Threads, topk64_smem(max_blocks), stream>>>(scores, kv, ta, idx_out,
-                                                                                          status);
-    return cudaGetLastError();
-  }
-  const size_t smem = static_cast<size_t>(max_blocks + kCandCap) * sizeof(uint32_t);
-  topk_kernel<<<dim3(kv.hkv, outer), topk_threads(max_blocks), smem, stream>>>(scores, kv, ta, idx_out, status);
-  return cudaGetLastError();
+  return launch_topk(scores, kv, ta, outer, idx_out, status, stream);
 }
 
 // Top-k over decode scores already in `scores` ([batch, hkv, max_blocks]).
 cudaError_t launch_topk_scores(const float* scores, const KvView& kv, int batch, const msa_select_cfg& cfg,
                                int32_t* idx_out, int k_total, int32_t* status, cudaStream_t stream) {
-  const int64_t max_blocks = kv.max_blocks();
-  TopkArgs ta{kv.hkv, 0, cfg.force_local, cfg.k_scored, k_total, max_blocks, {}};
-  if (cfg.k_scored <= 64 && max_blocks <= kTopk64MaxCand) {
-    topk64_kernel<<<dim3(kv.hkv, batch), kTopk64Threads, topk64_smem(max_blocks), stream>>>(scores, kv, ta, idx_out,
-                                                                                          status);
-    return cudaGetLastError();
-  }
-  const size_t smem = static_cast<size_t>(max_blocks + kCandCap) * sizeof(uint32_t);
-  topk_kernel<<<dim3(kv.hkv, batch), topk_threads(max_blocks), smem, stream>>>(scores, kv, ta, idx_out, status);
-  return cudaGetLastError();
+  TopkArgs ta{kv.hkv, 0, cfg.force_local, cfg.k_scored, k_total, kv.max_blocks(), {}};
+  return launch_topk(scores, kv, ta, batch, idx_out, status, stream);
+}
+
+// Token-max selection of prefill tiles (bf16): the tiles' index queries, the
+// token-level block maxima against the shared index-key head, then the top-k.
+cudaError_t launch_select_token_max_prefill(const CUtensorMap& tmi, const __nv_bfloat16* q, int hq,
+                                            const PrefillBatch& pb, const KvView& kv, const msa_select_cfg& cfg,
+                                            int32_t* idx_out, int k_total, float* scores, float* qidx_ws,
+                                            int32_t* status, cudaStream_t stream) {
+  const int n_tiles = pb.total_tiles();
+  const size_t smem = static_cast<size_t>(kBlock) * (hq / kv.hkv) * 256;
+  qidx_prefill_bf16_kernel<<<dim3(kv.hkv, n_tiles), kQidxThreads, smem, stream>>>(q, hq, kv.hkv, pb, qidx_ws);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  if ((err = launch_token_max_prefill_scores(tmi, kv, pb, qidx_ws, scores, status, stream)) != cudaSuccess) return err;
+  TopkArgs ta{kv.hkv, 1, cfg.force_local, cfg.k_scored, k_total, kv.max_blocks(), pb};
+  return launch_topk(scores, kv, ta, n_tiles, idx_out, status, stream);
 }
 
 cudaError_t set_select_decode_smem(size_t bytes) {

@@ -103,3 +103,66 @@ def test_token_max_decode_128k_sampled(dev):
     verify(inp, ik, res, [(0, 0), (3, 5), (7, 7)], 31, 32, stats)
     del inp, ik
     torch.cuda.empty_cache()
+
+
+# --------------------------------------------------------------------------- prefill tiles
+
+def run_token_max_prefill(inp, ik, k_scored, k_total, sink=False):
+    from sparse_attention_step_gb300 import msa
+    c = inp.cache
+    dev = inp.q.device
+    desc = msa.kv_desc(c.k, c.v, c.seq_lens, c.page_table)
+    hq, hkv = c.num_q_heads, c.num_kv_heads
+    n_tiles = msa.varlen_tiles(inp.q_counts)
+    ws = msa.Workspace(msa.msa_workspace_size(msa.MSA_OP_SELECT_PREFILL, desc, hq, 64 * n_tiles, k_total), dev)
+    max_blocks = desc.max_tokens // 64 if desc.layout == 0 else desc.max_pages_per_seq
+    idx = torch.full((n_tiles, hkv, k_total), -7, dtype=torch.int32, device=dev)
+    scores = torch.full((n_tiles * hkv, max_blocks), float("nan"), dtype=torch.float32, device=dev)
+    cfg = msa.select_cfg(k_scored, True, 64, mode=msa.MSA_SCORE_TOKEN_MAX, sink=sink)
+    msa.msa_select_topk_blocks_varlen(inp.q, hq, inp.q_starts, inp.q_counts, ik.kidx, desc, cfg, idx, k_total, scores,
+                                      ws.buf, ws.nbytes)
+    torch.cuda.synchronize()
+    return dict(idx=idx, scores=scores, status=msa.msa_read_device_status(ws.buf))
+
+
+@pytest.mark.parametrize("layout,hq,hkv", [("contiguous", 64, 8), ("paged", 16, 4), ("contiguous", 8, 1)])
+def test_token_max_prefill_tiles(dev, layout, hq, hkv):
+    # ragged chunks over a shared index-key head: one spanning two groups of 8
+    # tiles, one from an empty prefix, a 5-token one
+    from synth import make_prefill_batch_inputs
+    q_starts = [64 * 23, 0, 64 * 7, 64 * 40]
+    q_counts = [64 * 2 + 17, 64 * 3, 5, 64 * 9 + 1]
+    inp = make_prefill_batch_inputs(q_starts, q_counts, hkv, hq, "bf16", layout, seed=95, device=dev)
+    ik = make_index_keys(inp.cache, needles=2, seed=96)
+    k_scored, k_total = 6, 7
+    res = run_token_max_prefill(inp, ik, k_scored, k_total)
+    assert res["status"] == 0
+    grp = hq // hkv
+    for s, (q0, n) in enumerate(zip(q_starts, q_counts)):
+        kidx = to64(ik.rows(inp.cache, s))
+        qs = inp.q_rows(s)
+        for j in range((n + 63) // 64):
+            g = inp.tile_off[s] + j
+            for h in range(hkv):
+                q_tile = to64(qs[64 * j:min(n, 64 * j + 64), h * grp:(h + 1) * grp])
+                ref = O.prefill_tile_select_token_max(q_tile, j, q0, kidx, k_scored, k_total)
+                if ref["diag"] > 0:
+                    got = to64(res["scores"][g * hkv + h, :ref["diag"]])
+                    lim = 1e-5 * np.maximum(1.0, np.abs(ref["scores"])) + 1e-5 * np.abs(ref["q_idx"]).sum()
+                    assert (np.abs(got - ref["scores"]) <= lim).all(), f"token-max scores differ, seq {s} tile {j}"
+                check_selection(res["idx"][g, h].cpu().numpy(), ref["scores"], k_scored, ref["diag"], k_total)
+
+
+def test_token_max_prefill_sink(dev):
+    from synth import make_prefill_batch_inputs
+    from tests.test_gpu_sink import check_sink_row
+    inp = make_prefill_batch_inputs([64 * 12], [64 * 2 + 3], 2, 16, "bf16", "contiguous", seed=97, device=dev)
+    ik = make_index_keys(inp.cache, needles=1, seed=98)
+    res = run_token_max_prefill(inp, ik, 4, 6, sink=True)
+    assert res["status"] == 0
+    kidx = to64(ik.rows(inp.cache, 0))
+    for j in range(3):
+        for h in range(2):
+            q_tile = to64(inp.q[64 * j:min(131, 64 * j + 64), 8 * h:8 * h + 8])
+            ref = O.prefill_tile_select_token_max(q_tile, j, 64 * 12, kidx, 4, 6)
+            check_sink_row(res["idx"][j, h].cpu().numpy(), ref["scores"], 4, ref["diag"], 6, True)
