@@ -440,6 +440,14 @@ def extras_prefill(torch, msa, timer, steps, warmup, tflops_peak):
         inp.q, hq, n, inp.q_start, desc, idx, kt, SCALE, out, None, ws.buf, ws.nbytes), steps, warmup)
     dense_ms = time_op(torch, timer, lambda: msa.msa_dense_gqa_prefill(
         inp.q, hq, n, inp.q_start, desc, SCALE, out, None, ws.buf, ws.nbytes), 3, 1)
+    # the guide-literal Step 1 on the same chunk: token scores against one shared
+    # bf16 index-key head (N(0,1), seeded), block max pool, top-k
+    g_idx = torch.Generator(device="cuda")
+    g_idx.manual_seed(4007)
+    kidx = torch.randn(1, desc.max_tokens, 128, generator=g_idx, device="cuda").to(torch.bfloat16)
+    cfg_tm = msa.select_cfg(w["k_scored"], True, 64, inp.q_start, mode=msa.MSA_SCORE_TOKEN_MAX)
+    sel_tm_ms = time_op(torch, timer, lambda: msa.msa_select_topk_blocks(
+        inp.q, hq, n, kidx, desc, cfg_tm, idx, kt, None, ws.buf, ws.nbytes), steps, warmup)
     grp = hq // inp.num_kv_heads
     # algorithmic FLOPs: 4 * D per visible (query row, key) pair
     sel_pairs = 0
@@ -460,9 +468,10 @@ def extras_prefill(torch, msa, timer, steps, warmup, tflops_peak):
         "dense_us": dense_ms * 1e3, "dense_TFLOPs": dense_flop / (dense_ms * 1e-3) / 1e12,
         "dense_over_sparse_step": dense_ms / (sel_ms + att_ms),
         "pool_us": pool_ms * 1e3, "pool_GBps": total * inp.num_kv_heads * 256 / (pool_ms * 1e-3) / 1e9,
+        "select_token_max_us": sel_tm_ms * 1e3,
         "device_status": status,
     }
-    del inp, pooled, out
+    del inp, pooled, out, kidx
     torch.cuda.empty_cache()
     return res
 

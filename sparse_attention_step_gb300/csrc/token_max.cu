@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __gri
 // ---------------------------------------------------------------------------
 namespace {
 constexpr int kTpTiles = 8;   // tiles per group (the MMA's N)
-constexpr int kTpChunk = 64;  // index-key blocks per CTA
+constexpr int kTpChunk = 32;  // index-key blocks per CTA (two CTAs fit an SM)
 }  // namespace
 
 struct TokenMaxPrefillArgs {
@@ -278,17 +278,30 @@ __global__ void __launch_bounds__(kTmThreads) token_max_prefill_kernel(const __g
                 af[kk][2], af[kk][3]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
-      for (int h = 0; h < a.hkv; ++h) {
-        float hi[4] = {0.f, 0.f, 0.f, 0.f}, lo[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t* qh = qb + h * (8 * 2 * 2 * 32) + lane;
+      // every head's products at once (16 independent accumulator chains per
+      // k-step), so the tensor pipe, not the chain latency, sets the pace
+      float hi[kTmMaxHeads][4], lo[kTmMaxHeads][4];
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          mma_bf16(hi, af[kk][0], af[kk][1], af[kk][2], af[kk][3], qh[(kk * 4 + 0) * 32], qh[(kk * 4 + 2) * 32]);
-          mma_bf16(lo, af[kk][0], af[kk][1], af[kk][2], af[kk][3], qh[(kk * 4 + 1) * 32], qh[(kk * 4 + 3) * 32]);
+      for (int h = 0; h < kTmMaxHeads; ++h)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) hi[h][e] = lo[h][e] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+        for (int h = 0; h < kTmMaxHeads; ++h) {
+          if (h < a.hkv) {
+            const uint32_t* qh = qb + h * (8 * 2 * 2 * 32) + lane;
+            mma_bf16(hi[h], af[kk][0], af[kk][1], af[kk][2], af[kk][3], qh[(kk * 4 + 0) * 32], qh[(kk * 4 + 2) * 32]);
+            mma_bf16(lo[h], af[kk][0], af[kk][1], af[kk][2], af[kk][3], qh[(kk * 4 + 1) * 32], qh[(kk * 4 + 3) * 32]);
+          }
         }
+      }
+#pragma unroll
+      for (int h = 0; h < kTmMaxHeads; ++h) {
+        if (h >= a.hkv) break;
         // tokens g and g + 8 of this warp's 16, tiles 2c and 2c + 1
-        float m0 = fmaxf(hi[0] + lo[0], hi[2] + lo[2]);
-        float m1 = fmaxf(hi[1] + lo[1], hi[3] + lo[3]);
+        float m0 = fmaxf(hi[h][0] + lo[h][0], hi[h][2] + lo[h][2]);
+        float m1 = fmaxf(hi[h][1] + lo[h][1], hi[h][3] + lo[h][3]);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
           m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
