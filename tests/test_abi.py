@@ -106,3 +106,44 @@ def test_decode_and_prefill_arguments(lib):
                                      None) == msa.MSA_ERR_UNSUPPORTED
     assert lib.msa_dense_gqa_prefill(0x1, 16, 2000, 0, ctypes.byref(d1), 0.1, 0x1, None, 0x1, 1 << 20,
                                      None) == msa.MSA_ERR_INVALID_ARG
+
+
+def _batch(starts, counts):
+    n = len(starts)
+    return n, (ctypes.c_int64 * n)(*starts), (ctypes.c_int32 * n)(*counts)
+
+
+@pytest.mark.parametrize("starts,counts,expect", [
+    ([64], [10], msa.MSA_ERR_INVALID_ARG),                 # one chunk for a cache of two sequences
+    ([64, 100], [10, 20], msa.MSA_ERR_UNSUPPORTED),        # a start inside a block
+    ([64, 128], [10, -1], msa.MSA_ERR_INVALID_ARG),        # a negative count
+    ([-64, 128], [10, 1], msa.MSA_ERR_INVALID_ARG),        # a negative start
+    ([64, 128], [10, 1000], msa.MSA_ERR_INVALID_ARG),      # past the sequence's capacity (1024 tokens)
+])
+def test_chunk_batch_arguments(lib, starts, counts, expect):
+    # both batched-prefill entries check the chunk table on the host, before any launch
+    d = _desc()
+    n, st, ct = _batch(starts, counts)
+    assert lib.msa_sparse_attn_prefill_varlen(0x1, 16, n, st, ct, ctypes.byref(d), 0x1, 5, 0.1, 0x1, None, 0x1,
+                                              1 << 20, None) == expect
+    cfg = msa.select_cfg(4, True, 64)
+    assert lib.msa_select_topk_blocks_varlen(0x1, 16, n, st, ct, 0x1, ctypes.byref(d), ctypes.byref(cfg), 0x1, 5,
+                                             None, 0x1, 1 << 20, None) == expect
+
+
+def test_chunk_batch_needs_tiles_and_tables(lib):
+    d = _desc()
+    n, st, ct = _batch([0, 64], [64, 64])
+    decode_cfg = msa.select_cfg(4)  # q_tile 1: not a tile selection
+    assert lib.msa_select_topk_blocks_varlen(0x1, 16, n, st, ct, 0x1, ctypes.byref(d), ctypes.byref(decode_cfg), 0x1,
+                                             5, None, 0x1, 1 << 20, None) == msa.MSA_ERR_INVALID_ARG
+    cfg = msa.select_cfg(4, True, 64)
+    assert lib.msa_select_topk_blocks_varlen(0x1, 16, n, None, ct, 0x1, ctypes.byref(d), ctypes.byref(cfg), 0x1, 5,
+                                             None, 0x1, 1 << 20, None) == msa.MSA_ERR_INVALID_ARG
+    assert lib.msa_sparse_attn_prefill_varlen(0x1, 16, n, st, ct, ctypes.byref(d), None, 5, 0.1, 0x1, None, 0x1,
+                                              1 << 20, None) == msa.MSA_ERR_INVALID_ARG
+    # more sequences than one launch's table holds
+    big = _desc(batch=65)
+    n, st, ct = _batch([0] * 65, [1] * 65)
+    assert lib.msa_sparse_attn_prefill_varlen(0x1, 16, n, st, ct, ctypes.byref(big), 0x1, 5, 0.1, 0x1, None, 0x1,
+                                              1 << 20, None) == msa.MSA_ERR_UNSUPPORTED
