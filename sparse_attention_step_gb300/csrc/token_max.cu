@@ -13,6 +13,7 @@
 #include <float.h>
 
 #include "kernels.cuh"
+#include "tc.cuh"
 
 namespace msa {
 
@@ -165,18 +166,36 @@ __global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __gri
 
 // ---------------------------------------------------------------------------
 // Prefill tiles: the same token-level max-pooled score, for the 64-token query
-// tiles of a chunk batch. A CTA takes a chunk of index-key blocks of one
-// sequence and a group of up to 8 of its tiles, for every KV head: per block
-// and head, S[token, tile] = K_idx q_idx(tile, head)^T on mma.sync (the tiles
-// are the 8 columns; the fp32 index queries split into a bf16 head and a bf16
-// remainder, as above), and the max over the block's 64 tokens (four warps of
-// 16 tokens, combined with shared-memory atomics on order-preserving keys).
-// The index queries come from the workspace (the prefill index-query kernel).
-// grid (block chunks, tile groups).
+// tiles of a chunk batch, on the 5th-generation tensor cores. A CTA takes a
+// chunk of index-key blocks of one sequence and a group of up to 8 of its
+// tiles, for every KV head: the 64 index queries (tile x head) are the rows of
+// A, the block's 64 index-key tokens the columns of B, so
+//   D[query, token] = q_idx . K_idx[token]     tcgen05.mma M128 N64, fp32 in TMEM
+// with the fp32 index queries split into a bf16 head (k-steps 0-7) and a bf16
+// remainder (k-steps 8-15) accumulated into the same D, which reproduces the
+// fp32 products to ~2^-16 relative. A reads rows 64..127 as zeros. Each query
+// row sits in one TMEM lane, so the block maximum over the 64 tokens is a
+// reduction inside one thread. Warps: 0-1 read D (TMEM lanes 0-63), 2 the TMA
+// producer (4-stage ring of index-key blocks), 3 the TMEM allocator and MMA
+// issuer; D is double-buffered. The index queries come from the workspace
+// (the prefill index-query kernel). grid (block chunks, tile groups).
 // ---------------------------------------------------------------------------
 namespace {
-constexpr int kTpTiles = 8;   // tiles per group (the MMA's N)
-constexpr int kTpChunk = 32;  // index-key blocks per CTA (two CTAs fit an SM)
+constexpr int kTpTiles = 8;        // tiles per group
+constexpr int kTpChunk = 64;       // index-key blocks per CTA
+constexpr int kTpThreads = 128;
+constexpr int kTpStages = 4;
+constexpr int kTpABytes = 65536;   // A: head and remainder, 128 rows x 128 dims bf16 each
+struct TpTail {
+  uint64_t kv_full[kTpStages];
+  uint64_t kv_empty[kTpStages];
+  uint64_t s_full[2];
+  uint64_t s_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int32_t rowid[kTpChunk];
+};
+constexpr size_t kTpSmem = 1024 + kTpABytes + static_cast<size_t>(kTpStages) * kTmStage + sizeof(TpTail);
 }  // namespace
 
 struct TokenMaxPrefillArgs {
@@ -187,16 +206,14 @@ struct TokenMaxPrefillArgs {
   int32_t* status;
 };
 
-__global__ void __launch_bounds__(kTmThreads) token_max_prefill_kernel(const __grid_constant__ CUtensorMap tmi,
-                                                                       KvView kv, TokenMaxPrefillArgs a,
-                                                                       const PrefillBatch pb) {
+__global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const __grid_constant__ CUtensorMap tmi,
+                                                                        KvView kv, TokenMaxPrefillArgs a,
+                                                                        const PrefillBatch pb) {
   extern __shared__ __align__(1024) uint8_t tp_raw[];
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tp_raw) + 1023) & ~uintptr_t(1023));
-  // B fragments [head][kk][hlf][head / remainder][lane] and the block maxima as keys [block][head][tile]
-  uint32_t* qb = reinterpret_cast<uint32_t*>(ring + kTmStages * kTmStage);
-  uint32_t* part = qb + kTmMaxHeads * 8 * 2 * 2 * 32;
-  __shared__ uint64_t full[kTmStages], empty[kTmStages];
-  __shared__ int32_t rowid[kTpChunk];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tp_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* qa = base;                  // A operands, 128-byte swizzled, K-major
+  uint8_t* ring = base + kTpABytes;    // index-key blocks
+  TpTail& st = *reinterpret_cast<TpTail*>(ring + kTpStages * kTmStage);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seq = pb.seq_of_group(blockIdx.y);
@@ -206,15 +223,20 @@ __global__ void __launch_bounds__(kTmThreads) token_max_prefill_kernel(const __g
   const int64_t diag0 = pb.q_start[seq] / kBlock + j0;           // candidates of tile t0 + t: blocks < diag0 + t
   const int64_t n_max = diag0 + (t_end - t0) - 1;                // the group's most candidates
   const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kTpChunk;
-  if (b0 >= n_max) return;
+  if (b0 >= n_max) return;  // the whole CTA leaves before any barrier or allocation
   const int nblk = static_cast<int>(min(static_cast<int64_t>(kTpChunk), n_max - b0));
   pdl_wait();
 
   if (tid == 0) {
-    for (int i = 0; i < kTmStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kTmWarps);
+    for (int i = 0; i < kTpStages; ++i) {
+      mbar_init(&st.kv_full[i], 1);
+      mbar_init(&st.kv_empty[i], 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&st.s_full[i], 1);
+      mbar_init(&st.s_empty[i], 2);
+    }
+    mbar_init(&st.drain, 1);
     fence_mbar_init();
   }
   if (tid < kTpChunk) {
@@ -228,110 +250,123 @@ __global__ void __launch_bounds__(kTmThreads) token_max_prefill_kernel(const __g
         r = p < 0 ? -1 : p * kBlock;
       }
     }
-    rowid[tid] = r;
+    st.rowid[tid] = r;
   }
-  for (int i = tid; i < kTmMaxHeads * 8 * 2 * 32; i += blockDim.x) {
-    const int ln = i & 31, hlf = (i >> 5) & 1, kk = (i >> 6) & 7, h = i >> 9;
-    const int g = ln >> 2, c = ln & 3;
-    const int d = 16 * kk + 2 * c + 8 * hlf;
-    float x0 = 0.f, x1 = 0.f;
-    if (h < a.hkv && t0 + g < t_end) {
-      const float* qi = a.qidx + (static_cast<int64_t>(t0 + g) * a.hkv + h) * kHeadDim;
-      x0 = qi[d];
-      x1 = qi[d + 1];
+  // A: row r = 8 (tile) + head; 16-byte piece c16 of a row's 256 bytes goes to
+  // [operand][dim half][row][(c16 mod 8) ^ (row mod 8)] (the TMA 128-byte swizzle)
+  for (int i = tid; i < 128 * 16; i += kTpThreads) {
+    const int row = i >> 4, c16 = i & 15;
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = 0.f;
+    const int g = row >> 3, h = row & 7;
+    if (row < 64 && h < a.hkv && t0 + g < t_end) {
+      const float4* qi = reinterpret_cast<const float4*>(a.qidx + (static_cast<int64_t>(t0 + g) * a.hkv + h) * kHeadDim +
+                                                         8 * c16);
+      const float4 u = qi[0], v = qi[1];
+      x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w; x[4] = v.x; x[5] = v.y; x[6] = v.z; x[7] = v.w;
     }
-    const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
-    const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
-    const int at = (((h * 8 + kk) * 2 + hlf) * 2) * 32 + ln;
-    qb[at] = pack_bf16(h0, h1);
-    qb[at + 32] = pack_bf16(x0 - h0, x1 - h1);
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float h0 = __bfloat162float(__float2bfloat16_rn(x[2 * e]));
+      const float h1 = __bfloat162float(__float2bfloat16_rn(x[2 * e + 1]));
+      hi[e] = pack_bf16(h0, h1);
+      lo[e] = pack_bf16(x[2 * e] - h0, x[2 * e + 1] - h1);
+    }
+    const int off = (c16 >> 3) * 16384 + row * 128 + (((c16 & 7) ^ (row & 7)) << 4);
+    *reinterpret_cast<uint4*>(qa + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(qa + 32768 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
-  const uint32_t neg_inf = float_to_key(-INFINITY);
-  for (int i = tid; i < kTpChunk * kTmMaxHeads * kTpTiles; i += blockDim.x) part[i] = neg_inf;
+  fence_proxy_async();  // the tensor core reads A through the async proxy
+  if (warp == 3) {
+    tc::alloc(&st.tmem_base, 128);
+    tc::relinquish();
+  }
+  tc::fence_before();
   __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = st.tmem_base;
 
-  if (warp == kTmWarps) {
+  if (warp == 2) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmi);
+      int issued = 0;
       for (int j = 0; j < nblk; ++j) {
-        const int slot = j % kTmStages;
-        if (j >= kTmStages && !mbar_wait(&empty[slot], ((j / kTmStages) - 1) & 1, a.status, kIdScore)) break;
-        const int32_t y = rowid[j] < 0 ? 0 : rowid[j];
+        const int slot = j % kTpStages;
+        if (j >= kTpStages && !mbar_wait(&st.kv_empty[slot], ((j / kTpStages) - 1) & 1, a.status, kIdScore)) break;
+        const int32_t y = st.rowid[j] < 0 ? 0 : st.rowid[j];
         uint8_t* dst = ring + slot * kTmStage;
-        mbar_arrive_expect_tx(&full[slot], kTmStage);
-        tma_load_2d(dst, &tmi, 0, y, &full[slot]);
-        tma_load_2d(dst + kTmStage / 2, &tmi, 64, y, &full[slot]);
+        mbar_arrive_expect_tx(&st.kv_full[slot], kTmStage);
+        tma_load_2d(dst, &tmi, 0, y, &st.kv_full[slot]);
+        tma_load_2d(dst + kTmStage / 2, &tmi, 64, y, &st.kv_full[slot]);
+        issued = j + 1;
       }
+      // every load this thread issued has landed before the CTA may exit
+      for (int j = issued - kTpStages < 0 ? 0 : issued - kTpStages; j < issued; ++j)
+        mbar_wait(&st.kv_full[j % kTpStages], (j / kTpStages) & 1, a.status, kIdScore);
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kId = tc::idesc_bf16(128, 64, 0, 0);
+      const uint32_t a_addr = smem_u32(qa), r_addr = smem_u32(ring);
+      for (int j = 0; j < nblk; ++j) {
+        const int slot = j % kTpStages, buf = j & 1;
+        if (!mbar_wait(&st.kv_full[slot], (j / kTpStages) & 1, a.status, kIdScore)) break;
+        if (j >= 2 && !mbar_wait(&st.s_empty[buf], ((j >> 1) - 1) & 1, a.status, kIdScore)) break;
+        tc::fence_after();
+        const uint32_t d = tmem + buf * 64;
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          const int k8 = kk & 7;  // k-steps 8-15 repeat the dims with the remainder of the queries
+          const uint64_t ad = tc::sdesc_sw128(a_addr + (kk >> 3) * 32768 + (k8 >> 2) * 16384 + (k8 & 3) * 32, 16, 1024);
+          const uint64_t bd = tc::sdesc_sw128(r_addr + slot * kTmStage + (k8 >> 2) * 8192 + (k8 & 3) * 32, 16, 1024);
+          tc::mma_ss(d, ad, bd, kId, kk > 0 ? 1u : 0u);
+        }
+        tc::commit(&st.kv_empty[slot]);
+        tc::commit(&st.s_full[buf]);
+      }
+      tc::commit(&st.drain);
+      mbar_wait(&st.drain, 0, a.status, kIdScore);  // nothing of ours is left in flight
     }
   } else {
-    const int c = lane & 3;
-    const int krow = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
-    const int kchunk = lane >> 4;
+    // ------------------------------------------------------------ block maxima (query rows 0-63)
+    const int row = 32 * warp + lane;
+    const int g = row >> 3, h = row & 7;
+    const bool live = h < a.hkv && t0 + g < t_end;
+    const int64_t n_cand = diag0 + g;  // this tile's candidates
+    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    float* out = a.scores + (static_cast<int64_t>(live ? t0 + g : 0) * a.hkv + h) * a.max_blocks;
     for (int j = 0; j < nblk; ++j) {
-      const int slot = j % kTmStages;
-      if (!mbar_wait_warp(&full[slot], (j / kTmStages) & 1, a.status, kIdScore)) break;
-      const uint32_t sbase = smem_u32(ring + slot * kTmStage);
-      uint32_t af[8][4];  // this warp's 16 tokens of the block, all 128 dims
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        ldsm_x4(sbase + (kk >> 2) * (kTmStage / 2) + swz128(krow, (kk & 3) * 2 + kchunk), af[kk][0], af[kk][1],
-                af[kk][2], af[kk][3]);
+      const int buf = j & 1;
+      if (!mbar_wait_warp(&st.s_full[buf], (j >> 1) & 1, a.status, kIdScore)) break;
+      tc::fence_after();
+      uint32_t r0[32], r1[32];
+      tc::ld32(tmem + lane_base + buf * 64, r0);
+      tc::ld32(tmem + lane_base + buf * 64 + 32, r1);
+      tc::wait_ld();
+      tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
-      // every head's products at once (16 independent accumulator chains per
-      // k-step), so the tensor pipe, not the chain latency, sets the pace
-      float hi[kTmMaxHeads][4], lo[kTmMaxHeads][4];
+      if (lane == 0) mbar_arrive(&st.s_empty[buf]);
+      float m = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < kTmMaxHeads; ++h)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) hi[h][e] = lo[h][e] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-        for (int h = 0; h < kTmMaxHeads; ++h) {
-          if (h < a.hkv) {
-            const uint32_t* qh = qb + h * (8 * 2 * 2 * 32) + lane;
-            mma_bf16(hi[h], af[kk][0], af[kk][1], af[kk][2], af[kk][3], qh[(kk * 4 + 0) * 32], qh[(kk * 4 + 2) * 32]);
-            mma_bf16(lo[h], af[kk][0], af[kk][1], af[kk][2], af[kk][3], qh[(kk * 4 + 1) * 32], qh[(kk * 4 + 3) * 32]);
-          }
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < kTmMaxHeads; ++h) {
-        if (h >= a.hkv) break;
-        // tokens g and g + 8 of this warp's 16, tiles 2c and 2c + 1
-        float m0 = fmaxf(hi[h][0] + lo[h][0], hi[h][2] + lo[h][2]);
-        float m1 = fmaxf(hi[h][1] + lo[h][1], hi[h][3] + lo[h][3]);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, off));
-          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, off));
-        }
-        if (lane < 4) {
-          uint32_t* pj = part + (j * kTmMaxHeads + h) * kTpTiles;
-          atomicMax(pj + 2 * c, float_to_key(m0));
-          atomicMax(pj + 2 * c + 1, float_to_key(m1));
-        }
-      }
+      for (int c = 0; c < 32; ++c) m = fmaxf(m, fmaxf(__uint_as_float(r0[c]), __uint_as_float(r1[c])));
+      const int64_t b = b0 + j;
+      if (live && b < n_cand) out[b] = st.rowid[j] < 0 ? -INFINITY : m;  // bad page: never selected
     }
   }
   pdl_trigger();
+  tc::fence_before();
   __syncthreads();
-  for (int i = tid; i < nblk * a.hkv * kTpTiles; i += blockDim.x) {
-    const int g = i % kTpTiles, h = (i / kTpTiles) % a.hkv, j = i / (kTpTiles * a.hkv);
-    const int64_t b = b0 + j;
-    if (t0 + g >= t_end || b >= diag0 + g) continue;  // not a candidate of that tile
-    const uint32_t u = part[(j * kTmMaxHeads + h) * kTpTiles + g];
-    float m = __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
-    if (rowid[j] < 0) m = -INFINITY;  // bad page: never selected
-    a.scores[(static_cast<int64_t>(t0 + g) * a.hkv + h) * a.max_blocks + b] = m;
+  if (warp == 3) {
+    tc::fence_after();
+    tc::dealloc(tmem, 128);
   }
 }
 
-size_t token_max_prefill_smem_bytes() {
-  return 1024 + static_cast<size_t>(kTmStages) * kTmStage + kTmMaxHeads * 8 * 2 * 2 * 32 * sizeof(uint32_t) +
-         static_cast<size_t>(kTpChunk) * kTmMaxHeads * kTpTiles * sizeof(uint32_t);
-}
+size_t token_max_prefill_smem_bytes() { return kTpSmem; }
 
 cudaError_t launch_token_max_prefill_scores(const CUtensorMap& tmi, const KvView& kv, const PrefillBatch& pb,
                                             const float* qidx, float* scores, int32_t* status, cudaStream_t stream) {
@@ -348,7 +383,7 @@ cudaError_t launch_token_max_prefill_scores(const CUtensorMap& tmi, const KvView
   const int groups = pb.grp_off[pb.n_seqs];
   if (last <= 0 || groups == 0) return cudaSuccess;  // no candidates anywhere
   const unsigned chunks = static_cast<unsigned>((last + kTpChunk - 1) / kTpChunk);
-  token_max_prefill_kernel<<<dim3(chunks, groups), kTmThreads, token_max_prefill_smem_bytes(), stream>>>(tmi, kv, a,
+  token_max_prefill_kernel<<<dim3(chunks, groups), kTpThreads, token_max_prefill_smem_bytes(), stream>>>(tmi, kv, a,
                                                                                                           pb);
   return cudaGetLastError();
 }
