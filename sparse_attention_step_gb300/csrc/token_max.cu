@@ -167,23 +167,25 @@ __global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __gri
 // ---------------------------------------------------------------------------
 // Prefill tiles: the same token-level max-pooled score, for the 64-token query
 // tiles of a chunk batch, on the 5th-generation tensor cores. A CTA takes a
-// chunk of index-key blocks of one sequence and a group of up to 8 of its
-// tiles, for every KV head: the 64 index queries (tile x head) are the rows of
-// A, the block's 64 index-key tokens the columns of B, so
+// chunk of index-key blocks of one sequence and a group of up to 16 of its
+// tiles, for every KV head: the 128 index queries (tile x head) are the rows
+// of A, the block's 64 index-key tokens the columns of B, so
 //   D[query, token] = q_idx . K_idx[token]     tcgen05.mma M128 N64, fp32 in TMEM
 // with the fp32 index queries split into a bf16 head (k-steps 0-7) and a bf16
 // remainder (k-steps 8-15) accumulated into the same D, which reproduces the
-// fp32 products to ~2^-16 relative. A reads rows 64..127 as zeros. Each query
-// row sits in one TMEM lane, so the block maximum over the 64 tokens is a
-// reduction inside one thread. Warps: 0-1 read D (TMEM lanes 0-63), 2 the TMA
-// producer (4-stage ring of index-key blocks), 3 the TMEM allocator and MMA
-// issuer; D is double-buffered. The index queries come from the workspace
-// (the prefill index-query kernel). grid (block chunks, tile groups).
+// fp32 products to ~2^-16 relative (rows of absent tiles or heads are zeros).
+// Each query row sits in one TMEM lane, so the block maximum over the 64
+// tokens is a reduction inside one thread. Warps: 0-3 read D (TMEM lanes
+// 0-127), 4 the TMA producer (4-stage ring of index-key blocks), 5 the TMEM
+// allocator and MMA issuer; D is double-buffered. The index queries come from
+// the workspace (the prefill index-query kernel). grid (block chunks, groups
+// of 16 tiles of one sequence).
 // ---------------------------------------------------------------------------
 namespace {
-constexpr int kTpTiles = 8;        // tiles per group
+constexpr int kTpTiles = 16;       // tiles per group (x 8 heads = the MMA's 128 rows)
 constexpr int kTpChunk = 64;       // index-key blocks per CTA
-constexpr int kTpThreads = 128;
+constexpr int kTpThreads = 192;
+constexpr int kTpProducer = 4, kTpMma = 5;  // warps
 constexpr int kTpStages = 4;
 constexpr int kTpABytes = 65536;   // A: head and remainder, 128 rows x 128 dims bf16 each
 struct TpTail {
@@ -216,8 +218,15 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
   TpTail& st = *reinterpret_cast<TpTail*>(ring + kTpStages * kTmStage);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int seq = pb.seq_of_group(blockIdx.y);
-  const int j0 = (blockIdx.y - pb.grp_off[seq]) * kTpTiles;      // first tile of the group within its sequence
+  // the group's sequence: groups are counted sequence by sequence
+  int seq = 0, first = 0;
+  for (int sq = 0; sq < pb.n_seqs; ++sq) {
+    const int n_g = (pb.tile_off[sq + 1] - pb.tile_off[sq] + kTpTiles - 1) / kTpTiles;
+    seq = sq;
+    if (static_cast<int>(blockIdx.y) < first + n_g) break;
+    first += n_g;
+  }
+  const int j0 = (static_cast<int>(blockIdx.y) - first) * kTpTiles;  // first tile of the group within its sequence
   const int t0 = pb.tile_off[seq] + j0;                          // its global tile
   const int t_end = min(t0 + kTpTiles, pb.tile_off[seq + 1]);
   const int64_t diag0 = pb.q_start[seq] / kBlock + j0;           // candidates of tile t0 + t: blocks < diag0 + t
@@ -234,7 +243,7 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&st.s_full[i], 1);
-      mbar_init(&st.s_empty[i], 2);
+      mbar_init(&st.s_empty[i], 4);
     }
     mbar_init(&st.drain, 1);
     fence_mbar_init();
@@ -260,7 +269,7 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
 #pragma unroll
     for (int e = 0; e < 8; ++e) x[e] = 0.f;
     const int g = row >> 3, h = row & 7;
-    if (row < 64 && h < a.hkv && t0 + g < t_end) {
+    if (h < a.hkv && t0 + g < t_end) {
       const float4* qi = reinterpret_cast<const float4*>(a.qidx + (static_cast<int64_t>(t0 + g) * a.hkv + h) * kHeadDim +
                                                          8 * c16);
       const float4 u = qi[0], v = qi[1];
@@ -279,7 +288,7 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
     *reinterpret_cast<uint4*>(qa + 32768 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
   fence_proxy_async();  // the tensor core reads A through the async proxy
-  if (warp == 3) {
+  if (warp == kTpMma) {
     tc::alloc(&st.tmem_base, 128);
     tc::relinquish();
   }
@@ -288,7 +297,7 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
   tc::fence_after();
   const uint32_t tmem = st.tmem_base;
 
-  if (warp == 2) {
+  if (warp == kTpProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmi);
@@ -307,7 +316,7 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
       for (int j = issued - kTpStages < 0 ? 0 : issued - kTpStages; j < issued; ++j)
         mbar_wait(&st.kv_full[j % kTpStages], (j / kTpStages) & 1, a.status, kIdScore);
     }
-  } else if (warp == 3) {
+  } else if (warp == kTpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kId = tc::idesc_bf16(128, 64, 0, 0);
@@ -332,7 +341,7 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
       mbar_wait(&st.drain, 0, a.status, kIdScore);  // nothing of ours is left in flight
     }
   } else {
-    // ------------------------------------------------------------ block maxima (query rows 0-63)
+    // ------------------------------------------------------------ block maxima (query rows 0-127)
     const int row = 32 * warp + lane;
     const int g = row >> 3, h = row & 7;
     const bool live = h < a.hkv && t0 + g < t_end;
@@ -360,7 +369,7 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
   pdl_trigger();
   tc::fence_before();
   __syncthreads();
-  if (warp == 3) {
+  if (warp == kTpMma) {
     tc::fence_after();
     tc::dealloc(tmem, 128);
   }
@@ -380,7 +389,8 @@ cudaError_t launch_token_max_prefill_scores(const CUtensorMap& tmi, const KvView
   for (int s = 0; s < pb.n_seqs; ++s)
     if (pb.tile_off[s + 1] > pb.tile_off[s])
       last = max(last, pb.q_start[s] / kBlock + (pb.tile_off[s + 1] - pb.tile_off[s]) - 1);
-  const int groups = pb.grp_off[pb.n_seqs];
+  int groups = 0;  // groups of kTpTiles tiles, sequence by sequence
+  for (int s = 0; s < pb.n_seqs; ++s) groups += (pb.tile_off[s + 1] - pb.tile_off[s] + kTpTiles - 1) / kTpTiles;
   if (last <= 0 || groups == 0) return cudaSuccess;  // no candidates anywhere
   const unsigned chunks = static_cast<unsigned>((last + kTpChunk - 1) / kTpChunk);
   token_max_prefill_kernel<<<dim3(chunks, groups), kTpThreads, token_max_prefill_smem_bytes(), stream>>>(tmi, kv, a,

@@ -127,11 +127,11 @@ def run_token_max_prefill(inp, ik, k_scored, k_total, sink=False):
 
 @pytest.mark.parametrize("layout,hq,hkv", [("contiguous", 64, 8), ("paged", 16, 4), ("contiguous", 8, 1)])
 def test_token_max_prefill_tiles(dev, layout, hq, hkv):
-    # ragged chunks over a shared index-key head: one spanning two groups of 8
-    # tiles, one from an empty prefix, a 5-token one
+    # ragged chunks over a shared index-key head: one spanning two groups of 16
+    # tiles (and two of 8), one from an empty prefix, a 5-token one
     from synth import make_prefill_batch_inputs
     q_starts = [64 * 23, 0, 64 * 7, 64 * 40]
-    q_counts = [64 * 2 + 17, 64 * 3, 5, 64 * 9 + 1]
+    q_counts = [64 * 2 + 17, 64 * 3, 5, 64 * 17 + 1]
     inp = make_prefill_batch_inputs(q_starts, q_counts, hkv, hq, "bf16", layout, seed=95, device=dev)
     ik = make_index_keys(inp.cache, needles=2, seed=96)
     k_scored, k_total = 6, 7
