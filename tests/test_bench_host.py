@@ -1,0 +1,48 @@
+"""Host-side arithmetic of the benchmark and the binding (no GPU): the bytes a
+decode step is charged with, the per-step quantiles, and the chunk-batch
+helpers of the binding."""
+import os
+import sys
+import types
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from sparse_attention_step_gb300 import msa  # noqa: E402
+
+
+def test_decode_bytes_counts_candidates_selection_and_io():
+    # two sequences, 2 KV heads, 16 query heads, bf16: summaries of the complete
+    # blocks before the newest, k_total selected blocks of K and V, q and out
+    q = types.SimpleNamespace(numel=lambda: 2 * 16 * 128, element_size=lambda: 2)
+    inp = types.SimpleNamespace(lens=[64 * 10 + 5, 64 * 3], num_kv_heads=2, q=q)
+    pooled, sel, qo = bench.decode_bytes(inp, 4)
+    # candidates: min(full blocks, blocks - 1) = min(10, 10) and min(3, 2)
+    assert pooled == (10 + 2) * 2 * 128 * 2
+    # selected: min(k_total, blocks) = 4 and 3, each 64 x 128 x 2 bytes of K and of V
+    assert sel == (4 + 3) * 2 * 2 * 64 * 128 * 2
+    assert qo == 2 * (2 * 16 * 128 * 2)
+
+
+def test_decode_bytes_of_the_headline_workload():
+    # 8 x 131072 tokens, 8 KV heads, 64 query heads, 31 + 1 blocks: 100,909,056 bytes
+    q = types.SimpleNamespace(numel=lambda: 8 * 64 * 128, element_size=lambda: 2)
+    inp = types.SimpleNamespace(lens=[131072] * 8, num_kv_heads=8, q=q)
+    assert sum(bench.decode_bytes(inp, 32)) == 100909056
+
+
+def test_quantiles():
+    q = bench.quantiles_us([0.031, 0.030, 0.032, 0.029, 0.033, 0.030, 0.031, 0.030, 0.034, 0.030])
+    assert q == {"p10": 30.0, "p50": 30.5, "p90": 34.0}
+    assert bench.quantiles_us([]) is None
+
+
+def test_chunk_batch_helpers():
+    assert msa.varlen_tiles([0, 1, 64, 65, 128]) == 0 + 1 + 1 + 2 + 2
+    n, starts, counts = msa._host_batch([0, 64, 128], [5, 0, 70])
+    assert n == 3 and list(starts) == [0, 64, 128] and list(counts) == [5, 0, 70]
+    with pytest.raises(ValueError):
+        msa._host_batch([0, 64], [1])
