@@ -174,7 +174,7 @@ msa_status msa_pool_block_keys(const msa_kv_desc* kv /* host */, int64_t first_b
  *   [batch, max_tokens, 128], paged [num_pages, 64, 128] on the cache's pages
  *   -- and the score of block b is max_{t in b} q_idx . K_idx[t] (fp32), for
  *   decode and for prefill tiles alike. The index keys of a sequence are read
- *   once for all of its KV heads (decode) or once per group of 8 tiles
+ *   once for all of its KV heads (decode) or once per group of 16 tiles
  *   (prefill). */
 msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_q_tokens,
                                   const void* pooled, const msa_kv_desc* kv /* host */,
