@@ -596,6 +596,29 @@ def _oracle_unit(args):
     return time.perf_counter() - t0
 
 
+def host_cpu_model() -> str:
+    """The host CPU's name (x86: /proc/cpuinfo "model name"; Arm: the
+    implementer / part codes there), else the machine type."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model Name", "Processor"):
+            for line in info.splitlines():
+                if line.split(":")[0].strip() == key and ":" in line:
+                    return line.split(":", 1)[1].strip()
+        fields = {}
+        for line in info.splitlines():
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields.setdefault(k.strip(), v.strip())
+        if "CPU part" in fields:
+            return f"{platform.machine()} implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    except OSError:
+        pass
+    return platform.machine() or "unknown"
+
+
 class OraclePool:
     """The oracle as it stands, run on decode units of the 128K workload in a
     pool of single-threaded spawned workers, one per host core."""
@@ -658,7 +681,7 @@ def cpu_baseline(name: str, target_seconds: float = 15.0) -> dict:
             vals.append(step_s)
             rounds += 1
         return {"value": round(statistics.mean(vals) * 1e6, 1), "unit": UNIT, "cores": pool.cores, "kind": "oracle",
-                "sample": pool.describe(rounds)}
+                "cpu_model": host_cpu_model(), "sample": pool.describe(rounds)}
     finally:
         pool.close()
 
@@ -682,7 +705,7 @@ def run_reference(args):
                                    "head dim 128, 64-token blocks, top-31 scored blocks + newest block",
                        "global_batch": 8, "seq_len": 131072, "parallelism": "CPU oracle"},
             "cpu_baseline": {"value": round(val, 1), "unit": UNIT, "cores": pool.cores, "kind": "oracle",
-                             "sample": pool.describe(args.steps)},
+                             "cpu_model": host_cpu_model(), "sample": pool.describe(args.steps)},
             "e2e": {"value": round(val, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

@@ -46,3 +46,8 @@ def test_chunk_batch_helpers():
     assert n == 3 and list(starts) == [0, 64, 128] and list(counts) == [5, 0, 70]
     with pytest.raises(ValueError):
         msa._host_batch([0, 64], [1])
+
+
+def test_host_cpu_model_is_named():
+    name = bench.host_cpu_model()
+    assert isinstance(name, str) and name and name != "unknown"
