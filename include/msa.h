@@ -307,6 +307,15 @@ msa_status msa_sparse_attn_decode_noalloc(const void* q, int32_t num_q_heads, co
                                           const int32_t* idx, int32_t k_total, float scale, void* out, float* lse,
                                           msa_stream_t stream);
 
+/* Failure-detection self test (the guide has no counterpart; it checks the
+ * library's own error path): launches one warp that waits, with the same
+ * bounded spin every kernel of the library uses, on a barrier that nothing
+ * signals. After `limit_cycles` SM cycles (1000 .. 4e9; MSA_ERR_INVALID_ARG
+ * outside) the wait gives up, the status word of `ws` gets MSA_ERR_TIMEOUT and
+ * the kernel ends normally: no fault, no trap, the context stays usable.
+ * ws: at least the 256-byte header (MSA_ERR_WORKSPACE otherwise). */
+msa_status msa_selftest_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_cycles, msa_stream_t stream);
+
 /* Reads (and clears) the sticky device status word of `ws`: synchronises
  * `stream`, stores an msa_status in *status_out (host). */
 msa_status msa_read_device_status(const void* ws, msa_stream_t stream, int32_t* status_out /* host */);

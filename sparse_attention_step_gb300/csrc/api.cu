@@ -386,6 +386,21 @@ msa_status check_select(const void* q, int32_t num_q_heads, const void* pooled, 
   if (cfg->q_tile != 1 && cfg->q_tile != kBlock) return MSA_ERR_UNSUPPORTED;
   return MSA_OK;
 }
+// The failure-detection path on the device, exercised on purpose: one warp
+// waits, with a bounded spin, on a barrier that nothing will ever signal. The
+// wait gives up after `limit` SM cycles and records MSA_ERR_TIMEOUT in the
+// status word, as every bounded wait of the library does, and the kernel ends
+// normally (no fault, no trap), so the context stays usable.
+__global__ void selftest_wait_kernel(int32_t* status, long long limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  mbar_wait_warp_limit(&bar, 0, status, kIdSelfTest, limit);
+}
+
 }  // namespace
 }  // namespace msa
 
@@ -593,6 +608,13 @@ msa_status msa_sparse_decode_step_pool(const void* q, int32_t num_q_heads, void*
   if (cfg != nullptr && cfg->mode != MSA_SCORE_MEAN_POOLED_KEYS) return MSA_ERR_UNSUPPORTED;
   return decode_step_common(q, num_q_heads, pooled, pooled, kv, cfg, idx_out, k_total, scale, out, lse, ws, ws_bytes,
                             stream);
+}
+
+msa_status msa_selftest_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_cycles, msa_stream_t stream) {
+  if (ws == nullptr || ws_bytes < kWsHeader) return MSA_ERR_WORKSPACE;
+  if (limit_cycles < 1000 || limit_cycles > kWaitCycles) return MSA_ERR_INVALID_ARG;
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(ws_status(ws), limit_cycles);
+  return cuda_status(cudaGetLastError());
 }
 
 msa_status msa_read_device_status(const void* ws, msa_stream_t stream, int32_t* status_out) {

@@ -88,17 +88,21 @@ __device__ inline bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // `kWaitCycles` SM cycles (then the device status gets MSA_ERR_TIMEOUT and the
 // caller must stop using the buffer the barrier guards).
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
-__device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status, int where) {
+__device__ inline bool mbar_wait_limit(uint64_t* bar, uint32_t parity, int32_t* status, int where,
+                                       long long limit_cycles) {
   if (mbar_try_wait(bar, parity)) return true;
   long long t0 = clock64();
   while (true) {
     for (int i = 0; i < 256; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit_cycles) {
       set_status(status, MSA_ERR_TIMEOUT, where);
       return false;
     }
   }
+}
+__device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status, int where) {
+  return mbar_wait_limit(bar, parity, status, where, kWaitCycles);
 }
 
 // The whole warp waits, and leaves converged with the same result in every
@@ -107,6 +111,10 @@ __device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status
 // ldmatrix, mma.sync, tcgen05.ld) then runs once per part.
 __device__ inline bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int32_t* status, int where) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, where));
+}
+__device__ inline bool mbar_wait_warp_limit(uint64_t* bar, uint32_t parity, int32_t* status, int where,
+                                            long long limit_cycles) {
+  return __all_sync(0xffffffffu, mbar_wait_limit(bar, parity, status, where, limit_cycles));
 }
 
 // ---------------------------------------------------------------------------
@@ -320,6 +328,6 @@ struct KvView {
 };
 
 // Kernel ids recorded with a device status (WsHeader::where).
-enum KernelId { kIdPool = 1, kIdQidx = 2, kIdScore = 3, kIdTopk = 4, kIdDecode = 5, kIdPrefill = 6 };
+enum KernelId { kIdPool = 1, kIdQidx = 2, kIdScore = 3, kIdTopk = 4, kIdDecode = 5, kIdPrefill = 6, kIdSelfTest = 7 };
 
 }  // namespace msa

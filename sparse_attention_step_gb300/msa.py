@@ -31,7 +31,7 @@ EXPORTS = ["msa_workspace_size", "msa_workspace_init", "msa_pool_block_keys", "m
            "msa_sparse_attn_decode", "msa_sparse_attn_prefill", "msa_dense_gqa_decode", "msa_dense_gqa_prefill",
            "msa_read_device_status", "msa_status_string", "msa_version", "msa_sparse_attn_decode_noalloc",
            "msa_sparse_decode_step", "msa_sparse_decode_step_pool", "msa_select_topk_blocks_varlen",
-           "msa_sparse_attn_prefill_varlen"]
+           "msa_sparse_attn_prefill_varlen", "msa_selftest_wait_timeout"]
 
 
 class MsaError(RuntimeError):
@@ -79,6 +79,7 @@ _SIGS = {
                                              _P, _P, _SZ, _P]),
     "msa_sparse_attn_prefill_varlen": (_I32, [_P, _I32, _I32, _P, _P, _DESC, _P, _I32, ctypes.c_float, _P, _P, _P,
                                               _SZ, _P]),
+    "msa_selftest_wait_timeout": (_I32, [_P, _SZ, _I64, _P]),
     "msa_status_string": (ctypes.c_char_p, [_I32]),
     "msa_version": (_I32, []),
 }
@@ -268,6 +269,11 @@ def msa_sparse_attn_decode_noalloc(q, num_q_heads: int, desc: KvDesc, idx, k_tot
     _check(load().msa_sparse_attn_decode_noalloc(_ptr(q), num_q_heads, ctypes.byref(desc), _ptr(idx), k_total, scale,
                                                  _ptr(out), _ptr(lse), _stream(stream)),
            "msa_sparse_attn_decode_noalloc")
+
+
+def msa_selftest_wait_timeout(ws, ws_bytes: int, limit_cycles: int, stream=None) -> None:
+    _check(load().msa_selftest_wait_timeout(_ptr(ws), ws_bytes, limit_cycles, _stream(stream)),
+           "msa_selftest_wait_timeout")
 
 
 def msa_read_device_status(ws, stream=None) -> int:

@@ -215,6 +215,21 @@ def test_device_status_length_over_capacity(dev):
     assert res["status"] == msa.MSA_ERR_DEVICE_BOUNDS
 
 
+def test_bounded_wait_gives_up_and_reports(dev):
+    # a wait on a barrier that nothing signals gives up after its limit and
+    # records MSA_ERR_TIMEOUT (no fault, no trap); the context stays usable
+    from sparse_attention_step_gb300 import msa
+    ws = msa.Workspace(4096, dev)
+    msa.msa_selftest_wait_timeout(ws.buf, ws.nbytes, 2_000_000)  # about a millisecond
+    torch.cuda.synchronize()
+    assert msa.msa_read_device_status(ws.buf) == msa.MSA_ERR_TIMEOUT
+    assert msa.msa_read_device_status(ws.buf) == 0  # reading clears the word
+    res = run_decode(make_decode_inputs([64 * 8 + 3], 1, 4, "bf16", "contiguous", seed=4, device=dev), 2, 3)
+    assert res["status"] == 0
+    with pytest.raises(msa.MsaError):
+        msa.msa_selftest_wait_timeout(ws.buf, ws.nbytes, 10)  # below the smallest limit
+
+
 # --------------------------------------------------------------------------- full-size workloads, sampled units
 
 def _sampled_full(name, units_fn):
