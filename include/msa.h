@@ -292,17 +292,22 @@ msa_status msa_dense_gqa_prefill(const void* q, int32_t num_q_heads, int32_t n_q
  * counterpart to this call; it only changes where the split-K scratch lives.
  * Same arguments, layouts and results as msa_sparse_attn_decode, minus ws.
  *  - Scratch: a fixed 4 MiB device array inside this library, held by every
- *    GPU that loads it until the process exits. Shapes whose
- *    msa_workspace_size(MSA_OP_DECODE, ...) exceeds 4 MiB are rejected with
- *    MSA_ERR_WORKSPACE before any work is queued.
+ *    GPU that loads it until the process exits. bf16 caches combine their
+ *    splits inside a thread-block cluster and use none of it beyond a 256-byte
+ *    header. fp32 caches keep split-K tickets and partial results there: an
+ *    fp32 shape whose msa_workspace_size(MSA_OP_DECODE, ...) exceeds 4 MiB is
+ *    rejected with MSA_ERR_WORKSPACE before any work is queued.
  *  - The first call on a device looks up the array's device address (a
- *    one-time set-up per device); make that first call before any stream
- *    capture.
- *  - Every call on a device shares the one array and clears its counters at
- *    the start (a memset on `stream`): calls whose work overlaps on the GPU
- *    race; order them on one stream.
- *  - No device memory is allocated or freed. Data-dependent errors (bad page
- *    ids, lengths above capacity) are skipped without a status report. */
+ *    one-time set-up per device, cached for the life of the process); make
+ *    that first call before any stream capture, and do not call this entry
+ *    on a device after cudaDeviceReset (the cached address is then stale).
+ *  - Every call on a device shares the one array and (fp32) clears its
+ *    counters at the start (a memset on `stream`): calls whose work overlaps
+ *    on the GPU race; order them on one stream.
+ *  - No device memory is allocated or freed. There is no status word:
+ *    data-dependent errors (bad page ids, lengths above capacity) are skipped
+ *    and a bounded wait that gives up leaves its output incomplete, neither
+ *    reported. Use msa_sparse_attn_decode where those must be detected. */
 msa_status msa_sparse_attn_decode_noalloc(const void* q, int32_t num_q_heads, const msa_kv_desc* kv /* host */,
                                           const int32_t* idx, int32_t k_total, float scale, void* out, float* lse,
                                           msa_stream_t stream);

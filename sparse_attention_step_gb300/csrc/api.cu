@@ -693,11 +693,17 @@ extern "C" msa_status msa_sparse_attn_decode_noalloc(const void* q, int32_t num_
   if ((st = noalloc_scratch(&ws)) != MSA_OK) return st;
   if (!decode_units_fit(kv)) return MSA_ERR_UNSUPPORTED;
   const DecodeLayout L = decode_layout(kv, k_total, dev->num_sms, false);
-  if (L.total > kNoAllocScratchBytes) return MSA_ERR_WORKSPACE;  // beyond the fixed scratch
+  // bf16 combines its splits inside a thread-block cluster and needs no
+  // scratch beyond the header; fp32 uses the tickets and the partial results
+  const bool f32 = kv->dtype != MSA_DTYPE_BF16;
+  const size_t need = f32 ? L.total : kWsHeader;
+  if (need > kNoAllocScratchBytes) return MSA_ERR_WORKSPACE;  // beyond the fixed scratch
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // the array keeps the previous call's contents: the tickets must start at zero
-  const size_t units = static_cast<size_t>(kv->batch) * kv->num_kv_heads;
-  if (cudaMemsetAsync(ws + L.tickets, 0, units * sizeof(int32_t), s) != cudaSuccess) return MSA_ERR_CUDA;
+  if (f32) {
+    // the array keeps the previous call's contents: the tickets must start at zero
+    const size_t units = static_cast<size_t>(kv->batch) * kv->num_kv_heads;
+    if (cudaMemsetAsync(ws + L.tickets, 0, units * sizeof(int32_t), s) != cudaSuccess) return MSA_ERR_CUDA;
+  }
   DecodeArgs a;
   a.q = q;
   a.hq = num_q_heads;

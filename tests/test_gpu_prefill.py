@@ -6,7 +6,8 @@ import torch
 
 from oracle import msa_oracle as O
 from synth import make_prefill_inputs, make_workload, WORKLOADS
-from tests.parity import SCALE, SelectionStats, check_lse, check_output, check_selection, to64
+from tests.parity import (SCALE, PoolStats, SelectionStats, check_lse, check_output, check_pooled, check_selection,
+                          record, to64)
 
 pytestmark = pytest.mark.gpu
 
@@ -49,22 +50,28 @@ def run_prefill(inp, k_scored, k_total, dense=False, sparse=True):
     return res
 
 
+def gpu_pooled_head(inp, res, h, n_full):
+    if inp.layout == "contiguous":
+        return to64(res["pooled"][0, h, :n_full])
+    return to64(res["pooled"][inp.page_table[0, :n_full].long(), h])
+
+
 def verify_tiles(inp, res, tiles, heads, k_scored, k_total, rows_per_tile=None, stats=None, check_dense=False,
-                 check_sparse=True):
+                 check_sparse=True, pool_stats=None):
+    """Tiles are the chunk's queries that sit in one 64-token block
+    (O.prefill_tiles); tile j's list is idx[j]."""
     grp = inp.num_q_heads // inp.num_kv_heads
     total = inp.q_start + inp.n_new
+    part = {j: (lo, hi) for j, lo, hi in O.prefill_tiles(inp.q_start, inp.n_new)}
     for h in heads:
-        kr = to64(inp.kv_rows(h, "k"))
-        vr = to64(inp.kv_rows(h, "v"))
-        pooled, _ = O.pool_block_keys(kr, total, inp.dtype)
-        if inp.layout == "contiguous":
-            got_pool = res["pooled"][0, h, :total // 64]
-        else:
-            got_pool = res["pooled"][inp.page_table[0, :total // 64].long(), h]
-        assert np.array_equal(to64(got_pool), pooled), f"pooled keys differ, head {h}"
+        kr = inp.kv_rows(h, "k").cpu()
+        vr = inp.kv_rows(h, "v").cpu()
+        pooled, exact = O.pool_block_keys(kr, total, inp.dtype)
+        check_pooled(gpu_pooled_head(inp, res, h, total // 64), pooled, exact, inp.dtype,
+                     to64(kr) if inp.dtype == "f32" else None, pool_stats, f"pooled keys, head {h}")
         for j in tiles:
-            r0, r1 = 64 * j, min(inp.n_new, 64 * j + 64)
-            q_tile = to64(inp.q[r0:r1, h * grp:(h + 1) * grp])
+            r0, r1 = part[j]
+            q_tile = inp.q[r0:r1, h * grp:(h + 1) * grp].cpu()
             sel = O.prefill_tile_select(q_tile, j, inp.q_start, pooled, k_scored, k_total)
             got_idx = res["idx"][j, h].cpu().numpy()
             check_selection(got_idx, sel["scores"], k_scored, sel["diag"], k_total, stats)
@@ -82,6 +89,19 @@ def verify_tiles(inp, res, tiles, heads, k_scored, k_total, rows_per_tile=None, 
                     check_output(to64(res["dense_out"][r0 + r, h * grp:(h + 1) * grp]), od, inp.dtype,
                                  f"dense prefill row {r0 + r} head {h}")
                     check_lse(to64(res["dense_lse"][r0 + r, h * grp:(h + 1) * grp]), ld, "dense lse")
+
+
+def verify_tile_selection_all(inp, res, k_scored, k_total, stats):
+    """The selection rule on every (tile, KV head) unit of the chunk."""
+    grp = inp.num_q_heads // inp.num_kv_heads
+    total = inp.q_start + inp.n_new
+    idx = res["idx"].cpu().numpy()
+    q = inp.q.cpu()
+    for h in range(inp.num_kv_heads):
+        pooled, _ = O.pool_block_keys(inp.kv_rows(h, "k").cpu(), total, inp.dtype)
+        for j, r0, r1 in O.prefill_tiles(inp.q_start, inp.n_new):
+            sel = O.prefill_tile_select(q[r0:r1, h * grp:(h + 1) * grp], j, inp.q_start, pooled, k_scored, k_total)
+            check_selection(idx[j, h], sel["scores"], k_scored, sel["diag"], k_total, stats)
 
 
 @pytest.mark.parametrize("hq,hkv", [(16, 2), (8, 8), (16, 4)])
@@ -138,12 +158,18 @@ def test_prefill_from_empty_prefix(dev):
 
 def test_full_chunked_prefill(dev):
     """8192 new tokens on a 131072-token prefix, 8 KV heads, 64 query heads,
-    top-32 + diagonal: tiles and rows sampled across the chunk."""
+    top-32 + diagonal: the selection of every (tile, head) unit; outputs on 16
+    (tile, head) pairs spread over the chunk and the heads, 6 rows each."""
     w = WORKLOADS["prefill_8k_on_128k"]
     inp = make_workload("prefill_8k_on_128k", device=dev)
     res = run_prefill(inp, w["k_scored"], w["k_total"], dense=True)
     assert res["status"] == 0
-    stats = SelectionStats()
-    verify_tiles(inp, res, [0, 57, 127], [0, 5], w["k_scored"], w["k_total"], rows_per_tile=6, stats=stats,
-                 check_dense=True)
-    print("prefill selection", stats)
+    stats, pstats = SelectionStats(), PoolStats()
+    verify_tile_selection_all(inp, res, w["k_scored"], w["k_total"], stats)
+    n_tiles = (inp.n_new + 63) // 64
+    for i in range(16):
+        tile, head = (i * 37) % n_tiles, i % inp.num_kv_heads
+        verify_tiles(inp, res, [tile], [head], w["k_scored"], w["k_total"], rows_per_tile=6,
+                     check_dense=(i % 4 == 0), pool_stats=pstats if i < inp.num_kv_heads else None)
+    record("prefill_8k_on_128k (select + attend)", units=stats.units, near_ties=stats.near_ties,
+           summary_elements=pstats.elements, summary_one_step=pstats.differ)

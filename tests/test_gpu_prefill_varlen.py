@@ -8,7 +8,7 @@ import torch
 
 from oracle import msa_oracle as O
 from synth import make_prefill_batch_inputs
-from tests.parity import SCALE, check_lse, check_output, check_selection, to64
+from tests.parity import SCALE, check_lse, check_output, check_pooled, check_selection, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -83,14 +83,18 @@ def verify_against_oracle(inp, res, k_scored, k_total, rows_per_tile=7):
     grp = c.num_q_heads // hkv
     for s, (q0, n) in enumerate(zip(inp.q_starts, inp.q_counts)):
         total = q0 + n
-        qs = inp.q_rows(s)
+        qs = inp.q_rows(s).cpu()
         for h in range(hkv):
-            kr, vr = to64(c.kv_rows(s, h, "k")), to64(c.kv_rows(s, h, "v"))
-            pooled, _ = O.pool_block_keys(kr, total, c.dtype)
-            for j in range((n + 63) // 64):
+            kr, vr = c.kv_rows(s, h, "k").cpu(), c.kv_rows(s, h, "v").cpu()
+            pooled, exact = O.pool_block_keys(kr, total, c.dtype)
+            nf = total // 64
+            got_pool = res["pooled"][s, h, :nf] if c.layout == "contiguous" else \
+                res["pooled"][c.page_table[s, :nf].long(), h]
+            check_pooled(to64(got_pool), pooled, exact, c.dtype, to64(kr) if c.dtype == "f32" else None,
+                         what=f"pooled keys seq {s} head {h}")
+            for j, r0, r1 in O.prefill_tiles(q0, n):
                 g = inp.tile_off[s] + j
-                r0, r1 = 64 * j, min(n, 64 * j + 64)
-                q_tile = to64(qs[r0:r1, h * grp:(h + 1) * grp])
+                q_tile = qs[r0:r1, h * grp:(h + 1) * grp]
                 sel = O.prefill_tile_select(q_tile, j, q0, pooled, k_scored, k_total)
                 got_idx = res["idx"][g, h].cpu().numpy()
                 check_selection(got_idx, sel["scores"], k_scored, sel["diag"], k_total)

@@ -120,7 +120,8 @@ def test_prefill_sink(dev):
     torch.cuda.synchronize()
     assert msa.msa_read_device_status(ws.buf) == 0
     grp = hq // inp.num_kv_heads
-    pooled_h = [to64(pooled[0, h]) for h in range(inp.num_kv_heads)]
+    total = inp.q_start + n
+    pooled_h = [O.pool_block_keys(inp.kv_rows(h, "k").cpu(), total, "bf16")[0] for h in range(inp.num_kv_heads)]
     for j in range(n_tiles):
         rows = to64(inp.q[64 * j:64 * (j + 1)])
         for h in range(inp.num_kv_heads):

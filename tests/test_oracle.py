@@ -35,7 +35,7 @@ def test_bf16_rounding_matches_torch_conversion():
         np.array([0.0, -0.0, 1.0, -1.0, 3.0e38, -3.0e38, 1e-40, np.inf, -np.inf], dtype=np.float32),
     ])
     ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
-    got = O.round_f32_to_bf16(x)
+    got = O.round_to_bf16(x)
     assert np.array_equal(got, ref)
 
 
@@ -48,8 +48,8 @@ def test_bf16_rounding_ties_to_even():
         -(1.0 + ulp / 2): -1.0,
     }
     for x, want in cases.items():
-        assert O.round_f32_to_bf16(np.float32(x)) == want
-    assert np.isnan(O.round_f32_to_bf16(np.float32(np.nan)))
+        assert O.round_to_bf16(np.float32(x)) == want
+    assert np.isnan(O.round_to_bf16(np.float32(np.nan)))
 
 
 # --------------------------------------------------------------------------- pooling
@@ -76,7 +76,7 @@ def test_pool_closed_form_index_pattern():
 
 def test_pool_stored_value_within_rounding_bound_of_mean():
     d = O.HEAD_DIM
-    k = O.round_f32_to_bf16(RNG.standard_normal((64 * 40, d)).astype(np.float32))
+    k = O.round_to_bf16(RNG.standard_normal((64 * 40, d)).astype(np.float32))
     stored, exact = O.pool_block_keys(k, k.shape[0], "bf16")
     # fp32 sum of 64 terms: |err| <= 63 * 2^-24 * sum|x|; then a half bf16 ulp
     absmean = np.abs(k).reshape(40, 64, d).mean(axis=1)
@@ -322,7 +322,7 @@ def test_token_max_equals_summary_score_for_constant_blocks():
     # the summary key r (pooling 64 copies of r gives r exactly)
     rng = np.random.default_rng(7)
     nb = 5
-    r = O.round_f32_to_bf16(rng.standard_normal((nb, O.HEAD_DIM)).astype(np.float32))
+    r = O.round_to_bf16(rng.standard_normal((nb, O.HEAD_DIM)).astype(np.float32))
     kidx = np.repeat(r, O.BLOCK, axis=0)
     q = rng.standard_normal(O.HEAD_DIM)
     got = O.score_blocks_token_max(q, kidx, nb)
@@ -472,3 +472,190 @@ def test_boundary_gap_definition():
     assert O.boundary_gap(s, 6) is None
     assert O.boundary_gap(s, 0) is None
     assert O.boundary_gap(np.array([]), 3) is None
+
+
+# --------------------------------------------------------------------------- the double-precision reading of pooling
+
+def test_bf16_rounding_from_double_in_one_step():
+    # 1 + 2^-8 + 2^-30 lies just above the tie between 1 and 1 + 2^-7; a detour
+    # through binary32 would land exactly on the tie and round down to 1
+    assert O.round_to_bf16(1.0 + 2.0 ** -8 + 2.0 ** -30) == 1.0 + 2.0 ** -7
+    assert O.round_to_bf16(1.0 + 2.0 ** -8) == 1.0                      # the tie itself: to even
+    assert O.round_to_bf16(2.0 ** -134) == 0.0                          # half the smallest subnormal: to even
+    assert O.round_to_bf16(1.5 * 2.0 ** -134) == 2.0 ** -133
+    big = (2.0 - 2.0 ** -7) * 2.0 ** 127                                # largest finite bfloat16
+    assert O.round_to_bf16(big) == big
+    assert O.round_to_bf16(2.0 ** 128 - 2.0 ** 119) == np.inf           # halfway past it
+    assert O.round_to_bf16(2.0 ** 128 - 2.0 ** 119 - 2.0 ** 100) == big
+
+
+def test_pool_sums_in_double_and_rounds_once():
+    d = O.HEAD_DIM
+    # fp32 storage: one key 1.0 and 63 keys 2^-25. Summed in binary32 the small
+    # keys vanish (each is below half a unit of 1.0); the exact mean is
+    # 2^-6 + 63 * 2^-31, whose nearest binary32 value is 2^-6 + 2^-25
+    k = np.full((64, d), 2.0 ** -25, dtype=np.float32)
+    k[0] = 1.0
+    stored, exact = O.pool_block_keys(k, 64, "f32")
+    assert np.all(exact == 2.0 ** -6 + 63 * 2.0 ** -31)
+    assert np.all(stored == 2.0 ** -6 + 2.0 ** -25)
+    # bf16 storage: the mean of 32 ones and 32 values 1 + 2^-7 is the tie
+    # 1 + 2^-8 (rounds to the even 1.0); one more key on the high side moves the
+    # mean above the tie (rounds up)
+    k = np.ones((64, d))
+    k[:32] = 1.0 + 2.0 ** -7
+    stored, exact = O.pool_block_keys(k, 64, "bf16")
+    assert np.all(exact == 1.0 + 2.0 ** -8) and np.all(stored == 1.0)
+    k[32] = 1.0 + 2.0 ** -7
+    stored, _ = O.pool_block_keys(k, 64, "bf16")
+    assert np.all(stored == 1.0 + 2.0 ** -7)
+
+
+def test_pool_reads_bf16_bits_exactly():
+    # a bfloat16 tensor and its float64 values give the same summaries
+    g = torch.Generator().manual_seed(3)
+    k = torch.randn(64 * 5 + 9, O.HEAD_DIM, generator=g).to(torch.bfloat16)
+    a = O.pool_block_keys(k, k.shape[0], "bf16")
+    b = O.pool_block_keys(k.double().numpy(), k.shape[0], "bf16")
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# --------------------------------------------------------------------------- unit-parallel functions agree with the per-unit steps
+
+def test_decode_select_units_matches_the_per_unit_steps():
+    from synth import make_decode_inputs
+    lens = [64 * 37 + 5, 64 * 20, 63, 64, 64 * 9 + 1]
+    inp = make_decode_inputs(lens, 2, 8, "bf16", "contiguous", needles=2, seed=41)
+    hkv, grp = 2, 4
+    cap = inp.k.shape[2]
+    for force_local in (1, 0, 3):
+        r = O.decode_select_units(inp.q.view(len(lens) * hkv, grp, -1), inp.k.view(len(lens) * hkv, cap, -1),
+                                  [n for n in lens for _ in range(hkv)], "bf16", 5, 7, force_local,
+                                  want_scores=True, want_pooled=True)
+        for s, n in enumerate(lens):
+            for h in range(hkv):
+                u = s * hkv + h
+                qg, kr = inp.q[s, h * grp:(h + 1) * grp], inp.k[s, h]
+                pooled, _ = O.pool_block_keys(kr, n, "bf16")
+                assert np.array_equal(r["pooled"][u, :pooled.shape[0]], pooled)
+                nb, nbf = O.num_blocks(n), O.num_full_blocks(n)
+                n_cand = min(nbf, nb - 1) if force_local & 1 else nbf
+                n_cand = max(n_cand, 0)
+                scores = O.score_blocks(O.index_query(qg), pooled, n_cand)
+                assert np.array_equal(r["scores"][u, :n_cand], scores)
+                forced = nb - 1 if force_local & 1 and nb > 0 else None
+                if force_local & 2:
+                    has0 = nb > 0 and forced != 0
+                    want = O.select_blocks_sink(scores, 5, forced, 7, has0) if n_cand > 0 else \
+                        O.select_blocks(scores, 5, forced, 7) if not has0 else \
+                        np.array(sorted({0} | ({forced} if forced is not None else set())) + [-1] * 6)[:7]
+                else:
+                    want = O.select_blocks(scores, 5, forced, 7)
+                assert list(r["selected"][u]) == list(want), (force_local, s, h)
+                ranked = scores[1:] if force_local & 2 and n_cand > 0 else scores
+                gap = O.boundary_gap(ranked, 5)
+                if gap is None:
+                    assert np.isnan(r["gap"][u]).all()
+                else:
+                    assert tuple(r["gap"][u]) == gap
+
+
+def test_decode_step_units_matches_decode_unit():
+    from synth import make_decode_inputs
+    lens = [64 * 40 + 17, 64 * 33, 100]
+    inp = make_decode_inputs(lens, 2, 16, "bf16", "contiguous", needles=2, seed=7)
+    hkv, grp, cap = 2, 8, inp.k.shape[2]
+    mb = cap // 64
+    pooled = np.full((len(lens) * hkv, mb, O.HEAD_DIM), np.nan)
+    for s, n in enumerate(lens):
+        for h in range(hkv):
+            p, _ = O.pool_block_keys(inp.k[s, h], n, "bf16")
+            pooled[s * hkv + h, :p.shape[0]] = p
+    sel, o, lse = O.decode_step_units(inp.q.view(-1, grp, O.HEAD_DIM), pooled, inp.k.view(-1, cap, O.HEAD_DIM),
+                                      inp.v.view(-1, cap, O.HEAD_DIM), [n for n in lens for _ in range(hkv)], 6, 8,
+                                      1 / math.sqrt(128))
+    for s, n in enumerate(lens):
+        for h in range(hkv):
+            u = s * hkv + h
+            ref = O.decode_unit(inp.q[s, h * grp:(h + 1) * grp], inp.k[s, h], inp.v[s, h], n, 6, 8,
+                                1 / math.sqrt(128), "bf16")
+            assert list(sel[u]) == list(ref["selected"])
+            np.testing.assert_allclose(o[u], ref["o"], rtol=0, atol=1e-13)
+            np.testing.assert_allclose(lse[u], ref["lse"], rtol=0, atol=1e-13)
+
+
+# --------------------------------------------------------------------------- chunks that start inside a block
+
+@pytest.mark.parametrize("q_start,n_new", [(0, 1), (0, 64), (128, 200), (100, 1), (100, 28), (100, 29),
+                                           (100, 300), (63, 2), (4097, 4096)])
+def test_prefill_tiles_partition_the_chunk_by_block(q_start, n_new):
+    tiles = O.prefill_tiles(q_start, n_new)
+    rows = [r for _, lo, hi in tiles for r in range(lo, hi)]
+    assert rows == list(range(n_new))                       # every chunk row once, in order
+    assert [j for j, _, _ in tiles] == list(range(len(tiles)))
+    for j, lo, hi in tiles:
+        assert 0 < hi - lo <= 64
+        blocks = {(q_start + r) // 64 for r in range(lo, hi)}
+        assert blocks == {q_start // 64 + j}                # one block per tile: the diagonal one
+    if q_start % 64 == 0:
+        assert [(lo, hi) for _, lo, hi in tiles] == [(64 * j, min(n_new, 64 * j + 64)) for j in range(len(tiles))]
+    assert O.prefill_tiles(q_start, 0) == []
+
+
+@pytest.mark.parametrize("pos", [64 * 9, 64 * 9 + 1, 64 * 9 + 37, 64 * 9 + 63])
+def test_one_token_chunk_equals_the_decode_step(pos):
+    # a chunk of one token at position pos sees what a decode step whose newest
+    # token sits at pos sees: same index query, candidates, kept block, output
+    rng = np.random.default_rng(pos)
+    k = rng.standard_normal((64 * 11, O.HEAD_DIM))
+    v = rng.standard_normal((64 * 11, O.HEAD_DIM))
+    q = rng.standard_normal((1, 4, O.HEAD_DIM))
+    pooled, _ = O.pool_block_keys(k, pos + 1, "f32")
+    ((j, lo, hi),) = O.prefill_tiles(pos, 1)
+    for kk in (1, 3, 9, 20):
+        pre = O.prefill_tile_select(q[lo:hi], j, pos, pooled, kk, kk + 1)
+        dec = O.decode_unit(q[0], k, v, pos + 1, kk, kk + 1, 1 / math.sqrt(128), "f32", pooled=pooled)
+        assert list(pre["selected"]) == list(dec["selected"]) and pre["diag"] == dec["forced"]
+        np.testing.assert_array_equal(pre["scores"], dec["scores"])
+        o, lse = O.prefill_rows(q, [pos], k, v, pos + 1, pre["selected"], 1 / math.sqrt(128))
+        np.testing.assert_allclose(o[0], dec["o"], rtol=0, atol=1e-14)
+        np.testing.assert_allclose(lse[0], dec["lse"], rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("q_start,n_new", [(100, 90), (63, 70), (130, 5)])
+def test_unaligned_chunk_with_every_block_equals_dense(q_start, n_new):
+    rng = np.random.default_rng(q_start + n_new)
+    total = q_start + n_new
+    k = rng.standard_normal((total, O.HEAD_DIM))
+    v = rng.standard_normal((total, O.HEAD_DIM))
+    q = rng.standard_normal((n_new, 2, O.HEAD_DIM))
+    pooled, _ = O.pool_block_keys(k, total, "f32")
+    for j, lo, hi in O.prefill_tiles(q_start, n_new):
+        sel = O.prefill_tile_select(q[lo:hi], j, q_start, pooled, k_scored=64, k_total=6)
+        assert [b for b in sel["selected"] if b >= 0] == list(range(sel["diag"] + 1))
+        pos = q_start + np.arange(lo, hi)
+        o, lse = O.prefill_rows(q[lo:hi], pos, k, v, total, sel["selected"], 0.125)
+        for i in range(hi - lo):
+            od, ld = O.dense_gqa(q[lo + i], k, v, pos[i], 0.125)
+            np.testing.assert_allclose(o[i], od, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse[i], ld, rtol=0, atol=1e-12)
+
+
+def test_chunk_split_at_a_block_boundary_keeps_every_list():
+    # a tile's list depends only on its own queries and the summaries before
+    # it, so a chunk split at a block boundary gives the same lists
+    rng = np.random.default_rng(77)
+    q_start, n_new, cut = 100, 250, 28 + 64 * 2        # 100 + 156 = 256: a block boundary
+    total = q_start + n_new
+    k = rng.standard_normal((total, O.HEAD_DIM))
+    q = rng.standard_normal((n_new, 3, O.HEAD_DIM))
+    pooled, _ = O.pool_block_keys(k, total, "f32")
+    whole = [O.prefill_tile_select(q[lo:hi], j, q_start, pooled, 2, 3)["selected"]
+             for j, lo, hi in O.prefill_tiles(q_start, n_new)]
+    parts = [O.prefill_tile_select(q[lo:hi], j, q_start, pooled, 2, 3)["selected"]
+             for j, lo, hi in O.prefill_tiles(q_start, cut)]
+    parts += [O.prefill_tile_select(q[cut + lo:cut + hi], j, q_start + cut, pooled, 2, 3)["selected"]
+              for j, lo, hi in O.prefill_tiles(q_start + cut, n_new - cut)]
+    assert len(whole) == len(parts)
+    for a, b in zip(whole, parts):
+        assert list(a) == list(b)
