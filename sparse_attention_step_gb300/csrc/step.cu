@@ -8,11 +8,11 @@
 //      streams the summary rows (2-D TMA, 128 rows per 32 KB stage, a 3-stage
 //      ring) and eight warps dot them with the group's index query on the
 //      tensor cores (mma.sync, the query split into two bf16 parts).
-//   2. The CTA keeps its best 64 keys (register bitonic sorts and merges);
-//      after one cluster barrier every CTA gathers the C lists through
-//      distributed shared memory and merges them identically, so each holds
-//      the unit's top-k and takes its slice of the index list (the leader
-//      writes the list out).
+//   2. The CTA keeps its best k keys (a radix select finds its k-th largest
+//      key, the keys at or above it are gathered); after one cluster barrier
+//      every CTA gathers the C lists through distributed shared memory and
+//      selects from their union the same way, so each holds the unit's top-k
+//      and takes its slice of the index list (the leader writes it out).
 //   3. CTA r attends over its slice: the producer streams each 64x128 K and V
 //      block with 2-D TMA copies (128-byte swizzle) into the 3-stage ring;
 //      warps 0-3 consume every block in order (each warp 16 tokens: S = K Q^T
@@ -24,6 +24,8 @@
 //      partial into the shared memory of CTA p % C, and after one cluster
 //      barrier CTA r merges and writes output pieces r, r + C, ...
 #include <float.h>
+
+#include <algorithm>
 
 #include "kernels.cuh"
 #include "rows.cuh"
@@ -42,8 +44,6 @@ constexpr int kStRowsPerStage = kStStage / (kHeadDim * 2);  // 128 bf16 summary 
 constexpr int kStMaxChunk = 1024;                           // candidate rows per CTA
 constexpr int kStMaxList = 64;                              // selected blocks per CTA
 constexpr int kStMaxCluster = 16;
-constexpr int kStPrefetchExtra = 0;             // L2 prefetches per CTA beyond ceil(kk / C)
-constexpr int kStEarlyPrefetch = 4;             // blocks per CTA prefetched from the warp maxima
 constexpr int kStG = 8;                                     // heads per group handled
 constexpr int kStOS = kHeadDim + 4;                         // padded merge rows
 constexpr int kStRecv = 12;                                 // floats per pushed piece: O[8], M, L, pad
@@ -57,6 +57,7 @@ struct StepArgs {
   int k_scored, k_total, force_local;
   int chunk;  // candidate rows per CTA, a multiple of 128, <= kStMaxChunk
   int bps;    // index-list entries attended per CTA, <= kStMaxList
+  int samples_per_warp;  // 1, 2, 4 or 8 sample keys per compute warp for the selection bound
   float scale_log2;
   int32_t* idx_out;  // [batch, hkv, k_total]
   __nv_bfloat16* out;
@@ -76,11 +77,17 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(st_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* keys = reinterpret_cast<uint64_t*>(ring + kStages * kStStage);  // [kStMaxChunk]
   __shared__ uint64_t full[kStages], empty[kStages];
-  __shared__ uint64_t xlist[64];  // this CTA's best keys, read by the whole cluster
+  __shared__ uint64_t xlist2[64];    // exact path: this CTA's best kk keys
+  __shared__ uint32_t xsamp[64];     // this CTA's sample scores (read by the cluster)
+  __shared__ uint64_t xsurv[64];     // this CTA's keys scoring >= L (read by the cluster)
+  __shared__ int xnsurv;             // how many (may exceed 64: then only 64 are stored)
+  __shared__ uint32_t lbound;
+  __shared__ int ccount[kStMaxCluster];
+  __shared__ uint64_t sel_keys[64];  // the unit's selected keys
+  __shared__ RadixScratch radix;
+  __shared__ int n_sel;
   __shared__ int32_t blocks[kStMaxList];
-  __shared__ int sorted_blocks[64];
   __shared__ int n_blocks;
-  __shared__ uint64_t wbest[kStWarps];  // each compute warp's best key (early prefetch)
   __shared__ float qsum[kHeadDim];  // the group's index query (sum of its query heads), fp32
   __shared__ float wm[kStAttnWarps][kStG], wl[kStAttnWarps][kStG];
 
@@ -144,6 +151,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   __syncthreads();
 
   // ---------------------------------------------------------------- 1. scores
+  uint64_t lmax = 0ull;  // compute warps: the largest key this lane produced
   if (warp == kStWarps) {
     if (lane == 0) {
       // 128 summary rows per stage as two 64-column boxes (128-byte swizzle);
@@ -193,15 +201,23 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
         ldsm_x4(sbase + (kk2 >> 2) * (kStStage / 2) + swz128(krow, (kk2 & 3) * 2 + kchunk), a0, a1, a2, a3);
         mma_bf16(sacc, a0, a1, a2, a3, qb[kk2][0], qb[kk2][1]);
       }
+      uint64_t ka = 0ull, kb = 0ull;
       if (c == 0) {
         const int i0 = 16 * warp + g, i1 = i0 + 8;
         const int base = st * kStRowsPerStage;
-        if (i0 < n)
-          keys[base + i0] = (skip && r0 + base + i0 == 0) ? 0ull : sel_key(sacc[0] + sacc[1], static_cast<int>(r0 + base + i0));
-        if (i1 < n) keys[base + i1] = sel_key(sacc[2] + sacc[3], static_cast<int>(r0 + base + i1));
+        if (i0 < n) {
+          ka = (skip && r0 + base + i0 == 0) ? 0ull : sel_key(sacc[0] + sacc[1], static_cast<int>(r0 + base + i0));
+          keys[base + i0] = ka;
+        }
+        if (i1 < n) {
+          kb = sel_key(sacc[2] + sacc[3], static_cast<int>(r0 + base + i1));
+          keys[base + i1] = kb;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
+      lmax = ka > lmax ? ka : lmax;
+      lmax = kb > lmax ? kb : lmax;
     }
   }
   __syncthreads();  // every stage consumed: the ring is free until the attention phase
@@ -218,61 +234,101 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   }
 
   // ---------------------------------------------------------------- 2. selection
-  // (a) this CTA's best 64: each warp bitonic-sorts batches of 64 keys in
-  // registers and merges them into a running list; the eight warp lists are
-  // then merged pairwise. Key 0 pads and sorts last.
-  uint64_t* lists = reinterpret_cast<uint64_t*>(ring);  // [kStMaxCluster][64]
-  uint64_t* tmp = lists + kStMaxCluster * 64;           // [kStMaxCluster / 2][64]
+  // Fast path, exact by construction:
+  // (a) Samples: every compute warp offers the largest key of each of its p
+  //     lane groups (p per warp, chosen so the cluster holds >= 2 kk samples).
+  //     The samples are real keys, so their kk-th largest score L is at most
+  //     the score of the unit's kk-th key: every key of the selection scores
+  //     >= L.
+  // (b) After a cluster barrier every CTA gathers all samples through
+  //     distributed shared memory and finds L by rank counting; it keeps its
+  //     own keys scoring >= L (survivors, normally a few more than kk / C).
+  // (c) After a second cluster barrier every CTA gathers all survivors and
+  //     ranks them: the best kk, in rank order, are the unit's selection.
+  // If a CTA has more than 64 survivors or the union more than 256 (e.g.
+  // every score equal), every CTA takes the exact path instead: a radix
+  // select of its own kk best keys, an exchange, and a radix select over
+  // their union. The decision is the same in every CTA of the cluster.
+  uint64_t* lists = reinterpret_cast<uint64_t*>(ring);  // [C][64]: gathered keys
+  uint32_t* samp_all = reinterpret_cast<uint32_t*>(ring + 16384);  // [C * 8 * p] gathered sample scores
   const int kk = static_cast<int>(n_cand - skip < a.k_scored ? n_cand - skip : static_cast<int64_t>(a.k_scored));
+  const int p = a.samples_per_warp;  // 1, 2, 4 or 8
+  const int n_samp = kStWarps * p;
   if (warp < kStWarps) {
-    __syncwarp();
-    {
-      // The best key of the warp's first 64 rows goes to the producer, which
-      // pulls the K/V blocks of the CTA's leading warp maxima into L2 while
-      // the sort runs (HBM is otherwise idle then): the CTA's few best blocks
-      // are almost always among the unit's selection.
-      const int e0 = warp * 64 + 2 * lane;
-      const uint64_t x0 = e0 < rows ? keys[e0] : 0ull, x1 = e0 + 1 < rows ? keys[e0 + 1] : 0ull;
-      uint64_t m = x0 > x1 ? x0 : x1;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const uint64_t o = shfl_xor_u64(m, off);
-        m = o > m ? o : m;
-      }
-      if (lane == 0) wbest[warp] = m;
-      bar_arrive_warps(2, 32 * (kStWarps + 1));
+    // group max over the key-holding lanes (lane = 4 j, j = 0..7) of each group of 8 / p
+    uint64_t v = lmax;
+    for (int o = 1; o < 8 / p; o <<= 1) {
+      const uint64_t w2 = shfl_xor_u64(v, 4 * o);
+      v = w2 > v ? w2 : v;
     }
-    uint64_t run[2] = {0ull, 0ull};
-    for (int b = warp * 64; b < rows; b += kStWarps * 64) {
-      uint64_t x[2];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int e = b + 2 * lane + r;
-        x[r] = e < rows ? keys[e] : 0ull;
-      }
-      warp_sort64_desc(x);
-      if (b == warp * 64) {
-        run[0] = x[0];
-        run[1] = x[1];
-      } else {
-        warp_merge64_reg(run, x);
+    const int j = lane >> 2;
+    if ((lane & 3) == 0 && (j % (8 / p)) == 0) xsamp[warp * p + j / (8 / p)] = static_cast<uint32_t>(v >> 32);
+  }
+  __syncthreads();
+  if (C > 1) cluster_arrive();
+  if (C > 1) cluster_wait();
+  for (int i = tid; i < C * n_samp; i += blockDim.x) {
+    const int r = i / n_samp, j = i - r * n_samp;
+    samp_all[i] = C > 1 ? static_cast<uint32_t>(ld_dsmem_i32(dsmem_addr(smem_u32(xsamp + j), static_cast<uint32_t>(r))))
+                        : xsamp[j];
+  }
+  if (tid == 0) {
+    lbound = 0u;
+    n_sel = 0;
+  }
+  __syncthreads();
+  {
+    // L = the kk-th largest sample score: the value with fewer than kk samples
+    // above it and at least kk at or above it (equal values write the same L).
+    // q adjacent threads count for each sample and add their counts.
+    const int ns = C * n_samp;  // <= 128
+    const int q = ns <= 72 ? 4 : 2;
+    const int i = tid / q, part = tid - i * q;
+    const uint32_t v = i < ns ? samp_all[i] : 0u;
+    int gt = 0, ge = 0;
+    if (i < ns) {
+      for (int j = part; j < ns; j += q) {
+        const uint32_t u = samp_all[j];
+        gt += u > v ? 1 : 0;
+        ge += u >= v ? 1 : 0;
       }
     }
-    lists[warp * 64 + 2 * lane] = run[0];
-    lists[warp * 64 + 2 * lane + 1] = run[1];
-  } else {
-    bar_sync_warps(2, 32 * (kStWarps + 1));
-    const uint64_t m = lane < kStWarps ? wbest[lane] : 0ull;
-    int rk = 0;
-#pragma unroll
-    for (int j = 0; j < kStWarps; ++j) {
-      const uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(m), j);
-      const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(m >> 32), j);
-      rk += ((static_cast<uint64_t>(hi) << 32) | lo) > m ? 1 : 0;
+    for (int o = 1; o < q; o <<= 1) {
+      gt += __shfl_xor_sync(0xffffffffu, gt, o);
+      ge += __shfl_xor_sync(0xffffffffu, ge, o);
     }
-    const int n_early = min(kStEarlyPrefetch, (kk + C - 1) / C / 2);  // half the CTA's share of the list
-    if (lane < kStWarps && m != 0ull && rk < n_early) {
-      const int64_t row = kv.block_row(s, h, sel_block(m), a.status, kIdDecode);
+    if (i < ns && part == 0 && gt < kk && kk <= ge) lbound = v;
+  }
+  __syncthreads();
+  {
+    const uint32_t L = lbound;
+    for (int base = 0; base < rows; base += blockDim.x) {
+      const int i = base + tid;
+      const uint64_t key = i < rows ? keys[i] : 0ull;
+      const bool hit = key != 0ull && static_cast<uint32_t>(key >> 32) >= L;
+      const unsigned mk = __ballot_sync(0xffffffffu, hit);
+      int slot = 0;
+      if (lane == 0 && mk != 0u) slot = atomicAdd(&n_sel, __popc(mk));
+      slot = __shfl_sync(0xffffffffu, slot, 0);
+      const int pos = slot + __popc(mk & ((1u << lane) - 1u));
+      if (hit && pos < 64) xsurv[pos] = key;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) xnsurv = n_sel;
+  __syncthreads();
+  if (C > 1) cluster_arrive();
+  if (warp == kStWarps) {
+    // pull the K/V of this CTA's best survivors (about its share of the list,
+    // plus one) into L2; prefetching every survivor would waste bandwidth
+    const int ns = min(xnsurv, 64);
+    const int n_pf = min(ns, (kk + C - 1) / C + 1);
+    for (int j2 = lane; j2 < ns; j2 += 32) {
+      const uint64_t x = xsurv[j2];
+      int rk = 0;
+      for (int j3 = 0; j3 < ns; ++j3) rk += xsurv[j3] > x ? 1 : 0;
+      if (rk >= n_pf) continue;
+      const int64_t row = kv.block_row(s, h, sel_block(x), a.status, kIdDecode);
       if (row >= 0) {
         const int32_t y = static_cast<int32_t>(row);
         tma_prefetch_2d(&tmk, 0, y);
@@ -281,77 +337,72 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
         tma_prefetch_2d(&tmv, 64, y);
       }
     }
-  }
-  __syncthreads();
-  const uint64_t* mine = block_merge_lists(lists, tmp, kStWarps);
-  if (tid < 64) xlist[tid] = mine[tid];
-  // (b) every CTA of the cluster gathers the C lists through distributed
-  // shared memory and merges them the same way, so each one holds the same
-  // top 64 of the unit without a second cluster barrier. xlist is never
-  // written again, and no CTA exits before the closing cluster barrier.
-  // Meanwhile the producer warp starts pulling the K/V blocks of this CTA's
-  // own best candidates into L2: about kk / C of them end up selected, so the
-  // attention phase finds most of its blocks there. Its lanes take their keys
-  // (candidates lane and lane + 32) before the merge below reuses `mine`.
-  const int n_pf = min(kk, (kk + C - 1) / C + kStPrefetchExtra);
-  uint64_t pf_key[2] = {0ull, 0ull};
-  if (warp == kStWarps) {
-    pf_key[0] = lane < n_pf ? mine[lane] : 0ull;
-    pf_key[1] = lane + 32 < n_pf ? mine[lane + 32] : 0ull;
-  }
-  if (C > 1) cluster_arrive();
-  if (warp == kStWarps) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      if (pf_key[j] != 0ull) {
-        const int64_t row = kv.block_row(s, h, sel_block(pf_key[j]), a.status, kIdDecode);
-        if (row >= 0) {
-          const int32_t y = static_cast<int32_t>(row);
-          tma_prefetch_2d(&tmk, 0, y);
-          tma_prefetch_2d(&tmk, 64, y);
-          tma_prefetch_2d(&tmv, 0, y);
-          tma_prefetch_2d(&tmv, 64, y);
-        }
-      }
-    }
     __syncwarp();
-    if (C > 1) cluster_wait();
-  } else {
-    if (C > 1) cluster_wait();
-    else bar_sync_warps(1, 32 * kStWarps);
-    for (int i = tid; i < C * 64; i += 32 * kStWarps)
-      lists[i] = C > 1 ? ld_dsmem_u64(dsmem_addr(smem_u32(xlist + (i & 63)), static_cast<uint32_t>(i >> 6)))
-                       : xlist[i];
-    bar_sync_warps(1, 32 * kStWarps);
-    const uint64_t* best = warps_merge_lists(lists, tmp, C, kStWarps, 1);
-    if (tid < 64) {
-      // ascending block order by counting: the blocks are distinct, so each
-      // one's position is the number of selected blocks below it
-      const int b = tid < kk ? sel_block(best[tid]) : 0;
-      int pos = 0;
-#pragma unroll 4
-      for (int j = 0; j < kk; ++j) pos += sel_block(best[j]) < b ? 1 : 0;
-      if (tid < kk) sorted_blocks[pos] = b;
+  }
+  if (C > 1) cluster_wait();
+  if (tid < C) ccount[tid] = C > 1 ? ld_dsmem_i32(dsmem_addr(smem_u32(&xnsurv), static_cast<uint32_t>(tid))) : xnsurv;
+  if (tid < 64) sel_keys[tid] = 0ull;
+  __syncthreads();
+  int n_union = 0, overflow = 0;
+  for (int r = 0; r < C; ++r) {
+    overflow |= ccount[r] > 64 ? 1 : 0;
+    n_union += ccount[r];
+  }
+  const bool exact = kk == 0 || (!overflow && n_union <= 256 && n_union >= kk);
+  if (exact && kk > 0) {
+    for (int i = tid; i < n_union; i += blockDim.x) {
+      int r = 0, off = i;
+      while (off >= ccount[r]) off -= ccount[r++];
+      lists[i] = C > 1 ? ld_dsmem_u64(dsmem_addr(smem_u32(xsurv + off), static_cast<uint32_t>(r))) : xsurv[off];
+    }
+    __syncthreads();
+    // rank counting, q adjacent threads per key: the best kk go to sel_keys in rank order
+    const int q = n_union <= 72 ? 4 : (n_union <= 144 ? 2 : 1);
+    const int i = tid / q, part = tid - i * q;
+    const uint64_t x = i < n_union ? lists[i] : 0ull;
+    int cnt = 0;
+    if (i < n_union)
+      for (int j = part; j < n_union; j += q) cnt += lists[j] > x ? 1 : 0;
+    for (int o = 1; o < q; o <<= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    if (i < n_union && part == 0 && cnt < kk) sel_keys[cnt] = x;
+  } else if (!exact) {
+    // exact path: this CTA's kk best keys by radix select, a second exchange,
+    // and a radix select over their union
+    if (tid < 64) xlist2[tid] = 0ull;
+    const uint64_t t_local = block_kth_largest(keys, rows, kk, radix);
+    block_compact_ge(keys, rows, t_local, xlist2, 64, &n_sel);
+    if (C > 1) cluster_sync();
+    for (int i = tid; i < C * 64; i += blockDim.x)
+      lists[i] = C > 1 ? ld_dsmem_u64(dsmem_addr(smem_u32(xlist2 + (i & 63)), static_cast<uint32_t>(i >> 6)))
+                       : xlist2[i];
+    __syncthreads();
+    const uint64_t t_unit = block_kth_largest(lists, C * 64, kk, radix);
+    uint64_t* picked = lists + 1024;  // past the C * 64 gathered keys
+    block_compact_ge(lists, C * 64, t_unit, picked, 64, &n_sel);
+    // rank order (the compaction's order differs between CTAs)
+    if (tid < kk) {
+      const uint64_t x = picked[tid];
+      int cnt = 0;
+      for (int j = 0; j < kk; ++j) cnt += picked[j] > x ? 1 : 0;
+      sel_keys[cnt] = x;
     }
   }
   __syncthreads();
-  // (c) the unit's list: kk blocks ascending, then the forced block, then -1.
-  // The leader writes it out; every CTA takes its slice.
-  // (block 0 leads when it is kept as the attention sink)
-  auto list_at = [&](int i) -> int32_t {
+  // (c) the unit's list. Attention slices use the rank order (the same in
+  // every CTA of the cluster): block 0 first when kept as the attention sink,
+  // then the kk selected blocks, then the forced newest block, then -1. The
+  // leader writes the list sorted ascending to idx_out while the attention
+  // runs (warps 5-7 are idle then).
+  auto slice_at = [&](int i) -> int32_t {
     const int j = i - keep0;
-    return j < 0 ? 0 : j < kk ? sorted_blocks[j] : (j == kk && forced >= 0 ? static_cast<int32_t>(forced) : -1);
+    return j < 0 ? 0 : j < kk ? sel_block(sel_keys[j]) : (j == kk && forced >= 0 ? static_cast<int32_t>(forced) : -1);
   };
-  if (rank == 0) {
-    int32_t* out = a.idx_out + unit * a.k_total;
-    for (int i = tid; i < a.k_total; i += blockDim.x) out[i] = list_at(i);
-  }
   if (warp == 0) {
     const int lo = rank * a.bps, hi = min(a.k_total, lo + a.bps);
     int n = 0;
     for (int b0 = lo; b0 < hi; b0 += 32) {
       const int i = b0 + lane;
-      const int32_t b = i >= hi ? -1 : list_at(i);
+      const int32_t b = i >= hi ? -1 : slice_at(i);
       if (b >= nb) set_status(a.status, MSA_ERR_DEVICE_BOUNDS, kIdDecode);
       const bool ok = b >= 0 && b < nb;
       const unsigned m = __ballot_sync(0xffffffffu, ok);
@@ -453,6 +504,22 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     for (int off = 4; off < 32; off <<= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, off);
       l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+  } else if (warp > kStAttnWarps && rank == 0) {
+    // warps 5-7 of the leader: the unit's list, ascending (block 0 when kept as
+    // the sink, the kk selected blocks by counting -- each one's position is
+    // the number of selected blocks below it -- the newest block, then -1)
+    const int t = tid - 32 * (kStAttnWarps + 1);
+    int32_t* out = a.idx_out + unit * a.k_total;
+    if (t < kk) {
+      const int b = sel_block(sel_keys[t]);
+      int pos = 0;
+      for (int j = 0; j < kk; ++j) pos += sel_block(sel_keys[j]) < b ? 1 : 0;
+      out[keep0 + pos] = b;
+    }
+    for (int i = t; i < a.k_total; i += 32 * (kStWarps - kStAttnWarps - 1)) {
+      if (i >= keep0 && i < keep0 + kk) continue;
+      out[i] = (i < keep0) ? 0 : (i == keep0 + kk && forced >= 0 ? static_cast<int32_t>(forced) : -1);
     }
   } else if (warp == kStAttnWarps && lane < 16 && rank == 0 && a.pooled_out != nullptr && forced >= 0 &&
              len % kBlock == 0) {
@@ -685,6 +752,11 @@ cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, c
   a.force_local = cfg.force_local;
   a.chunk = chunk;
   a.bps = bps;
+  // sample keys per compute warp: the fewest that give the cluster at least
+  // twice k_scored samples (their k-th largest bounds the selection from below)
+  int p = 1;
+  while (p < 8 && C * kStWarps * p < 2 * cfg.k_scored) p *= 2;
+  a.samples_per_warp = p;
   a.scale_log2 = scale_log2;
   a.idx_out = idx_out;
   a.out = out;

@@ -403,6 +403,172 @@ __device__ inline bool block_select(const uint64_t* keys, int n, int k, uint64_t
   return true;
 }
 
+__device__ inline uint64_t shfl_idx_u64(uint64_t v, int src) {
+  const uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(v), src);
+  const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(v >> 32), src);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ inline uint64_t shfl_up_u64(uint64_t v, int d) {
+  const uint32_t lo = __shfl_up_sync(0xffffffffu, static_cast<uint32_t>(v), d);
+  const uint32_t hi = __shfl_up_sync(0xffffffffu, static_cast<uint32_t>(v >> 32), d);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// A warp's running top-32: lane i holds the i-th largest key seen so far
+// (descending over the lanes, 0 where the list is not full). Inserts the keys
+// a and b of every lane (0 = none): a key enters only if it beats the current
+// last entry; each one is placed by a ballot (how many entries are larger)
+// and a shift of the entries below it. Costs one short round per key that
+// enters, so once the list holds high keys most new keys are dropped by the
+// first compare. Every lane of the warp calls this.
+__device__ inline void warp_list32_insert2(uint64_t& list, uint64_t a, uint64_t b) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t last = shfl_idx_u64(list, 31);
+  unsigned ma = __ballot_sync(0xffffffffu, a > last);
+  unsigned mb = __ballot_sync(0xffffffffu, b > last);
+  while ((ma | mb) != 0u) {
+    uint64_t x;
+    if (ma != 0u) {
+      const int src = __ffs(ma) - 1;
+      ma &= ma - 1u;
+      x = shfl_idx_u64(a, src);
+    } else {
+      const int src = __ffs(mb) - 1;
+      mb &= mb - 1u;
+      x = shfl_idx_u64(b, src);
+    }
+    const int pos = __popc(__ballot_sync(0xffffffffu, list > x));  // entries larger than x
+    const uint64_t up = shfl_up_u64(list, 1);
+    if (pos < 32) list = lane < pos ? list : (lane == pos ? x : up);
+  }
+}
+
+// Shared scratch of block_kth_largest.
+struct RadixScratch {
+  uint32_t hist[256];
+  uint64_t bin_keys[32];
+  uint64_t prefix, mask, kth;
+  int need, done, n_bin;
+};
+
+// The kk-th largest (kk >= 1) of the nonzero keys in keys[0..n) (nonzero keys
+// are distinct: they carry the block index), or 1 when fewer than kk keys are
+// nonzero (every nonzero key is >= 1). A most-significant-digit radix select:
+// each pass counts, among the keys that share the digits fixed so far, the
+// next 8-bit digit (lanes with the same digit add their count with one atomic,
+// so a crowded digit costs one atomic per warp), and one warp finds the digit
+// that holds the kk-th key. Once that digit holds at most 32 keys they are
+// gathered and ranked by pairwise counting. Typical scores need two passes.
+// Every thread of the CTA calls this (it uses __syncthreads).
+__device__ inline uint64_t block_kth_largest(const uint64_t* keys, int n, int kk, RadixScratch& rs) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nth = blockDim.x;
+  if (tid == 0) {
+    rs.prefix = 0ull;
+    rs.mask = 0ull;
+    rs.need = kk;
+    rs.done = 0;
+    rs.kth = 1ull;
+  }
+  for (int shift = 56;; shift -= 8) {
+    for (int i = tid; i < 256; i += nth) rs.hist[i] = 0u;
+    __syncthreads();
+    const uint64_t prefix = rs.prefix, mask = rs.mask;
+    for (int base = 0; base < n; base += nth) {
+      const int i = base + tid;
+      const uint64_t key = i < n ? keys[i] : 0ull;
+      const bool in = key != 0ull && (key & mask) == prefix;
+      const int digit = in ? static_cast<int>((key >> shift) & 255u) : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, digit);
+      if (in && (__ffs(peers) - 1) == lane) atomicAdd(&rs.hist[digit], static_cast<uint32_t>(__popc(peers)));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l holds digits 255 - 8 l - j, j = 0..7 (descending over the warp)
+      uint32_t h[8], sum = 0u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        h[j] = rs.hist[255 - 8 * lane - j];
+        sum += h[j];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+      const uint32_t need = static_cast<uint32_t>(rs.need);
+      if (total < need) {
+        // fewer keys than kk (only possible in the first pass): all are kept
+        if (lane == 0) rs.done = 1;
+      } else {
+        uint32_t above = incl - sum;
+        if (above < need && incl >= need) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (above + h[j] >= need) {
+              const int d = 255 - 8 * lane - j;
+              rs.prefix = prefix | (static_cast<uint64_t>(d) << shift);
+              rs.mask = mask | (0xFFull << shift);
+              rs.need = static_cast<int>(need - above);
+              if (h[j] <= 32u || shift == 0) {
+                rs.done = 2;
+                rs.n_bin = 0;
+              }
+              break;
+            }
+            above += h[j];
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (rs.done != 0) break;
+  }
+  if (rs.done == 2) {
+    const uint64_t prefix = rs.prefix, mask = rs.mask;
+    for (int i = tid; i < n; i += nth) {
+      const uint64_t key = keys[i];
+      if (key != 0ull && (key & mask) == prefix) {
+        const int slot = atomicAdd(&rs.n_bin, 1);
+        if (slot < 32) rs.bin_keys[slot] = key;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int nb = min(rs.n_bin, 32);
+      const uint64_t me = lane < nb ? rs.bin_keys[lane] : 0ull;
+      int rank = 0;
+      for (int j = 0; j < nb; ++j) rank += rs.bin_keys[j] > me ? 1 : 0;
+      if (lane < nb && rank == rs.need - 1) rs.kth = me;
+    }
+    __syncthreads();
+  }
+  return rs.kth;
+}
+
+// Append every nonzero key >= t of keys[0..n) to out (order unspecified) and
+// return how many there are. `count` is a shared counter; every thread of the
+// CTA calls this (it uses __syncthreads).
+__device__ inline int block_compact_ge(const uint64_t* keys, int n, uint64_t t, uint64_t* out, int cap, int* count) {
+  const int tid = threadIdx.x, lane = tid & 31, nth = blockDim.x;
+  if (tid == 0) *count = 0;
+  __syncthreads();
+  for (int base = 0; base < n; base += nth) {
+    const int i = base + tid;
+    const uint64_t key = i < n ? keys[i] : 0ull;
+    const bool hit = key != 0ull && key >= t;
+    const unsigned m = __ballot_sync(0xffffffffu, hit);
+    int slot = 0;
+    if (lane == 0 && m != 0u) slot = atomicAdd(count, __popc(m));
+    slot = __shfl_sync(0xffffffffu, slot, 0);
+    const int pos = slot + __popc(m & ((1u << lane) - 1u));
+    if (hit && pos < cap) out[pos] = key;
+  }
+  __syncthreads();
+  return min(*count, cap);
+}
+
 // One warp: sort up to 64 block ids ascending (entries >= n are padding).
 __device__ inline void warp_sort64_blocks_asc(const uint64_t* top, int n, int* out) {
   const int lane = threadIdx.x & 31;
