@@ -8,11 +8,14 @@
 //      streams the summary rows (2-D TMA, 128 rows per 32 KB stage, a 3-stage
 //      ring) and eight warps dot them with the group's index query on the
 //      tensor cores (mma.sync, the query split into two bf16 parts).
-//   2. The CTA keeps its best k keys (a radix select finds its k-th largest
-//      key, the keys at or above it are gathered); after one cluster barrier
-//      every CTA gathers the C lists through distributed shared memory and
-//      selects from their union the same way, so each holds the unit's top-k
-//      and takes its slice of the index list (the leader writes it out).
+//   2. Selection in two cluster exchanges, exact by construction: each warp
+//      offers the running maxima of its keys as samples; the k-th largest
+//      sample score L bounds the unit's k-th score from below, so each CTA
+//      keeps only its keys scoring >= L; every CTA then gathers that small
+//      union through distributed shared memory and ranks it, so each holds
+//      the unit's top-k and takes its slice of the list (the leader writes
+//      the list out, sorted, while the attention runs). A union too large
+//      for this (e.g. every score equal) takes an exact radix-select path.
 //   3. CTA r attends over its slice: the producer streams each 64x128 K and V
 //      block with 2-D TMA copies (128-byte swizzle) into the 3-stage ring;
 //      warps 0-3 consume every block in order (each warp 16 tokens: S = K Q^T
@@ -80,12 +83,12 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   __shared__ uint64_t xlist2[64];    // exact path: this CTA's best kk keys
   __shared__ uint32_t xsamp[64];     // this CTA's sample scores (read by the cluster)
   __shared__ uint64_t xsurv[64];     // this CTA's keys scoring >= L (read by the cluster)
-  __shared__ int xnsurv;             // how many (may exceed 64: then only 64 are stored)
   __shared__ uint32_t lbound;
   __shared__ int ccount[kStMaxCluster];
   __shared__ uint64_t sel_keys[64];  // the unit's selected keys
   __shared__ RadixScratch radix;
-  __shared__ int n_sel;
+  __shared__ int n_sel;   // this CTA's survivor count (may exceed 64: then only 64 are stored)
+  __shared__ int n_sel2;  // counter of the exact path
   __shared__ int32_t blocks[kStMaxList];
   __shared__ int n_blocks;
   __shared__ float qsum[kHeadDim];  // the group's index query (sum of its query heads), fp32
@@ -281,16 +284,18 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     // L = the kk-th largest sample score: the value with fewer than kk samples
     // above it and at least kk at or above it (equal values write the same L).
     // q adjacent threads count for each sample and add their counts.
-    const int ns = C * n_samp;  // <= 128
+    const int ns = C * n_samp;  // <= 128, a multiple of 8
     const int q = ns <= 72 ? 4 : 2;
     const int i = tid / q, part = tid - i * q;
     const uint32_t v = i < ns ? samp_all[i] : 0u;
     int gt = 0, ge = 0;
     if (i < ns) {
-      for (int j = part; j < ns; j += q) {
-        const uint32_t u = samp_all[j];
-        gt += u > v ? 1 : 0;
-        ge += u >= v ? 1 : 0;
+      const uint4* s4 = reinterpret_cast<const uint4*>(samp_all);
+#pragma unroll 4
+      for (int j = part; j < ns / 4; j += q) {
+        const uint4 u = s4[j];
+        gt += (u.x > v) + (u.y > v) + (u.z > v) + (u.w > v);
+        ge += (u.x >= v) + (u.y >= v) + (u.z >= v) + (u.w >= v);
       }
     }
     for (int o = 1; o < q; o <<= 1) {
@@ -314,33 +319,12 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
       if (hit && pos < 64) xsurv[pos] = key;
     }
   }
-  __syncthreads();
-  if (tid == 0) xnsurv = n_sel;
+  // n_sel now holds this CTA's survivor count (read by the cluster; the exact
+  // path counts with n_sel2, so it is never written again)
   __syncthreads();
   if (C > 1) cluster_arrive();
-  if (warp == kStWarps) {
-    // pull the K/V of this CTA's best survivors (about its share of the list,
-    // plus one) into L2; prefetching every survivor would waste bandwidth
-    const int ns = min(xnsurv, 64);
-    const int n_pf = min(ns, (kk + C - 1) / C + 1);
-    for (int j2 = lane; j2 < ns; j2 += 32) {
-      const uint64_t x = xsurv[j2];
-      int rk = 0;
-      for (int j3 = 0; j3 < ns; ++j3) rk += xsurv[j3] > x ? 1 : 0;
-      if (rk >= n_pf) continue;
-      const int64_t row = kv.block_row(s, h, sel_block(x), a.status, kIdDecode);
-      if (row >= 0) {
-        const int32_t y = static_cast<int32_t>(row);
-        tma_prefetch_2d(&tmk, 0, y);
-        tma_prefetch_2d(&tmk, 64, y);
-        tma_prefetch_2d(&tmv, 0, y);
-        tma_prefetch_2d(&tmv, 64, y);
-      }
-    }
-    __syncwarp();
-  }
   if (C > 1) cluster_wait();
-  if (tid < C) ccount[tid] = C > 1 ? ld_dsmem_i32(dsmem_addr(smem_u32(&xnsurv), static_cast<uint32_t>(tid))) : xnsurv;
+  if (tid < C) ccount[tid] = C > 1 ? ld_dsmem_i32(dsmem_addr(smem_u32(&n_sel), static_cast<uint32_t>(tid))) : n_sel;
   if (tid < 64) sel_keys[tid] = 0ull;
   __syncthreads();
   int n_union = 0, overflow = 0;
@@ -355,14 +339,21 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
       while (off >= ccount[r]) off -= ccount[r++];
       lists[i] = C > 1 ? ld_dsmem_u64(dsmem_addr(smem_u32(xsurv + off), static_cast<uint32_t>(r))) : xsurv[off];
     }
+    if (tid == 0) lists[n_union] = 0ull;
     __syncthreads();
     // rank counting, q adjacent threads per key: the best kk go to sel_keys in rank order
     const int q = n_union <= 72 ? 4 : (n_union <= 144 ? 2 : 1);
     const int i = tid / q, part = tid - i * q;
     const uint64_t x = i < n_union ? lists[i] : 0ull;
     int cnt = 0;
-    if (i < n_union)
-      for (int j = part; j < n_union; j += q) cnt += lists[j] > x ? 1 : 0;
+    if (i < n_union) {
+      const ulonglong2* l2 = reinterpret_cast<const ulonglong2*>(lists);  // lists[n_union] is 0 (padding)
+#pragma unroll 4
+      for (int j = part; j < (n_union + 1) / 2; j += q) {
+        const ulonglong2 y = l2[j];
+        cnt += (y.x > x) + (y.y > x);
+      }
+    }
     for (int o = 1; o < q; o <<= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
     if (i < n_union && part == 0 && cnt < kk) sel_keys[cnt] = x;
   } else if (!exact) {
@@ -370,7 +361,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     // and a radix select over their union
     if (tid < 64) xlist2[tid] = 0ull;
     const uint64_t t_local = block_kth_largest(keys, rows, kk, radix);
-    block_compact_ge(keys, rows, t_local, xlist2, 64, &n_sel);
+    block_compact_ge(keys, rows, t_local, xlist2, 64, &n_sel2);
     if (C > 1) cluster_sync();
     for (int i = tid; i < C * 64; i += blockDim.x)
       lists[i] = C > 1 ? ld_dsmem_u64(dsmem_addr(smem_u32(xlist2 + (i & 63)), static_cast<uint32_t>(i >> 6)))
@@ -378,7 +369,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     __syncthreads();
     const uint64_t t_unit = block_kth_largest(lists, C * 64, kk, radix);
     uint64_t* picked = lists + 1024;  // past the C * 64 gathered keys
-    block_compact_ge(lists, C * 64, t_unit, picked, 64, &n_sel);
+    block_compact_ge(lists, C * 64, t_unit, picked, 64, &n_sel2);
     // rank order (the compaction's order differs between CTAs)
     if (tid < kk) {
       const uint64_t x = picked[tid];

@@ -403,46 +403,6 @@ __device__ inline bool block_select(const uint64_t* keys, int n, int k, uint64_t
   return true;
 }
 
-__device__ inline uint64_t shfl_idx_u64(uint64_t v, int src) {
-  const uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(v), src);
-  const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(v >> 32), src);
-  return (static_cast<uint64_t>(hi) << 32) | lo;
-}
-__device__ inline uint64_t shfl_up_u64(uint64_t v, int d) {
-  const uint32_t lo = __shfl_up_sync(0xffffffffu, static_cast<uint32_t>(v), d);
-  const uint32_t hi = __shfl_up_sync(0xffffffffu, static_cast<uint32_t>(v >> 32), d);
-  return (static_cast<uint64_t>(hi) << 32) | lo;
-}
-
-// A warp's running top-32: lane i holds the i-th largest key seen so far
-// (descending over the lanes, 0 where the list is not full). Inserts the keys
-// a and b of every lane (0 = none): a key enters only if it beats the current
-// last entry; each one is placed by a ballot (how many entries are larger)
-// and a shift of the entries below it. Costs one short round per key that
-// enters, so once the list holds high keys most new keys are dropped by the
-// first compare. Every lane of the warp calls this.
-__device__ inline void warp_list32_insert2(uint64_t& list, uint64_t a, uint64_t b) {
-  const int lane = threadIdx.x & 31;
-  const uint64_t last = shfl_idx_u64(list, 31);
-  unsigned ma = __ballot_sync(0xffffffffu, a > last);
-  unsigned mb = __ballot_sync(0xffffffffu, b > last);
-  while ((ma | mb) != 0u) {
-    uint64_t x;
-    if (ma != 0u) {
-      const int src = __ffs(ma) - 1;
-      ma &= ma - 1u;
-      x = shfl_idx_u64(a, src);
-    } else {
-      const int src = __ffs(mb) - 1;
-      mb &= mb - 1u;
-      x = shfl_idx_u64(b, src);
-    }
-    const int pos = __popc(__ballot_sync(0xffffffffu, list > x));  // entries larger than x
-    const uint64_t up = shfl_up_u64(list, 1);
-    if (pos < 32) list = lane < pos ? list : (lane == pos ? x : up);
-  }
-}
-
 // Shared scratch of block_kth_largest.
 struct RadixScratch {
   uint32_t hist[256];
