@@ -417,3 +417,60 @@ int ora_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Chunked-prefill tiles (guide §1, Step 1 and Step 2; §3: during prefill the
+ * index branch still scans the whole input): for n_units (tile, KV head)
+ * units of one sequence, unit u = tile tiles[u] of KV head heads[u], whose
+ * queries are chunk rows row_lo[u] .. row_hi[u] - 1 at absolute positions
+ * q_start + row: the index query is the sum of those rows' G heads; the
+ * candidates are the blocks before the tile's diagonal block
+ * q_start / 64 + tiles[u] (always kept); selection as ora_select_blocks; each
+ * row then attends, causally, over the tokens <= its position of the listed
+ * blocks. q: [n_rows][Hq][128]; k, v: [Hkv][T][128] (row stride 128);
+ * pooled: [Hkv][max_blocks][128] stored summaries. Outputs: sel
+ * [n_units][k_total]; o [n_rows][Hq][128] and lse [n_rows][Hq] for the rows
+ * and heads of the listed units (others untouched). */
+int ora_prefill_tile_units(int64_t n_units, const int64_t* tiles, const int64_t* heads, const int64_t* row_lo,
+                           const int64_t* row_hi, int64_t q_start, const void* q, int qtype, int Hq, int G,
+                           const double* pooled, int64_t max_blocks, const void* k, const void* v, int kvtype,
+                           int64_t T, int64_t k_scored, int64_t k_total, double scale, int64_t* sel, double* o,
+                           double* lse) {
+  int bad = 0;
+  int esz_q = qtype == ORA_F64 ? 8 : qtype == ORA_F32 ? 4 : 2;
+  int esz_kv = kvtype == ORA_F64 ? 8 : kvtype == ORA_F32 ? 4 : 2;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int64_t u = 0; u < n_units; ++u) {
+    int64_t h = heads[u], diag = q_start / ORA_BLOCK + tiles[u];
+    if (diag > max_blocks) {
+      bad |= 1;
+      continue;
+    }
+    double qi[ORA_D];
+    for (int d = 0; d < ORA_D; ++d) {
+      double acc = 0.0;
+      for (int64_t r = row_lo[u]; r < row_hi[u]; ++r)
+        for (int g = 0; g < G; ++g) acc += ld(q, qtype, (r * Hq + h * G + g) * ORA_D + d);
+      qi[d] = acc;
+    }
+    double* sc = (double*)malloc((size_t)(diag > 0 ? diag : 1) * sizeof(double));
+    ora_score_blocks(qi, pooled + h * max_blocks * ORA_D, diag, sc);
+    int64_t* s = sel + u * k_total;
+    if (ora_select_blocks(sc, diag, k_scored, diag, 0, 0, k_total, s) < 0) bad |= 1;
+    free(sc);
+    const char* kb = (const char*)k + h * T * ORA_D * esz_kv;
+    const char* vb = (const char*)v + h * T * ORA_D * esz_kv;
+    int64_t* toks = (int64_t*)malloc((size_t)(k_total * ORA_BLOCK + 1) * sizeof(int64_t));
+    for (int64_t r = row_lo[u]; r < row_hi[u]; ++r) {
+      int64_t pos = q_start + r, nt = 0;
+      for (int64_t i = 0; i < k_total; ++i) {
+        if (s[i] < 0) continue;
+        for (int64_t t = s[i] * ORA_BLOCK; t < s[i] * ORA_BLOCK + ORA_BLOCK && t <= pos && t < T; ++t) toks[nt++] = t;
+      }
+      const char* qr = (const char*)q + (r * Hq + h * G) * ORA_D * esz_q;
+      ora_attend(qr, qtype, G, kb, vb, kvtype, ORA_D, toks, nt, scale, o + (r * Hq + h * G) * ORA_D, lse + r * Hq + h * G,
+                 NULL);
+    }
+    free(toks);
+  }
+  return bad ? -1 : 0;
+}

@@ -70,6 +70,8 @@ def _load():
             "ora_dense_gqa": (None, [P, I, I64, P, P, I, I64, I64, D, P, P]),
             "ora_decode_select_units": (I, [I64, P, I, I, P, I, I64, I64, P, I, I64, I, I64, I64, P, P, P, P]),
             "ora_decode_step_units": (I, [I64, P, I, I, P, I64, P, P, I, I64, I64, P, I64, I, I64, D, P, P, P]),
+            "ora_prefill_tile_units": (I, [I64, P, P, P, P, I64, P, I, I, I, P, I64, P, P, I, I64, I64, I64, D, P, P,
+                                            P]),
             "ora_num_threads": (I, []),
         }
         for name, (res, args) in sigs.items():
@@ -504,4 +506,32 @@ def decode_step_units(q, pooled, k, v, lens, k_scored, k_total, scale, force_loc
                                        int(k_total), float(scale), _ptr(sel), _ptr(o), _ptr(lse))
     if rc != 0:
         raise ValueError("bad arguments to decode_step_units")
+    return sel, o, lse
+
+
+def prefill_tile_units(units, q_start, q, pooled, k, v, k_scored, k_total, scale):
+    """Select and attend for chunked-prefill units of one sequence, in C with
+    OpenMP across units. ``units``: [(tile, head)]; tiles follow
+    :func:`prefill_tiles`. ``q`` [n_rows, Hq, D]; ``pooled`` [Hkv, max_blocks, D]
+    (float64 stored summaries); ``k``, ``v`` [Hkv, T, D]. Returns (selected
+    [U, k_total], o [n_rows, Hq, D], lse [n_rows, Hq]) (rows and heads of
+    units not listed are NaN)."""
+    qs, ks, vs = _Src(q), _Src(k), _Src(v)
+    n_rows, hq = qs.shape[0], qs.shape[1]
+    hkv, t = ks.shape[0], ks.shape[1]
+    g = hq // hkv
+    part = {j: (lo, hi) for j, lo, hi in prefill_tiles(q_start, n_rows)}
+    tiles = np.ascontiguousarray([u[0] for u in units], dtype=np.int64)
+    heads = np.ascontiguousarray([u[1] for u in units], dtype=np.int64)
+    lo = np.ascontiguousarray([part[u[0]][0] for u in units], dtype=np.int64)
+    hi = np.ascontiguousarray([part[u[0]][1] for u in units], dtype=np.int64)
+    pl = _f64(pooled)
+    sel = np.empty((len(units), int(k_total)), dtype=np.int64)
+    o = np.full((n_rows, hq, HEAD_DIM), np.nan)
+    lse = np.full((n_rows, hq), np.nan)
+    rc = _load().ora_prefill_tile_units(len(units), _ptr(tiles), _ptr(heads), _ptr(lo), _ptr(hi), int(q_start),
+                                        qs.ptr, qs.type, hq, g, _ptr(pl), pl.shape[1], ks.ptr, vs.ptr, ks.type, t,
+                                        int(k_scored), int(k_total), float(scale), _ptr(sel), _ptr(o), _ptr(lse))
+    if rc != 0:
+        raise ValueError("bad arguments to prefill_tile_units")
     return sel, o, lse

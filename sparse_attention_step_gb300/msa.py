@@ -200,9 +200,29 @@ def _host_batch(q_starts, q_counts):
     return n, (ctypes.c_int64 * n)(*[int(x) for x in q_starts]), (ctypes.c_int32 * n)(*[int(x) for x in q_counts])
 
 
-def varlen_tiles(q_counts) -> int:
-    """Global 64-token tiles of a chunk batch (rows of the varlen index lists)."""
-    return sum((int(c) + 63) // 64 for c in q_counts)
+def chunk_tiles(q_start: int, n: int) -> int:
+    """Query tiles of a chunk of n new tokens at absolute positions q_start ..
+    q_start + n - 1: its queries grouped by the 64-token block they sit in
+    (rows of the chunk's index lists)."""
+    q_start, n = int(q_start), int(n)
+    if n <= 0:
+        return 0
+    return (q_start + n - 1) // 64 - q_start // 64 + 1
+
+
+def chunk_tile_rows(q_start: int, n: int) -> list:
+    """[(tile, first chunk row, end chunk row)] of a chunk's query tiles."""
+    q_start, n = int(q_start), int(n)
+    b0 = q_start // 64
+    return [(j, max(0, (b0 + j) * 64 - q_start), min(n, (b0 + j + 1) * 64 - q_start))
+            for j in range(chunk_tiles(q_start, n))]
+
+
+def varlen_tiles(q_counts, q_starts=None) -> int:
+    """Global query tiles of a chunk batch (rows of the varlen index lists)."""
+    if q_starts is None:
+        q_starts = [0] * len(q_counts)
+    return sum(chunk_tiles(a, c) for a, c in zip(q_starts, q_counts))
 
 
 def msa_select_topk_blocks_varlen(q, num_q_heads: int, q_starts, q_counts, pooled, desc: KvDesc, cfg: SelectCfg,

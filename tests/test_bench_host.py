@@ -40,6 +40,30 @@ def test_quantiles():
     assert bench.quantiles_us([]) is None
 
 
+def test_chunk_tiles_group_queries_by_block():
+    assert msa.chunk_tiles(0, 0) == 0 and msa.chunk_tiles(128, 1) == 1 and msa.chunk_tiles(128, 64) == 1
+    assert msa.chunk_tiles(128, 65) == 2 and msa.chunk_tiles(100, 28) == 1 and msa.chunk_tiles(100, 29) == 2
+    assert msa.chunk_tile_rows(100, 100) == [(0, 0, 28), (1, 28, 92), (2, 92, 100)]
+    assert msa.chunk_tile_rows(64, 130) == [(0, 0, 64), (1, 64, 128), (2, 128, 130)]
+    assert msa.varlen_tiles([5, 70], [100, 60]) == 2 + 2
+
+
+def test_prefill_flop_of_the_benchmark_chunk():
+    # 8192 queries on a 131072-token prefix, 64 query heads, top-32 + diagonal:
+    # 558.5 GFLOP sparse, 36.28 TFLOP dense (4 * 128 per visible pair)
+    sparse, dense = bench.prefill_flop(131072, 8192, 32, 8, 8)
+    assert sparse == 4 * 128 * 64 * (8192 * 32 * 64 + 128 * (64 * 65 // 2))
+    assert round(sparse / 1e9, 1) == 558.5 and round(dense / 1e12, 2) == 36.28
+
+
+def test_replicas_keep_inputs_out_of_l2():
+    # the other replicas' steps between two uses of one move > 3 x 129 MB
+    for step_bytes in (50_362_368, 100_909_056, 642_000_000):
+        r = bench.replicas_needed(step_bytes)
+        assert (r - 1) * step_bytes > 3 * bench.L2_BYTES and r >= 2
+    assert bench.replicas_needed(100_909_056) == 6 and bench.replicas_needed(50_362_368) == 10
+
+
 def test_chunk_batch_helpers():
     assert msa.varlen_tiles([0, 1, 64, 65, 128]) == 0 + 1 + 1 + 2 + 2
     n, starts, counts = msa._host_batch([0, 64, 128], [5, 0, 70])

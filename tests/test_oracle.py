@@ -659,3 +659,31 @@ def test_chunk_split_at_a_block_boundary_keeps_every_list():
     assert len(whole) == len(parts)
     for a, b in zip(whole, parts):
         assert list(a) == list(b)
+
+
+@pytest.mark.parametrize("q_start,n_new", [(128, 150), (100, 90)])
+def test_prefill_tile_units_matches_the_per_unit_steps(q_start, n_new):
+    rng = np.random.default_rng(q_start)
+    hkv, hq = 2, 6
+    total = q_start + n_new
+    k = rng.standard_normal((hkv, total, O.HEAD_DIM))
+    v = rng.standard_normal((hkv, total, O.HEAD_DIM))
+    q = rng.standard_normal((n_new, hq, O.HEAD_DIM))
+    mb = O.num_blocks(total)
+    pooled = np.full((hkv, mb, O.HEAD_DIM), np.nan)
+    for h in range(hkv):
+        p, _ = O.pool_block_keys(k[h], total, "f32")
+        pooled[h, :p.shape[0]] = p
+    tiles = O.prefill_tiles(q_start, n_new)
+    units = [(j, h) for j, _, _ in tiles for h in range(hkv)]
+    sel, o, lse = O.prefill_tile_units(units, q_start, q, pooled, k, v, 2, 3, 0.125)
+    part = {j: (lo, hi) for j, lo, hi in tiles}
+    for u, (j, h) in enumerate(units):
+        lo, hi = part[j]
+        grp = hq // hkv
+        ref = O.prefill_tile_select(q[lo:hi, h * grp:(h + 1) * grp], j, q_start, pooled[h], 2, 3)
+        assert list(sel[u]) == list(ref["selected"])
+        ro, rl = O.prefill_rows(q[lo:hi, h * grp:(h + 1) * grp], q_start + np.arange(lo, hi), k[h], v[h], total,
+                                ref["selected"], 0.125)
+        np.testing.assert_allclose(o[lo:hi, h * grp:(h + 1) * grp], ro, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[lo:hi, h * grp:(h + 1) * grp], rl, rtol=0, atol=1e-13)
