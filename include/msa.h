@@ -108,7 +108,7 @@ typedef struct msa_select_cfg {
                           replacements of the sliding window). Kept blocks are not scored. */
   int32_t q_tile;      /* 1: decode (one token per sequence); 64: prefill tiles */
   int32_t mode;        /* msa_score_mode */
-  int64_t q_start;     /* prefill: absolute position of the first query token, a multiple of 64 */
+  int64_t q_start;     /* prefill: absolute position of the first query token (any position) */
 } msa_select_cfg;
 
 /* Operation ids for msa_workspace_size. */
@@ -119,9 +119,11 @@ typedef enum msa_op {
   MSA_OP_PREFILL = 3,
   MSA_OP_DENSE_DECODE = 4,
   MSA_OP_DENSE_PREFILL = 5,
-  MSA_OP_SELECT_PREFILL = 6, /* msa_select_topk_blocks with q_tile 64, and
+  MSA_OP_SELECT_PREFILL = 6, /* msa_select_topk_blocks with q_tile 64 (n_q_tokens =
+                                the chunk's tokens), and
                                 msa_select_topk_blocks_varlen with n_q_tokens =
-                                64 * sum over s of ceil(q_counts[s] / 64) */
+                                64 * the batch's query tiles (see
+                                msa_select_topk_blocks_varlen) */
   MSA_OP_DECODE_STEP = 7     /* msa_sparse_decode_step */
 } msa_op;
 
@@ -155,10 +157,15 @@ msa_status msa_pool_block_keys(const msa_kv_desc* kv /* host */, int64_t first_b
  *   q_idx = sum of the group's G query heads (fp32); candidates are the
  *   complete blocks, minus the newest block nb-1 (nb = ceil(seq_len/64)) when
  *   force_local. Output idx_out [batch, Hkv, k_total].
- * Prefill (cfg->q_tile == 64, batch 1, contiguous or paged cache): q [n_q_tokens, Hq, 128]; unit =
- *   (tile j, KV head); q_idx = sum over the tile's tokens and the group's
- *   heads; candidates are the blocks before the diagonal block
- *   q_start/64 + j. Output idx_out [ceil(n_q_tokens/64), Hkv, k_total].
+ * Prefill (cfg->q_tile == 64, batch 1, contiguous or paged cache): q [n_q_tokens, Hq, 128] at
+ *   absolute positions cfg->q_start + r (any q_start). The chunk's query
+ *   tiles are its tokens grouped by the 64-token block they sit in: tile j
+ *   holds the tokens whose position is in block q_start/64 + j (its diagonal
+ *   block), so a chunk that starts inside a block has a shorter first tile;
+ *   there are n_tiles = (q_start + n_q_tokens - 1)/64 - q_start/64 + 1 tiles.
+ *   Unit = (tile j, KV head); q_idx = sum over the tile's tokens and the
+ *   group's heads; candidates are the blocks before the diagonal block.
+ *   Output idx_out [n_tiles, Hkv, k_total].
  * Scores are q_idx . pooled[b] in fp32 (unscaled). The top min(k_scored, n)
  * candidates by (score descending, block ascending) plus the forced block are
  * written sorted ascending, padded with -1;
@@ -184,12 +191,14 @@ msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_
 /* Step 1b/1c for a batch of chunks (guide §1, Step 1, applied to the prefill
  * chunk of every sequence of a batch at once): sequence s (n_seqs ==
  * kv->batch, at most 64) has q_counts[s] >= 0 new tokens at absolute positions
- * q_starts[s] + r (q_starts[s] a multiple of 64, q_starts[s] + q_counts[s]
- * within the sequence's capacity; both arrays on the host). q holds the
- * sequences' tokens back to back: [sum q_counts, Hq, 128], sequence s from row
- * q_off[s] = q_counts[0] + ... + q_counts[s-1]. Its tiles j = 0 ..
- * ceil(q_counts[s]/64) - 1 are numbered globally in the same order (tile_off[s]
- * + j), and idx_out [total tiles, Hkv, k_total] gets, for global tile
+ * q_starts[s] + r (q_starts[s] + q_counts[s] within the sequence's capacity;
+ * both arrays on the host). q holds the sequences' tokens back to back:
+ * [sum q_counts, Hq, 128], sequence s from row q_off[s] = q_counts[0] + ... +
+ * q_counts[s-1]. Its query tiles (tokens grouped by the 64-token block they sit
+ * in, as for msa_select_topk_blocks: n_s = (q_starts[s] + q_counts[s] - 1)/64 -
+ * q_starts[s]/64 + 1 tiles, none for an empty chunk) are numbered globally in
+ * the same order (tile_off[s] + j), and idx_out [total tiles, Hkv, k_total]
+ * gets, for global tile
  * tile_off[s] + j, exactly what msa_select_topk_blocks (q_tile 64, q_start =
  * q_starts[s]) gives for tile j of sequence s alone, scored against sequence
  * s's summaries (pooled [batch, Hkv, max_blocks, 128] contiguous, or the
@@ -217,9 +226,10 @@ msa_status msa_sparse_attn_decode(const void* q, int32_t num_q_heads, const msa_
 
 /* Step 2, chunked prefill (guide §1, Step 2, and §3: during prefill the
  * savings fall on the main attention). Batch 1, bf16, contiguous or paged
- * cache (q_start + n_q_tokens within its capacity); query token r sits at
- * absolute position p = q_start + r and attends to the tokens t <= p of the
- * blocks idx[r / 64, h, :] (idx from msa_select_topk_blocks with q_tile 64).
+ * cache (q_start + n_q_tokens within its capacity, any q_start); query token r
+ * sits at absolute position p = q_start + r and attends to the tokens t <= p
+ * of the blocks idx[p / 64 - q_start / 64, h, :] (its tile's list, idx from
+ * msa_select_topk_blocks with q_tile 64).
  * At most 512 entries of a list may be valid blocks (-1 padding is free); a
  * longer list is cut there and the device status records MSA_ERR_UNSUPPORTED.
  * out [n_q_tokens, Hq, 128] KV dtype; lse (nullable) [n_q_tokens, Hq] fp32. */

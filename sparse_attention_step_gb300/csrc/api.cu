@@ -149,7 +149,9 @@ struct SelectLayout {
 };
 SelectLayout select_layout(const msa_kv_desc* kv, int n_q_tokens, int prefill) {
   SelectLayout L;
-  const int64_t units = prefill ? static_cast<int64_t>((n_q_tokens + kBlock - 1) / kBlock) * kv->num_kv_heads
+  // prefill: one tile more than n_q_tokens / 64 covers a chunk of n_q_tokens
+  // tokens that starts inside a block
+  const int64_t units = prefill ? static_cast<int64_t>((n_q_tokens + kBlock - 1) / kBlock + 1) * kv->num_kv_heads
                                 : static_cast<int64_t>(kv->batch) * kv->num_kv_heads;
   L.scores = kWsRegion;
   size_t off = kWsRegion + align_up(static_cast<size_t>(units) * kv_max_blocks(kv) * sizeof(float), 256);
@@ -246,8 +248,8 @@ msa_status decode_common(const void* q, int hq, const msa_kv_desc* kv, const int
 }
 
 // Host checks of a chunk batch against the cache: sequence s's new tokens
-// [q_starts[s], q_starts[s] + q_counts[s]) start on a block boundary and fit
-// in its capacity. Fills *pb; *n_tokens gets the rows of q and out.
+// [q_starts[s], q_starts[s] + q_counts[s]) fit in its capacity. Fills *pb;
+// *n_tokens gets the rows of q and out.
 msa_status build_batch(const msa_kv_desc* kv, int n_seqs, const int64_t* q_starts, const int32_t* q_counts,
                        PrefillBatch* pb, int64_t* n_tokens) {
   if (n_seqs != kv->batch || q_starts == nullptr || q_counts == nullptr) return MSA_ERR_INVALID_ARG;
@@ -256,10 +258,9 @@ msa_status build_batch(const msa_kv_desc* kv, int n_seqs, const int64_t* q_start
   const int64_t cap = kv_max_blocks(kv) * kBlock;
   for (int s = 0; s < n_seqs; ++s) {
     if (q_counts[s] < 0 || q_starts[s] < 0) return MSA_ERR_INVALID_ARG;
-    if (q_starts[s] % kBlock != 0) return MSA_ERR_UNSUPPORTED;
     if (q_starts[s] + q_counts[s] > cap) return MSA_ERR_INVALID_ARG;
     total += q_counts[s];
-    tiles += (q_counts[s] + kBlock - 1) / kBlock;
+    tiles += chunk_tiles(q_starts[s], q_counts[s]);
   }
   if (total >= (int64_t(1) << 31) || tiles > 65535) return MSA_ERR_UNSUPPORTED;
   if (!make_prefill_batch(n_seqs, q_starts, q_counts, pb)) return MSA_ERR_INVALID_ARG;

@@ -7,10 +7,13 @@
 namespace msa {
 
 // Sequences of a (batched) chunked prefill: sequence s has q_cnt[s] new
-// tokens at absolute positions q_start[s] + r (q_start[s] a multiple of 64),
-// stored in rows q_off[s] + r of q and out; its 64-token tiles are global
-// tiles tile_off[s] .. tile_off[s + 1] - 1, and the prefill scorer takes them
-// in groups of 8 (global groups grp_off[s] .. grp_off[s + 1] - 1).
+// tokens at absolute positions q_start[s] + r, stored in rows q_off[s] + r of
+// q and out. Its query tiles are its tokens grouped by the 64-token block they
+// sit in: tile j holds the chunk rows r with (q_start[s] + r) / 64 ==
+// q_start[s] / 64 + j (its diagonal block), so a chunk that starts inside a
+// block has a shorter first tile. They are global tiles tile_off[s] ..
+// tile_off[s + 1] - 1, and the prefill scorer takes them in groups of 8
+// (global groups grp_off[s] .. grp_off[s + 1] - 1).
 constexpr int kMaxPrefillSeqs = 64;
 struct PrefillBatch {
   int n_seqs;
@@ -30,7 +33,18 @@ struct PrefillBatch {
     return s;
   }
   __host__ __device__ int total_tiles() const { return tile_off[n_seqs]; }
+  // Chunk row (within sequence s) of the first position of global tile
+  // `tile`'s block: row tile_row0 + i sits at position 64 * diag + i. Negative
+  // for the first tile of a chunk that starts inside a block; the tile's rows
+  // are [max(0, tile_row0), min(q_cnt[s], tile_row0 + 64)).
+  __host__ __device__ int tile_row0(int s, int tile) const {
+    return (tile - tile_off[s]) * 64 - static_cast<int>(q_start[s] % 64);
+  }
 };
+// Query tiles of a chunk of n tokens from absolute position q_start.
+__host__ __device__ inline int32_t chunk_tiles(int64_t q_start, int32_t n) {
+  return n <= 0 ? 0 : static_cast<int32_t>((q_start + n - 1) / 64 - q_start / 64 + 1);
+}
 // Fills b from host arrays; false when n_seqs is out of [1, kMaxPrefillSeqs]
 // or a count is negative.
 bool make_prefill_batch(int n_seqs, const int64_t* q_starts, const int32_t* q_counts, PrefillBatch* b);

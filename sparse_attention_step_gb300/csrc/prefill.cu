@@ -109,8 +109,8 @@ __global__ void __launch_bounds__(kPfThreads) prefill_bf16_kernel(const __grid_c
   for (int hr = 0; hr < 2; ++hr) {
     const int r = rg * kPfRows + 16 * warp + g + 8 * hr;
     const int t = r / a.grp, gh = r % a.grp;
-    const int64_t tq = static_cast<int64_t>(jt) * kBlock + t;  // query index within its sequence's chunk
-    live[hr] = (t < kBlock) && (tq < a.batch.q_cnt[seq]);
+    const int64_t tq = a.batch.tile_row0(seq, tile) + t;  // query index within its sequence's chunk
+    live[hr] = (t < kBlock) && tq >= 0 && (tq < a.batch.q_cnt[seq]);
     pos[hr] = q_start + tq;
     qrow[hr] = live[hr] ? (a.batch.q_off[seq] + tq) * a.hq + h * a.grp + gh : 0;
   }
@@ -157,8 +157,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_bf16_kernel(const __grid_c
     }
     // mask and scale
     const int64_t key0 = static_cast<int64_t>(b) * kBlock;
-    const bool need_mask = (key0 + kBlock - 1 > q_start + static_cast<int64_t>(jt) * kBlock) ||
-                           (key0 + kBlock > len);
+    const bool need_mask = (key0 + kBlock - 1 > diag * kBlock) || (key0 + kBlock > len);
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {

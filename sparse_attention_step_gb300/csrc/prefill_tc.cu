@@ -172,7 +172,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
       mbar_arrive_expect_tx(&st.q_full, kQBytes);
-      const int32_t tok0 = a.batch.q_off[seq] + jt * kBlock + rh * (kTcTiles * 16);
+      // first token of the row half (may be before the chunk, then the load
+      // reads the fill value or another sequence's rows, never used)
+      const int32_t tok0 = a.batch.q_off[seq] + a.batch.tile_row0(seq, tile) + rh * (kTcTiles * 16);
       for (int t = 0; t < kTcTiles; ++t)
         for (int half = 0; half < 2; ++half)
           tma_load_3d(qs + t * 32768 + half * 16384, &tmq, 64 * half, h * 8, tok0 + 16 * t, &st.q_full);
@@ -266,8 +268,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     const int bar_id = 1 + t;               // the tile's 8 softmax warps
     const int tt = rh * (kTcTiles * 16) + 16 * t + (r >> 3);  // token within the 64-token tile
     const int head = h * 8 + (r & 7);
-    const int64_t tl = static_cast<int64_t>(jt) * kBlock + tt;  // token within its sequence's chunk
-    const bool live = tl < a.batch.q_cnt[seq];
+    const int64_t tl = a.batch.tile_row0(seq, tile) + tt;  // token within its sequence's chunk
+    const bool live = tl >= 0 && tl < a.batch.q_cnt[seq];
     const int64_t tq = a.batch.q_off[seq] + tl;                 // its row in q and out
     float m = -INFINITY, l = 0.f;  // running max (log2 units) and this half's running sum
     bool ok = true;

@@ -41,9 +41,9 @@ __global__ void __launch_bounds__(256) qidx_prefill_kernel(const T* __restrict__
   const int e = threadIdx.x & 15, slot = threadIdx.x >> 4;
   const int grp = hq / hkv;
   const int s = pb.seq_of_tile(tile);
-  const int j0 = (tile - pb.tile_off[s]) * kBlock;  // first token of the tile within its sequence
-  const int r0 = pb.q_off[s] + j0;                  // its row in q
-  const int n_rows = (min(pb.q_cnt[s], j0 + kBlock) - j0) * grp;  // token-major, head-minor
+  const int j0 = max(pb.tile_row0(s, tile), 0);                                       // the tile's first token
+  const int r0 = pb.q_off[s] + j0;                                                    // its row in q
+  const int n_rows = (min(pb.q_cnt[s], pb.tile_row0(s, tile) + kBlock) - j0) * grp;  // token-major, head-minor
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
@@ -87,9 +87,9 @@ __global__ void __launch_bounds__(kQidxThreads) qidx_prefill_bf16_kernel(const _
   const int tile = blockIdx.y;  // global tile
   const int grp = hq / hkv;
   const int s = pb.seq_of_tile(tile);
-  const int j0 = (tile - pb.tile_off[s]) * kBlock;
+  const int j0 = max(pb.tile_row0(s, tile), 0);  // the tile's first token within its sequence's chunk
   const int r0 = pb.q_off[s] + j0;
-  const int n_rows = (min(pb.q_cnt[s], j0 + kBlock) - j0) * grp;  // token-major, head-minor
+  const int n_rows = (min(pb.q_cnt[s], pb.tile_row0(s, tile) + kBlock) - j0) * grp;  // token-major, head-minor
   const int tid = threadIdx.x;
   for (int i = tid; i < n_rows * 16; i += kQidxThreads) {
     const int row = i >> 4, pc = i & 15;
@@ -1100,7 +1100,7 @@ bool make_prefill_batch(int n_seqs, const int64_t* q_starts, const int32_t* q_co
     b->q_cnt[s] = q_counts[s];
     b->tile_off[s] = tiles;
     b->grp_off[s] = groups;
-    const int32_t t = (q_counts[s] + kBlock - 1) / kBlock;
+    const int32_t t = chunk_tiles(q_starts[s], q_counts[s]);
     off += q_counts[s];
     tiles += t;
     groups += (t + kPsTiles - 1) / kPsTiles;

@@ -283,7 +283,12 @@ class PrefillBatchInputs:
 
     @property
     def tile_off(self) -> list:
-        return [sum(-(-c // BLOCK) for c in self.q_counts[:s]) for s in range(len(self.q_counts) + 1)]
+        """Global index of each sequence's first query tile (tiles group a
+        chunk's tokens by the 64-token block they sit in)."""
+        def tiles(a, c):
+            return 0 if c <= 0 else (a + c - 1) // BLOCK - a // BLOCK + 1
+        return [sum(tiles(a, c) for a, c in zip(self.q_starts[:s], self.q_counts[:s]))
+                for s in range(len(self.q_counts) + 1)]
 
     def q_rows(self, s: int) -> torch.Tensor:
         o = self.q_off[s]
@@ -292,11 +297,10 @@ class PrefillBatchInputs:
 
 def make_prefill_batch_inputs(q_starts, q_counts, num_kv_heads: int, num_q_heads: int, dtype: str = "bf16",
                               layout: str = "contiguous", seed: int = 0, device="cpu") -> PrefillBatchInputs:
-    """Chunks of ``q_counts[s]`` new tokens after ``q_starts[s]``-token prefixes
-    (multiples of 64), one per sequence of a shared cache."""
+    """Chunks of ``q_counts[s]`` new tokens after ``q_starts[s]``-token prefixes,
+    one per sequence of a shared cache."""
     q_starts = [int(x) for x in q_starts]
     q_counts = [int(x) for x in q_counts]
-    assert all(x % BLOCK == 0 for x in q_starts)
     lens = [a + c for a, c in zip(q_starts, q_counts)]
     cache = make_decode_inputs([max(n, 1) for n in lens], num_kv_heads, num_q_heads, dtype, layout, seed=seed,
                                device=device)

@@ -86,10 +86,12 @@ def test_head_and_selection_arguments(lib):
     bad = msa.select_cfg(4, q_tile=3)
     assert lib.msa_select_topk_blocks(0x1, 16, 1, 0x1, ctypes.byref(d), ctypes.byref(bad), 0x1, 5, None, 0x1, 1 << 20,
                                       None) == msa.MSA_ERR_UNSUPPORTED
-    unaligned = msa.select_cfg(4, q_tile=64, q_start=100)
+    # a chunk may start anywhere, but must fit in the cache (1024 tokens) and not start before it
     d1 = _desc(batch=1)
-    assert lib.msa_select_topk_blocks(0x1, 16, 64, 0x1, ctypes.byref(d1), ctypes.byref(unaligned), 0x1, 5, None, 0x1,
-                                      1 << 20, None) == msa.MSA_ERR_UNSUPPORTED
+    for q_start in (1000, -1):
+        cfg_p = msa.select_cfg(4, q_tile=64, q_start=q_start)
+        assert lib.msa_select_topk_blocks(0x1, 16, 64, 0x1, ctypes.byref(d1), ctypes.byref(cfg_p), 0x1, 5, None, 0x1,
+                                          1 << 20, None) == msa.MSA_ERR_INVALID_ARG
 
 
 def test_decode_and_prefill_arguments(lib):
@@ -102,8 +104,9 @@ def test_decode_and_prefill_arguments(lib):
     assert lib.msa_sparse_attn_prefill(0x1, 16, 64, 0, ctypes.byref(d), 0x1, 5, 0.1, 0x1, None, 0x1, 1 << 20,
                                        None) == msa.MSA_ERR_UNSUPPORTED
     d1 = _desc(batch=1)
-    assert lib.msa_dense_gqa_prefill(0x1, 16, 64, 32, ctypes.byref(d1), 0.1, 0x1, None, 0x1, 1 << 20,
-                                     None) == msa.MSA_ERR_UNSUPPORTED
+    # any start, but the chunk must fit in the cache's 1024 tokens
+    assert lib.msa_dense_gqa_prefill(0x1, 16, 64, 980, ctypes.byref(d1), 0.1, 0x1, None, 0x1, 1 << 20,
+                                     None) == msa.MSA_ERR_INVALID_ARG
     assert lib.msa_dense_gqa_prefill(0x1, 16, 2000, 0, ctypes.byref(d1), 0.1, 0x1, None, 0x1, 1 << 20,
                                      None) == msa.MSA_ERR_INVALID_ARG
 
@@ -115,7 +118,7 @@ def _batch(starts, counts):
 
 @pytest.mark.parametrize("starts,counts,expect", [
     ([64], [10], msa.MSA_ERR_INVALID_ARG),                 # one chunk for a cache of two sequences
-    ([64, 100], [10, 20], msa.MSA_ERR_UNSUPPORTED),        # a start inside a block
+    ([64, 1000], [10, 30], msa.MSA_ERR_INVALID_ARG),       # a start inside a block, past the capacity
     ([64, 128], [10, -1], msa.MSA_ERR_INVALID_ARG),        # a negative count
     ([-64, 128], [10, 1], msa.MSA_ERR_INVALID_ARG),        # a negative start
     ([64, 128], [10, 1000], msa.MSA_ERR_INVALID_ARG),      # past the sequence's capacity (1024 tokens)

@@ -18,12 +18,17 @@ def dev(lib):
     return torch.device("cuda:0")
 
 
+def msa_tiles(inp):
+    from sparse_attention_step_gb300 import msa
+    return msa.chunk_tiles(inp.q_start, inp.n_new)
+
+
 def run_prefill(inp, k_scored, k_total, dense=False, sparse=True):
     from sparse_attention_step_gb300 import msa
     dev = inp.q.device
     desc = msa.kv_desc(inp.k, inp.v, inp.seq_lens, inp.page_table)
     hq, n = inp.num_q_heads, inp.n_new
-    n_tiles = (n + 63) // 64
+    n_tiles = msa.chunk_tiles(inp.q_start, n)
     need = max(msa.msa_workspace_size(msa.MSA_OP_SELECT_PREFILL, desc, hq, n, k_total),
                msa.msa_workspace_size(msa.MSA_OP_PREFILL, desc, hq, n, k_total))
     ws = msa.Workspace(need, dev)
@@ -104,12 +109,71 @@ def verify_tile_selection_all(inp, res, k_scored, k_total, stats):
             check_selection(idx[j, h], sel["scores"], k_scored, sel["diag"], k_total, stats)
 
 
+@pytest.mark.parametrize("layout", ["contiguous", "paged"])
+@pytest.mark.parametrize("prefix,n_new,hq,hkv", [
+    (64 * 10 + 37, 64 * 3 + 5, 64, 8),   # tcgen05 kernel: a short first tile, a ragged last tile
+    (64 * 10 + 37, 64 * 3 + 5, 16, 2),   # mma.sync kernel, same chunk
+    (100, 28, 64, 8),                    # the chunk fills the rest of one block: one tile
+    (100, 29, 16, 4),                    # one token into the next block: two tiles
+    (63, 1, 64, 8),                      # one token completing block 0
+    (64 * 7 + 1, 64 * 2, 32, 4),         # starts one past a block boundary
+])
+def test_prefill_chunk_starting_inside_a_block(dev, layout, prefix, n_new, hq, hkv):
+    """Chunks whose first token is not on a block boundary: the tiles are the
+    chunk's queries grouped by block (a shorter first tile), each with its own
+    diagonal block; selection and attention against the oracle, dense too."""
+    inp = make_prefill_inputs(prefix, n_new, hkv, hq, "bf16", seed=prefix + n_new, device=dev, layout=layout)
+    k_scored = 4
+    res = run_prefill(inp, k_scored, k_scored + 1, dense=True)
+    assert res["status"] == 0
+    tiles = O.prefill_tiles(inp.q_start, inp.n_new)
+    assert res["idx"].shape[0] == len(tiles)
+    verify_tiles(inp, res, [j for j, _, _ in tiles], range(hkv), k_scored, k_scored + 1, check_dense=True)
+
+
+def test_prefill_unaligned_every_block_equals_dense(dev):
+    inp = make_prefill_inputs(64 * 6 + 21, 64 * 2 + 50, 8, 64, "bf16", seed=33, device=dev)
+    res = run_prefill(inp, 1000, 1001, dense=True)
+    assert res["status"] == 0
+    d = (res["out"].float() - res["dense_out"].float()).abs().max().item()
+    assert d <= 2e-2
+
+
+def test_prefill_split_at_a_block_boundary_matches_the_whole_chunk(dev):
+    """A chunk split at a block boundary into two calls gives the same index
+    lists as the whole chunk (a tile's list depends only on its own queries
+    and the blocks before it), and the same outputs within the bf16 tolerance."""
+    from sparse_attention_step_gb300 import msa
+    inp = make_prefill_inputs(64 * 9 + 40, 24 + 64 * 3 + 10, 8, 64, "bf16", seed=44, device=dev)
+    whole = run_prefill(inp, 5, 6)
+    cut = 24 + 64  # 64 * 9 + 40 + 88 = 64 * 11: a block boundary
+    desc = msa.kv_desc(inp.k, inp.v, inp.seq_lens, inp.page_table)
+    hq = inp.num_q_heads
+    ws = msa.Workspace(max(msa.msa_workspace_size(msa.MSA_OP_SELECT_PREFILL, desc, hq, inp.n_new, 6),
+                           msa.msa_workspace_size(msa.MSA_OP_PREFILL, desc, hq, inp.n_new, 6)), dev)
+    msa.msa_pool_block_keys(desc, 0, -1, whole["pooled"], ws.buf, ws.nbytes)
+    for lo, hi in ((0, cut), (cut, inp.n_new)):
+        q0 = inp.q_start + lo
+        q = inp.q[lo:hi].contiguous()
+        nt = msa.chunk_tiles(q0, hi - lo)
+        idx = torch.full((nt, inp.num_kv_heads, 6), -7, dtype=torch.int32, device=dev)
+        out = torch.empty_like(q)
+        msa.msa_select_topk_blocks(q, hq, hi - lo, whole["pooled"], desc, msa.select_cfg(5, True, 64, q0), idx, 6,
+                                   None, ws.buf, ws.nbytes)
+        msa.msa_sparse_attn_prefill(q, hq, hi - lo, q0, desc, idx, 6, SCALE, out, None, ws.buf, ws.nbytes)
+        torch.cuda.synchronize()
+        t0 = (q0 // 64) - (inp.q_start // 64)
+        assert torch.equal(idx, whole["idx"][t0:t0 + nt]), f"lists of rows {lo}..{hi}"
+        assert (out.float() - whole["out"][lo:hi].float()).abs().max().item() <= 2e-2
+    assert msa.msa_read_device_status(ws.buf) == 0
+
+
 @pytest.mark.parametrize("hq,hkv", [(16, 2), (8, 8), (16, 4)])
 def test_prefill_small(dev, hq, hkv):
     inp = make_prefill_inputs(64 * 10, 64 * 3 + 37, hkv, hq, "bf16", seed=hq + hkv, device=dev)
     res = run_prefill(inp, 4, 5, dense=True)
     assert res["status"] == 0
-    n_tiles = (inp.n_new + 63) // 64
+    n_tiles = msa_tiles(inp)
     verify_tiles(inp, res, range(n_tiles), range(hkv), 4, 5, check_dense=True)
 
 
@@ -119,7 +183,7 @@ def test_prefill_paged_cache(dev, hq, hkv):
     inp = make_prefill_inputs(64 * 37, 64 * 3 + 21, hkv, hq, "bf16", seed=71, device=dev, layout="paged")
     res = run_prefill(inp, 6, 7, dense=True)
     assert res["status"] == 0
-    n_tiles = (inp.n_new + 63) // 64
+    n_tiles = msa_tiles(inp)
     verify_tiles(inp, res, range(n_tiles), range(hkv), 6, 7, rows_per_tile=9, check_dense=True)
 
 
@@ -166,7 +230,7 @@ def test_full_chunked_prefill(dev):
     assert res["status"] == 0
     stats, pstats = SelectionStats(), PoolStats()
     verify_tile_selection_all(inp, res, w["k_scored"], w["k_total"], stats)
-    n_tiles = (inp.n_new + 63) // 64
+    n_tiles = msa_tiles(inp)
     for i in range(16):
         tile, head = (i * 37) % n_tiles, i % inp.num_kv_heads
         verify_tiles(inp, res, [tile], [head], w["k_scored"], w["k_total"], rows_per_tile=6,

@@ -32,7 +32,7 @@ def run_varlen(inp, k_scored, k_total):
     dev = inp.q.device
     desc = msa.kv_desc(c.k, c.v, c.seq_lens, c.page_table)
     hq, hkv = c.num_q_heads, c.num_kv_heads
-    n_tiles = msa.varlen_tiles(inp.q_counts)
+    n_tiles = msa.varlen_tiles(inp.q_counts, inp.q_starts)
     ws = _workspace(msa, desc, hq, n_tiles, k_total, dev)
     pooled = torch.full(msa.pooled_shape(desc), float("nan"), dtype=c.k.dtype, device=dev)
     msa.msa_pool_block_keys(desc, 0, -1, pooled, ws.buf, ws.nbytes)
@@ -63,7 +63,7 @@ def run_single(inp, s, pooled, k_scored, k_total):
         pool_s = pooled
     hq, hkv = c.num_q_heads, c.num_kv_heads
     n = inp.q_counts[s]
-    n_tiles = (n + 63) // 64
+    n_tiles = msa.chunk_tiles(inp.q_starts[s], n)
     ws = _workspace(msa, desc, hq, n_tiles, k_total, dev)
     q = inp.q_rows(s).contiguous()
     idx = torch.full((n_tiles, hkv, k_total), -7, dtype=torch.int32, device=dev)
@@ -105,11 +105,14 @@ def verify_against_oracle(inp, res, k_scored, k_total, rows_per_tile=7):
                 check_lse(to64(res["lse"][at, h * grp:(h + 1) * grp]), lse)
 
 
+@pytest.mark.parametrize("aligned", [True, False])
 @pytest.mark.parametrize("layout,hq,hkv", [("contiguous", 64, 8), ("paged", 16, 4), ("contiguous", 16, 2)])
-def test_prefill_batch(dev, layout, hq, hkv):
+def test_prefill_batch(dev, layout, hq, hkv, aligned):
     # ragged chunks: a long one, one from an empty prefix, a 5-token one, an
-    # empty one and one that ends on a tile boundary
-    q_starts = [64 * 23, 0, 64 * 7, 64 * 3, 64 * 40]
+    # empty one and one that ends on a tile boundary; unaligned: the same
+    # chunks starting inside blocks (as every chunk after the first of a
+    # serving loop does)
+    q_starts = [64 * 23, 0, 64 * 7, 64 * 3, 64 * 40] if aligned else [64 * 23 + 17, 0, 64 * 7 + 62, 64 * 3 + 5, 64 * 40 + 1]
     q_counts = [64 * 2 + 17, 64 * 3, 5, 0, 64]
     inp = make_prefill_batch_inputs(q_starts, q_counts, hkv, hq, "bf16", layout, seed=91, device=dev)
     k_scored, k_total = 6, 7
@@ -136,8 +139,8 @@ def test_prefill_batch_rejects_bad_batches(dev):
     idx = torch.zeros(2, 2, 5, dtype=torch.int32, device=dev)
     out = torch.empty_like(inp.q)
     cases = [([64], [10], msa.MSA_ERR_INVALID_ARG),               # one sequence for a batch of two
-             ([64, 100], [10, 20], msa.MSA_ERR_UNSUPPORTED),      # start not on a block boundary
              ([64, 128], [10, -1], msa.MSA_ERR_INVALID_ARG),      # negative count
+             ([-1, 128], [10, 10], msa.MSA_ERR_INVALID_ARG),      # negative start
              ([64, 128], [10, 10 ** 6], msa.MSA_ERR_INVALID_ARG)]  # past the cache's capacity
     for starts, counts, want in cases:
         with pytest.raises(msa.MsaError) as e:

@@ -113,7 +113,7 @@ def test_prefill_sink(dev):
                            for op in (msa.MSA_OP_POOL, msa.MSA_OP_SELECT_PREFILL, msa.MSA_OP_PREFILL)), dev)
     pooled = torch.zeros(msa.pooled_shape(desc), dtype=inp.k.dtype, device=dev)
     msa.msa_pool_block_keys(desc, 0, -1, pooled, ws.buf, ws.nbytes)
-    n_tiles = (n + 63) // 64
+    n_tiles = msa.chunk_tiles(inp.q_start, n)
     idx = torch.full((n_tiles, inp.num_kv_heads, k_total), -7, dtype=torch.int32, device=dev)
     cfg = msa.select_cfg(k_scored, True, 64, inp.q_start, sink=True)
     msa.msa_select_topk_blocks(inp.q, hq, n, pooled, desc, cfg, idx, k_total, None, ws.buf, ws.nbytes)

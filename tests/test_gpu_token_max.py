@@ -113,7 +113,7 @@ def run_token_max_prefill(inp, ik, k_scored, k_total, sink=False):
     dev = inp.q.device
     desc = msa.kv_desc(c.k, c.v, c.seq_lens, c.page_table)
     hq, hkv = c.num_q_heads, c.num_kv_heads
-    n_tiles = msa.varlen_tiles(inp.q_counts)
+    n_tiles = msa.varlen_tiles(inp.q_counts, inp.q_starts)
     ws = msa.Workspace(msa.msa_workspace_size(msa.MSA_OP_SELECT_PREFILL, desc, hq, 64 * n_tiles, k_total), dev)
     max_blocks = desc.max_tokens // 64 if desc.layout == 0 else desc.max_pages_per_seq
     idx = torch.full((n_tiles, hkv, k_total), -7, dtype=torch.int32, device=dev)
@@ -125,12 +125,14 @@ def run_token_max_prefill(inp, ik, k_scored, k_total, sink=False):
     return dict(idx=idx, scores=scores, status=msa.msa_read_device_status(ws.buf))
 
 
-@pytest.mark.parametrize("layout,hq,hkv", [("contiguous", 64, 8), ("paged", 16, 4), ("contiguous", 8, 1)])
-def test_token_max_prefill_tiles(dev, layout, hq, hkv):
+@pytest.mark.parametrize("layout,hq,hkv,shift", [("contiguous", 64, 8, 0), ("paged", 16, 4, 0), ("contiguous", 8, 1, 0),
+                                                 ("contiguous", 64, 8, 37), ("paged", 16, 4, 11)])
+def test_token_max_prefill_tiles(dev, layout, hq, hkv, shift):
     # ragged chunks over a shared index-key head: one spanning two groups of 16
-    # tiles (and two of 8), one from an empty prefix, a 5-token one
+    # tiles (and two of 8), one from an empty prefix, a 5-token one; with a
+    # shift the chunks start inside blocks
     from synth import make_prefill_batch_inputs
-    q_starts = [64 * 23, 0, 64 * 7, 64 * 40]
+    q_starts = [64 * 23 + shift, 0, 64 * 7 + shift, 64 * 40 + shift]
     q_counts = [64 * 2 + 17, 64 * 3, 5, 64 * 17 + 1]
     inp = make_prefill_batch_inputs(q_starts, q_counts, hkv, hq, "bf16", layout, seed=95, device=dev)
     ik = make_index_keys(inp.cache, needles=2, seed=96)
@@ -141,10 +143,10 @@ def test_token_max_prefill_tiles(dev, layout, hq, hkv):
     for s, (q0, n) in enumerate(zip(q_starts, q_counts)):
         kidx = to64(ik.rows(inp.cache, s))
         qs = inp.q_rows(s)
-        for j in range((n + 63) // 64):
+        for j, lo, hi in O.prefill_tiles(q0, n):
             g = inp.tile_off[s] + j
             for h in range(hkv):
-                q_tile = to64(qs[64 * j:min(n, 64 * j + 64), h * grp:(h + 1) * grp])
+                q_tile = to64(qs[lo:hi, h * grp:(h + 1) * grp])
                 ref = O.prefill_tile_select_token_max(q_tile, j, q0, kidx, k_scored, k_total)
                 if ref["diag"] > 0:
                     got = to64(res["scores"][g * hkv + h, :ref["diag"]])
