@@ -147,12 +147,10 @@ int32_t* ws_status(void* ws) { return ws == nullptr ? nullptr : reinterpret_cast
 struct SelectLayout {
   size_t scores = 0, qidx = 0, cand = 0, total = 0;
 };
-SelectLayout select_layout(const msa_kv_desc* kv, int n_q_tokens, int prefill) {
+// prefill: `tiles` query tiles (decode: ignored).
+SelectLayout select_layout(const msa_kv_desc* kv, int64_t tiles, int prefill) {
   SelectLayout L;
-  // prefill: one tile more than n_q_tokens / 64 covers a chunk of n_q_tokens
-  // tokens that starts inside a block
-  const int64_t units = prefill ? static_cast<int64_t>((n_q_tokens + kBlock - 1) / kBlock + 1) * kv->num_kv_heads
-                                : static_cast<int64_t>(kv->batch) * kv->num_kv_heads;
+  const int64_t units = prefill ? tiles * kv->num_kv_heads : static_cast<int64_t>(kv->batch) * kv->num_kv_heads;
   L.scores = kWsRegion;
   size_t off = kWsRegion + align_up(static_cast<size_t>(units) * kv_max_blocks(kv) * sizeof(float), 256);
   L.qidx = off;
@@ -333,7 +331,7 @@ msa_status select_common(const void* q, int32_t num_q_heads, int32_t n_q_tokens,
   if (kv_max_blocks(kv) > kMaxTopkCandidates) return MSA_ERR_UNSUPPORTED;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != MSA_OK) return st;
-  SelectLayout L = select_layout(kv, prefill ? kBlock * pb->total_tiles() : 1, prefill);
+  SelectLayout L = select_layout(kv, prefill ? pb->total_tiles() : 0, prefill);
   if ((st = check_ws(ws, ws_bytes, L.total)) != MSA_OK) return st;
   if (prefill && pb->total_tiles() == 0) return MSA_OK;  // no new tokens
   float* scores = scores_out != nullptr ? scores_out : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.scores);
@@ -429,8 +427,11 @@ size_t msa_workspace_size(int32_t op, const msa_kv_desc* kv, int32_t num_q_heads
   if (validate_kv(kv) != MSA_OK) return 0;
   switch (op) {
     case MSA_OP_POOL: return kWsHeader;
-    case MSA_OP_SELECT: return select_layout(kv, 1, 0).total;
-    case MSA_OP_SELECT_PREFILL: return n_q_tokens > 0 ? select_layout(kv, n_q_tokens, 1).total : 0;
+    case MSA_OP_SELECT: return select_layout(kv, 0, 0).total;
+    // one tile more than n_q_tokens / 64 covers a chunk of n_q_tokens tokens
+    // that starts inside a block
+    case MSA_OP_SELECT_PREFILL:
+      return n_q_tokens > 0 ? select_layout(kv, (n_q_tokens + kBlock - 1) / kBlock + 1, 1).total : 0;
     case MSA_OP_DECODE:
       if (k_total <= 0) return 0;
       return decode_layout(kv, k_total, num_sms_current(), false).total;
@@ -439,7 +440,7 @@ size_t msa_workspace_size(int32_t op, const msa_kv_desc* kv, int32_t num_q_heads
     case MSA_OP_DENSE_PREFILL: return kWsHeader;
     case MSA_OP_DECODE_STEP:
       if (k_total <= 0) return 0;
-      return std::max(select_layout(kv, 1, 0).total, decode_layout(kv, k_total, num_sms_current(), false).total);
+      return std::max(select_layout(kv, 0, 0).total, decode_layout(kv, k_total, num_sms_current(), false).total);
     default: return 0;
   }
   (void)num_q_heads;
