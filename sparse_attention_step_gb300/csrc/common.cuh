@@ -55,6 +55,15 @@ __device__ inline uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// `raw` (dynamic shared memory) advanced to the next 1024-byte boundary, the
+// alignment 128-byte swizzled tiles need. Offsetting the array itself, not
+// rounding an integer, keeps every access through the result a
+// shared-memory access (the compiler can no longer tell after an integer
+// round trip, and falls back to generic loads and stores).
+__device__ inline uint8_t* smem_align1024(uint8_t* raw) {
+  return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------

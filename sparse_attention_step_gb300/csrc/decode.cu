@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_bf16_kernel(const __grid_c
                                                                  const __grid_constant__ CUtensorMap tmv, KvView kv,
                                                                  DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem_align1024(smem_raw);
   DecodeSmemTail& st = *reinterpret_cast<DecodeSmemTail*>(ring + kStages * kStageBytes);
 
   const int split = blockIdx.x, h = blockIdx.y, s = blockIdx.z;

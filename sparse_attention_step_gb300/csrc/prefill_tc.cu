@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
                                                                   const __grid_constant__ CUtensorMap tmv, KvView kv,
                                                                   PrefillArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* base = smem_align1024(smem_raw);
   uint8_t* qs = base;
   uint8_t* kvs = base + kQBytes;
   TcTail& st = *reinterpret_cast<TcTail*>(kvs + kKVBytes);

@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
                                                                    const __grid_constant__ CUtensorMap tmpool, KvView kv,
                                                                    StepArgs a) {
   extern __shared__ __align__(1024) uint8_t st_raw[];
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(st_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem_align1024(st_raw);  // keys and the selection buffers follow in shared memory
   uint64_t* keys = reinterpret_cast<uint64_t*>(ring + kStages * kStStage);  // [kStMaxChunk]
   __shared__ uint64_t full[kStages], empty[kStages];
   __shared__ uint64_t xlist2[64];    // exact path: this CTA's best kk keys

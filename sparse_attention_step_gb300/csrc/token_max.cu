@@ -43,7 +43,7 @@ struct TokenMaxArgs {
 __global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __grid_constant__ CUtensorMap tmi,
                                                                      KvView kv, TokenMaxArgs a) {
   extern __shared__ __align__(1024) uint8_t tm_raw[];
-  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tm_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem_align1024(tm_raw);
   __shared__ uint64_t full[kTmStages], empty[kTmStages];
   __shared__ float qsum[kTmMaxHeads][kHeadDim];
   __shared__ int32_t rowid[kTmMaxChunk];                      // first index-key row of each block, -1 = bad page
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
                                                                         KvView kv, TokenMaxPrefillArgs a,
                                                                         const PrefillBatch pb) {
   extern __shared__ __align__(1024) uint8_t tp_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tp_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* base = smem_align1024(tp_raw);
   uint8_t* qa = base;                  // A operands, 128-byte swizzled, K-major
   uint8_t* ring = base + kTpABytes;    // index-key blocks
   TpTail& st = *reinterpret_cast<TpTail*>(ring + kTpStages * kTmStage);
