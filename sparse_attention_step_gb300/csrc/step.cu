@@ -224,17 +224,6 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     }
   }
   __syncthreads();  // every stage consumed: the ring is free until the attention phase
-  if (tid == 0) {
-    // the ring's barriers restart for the attention phase (one warp quartet
-    // consumes each block); nothing waits on them until then
-    for (int i = 0; i < kStages; ++i) {
-      mbar_inval(&full[i]);
-      mbar_inval(&empty[i]);
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kStAttnWarps);
-    }
-    fence_mbar_init();
-  }
 
   // ---------------------------------------------------------------- 2. selection
   // Fast path, exact by construction:
@@ -269,6 +258,19 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   }
   __syncthreads();
   if (C > 1) cluster_arrive();
+  if (warp == kStWarps && lane == 0) {
+    // the ring's barriers restart for the attention phase (one warp quartet
+    // consumes each block); nothing waits on them until then, and the
+    // producer does this while the cluster catches up
+    for (int i = 0; i < kStages; ++i) {
+      mbar_inval(&full[i]);
+      mbar_inval(&empty[i]);
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kStAttnWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncwarp();
   if (C > 1) cluster_wait();
   for (int i = tid; i < C * n_samp; i += blockDim.x) {
     const int r = i / n_samp, j = i - r * n_samp;
