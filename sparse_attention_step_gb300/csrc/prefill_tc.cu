@@ -4,26 +4,33 @@
 //
 // One CTA owns 256 query rows of a (64-token tile, KV head) unit: 32 tokens x
 // the 8 heads of the group, as two M = 128 tiles (rows token-major,
-// head-minor). For every selected 64-key block:
-//   S_t = Q_t K^T      tcgen05.mma M128 N64 K16 x 8, bf16 -> fp32 in TMEM
+// head-minor). The selected blocks are taken two at a time (a pair of 128
+// keys; an odd count ends with a single block). For every pair:
+//   S_t = Q_t K^T      tcgen05.mma M128 N128 K16 x 8 (N64 for a single
+//                      block), bf16 -> fp32 in TMEM
 //   softmax            tcgen05.ld of the scores, causal mask on the diagonal
 //                      block, online max with lazy rescaling (O is rescaled
 //                      in TMEM only when the running max grows by more than
 //                      2^8), exp2; P (bf16, two per 32-bit column) is stored
 //                      back over the scores it came from
-//   O_t += P_t V       tcgen05.mma M128 N128 K16 x 4 with A = P read from
-//                      TMEM and V read MN-major from shared memory
+//   O_t += P_t V       tcgen05.mma M128 N128 K16 x 8 (x 4) with A = P read
+//                      from TMEM and V read MN-major from shared memory
+// An M128 MMA costs about the same at N = 64 as at N = 128, so scoring a pair
+// at once halves the tensor time of Q K^T against one block at a time.
 // Warp roles: warps 0-7 softmax of tile 0 and warps 8-15 of tile 1; within a
-// tile, warps 0-3 take score columns 0-31 and warps 4-7 columns 32-63 of the
-// rows in TMEM lanes 32 (w mod 4) .. (a warp reaches only those lanes); the
-// two halves of a row exchange their maxima and sums through shared memory
-// (a named barrier per tile). Warp 16 is the TMA producer (Q once, then a
-// 4-stage K/V ring), warp 17 the TMEM allocator and MMA issuer. The two tiles
+// tile, warps 0-3 take the pair's first block (score columns 0-63) and warps
+// 4-7 its second (columns 64-127) for the rows in TMEM lanes 32 (w mod 4) ..
+// (a warp reaches only those lanes); the two halves of a row exchange their
+// maxima and sums through shared memory (a named barrier per tile). Warp 16 is
+// the TMA producer (Q once, then 2-stage K and V rings of one pair each; K of
+// a stage is released once both tiles' S are computed, V once both tiles'
+// O += P V are), warp 17 the TMEM allocator and MMA issuer. The two tiles
 // ping-pong: the tensor core runs one tile's MMAs while the other tile's
-// softmax runs, and S is double-buffered so S of the next block is computed
-// while the softmax of this one runs (it is issued after O += P V of the block
-// two back, whose P shares its buffer). TMEM: S / P of tile t in
-// [128 t, 128 t + 128) (two 64-column buffers), O_t in [256 + 128 t, 384 + 128 t).
+// softmax runs; the tensor core executes in issue order, so S of the next
+// pair, issued after O += P V of this one, never overwrites a P still to be
+// read, and once it has completed O of the tile is quiet for the softmax to
+// rescale. TMEM: S / P of tile t in [128 t, 128 t + 128), O_t in
+// [256 + 128 t, 384 + 128 t).
 #include <float.h>
 
 #include "kernels.cuh"
@@ -34,24 +41,26 @@ namespace msa {
 namespace {
 
 constexpr int kTcTiles = 2;
-constexpr int kTcStages = 4;
+constexpr int kTcStages = 2;        // K and V rings, one pair of blocks per stage
+constexpr int kPairBytes = 32768;   // two blocks x 64 rows x 128 dims of K (or V), bf16
 constexpr int kSoftmaxWarps = 16;
 constexpr int kTcThreads = 32 * (kSoftmaxWarps + 2);
 constexpr int kProducerWarp = kSoftmaxWarps;
 constexpr int kMmaWarp = kSoftmaxWarps + 1;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kQBytes = kTcTiles * 2 * 16384;   // two tiles x two 64-dim halves
-constexpr int kKVBytes = kTcStages * 32768;
+constexpr int kRingBytes = kTcStages * kPairBytes;
 constexpr int kMaxList = 512;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (factor 256)
 
 struct TcTail {
   uint64_t q_full;
-  uint64_t kv_full[kTcStages];
-  uint64_t kv_empty[kTcStages];
-  uint64_t s_full[kTcTiles][2];  // S of a tile, double-buffered
+  uint64_t k_full[kTcStages];
+  uint64_t k_empty[kTcStages];
+  uint64_t v_full[kTcStages];
+  uint64_t v_empty[kTcStages];
+  uint64_t s_full[kTcTiles];
   uint64_t p_full[kTcTiles];
-  uint64_t pv_done[kTcTiles];    // O += P V of the tile's latest block has completed
   uint64_t o_final[kTcTiles];
   uint64_t drain;
   uint32_t tmem_base;
@@ -60,7 +69,7 @@ struct TcTail {
   int32_t blocks[kMaxList];
 };
 
-constexpr size_t kTcSmem = 1024 + kQBytes + kKVBytes + sizeof(TcTail);
+constexpr size_t kTcSmem = 1024 + kQBytes + 2 * kRingBytes + sizeof(TcTail);
 
 __device__ inline float ex2_approx(float x) {
   float y;
@@ -107,8 +116,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = smem_align1024(smem_raw);
   uint8_t* qs = base;
-  uint8_t* kvs = base + kQBytes;
-  TcTail& st = *reinterpret_cast<TcTail*>(kvs + kKVBytes);
+  uint8_t* ks = base + kQBytes;            // K ring: [stage][dim half][128 keys][128 B]
+  uint8_t* vs = ks + kRingBytes;           // V ring, the same layout
+  TcTail& st = *reinterpret_cast<TcTail*>(vs + kRingBytes);
 
   const int rh = blockIdx.x, h = blockIdx.y, tile = blockIdx.z;  // tile: global over the batch
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -140,14 +150,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     st.abort = 0;
     mbar_init(&st.q_full, 1);
     for (int i = 0; i < kTcStages; ++i) {
-      mbar_init(&st.kv_full[i], 1);
-      mbar_init(&st.kv_empty[i], 1);
+      mbar_init(&st.k_full[i], 1);
+      mbar_init(&st.k_empty[i], 1);
+      mbar_init(&st.v_full[i], 1);
+      mbar_init(&st.v_empty[i], 1);
     }
     for (int t = 0; t < kTcTiles; ++t) {
-      mbar_init(&st.s_full[t][0], 1);
-      mbar_init(&st.s_full[t][1], 1);
+      mbar_init(&st.s_full[t], 1);
       mbar_init(&st.p_full[t], kSoftmaxWarps / 2);
-      mbar_init(&st.pv_done[t], 1);
       mbar_init(&st.o_final[t], 1);
     }
     mbar_init(&st.drain, 1);
@@ -161,9 +171,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   __syncthreads();
   tc::fence_after();
   const int nblk = st.n_blocks;
+  const int npair = (nblk + 1) >> 1;
   const bool dense = a.idx == nullptr;
   const uint32_t tmem = st.tmem_base;
   volatile int32_t* abort = &st.abort;
+  auto blocks_in = [&](int i) { return nblk - 2 * i >= 2 ? 2 : 1; };  // blocks in pair i
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -178,79 +190,102 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       for (int t = 0; t < kTcTiles; ++t)
         for (int half = 0; half < 2; ++half)
           tma_load_3d(qs + t * 32768 + half * 16384, &tmq, 64 * half, h * 8, tok0 + 16 * t, &st.q_full);
-      int issued = 0;
-      for (int i = 0; i < nblk; ++i) {
-        const int stg = i % kTcStages;
-        if (i >= kTcStages && !wait_or_abort(&st.kv_empty[stg], ((i / kTcStages) - 1) & 1, abort, a.status)) break;
-        const int b = dense ? i : st.blocks[i];
-        const int64_t row = kv.block_row(seq, h, b, a.status, kIdPrefill);
-        const int32_t y = static_cast<int32_t>(row < 0 ? 0 : row);
-        uint8_t* dst = kvs + stg * 32768;
-        mbar_arrive_expect_tx(&st.kv_full[stg], 32768);
-        tma_load_2d(dst, &tmk, 0, y, &st.kv_full[stg]);
-        tma_load_2d(dst + 8192, &tmk, 64, y, &st.kv_full[stg]);
-        tma_load_2d(dst + 16384, &tmv, 0, y, &st.kv_full[stg]);
-        tma_load_2d(dst + 24576, &tmv, 64, y, &st.kv_full[stg]);
-        issued = i + 1;
+      int issued_k = 0, issued_v = 0;
+      for (int i = 0; i < npair; ++i) {
+        const int stg = i % kTcStages, use = i / kTcStages, nb = blocks_in(i);
+        auto row_of = [&](int j) {
+          const int b = dense ? 2 * i + j : st.blocks[2 * i + j];
+          const int64_t row = kv.block_row(seq, h, b, a.status, kIdPrefill);
+          return static_cast<int32_t>(row < 0 ? 0 : row);
+        };
+        const int32_t y0 = row_of(0), y1 = nb == 2 ? row_of(1) : 0;
+        // block j of the pair: rows [64 j, 64 j + 64) of each 64-dim half
+        if (i >= kTcStages && !wait_or_abort(&st.k_empty[stg], (use - 1) & 1, abort, a.status)) break;
+        mbar_arrive_expect_tx(&st.k_full[stg], nb * 16384);
+        for (int j = 0; j < nb; ++j)
+          for (int hd = 0; hd < 2; ++hd)
+            tma_load_2d(ks + stg * kPairBytes + hd * 16384 + j * 8192, &tmk, 64 * hd, j ? y1 : y0, &st.k_full[stg]);
+        issued_k = i + 1;
+        if (i >= kTcStages && !wait_or_abort(&st.v_empty[stg], (use - 1) & 1, abort, a.status)) break;
+        mbar_arrive_expect_tx(&st.v_full[stg], nb * 16384);
+        for (int j = 0; j < nb; ++j)
+          for (int hd = 0; hd < 2; ++hd)
+            tma_load_2d(vs + stg * kPairBytes + hd * 16384 + j * 8192, &tmv, 64 * hd, j ? y1 : y0, &st.v_full[stg]);
+        issued_v = i + 1;
       }
       // drain: every load this thread issued has landed before the CTA may exit
       mbar_wait(&st.q_full, 0, a.status, kIdPrefill);
-      for (int i = issued - kTcStages < 0 ? 0 : issued - kTcStages; i < issued; ++i)
-        mbar_wait(&st.kv_full[i % kTcStages], (i / kTcStages) & 1, a.status, kIdPrefill);
+      for (int i = issued_k - kTcStages < 0 ? 0 : issued_k - kTcStages; i < issued_k; ++i)
+        mbar_wait(&st.k_full[i % kTcStages], (i / kTcStages) & 1, a.status, kIdPrefill);
+      for (int i = issued_v - kTcStages < 0 ? 0 : issued_v - kTcStages; i < issued_v; ++i)
+        mbar_wait(&st.v_full[i % kTcStages], (i / kTcStages) & 1, a.status, kIdPrefill);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdS = tc::idesc_bf16(128, 64, 0, 0);
+      constexpr uint32_t kIdS2 = tc::idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t kIdS1 = tc::idesc_bf16(128, 64, 0, 0);
       constexpr uint32_t kIdO = tc::idesc_bf16(128, 128, 0, 1);
-      const uint32_t q_addr = smem_u32(qs), kv_addr = smem_u32(kvs);
-      auto issue_s = [&](int t, int buf, int stg) {
-        const uint32_t d = tmem + t * 128 + buf * 64;
+      const uint32_t q_addr = smem_u32(qs), k_addr = smem_u32(ks), v_addr = smem_u32(vs);
+      // S_t = Q_t K^T over the pair's keys (K-major, 128 B rows, 8-row groups 1 KB apart)
+      auto issue_s = [&](int t, int i) {
+        const uint32_t d = tmem + t * 128;
+        const uint32_t id = blocks_in(i) == 2 ? kIdS2 : kIdS1;
+        const uint32_t kb = k_addr + (i % kTcStages) * kPairBytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           const uint64_t ad = tc::sdesc_sw128(q_addr + t * 32768 + off, 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(kv_addr + stg * 32768 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-          tc::mma_ss(d, ad, bd, kIdS, kk > 0);
+          const uint64_t bd = tc::sdesc_sw128(kb + off, 16, 1024);
+          tc::mma_ss(d, ad, bd, id, kk > 0);
         }
       };
-      // O_t += P V with P (bf16, packed in pairs) in the S buffer of its block
-      auto issue_pv = [&](int t, int buf, int stg, bool acc) {
+      // O_t += P V with P (bf16, packed in pairs) over the scores of the pair;
+      // V MN-major: 16 keys a step, the two 64-dim halves 16 KB apart
+      auto issue_pv = [&](int t, int i) {
         const uint32_t d = tmem + 256 + t * 128;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bd = tc::sdesc_sw128(kv_addr + stg * 32768 + 16384 + ks * 2048, 8192, 1024);
-          tc::mma_ts(d, tmem + t * 128 + buf * 64 + 8 * ks, bd, kIdO, (acc || ks > 0) ? 1u : 0u);
+        const uint32_t vb = v_addr + (i % kTcStages) * kPairBytes;
+        const int steps = 4 * blocks_in(i);
+        for (int s = 0; s < steps; ++s) {
+          const uint64_t bd = tc::sdesc_sw128(vb + s * 2048, 16384, 1024);
+          tc::mma_ts(d, tmem + t * 128 + 8 * s, bd, kIdO, (i > 0 || s > 0) ? 1u : 0u);
         }
-      };
-      // S_{i+1} of both tiles is issued before O += P_i V_i, into the other S
-      // buffer, so a tile's softmax of block i+1 never waits for the tensor
-      // core to finish block i.
-      auto issue_s_all = [&](int i) -> bool {
-        const int stg = i % kTcStages;
-        if (!wait_or_abort(&st.kv_full[stg], (i / kTcStages) & 1, abort, a.status)) return false;
-        tc::fence_after();
-        for (int t = 0; t < kTcTiles; ++t) {
-          issue_s(t, i & 1, stg);
-          tc::commit(&st.s_full[t][i & 1]);
-        }
-        return true;
       };
       bool ok = wait_or_abort(&st.q_full, 0, abort, a.status);
       tc::fence_after();
-      if (ok && nblk > 0) ok = issue_s_all(0);
-      for (int i = 0; ok && i < nblk; ++i) {
-        // buffer (i + 1) & 1 was last read by the softmax of block i - 1,
-        // whose P this thread has already waited for
-        if (i + 1 < nblk && !(ok = issue_s_all(i + 1))) break;
+      if (ok && npair > 0 && (ok = wait_or_abort(&st.k_full[0], 0, abort, a.status))) {
+        tc::fence_after();
         for (int t = 0; t < kTcTiles; ++t) {
-          if (!(ok = wait_or_abort(&st.p_full[t], i & 1, abort, a.status))) break;
-          tc::fence_after();
-          issue_pv(t, i & 1, i % kTcStages, i > 0);
-          tc::commit(&st.pv_done[t]);
+          issue_s(t, 0);
+          tc::commit(&st.s_full[t]);
         }
-        if (!ok) break;
-        tc::commit(&st.kv_empty[i % kTcStages]);
+        tc::commit(&st.k_empty[0]);  // the K stage is free once both tiles' S have completed
+      }
+      // tensor-core order per pair i: O_0 += P_0 V, S_0 of pair i + 1,
+      // O_1 += P_1 V, S_1 of pair i + 1
+      for (int i = 0; ok && i < npair; ++i) {
+        const int stg = i % kTcStages;
+        const bool next = i + 1 < npair;
+        if (!(ok = wait_or_abort(&st.v_full[stg], (i / kTcStages) & 1, abort, a.status))) break;
+        if (!(ok = wait_or_abort(&st.p_full[0], i & 1, abort, a.status))) break;
+        tc::fence_after();
+        issue_pv(0, i);
+        if (next) {
+          if (!(ok = wait_or_abort(&st.k_full[(i + 1) % kTcStages], ((i + 1) / kTcStages) & 1, abort, a.status)))
+            break;
+          tc::fence_after();
+          issue_s(0, i + 1);
+          tc::commit(&st.s_full[0]);
+        }
+        if (!(ok = wait_or_abort(&st.p_full[1], i & 1, abort, a.status))) break;
+        tc::fence_after();
+        issue_pv(1, i);
+        tc::commit(&st.v_empty[stg]);
+        if (next) {
+          issue_s(1, i + 1);
+          tc::commit(&st.s_full[1]);
+          tc::commit(&st.k_empty[(i + 1) % kTcStages]);
+        }
       }
       for (int t = 0; t < kTcTiles; ++t) tc::commit(&st.o_final[t]);
       tc::commit(&st.drain);
@@ -258,10 +293,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     }
   } else {
     // ------------------------------------------------------------ softmax
-    __shared__ float xmax[2][kTcTiles][2][128];  // [block parity][tile][half][row]
+    __shared__ float xmax[2][kTcTiles][2][128];  // [pair parity][tile][half][row]
     __shared__ float xsum[kTcTiles][2][128];
     const int t = warp >> 3;                // tile
-    const int hf = (warp >> 2) & 1;         // score columns [32 hf, 32 hf + 32)
+    const int hf = (warp >> 2) & 1;         // block of the pair: score columns [64 hf, 64 hf + 64)
     const int q4 = warp & 3;                // TMEM lane quadrant
     const int r = 32 * q4 + lane;           // row within the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
@@ -276,37 +311,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     // Every warp of the tile runs every iteration and every named barrier, even
     // after a wait gave up (then it skips the work), so no partner warp can be
     // left waiting at a barrier.
-    for (int i = 0; i < nblk; ++i) {
-      ok = __all_sync(0xffffffffu, ok && wait_or_abort(&st.s_full[t][i & 1], (i >> 1) & 1, abort, a.status));
+    for (int i = 0; i < npair; ++i) {
+      ok = __all_sync(0xffffffffu, ok && wait_or_abort(&st.s_full[t], i & 1, abort, a.status));
       tc::fence_after();
-      // O and this tile's P buffer are touched only once O += P V of block
-      // i - 1 has completed
-      bool pv_seen = i == 0;
-      auto wait_pv = [&]() {
-        if (pv_seen) return;
-        ok = __all_sync(0xffffffffu, ok && wait_or_abort(&st.pv_done[t], (i - 1) & 1, abort, a.status));
-        tc::fence_after();
-        pv_seen = true;
-      };
-      uint32_t sr[32];
-      if (ok) {
-        tc::ld32(tmem + lane_base + t * 128 + (i & 1) * 64 + 32 * hf, sr);
+      const bool have = hf < blocks_in(i);  // the odd last pair has no second block
+      uint32_t sa[32], sb[32];
+      if (ok && have) {
+        const uint32_t sad = tmem + lane_base + t * 128 + 64 * hf;
+        tc::ld32(sad, sa);
+        tc::ld32(sad + 32, sb);
         tc::wait_ld();
       } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) sr[c] = __float_as_uint(-INFINITY);
+        for (int c = 0; c < 32; ++c) sa[c] = sb[c] = __float_as_uint(-INFINITY);
       }
-      const int b = dense ? i : st.blocks[i];
+      const int b = !have ? -1 : dense ? 2 * i + hf : st.blocks[2 * i + hf];
       if (b == diag) {  // causal mask inside the diagonal block
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (32 * hf + c > tt) sr[c] = __float_as_uint(-INFINITY);
+        for (int c = 0; c < 32; ++c) {
+          if (c > tt) sa[c] = __float_as_uint(-INFINITY);
+          if (32 + c > tt) sb[c] = __float_as_uint(-INFINITY);
+        }
       }
       float mx;
       {
         float t16[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) t16[c] = fmaxf(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
+        for (int c = 0; c < 16; ++c)
+          t16[c] = fmaxf(fmaxf(__uint_as_float(sa[2 * c]), __uint_as_float(sa[2 * c + 1])),
+                         fmaxf(__uint_as_float(sb[2 * c]), __uint_as_float(sb[2 * c + 1])));
 #pragma unroll
         for (int w = 8; w > 0; w >>= 1)
 #pragma unroll
@@ -319,46 +352,53 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       const float m_blk = mx * a.scale_log2;  // -inf stays -inf
       const float m_new = fmaxf(m, m_blk);
       const bool need = (m == -INFINITY) ? (m_new != -INFINITY) : (m_new > m + kRescaleLog2);
-      if (__any_sync(0xffffffffu, need)) {
-        wait_pv();
-        const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
-        if (i > 0 && ok) {
-#pragma unroll 1
-          for (int cc = 0; cc < 2; ++cc) {
-            uint32_t o[32];
-            const uint32_t oa = tmem + lane_base + 256 + t * 128 + 64 * hf + cc * 32;
-            tc::ld32(oa, o);
-            tc::wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tc::st32(oa, o);
-          }
-          tc::wait_st();
-        }
+      // the rows of this warp (the same rows as the partner warp of the other
+      // half, so both take the same decision) move to the new max together
+      const bool resc = __any_sync(0xffffffffu, need);
+      float alpha = 1.f;
+      if (resc) {
+        alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
         l *= alpha;
         m = m_new;
       }
       const float neg_ref = (m == -INFINITY) ? 0.f : -m;
       const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nr2 = make_float2(neg_ref, neg_ref);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
-      uint32_t pk[16];
+      // P replaces the scores it came from: columns [32 hf, 32 hf + 32) of the
+      // tile's S buffer hold keys [64 hf, 64 hf + 64) in pairs (the other
+      // half read those columns before the barrier above). The next S into
+      // the buffer is issued after O += P V of this pair.
+      auto exp_store = [&](const uint32_t (&sr)[32], uint32_t col) {
+        uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float2 x = ffma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc2, nr2);
-        const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-        if (c & 1) acc1 = fadd2(acc1, pp);
-        else acc0 = fadd2(acc0, pp);
-        pk[c] = pack_bf16(pp.x, pp.y);
-      }
+        for (int c = 0; c < 16; ++c) {
+          const float2 x = ffma2(make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc2, nr2);
+          const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          if (c & 1) acc1 = fadd2(acc1, pp);
+          else acc0 = fadd2(acc0, pp);
+          pk[c] = pack_bf16(pp.x, pp.y);
+        }
+        if (ok && have) tc::st16(tmem + lane_base + t * 128 + col, pk);
+      };
+      exp_store(sa, 32 * hf);
+      exp_store(sb, 32 * hf + 16);
       const float2 acc = fadd2(acc0, acc1);
       const float sum = acc.x + acc.y;
-      // P replaces the scores it came from: columns [16 hf, 16 hf + 16) of
-      // this block's S buffer hold keys [32 hf, 32 hf + 32) in pairs. The
-      // next S into this buffer is issued after O += P V of this block.
-      if (ok) {
-        tc::st16(tmem + lane_base + t * 128 + (i & 1) * 64 + 16 * hf, pk);
-        tc::wait_st();
+      // O of this half rescaled to the new max (after the scores are consumed,
+      // to keep the registers of both under the per-thread budget)
+      if (resc && i > 0 && ok) {
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t o[32];
+          const uint32_t oa = tmem + lane_base + 256 + t * 128 + 64 * hf + cc * 32;
+          tc::ld32(oa, o);
+          tc::wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+          tc::st32(oa, o);
+        }
       }
+      tc::wait_st();
       l += sum;
       tc::fence_before();
       __syncwarp();
