@@ -93,6 +93,11 @@ __device__ inline float2 fadd2(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
 }
+__device__ inline float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 __device__ inline void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -335,16 +340,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       }
       float mx;
       {
-        float t16[16];
+        auto val = [&](int k) { return __uint_as_float(k < 32 ? sa[k] : sb[k - 32]); };
+        float u[22], w[8];
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          t16[c] = fmaxf(fmaxf(__uint_as_float(sa[2 * c]), __uint_as_float(sa[2 * c + 1])),
-                         fmaxf(__uint_as_float(sb[2 * c]), __uint_as_float(sb[2 * c + 1])));
+        for (int k = 0; k < 21; ++k) u[k] = fmax3(val(3 * k), val(3 * k + 1), val(3 * k + 2));
+        u[21] = val(63);
 #pragma unroll
-        for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-          for (int c = 0; c < w; ++c) t16[c] = fmaxf(t16[c], t16[c + w]);
-        mx = t16[0];
+        for (int k = 0; k < 7; ++k) w[k] = fmax3(u[3 * k], u[3 * k + 1], u[3 * k + 2]);
+        w[7] = u[21];
+        mx = fmax3(fmax3(w[0], w[1], w[2]), fmax3(w[3], w[4], w[5]), fmaxf(w[6], w[7]));
       }
       xmax[i & 1][t][hf][r] = mx;
       named_bar_sync(bar_id, 256);
