@@ -131,28 +131,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   const int jt = tile - a.batch.tile_off[seq];  // tile within its sequence
   const int64_t diag = a.batch.q_start[seq] / kBlock + jt;
 
-  if (tid == 0) {
-    int n = 0;
-    if (a.idx != nullptr) {
-      const int32_t* list = a.idx + (static_cast<int64_t>(tile) * a.hkv + h) * a.k_total;
-      for (int i = 0; i < a.k_total; ++i) {
-        const int32_t b = list[i];
-        if (b < 0) continue;
-        if (b > diag) {
-          set_status(a.status, MSA_ERR_DEVICE_BOUNDS, kIdPrefill);
-          continue;
-        }
-        if (n == kMaxList) {  // more valid entries than the kernel holds
-          set_status(a.status, MSA_ERR_UNSUPPORTED, kIdPrefill);
-          break;
-        }
-        st.blocks[n++] = b;
-      }
-    } else {
-      n = static_cast<int>(diag + 1);
-    }
-    st.n_blocks = n;
-    st.abort = 0;
+  if (warp == kProducerWarp && lane == 0) {
     mbar_init(&st.q_full, 1);
     for (int i = 0; i < kTcStages; ++i) {
       mbar_init(&st.k_full[i], 1);
@@ -167,6 +146,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     }
     mbar_init(&st.drain, 1);
     fence_mbar_init();
+    // Q needs nothing of the list: its load starts while the list is read
+    tma_prefetch_desc(&tmq);
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+    mbar_arrive_expect_tx(&st.q_full, kQBytes);
+    // first token of the row half (may be before the chunk, then the load
+    // reads the fill value or another sequence's rows, never used)
+    const int32_t tok0 = a.batch.q_off[seq] + a.batch.tile_row0(seq, tile) + rh * (kTcTiles * 16);
+    for (int t = 0; t < kTcTiles; ++t)
+      for (int half = 0; half < 2; ++half)
+        tma_load_3d(qs + t * 32768 + half * 16384, &tmq, 64 * half, h * 8, tok0 + 16 * t, &st.q_full);
+  }
+  if (warp == 0) {
+    // the valid entries of the unit's list, in order, read 32 at a time
+    int n = 0;
+    if (a.idx != nullptr) {
+      const int32_t* list = a.idx + (static_cast<int64_t>(tile) * a.hkv + h) * a.k_total;
+      for (int base = 0; base < a.k_total; base += 32) {
+        const int32_t b = base + lane < a.k_total ? list[base + lane] : -1;
+        if (b > diag) set_status(a.status, MSA_ERR_DEVICE_BOUNDS, kIdPrefill);
+        const bool keep = b >= 0 && b <= diag;
+        const uint32_t ballot = __ballot_sync(0xffffffffu, keep);
+        const int pos = n + __popc(ballot & ((1u << lane) - 1u));
+        if (keep && pos < kMaxList) st.blocks[pos] = b;
+        n += __popc(ballot);
+      }
+      if (n > kMaxList) {  // more valid entries than the kernel holds
+        if (lane == 0) set_status(a.status, MSA_ERR_UNSUPPORTED, kIdPrefill);
+        n = kMaxList;
+      }
+    } else {
+      n = static_cast<int>(diag + 1);
+    }
+    if (lane == 0) {
+      st.n_blocks = n;
+      st.abort = 0;
+    }
   }
   if (warp == kMmaWarp) {
     tc::alloc(&st.tmem_base, kTmemCols);
@@ -185,16 +201,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmq);
-      tma_prefetch_desc(&tmk);
-      tma_prefetch_desc(&tmv);
-      mbar_arrive_expect_tx(&st.q_full, kQBytes);
-      // first token of the row half (may be before the chunk, then the load
-      // reads the fill value or another sequence's rows, never used)
-      const int32_t tok0 = a.batch.q_off[seq] + a.batch.tile_row0(seq, tile) + rh * (kTcTiles * 16);
-      for (int t = 0; t < kTcTiles; ++t)
-        for (int half = 0; half < 2; ++half)
-          tma_load_3d(qs + t * 32768 + half * 16384, &tmq, 64 * half, h * 8, tok0 + 16 * t, &st.q_full);
       int issued_k = 0, issued_v = 0;
       for (int i = 0; i < npair; ++i) {
         const int stg = i % kTcStages, use = i / kTcStages, nb = blocks_in(i);
@@ -323,8 +329,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       uint32_t sa[32], sb[32];
       if (ok && have) {
         const uint32_t sad = tmem + lane_base + t * 128 + 64 * hf;
-        tc::ld32(sad, sa);
-        tc::ld32(sad + 32, sb);
+        tc::ld64(sad, sa, sb);
         tc::wait_ld();
       } else {
 #pragma unroll
