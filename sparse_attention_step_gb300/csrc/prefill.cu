@@ -47,32 +47,35 @@ __global__ void __launch_bounds__(kPfThreads) prefill_bf16_kernel(const __grid_c
   const int64_t len = kv.seq_len(seq, a.status, kIdPrefill);
   const int64_t diag = q_start / kBlock + jt;
 
-  if (tid == 0) {
+  if (warp == 0) {
+    // the valid entries of the unit's list, in order, read 32 at a time
     int n = 0;
     if (a.idx != nullptr) {
       const int32_t* list = a.idx + (static_cast<int64_t>(tile) * a.hkv + h) * a.k_total;
-      for (int i = 0; i < a.k_total; ++i) {
-        const int32_t b = list[i];
-        if (b < 0) continue;
-        if (b > diag) {
-          set_status(a.status, MSA_ERR_DEVICE_BOUNDS, kIdPrefill);
-          continue;
-        }
-        if (n == kPfMaxList) {  // more valid entries than the kernel holds
-          set_status(a.status, MSA_ERR_UNSUPPORTED, kIdPrefill);
-          break;
-        }
-        st.blocks[n++] = b;
+      for (int base = 0; base < a.k_total; base += 32) {
+        const int32_t b = base + lane < a.k_total ? list[base + lane] : -1;
+        if (b > diag) set_status(a.status, MSA_ERR_DEVICE_BOUNDS, kIdPrefill);
+        const bool keep = b >= 0 && b <= diag;
+        const uint32_t ballot = __ballot_sync(0xffffffffu, keep);
+        const int pos = n + __popc(ballot & ((1u << lane) - 1u));
+        if (keep && pos < kPfMaxList) st.blocks[pos] = b;
+        n += __popc(ballot);
+      }
+      if (n > kPfMaxList) {  // more valid entries than the kernel holds
+        if (lane == 0) set_status(a.status, MSA_ERR_UNSUPPORTED, kIdPrefill);
+        n = kPfMaxList;
       }
     } else {
       n = static_cast<int>(diag + 1);  // every causal block (list not materialised)
     }
-    st.n_blocks = n;
-    for (int i = 0; i < kPfStages; ++i) {
-      mbar_init(&st.full[i], 1);
-      mbar_init(&st.empty[i], kPfWarps);
+    if (lane == 0) {
+      st.n_blocks = n;
+      for (int i = 0; i < kPfStages; ++i) {
+        mbar_init(&st.full[i], 1);
+        mbar_init(&st.empty[i], kPfWarps);
+      }
+      fence_mbar_init();
     }
-    fence_mbar_init();
   }
   __syncthreads();
   const int nblk = st.n_blocks;
