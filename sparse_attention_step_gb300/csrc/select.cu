@@ -717,8 +717,38 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
     }
     fence_mbar_init();
   }
-  if (kv.layout == MSA_KV_PAGED)
-    for (int i = tid; i < rows; i += blockDim.x) pages[i] = kv.page(s, r0 + i, status, kIdScore);
+  // bf16: the group's query rows are loaded now and summed once the page ids
+  // are in, so the two latencies overlap
+  float xq[kMaxGroupHeads];
+  if constexpr (sizeof(T) == 2) {
+    if (tid < kHeadDim) {
+      const T* qg = q + (static_cast<int64_t>(s) * a.hq + h * grp) * kHeadDim + tid;
+#pragma unroll
+      for (int g = 0; g < kMaxGroupHeads; ++g) xq[g] = g < grp ? __bfloat162float(qg[g * kHeadDim]) : 0.f;
+    }
+  }
+  if (kv.layout == MSA_KV_PAGED) {
+    // the chunk's page ids, eight loads in flight per thread before any check
+    const int32_t* pt = kv.page_table + static_cast<int64_t>(s) * kv.max_pages + r0;
+    for (int b0 = 0; b0 < rows; b0 += 8 * kSelThreads) {
+      int32_t v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = b0 + u * kSelThreads + tid;
+        v[u] = i < rows ? pt[i] : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = b0 + u * kSelThreads + tid;
+        if (i >= rows) continue;
+        if (v[u] < 0 || v[u] >= kv.num_pages) {
+          set_status(status, MSA_ERR_DEVICE_BOUNDS, kIdScore);
+          v[u] = -1;
+        }
+        pages[i] = v[u];
+      }
+    }
+  }
   __syncthreads();
 
   auto emit = [&](int i, float part, bool ok) {  // row i of the chunk
@@ -735,13 +765,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
     // into a bf16 head and remainder (as in the fused step).
     __shared__ float qsum[kHeadDim];
     if (tid < kHeadDim) {
-      const T* qg = q + (static_cast<int64_t>(s) * a.hq + h * grp) * kHeadDim + tid;
-      float x[kMaxGroupHeads];
-#pragma unroll
-      for (int g = 0; g < kMaxGroupHeads; ++g) x[g] = g < grp ? __bfloat162float(qg[g * kHeadDim]) : 0.f;
       float acc = 0.f;
 #pragma unroll
-      for (int g = 0; g < kMaxGroupHeads; ++g) acc += x[g];
+      for (int g = 0; g < kMaxGroupHeads; ++g) acc += xq[g];
       qsum[tid] = acc;
     }
     __syncthreads();
