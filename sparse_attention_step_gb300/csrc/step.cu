@@ -89,8 +89,6 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   __shared__ RadixScratch radix;
   __shared__ int n_sel;   // this CTA's survivor count (may exceed 64: then only 64 are stored)
   __shared__ int n_sel2;  // counter of the exact path
-  __shared__ int32_t blocks[kStMaxList];
-  __shared__ int n_blocks;
   __shared__ float qsum[kHeadDim];  // the group's index query (sum of its query heads), fp32
   __shared__ float wm[kStAttnWarps][kStG], wl[kStAttnWarps][kStG];
 
@@ -390,22 +388,12 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     const int j = i - keep0;
     return j < 0 ? 0 : j < kk ? sel_block(sel_keys[j]) : (j == kk && forced >= 0 ? static_cast<int32_t>(forced) : -1);
   };
-  if (warp == 0) {
-    const int lo = rank * a.bps, hi = min(a.k_total, lo + a.bps);
-    int n = 0;
-    for (int b0 = lo; b0 < hi; b0 += 32) {
-      const int i = b0 + lane;
-      const int32_t b = i >= hi ? -1 : slice_at(i);
-      if (b >= nb) set_status(a.status, MSA_ERR_DEVICE_BOUNDS, kIdDecode);
-      const bool ok = b >= 0 && b < nb;
-      const unsigned m = __ballot_sync(0xffffffffu, ok);
-      if (ok) blocks[n + __popc(m & ((1u << lane) - 1u))] = b;
-      n += __popc(m);
-    }
-    if (lane == 0) n_blocks = n;
-  }
-  __syncthreads();
-  const int nblk = n_blocks;
+  // The list's valid entries are a prefix (block 0, the kk blocks, the newest
+  // block; -1 after them), so this CTA's slice needs no compaction: every
+  // thread knows its length and reads its entries straight from sel_keys.
+  const int lo = rank * a.bps, hi = min(a.k_total, lo + a.bps);
+  const int n_valid = keep0 + kk + (forced >= 0 ? 1 : 0);
+  const int nblk = max(0, min(hi, n_valid) - lo);
 
   // ---------------------------------------------------------------- 3. attention
   const int g = lane >> 2, c = lane & 3;
@@ -419,7 +407,9 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
       for (int i = 0; i < nblk; ++i) {
         const int slot = i % kStages;
         if (i >= kStages && !mbar_wait(&empty[slot], ((i / kStages) - 1) & 1, a.status, kIdDecode)) break;
-        const int64_t row = kv.block_row(s, h, blocks[i], a.status, kIdDecode);
+        const int32_t b = slice_at(lo + i);
+        if (b >= nb) set_status(a.status, MSA_ERR_DEVICE_BOUNDS, kIdDecode);  // its keys are masked below
+        const int64_t row = b < nb ? kv.block_row(s, h, b, a.status, kIdDecode) : -1;
         const int32_t y = static_cast<int32_t>(row < 0 ? 0 : row);
         uint8_t* dst = ring + slot * kStStage;
         mbar_arrive_expect_tx(&full[slot], kStStage);
@@ -456,7 +446,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
         ldsm_x4(kbase + (kk2 >> 2) * 8192 + swz128(krow, (kk2 & 3) * 2 + kchunk), a0, a1, a2, a3);
         mma_bf16(sacc, a0, a1, a2, a3, qb[kk2][0], qb[kk2][1]);
       }
-      const int64_t tok = static_cast<int64_t>(blocks[i]) * kBlock + 16 * wq + g;
+      const int64_t tok = static_cast<int64_t>(slice_at(lo + i)) * kBlock + 16 * wq + g;
       const bool v0 = tok < len, v1 = tok + 8 < len;
       const float s0 = v0 ? sacc[0] * a.scale_log2 : -INFINITY;
       const float s1 = v0 ? sacc[1] * a.scale_log2 : -INFINITY;
