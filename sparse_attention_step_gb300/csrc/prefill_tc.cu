@@ -420,25 +420,47 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     ok = __all_sync(0xffffffffu, ok && wait_or_abort(&st.o_final[t], 0, abort, a.status));
     tc::fence_after();
     const float inv = (L > 0.f) ? 1.f / L : 0.f;
-    __nv_bfloat16* dst = a.out + (tq * a.hq + head) * kHeadDim + 64 * hf;
+    // O / l in bf16 goes through the tile's half of the Q buffer (idle: every
+    // MMA has completed), one 256-byte row per score row with its 16-byte
+    // chunks XOR-swizzled by the row, so that the global stores below are
+    // whole 512-byte runs instead of one 16-byte piece per row
+    uint8_t* ob = qs + t * 32768;
 #pragma unroll 1
     for (int cc = 0; cc < 2; ++cc) {
       uint32_t o[32];
       tc::ld32(tmem + lane_base + 256 + t * 128 + 64 * hf + cc * 32, o);
       tc::wait_ld();
-      if (live) {
-        if (nblk == 0 || !ok) {
+      if (nblk == 0 || !ok) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = 0u;
-        }
+        for (int j = 0; j < 32; ++j) o[j] = 0u;
+      }
 #pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-          uint4 v;
-          v.x = pack_bf16(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv);
-          v.y = pack_bf16(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
-          v.z = pack_bf16(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv);
-          v.w = pack_bf16(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv);
-          *reinterpret_cast<uint4*>(dst + cc * 32 + j) = v;
+      for (int j = 0; j < 32; j += 8) {
+        uint4 v;
+        v.x = pack_bf16(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv);
+        v.y = pack_bf16(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
+        v.z = pack_bf16(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv);
+        v.w = pack_bf16(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv);
+        const int c = 8 * hf + 4 * cc + j / 8;  // 16-byte chunk of the row
+        *reinterpret_cast<uint4*>(ob + r * 256 + ((c ^ (r & 7)) << 4)) = v;
+      }
+    }
+    named_bar_sync(bar_id, 256);
+    {
+      // warp w of the tile stores tokens 2w and 2w + 1 of the tile: a token's
+      // 8 heads are 2 KB contiguous in the output, 512 bytes per instruction
+      const int wt = warp & 7;
+#pragma unroll 1
+      for (int jj = 0; jj < 2; ++jj) {
+        const int j = 2 * wt + jj;
+        const int64_t tlj = a.batch.tile_row0(seq, tile) + rh * (kTcTiles * 16) + 16 * t + j;
+        if (tlj < 0 || tlj >= a.batch.q_cnt[seq]) continue;
+        uint4* gdst = reinterpret_cast<uint4*>(a.out + ((a.batch.q_off[seq] + tlj) * a.hq + h * 8) * kHeadDim);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const int qq = 32 * p + lane;  // 16-byte chunk of the token's 2 KB
+          const int row = 8 * j + (qq >> 4), c = qq & 15;
+          gdst[qq] = *reinterpret_cast<const uint4*>(ob + row * 256 + ((c ^ (row & 7)) << 4));
         }
       }
     }
