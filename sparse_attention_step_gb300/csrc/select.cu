@@ -666,6 +666,56 @@ __global__ void __launch_bounds__(kTopk64Threads) topk64_kernel(const float* __r
   write_selection(top, max(k, 0), forced, keep0, a.k_total, idx_out + unit * a.k_total, sorted_blocks);
 }
 
+// The k best of n distinct keys through a sampled lower bound: the k-th
+// largest of ns sample keys (each the largest of a group of the keys, so
+// real keys) bounds the k-th best key from below; the keys at or above it
+// (the survivors, a few more than k) are ranked by counting. Returns false,
+// the same in every thread, when fewer than k samples are nonzero or more
+// than 256 keys survive; the caller then selects otherwise. Every thread of
+// the CTA calls this after writing the samples.
+__device__ inline bool sampled_top(const uint64_t* keys, int n, int k, const uint64_t* smp, int ns, uint64_t* surv,
+                                   uint64_t* top, uint64_t* lb, int* n_surv) {
+  const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31;
+  if (tid == 0) {
+    *lb = 0ull;
+    *n_surv = 0;
+  }
+  __syncthreads();
+  if (tid < ns) {
+    const uint64_t v = smp[tid];
+    int gt = 0, ge = 0;
+    for (int j = 0; j < ns; ++j) {
+      gt += smp[j] > v ? 1 : 0;
+      ge += smp[j] >= v ? 1 : 0;
+    }
+    if (v != 0ull && gt < k && k <= ge) *lb = v;
+  }
+  __syncthreads();
+  const uint64_t L = *lb;
+  if (L == 0ull) return false;
+  for (int base = 0; base < n; base += nth) {
+    const int i = base + tid;
+    const bool hit = i < n && keys[i] >= L;
+    const unsigned mk = __ballot_sync(0xffffffffu, hit);
+    int slot = 0;
+    if (lane == 0 && mk != 0u) slot = atomicAdd(n_surv, __popc(mk));
+    slot = __shfl_sync(0xffffffffu, slot, 0);
+    const int pos = slot + __popc(mk & ((1u << lane) - 1u));
+    if (hit && pos < 256) surv[pos] = keys[i];
+  }
+  __syncthreads();
+  const int m = *n_surv;
+  if (m > 256) return false;
+  for (int i = tid; i < m; i += nth) {
+    const uint64_t x = surv[i];
+    int gt = 0;
+    for (int j = 0; j < m; ++j) gt += surv[j] > x ? 1 : 0;
+    if (gt < k) top[gt] = x;
+  }
+  __syncthreads();
+  return true;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* __restrict__ q,
                                                                    const T* __restrict__ pooled, KvView kv,
@@ -751,12 +801,18 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
   }
   __syncthreads();
 
-  auto emit = [&](int i, float part, bool ok) {  // row i of the chunk
+  auto emit = [&](int i, float part, bool ok) -> uint64_t {  // row i of the chunk
     const int64_t b = r0 + i;
     ok = ok && !(skip && b == 0);
-    keys[i] = ok ? sel_key(part, static_cast<int>(b)) : 0ull;
+    const uint64_t key = ok ? sel_key(part, static_cast<int>(b)) : 0ull;
+    keys[i] = key;
     if (a.scores_out != nullptr) a.scores_out[unit * a.max_blocks + b] = ok ? part : -INFINITY;
+    return key;
   };
+  // bf16: each scoring lane's largest key of its even and of its odd stages,
+  // 64 samples for the sampled bound of the chunk's top-k
+  __shared__ uint64_t smp[64];
+  uint64_t smax0 = 0ull, smax1 = 0ull;
   if constexpr (sizeof(T) == 2) {
     // bf16: every compute thread gathers 16-byte pieces of the stage's 64
     // summary rows with cp.async (contiguous or one row per page alike) into
@@ -834,7 +890,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
             const int i = base + 16 * warp + g + 8 * hh;
             if (i < rows) {
               const bool ok = kv.layout == MSA_KV_CONTIGUOUS || pages[i] >= 0;
-              emit(i, sacc[2 * hh] + sacc[2 * hh + 1], ok);
+              const uint64_t kx = emit(i, sacc[2 * hh] + sacc[2 * hh + 1], ok);
+              if (st & 1) smax1 = kx > smax1 ? kx : smax1;
+              else smax0 = kx > smax0 ? kx : smax0;
             }
           }
         }
@@ -922,7 +980,19 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
   const int kk = static_cast<int>(n_cand - skip < a.k_scored ? n_cand - skip : static_cast<int64_t>(a.k_scored));
   int32_t* out = idx_out + unit * a.k_total;
   const int kk_local = min(kk, rows - (c == 0 ? skip : 0));
-  if (kk_local > 0) choose_top(keys, rows, kk_local, ring, top, scr, &count);
+  if (kk_local > 0) {
+    bool done = false;
+    if constexpr (sizeof(T) == 2) {
+      __shared__ uint64_t s_lb;
+      __shared__ int s_nsurv;
+      if (warp < 4 && (lane & 3) == 0) {
+        smp[2 * (8 * warp + (lane >> 2))] = smax0;
+        smp[2 * (8 * warp + (lane >> 2)) + 1] = smax1;
+      }
+      done = sampled_top(keys, rows, kk_local, smp, 64, reinterpret_cast<uint64_t*>(ring), top, &s_lb, &s_nsurv);
+    }
+    if (!done) choose_top(keys, rows, kk_local, ring, top, scr, &count);
+  }
   if (my_chunks == 1) {
     write_selection(top, kk, forced, keep0, a.k_total, out, sorted_blocks);
     return;
