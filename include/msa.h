@@ -43,9 +43,10 @@
  *   KV contiguous  k, v: [batch, num_kv_heads, max_tokens, 128]
  *   KV paged       k, v: [num_pages, num_kv_heads, 64, 128], page_table
  *                  [batch, max_pages_per_seq] int32 (logical block -> page)
- *   pooled keys (same dtype as KV):
+ *   pooled keys (same dtype as KV), per (sequence, KV head) in logical block
+ *   order for both cache layouts, so a unit's candidates are one run of rows:
  *     contiguous   [batch, num_kv_heads, max_tokens/64, 128]
- *     paged        [num_pages, num_kv_heads, 128]  (one summary per page)
+ *     paged        [batch, num_kv_heads, max_pages_per_seq, 128]
  *   Query head j belongs to KV head j / G, G = num_q_heads / num_kv_heads.
  */
 #ifndef MSA_H_
@@ -146,7 +147,9 @@ msa_status msa_workspace_init(void* ws, size_t bytes, msa_stream_t stream);
  * fp32 sum in row order, one multiply by 1/64, rounded to nearest even into
  * the KV dtype. Partial blocks are left untouched. Bad page ids set
  * MSA_ERR_DEVICE_BOUNDS in the status word when `ws` is given (ws may be NULL:
- * then bad pages are skipped silently). */
+ * then bad pages are skipped silently); a skipped block's summary is not
+ * written, the selection scores whatever that row holds, and the attention
+ * reports the page again when the block is selected. */
 msa_status msa_pool_block_keys(const msa_kv_desc* kv /* host */, int64_t first_block, int64_t n_blocks,
                                void* pooled, void* ws, size_t ws_bytes, msa_stream_t stream);
 
@@ -201,8 +204,8 @@ msa_status msa_select_topk_blocks(const void* q, int32_t num_q_heads, int32_t n_
  * gets, for global tile
  * tile_off[s] + j, exactly what msa_select_topk_blocks (q_tile 64, q_start =
  * q_starts[s]) gives for tile j of sequence s alone, scored against sequence
- * s's summaries (pooled [batch, Hkv, max_blocks, 128] contiguous, or the
- * cache's pages; in token-max mode the index-key cache). cfg->q_tile must be
+ * s's summaries (pooled [batch, Hkv, max_blocks, 128]; in token-max mode the
+ * index-key cache). cfg->q_tile must be
  * 64 (cfg->q_start is ignored); fp32 caches take one sequence only
  * (MSA_ERR_UNSUPPORTED above). A batch with no new tokens queues nothing. */
 msa_status msa_select_topk_blocks_varlen(const void* q, int32_t num_q_heads, int32_t n_seqs,
@@ -255,9 +258,10 @@ msa_status msa_sparse_attn_prefill_varlen(const void* q, int32_t num_q_heads, in
 /* One whole decode step (guide §1, Step 1 then Step 2): the index lists of
  * msa_select_topk_blocks (decode, cfg->q_tile == 1) written to idx_out, and
  * the attention of msa_sparse_attn_decode over them written to out / lse,
- * with the same results. For a contiguous bf16 cache with k_scored <= 64 it
- * runs as one kernel: one thread-block cluster per (sequence, KV head) scores
- * the summaries, selects and attends, exchanging the lists and the partial
+ * with the same results. For a bf16 cache with k_scored <= 64 it runs as one
+ * kernel (for a paged cache, when the step's grid fits one wave of the
+ * device): one thread-block cluster per (sequence, KV head) scores the
+ * summaries, selects and attends, exchanging the lists and the partial
  * results through distributed shared memory (nothing round-trips through the
  * workspace); otherwise it launches the two kernels in turn. ws must hold
  * msa_workspace_size(MSA_OP_DECODE_STEP, ...) bytes. */

@@ -561,11 +561,14 @@ msa_status decode_step_common(const void* q, int32_t num_q_heads, const void* po
   if ((st = device_info(&dev)) != MSA_OK) return st;
   int C = 0, chunk = 0, bps = 0;
   const int64_t units = static_cast<int64_t>(kv->batch) * kv->num_kv_heads;
-  const bool fused = kv->dtype == MSA_DTYPE_BF16 && kv->layout == MSA_KV_CONTIGUOUS &&
-                     cfg->mode == MSA_SCORE_MEAN_POOLED_KEYS && cfg->k_scored >= 0 &&
+  // A paged cache takes the fused step only when its grid is one wave (a
+  // ragged batch of long and short sequences is left to the chunked selection,
+  // which sizes its pieces per sequence).
+  const bool fused = kv->dtype == MSA_DTYPE_BF16 && cfg->mode == MSA_SCORE_MEAN_POOLED_KEYS && cfg->k_scored >= 0 &&
                      k_total >= std::min<int64_t>(cfg->k_scored, kv_max_blocks(kv)) + forced_count(cfg) &&
                      step_shape(units, kv_max_blocks(kv), cfg->k_scored, k_total, dev->num_sms, dev->step_clusters, &C,
-                                &chunk, &bps);
+                                &chunk, &bps) &&
+                     (kv->layout == MSA_KV_CONTIGUOUS || units * C <= 2LL * dev->num_sms);
   if (!fused) {
     // the same step as two launches (plus the pooling of just-filled blocks)
     st = msa_select_topk_blocks(q, num_q_heads, 1, pooled, kv, cfg, idx_out, k_total, nullptr, ws, ws_bytes, stream);

@@ -325,11 +325,11 @@ struct KvView {
     int32_t p = page(s, b, status, where);
     return p < 0 ? -1 : (static_cast<int64_t>(p) * hkv + h) * kBlock;
   }
-  // Row of the pooled summary key of block b of (s, h), or -1 for a bad page.
-  __device__ int64_t pooled_row(int s, int h, int64_t b, int32_t* status, int where) const {
-    if (layout == MSA_KV_CONTIGUOUS) return (static_cast<int64_t>(s) * hkv + h) * (max_tokens / kBlock) + b;
-    int32_t p = page(s, b, status, where);
-    return p < 0 ? -1 : static_cast<int64_t>(p) * hkv + h;
+  // Row of the pooled summary key of block b of (s, h). Summaries are kept per
+  // (sequence, KV head) in logical block order for both cache layouts, so a
+  // unit's candidates are one contiguous run of rows.
+  __device__ int64_t pooled_row(int s, int h, int64_t b) const {
+    return (static_cast<int64_t>(s) * hkv + h) * max_blocks() + b;
   }
   __host__ __device__ int64_t max_blocks() const {
     return layout == MSA_KV_CONTIGUOUS ? max_tokens / kBlock : static_cast<int64_t>(max_pages);

@@ -77,8 +77,8 @@ __global__ void __launch_bounds__(kPoolThreads) pool_block_keys_kernel(const T* 
   }
   if ((b + 1) * kBlock > len) return;  // partial or absent block: not pooled
   const int64_t row = kv.block_row(s, h, b, status, kIdPool);
-  const int64_t prow = kv.pooled_row(s, h, b, status, kIdPool);
-  if (row < 0 || prow < 0) return;
+  const int64_t prow = kv.pooled_row(s, h, b);
+  if (row < 0) return;  // bad page: reported, its summary not written
   const T* src = k + row * kHeadDim + 8 * e;
   float acc[8];
 #pragma unroll
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kPoolThreads) pool_block_keys_kernel(const T* 
 template <typename T>
 cudaError_t launch_pool(const T* k, const KvView& kv, int batch, int64_t first_block, int64_t n_blocks,
                         T* pooled, int32_t* status, cudaStream_t stream) {
-  int64_t span = kv.layout == MSA_KV_CONTIGUOUS ? kv.max_tokens / kBlock : kv.max_pages;
+  int64_t span = kv.max_blocks();
   span -= first_block;
   if (n_blocks >= 0 && n_blocks < span) span = n_blocks;
   if (span <= 0) return cudaSuccess;

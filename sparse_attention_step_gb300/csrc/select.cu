@@ -208,12 +208,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const T* __restric
       const int64_t b = r0 + u * kRowsPerIter + hw;
       have[u] = b < n_max && b < row_end;
       if (have[u]) {
-        const int64_t prow = kv.pooled_row(seq, h, b, status, kIdScore);
-        if (prow < 0) {
-          have[u] = false;
-        } else {
-          kp[u].load(pooled + prow * kHeadDim + 8 * e);
-        }
+        kp[u].load(pooled + kv.pooled_row(seq, h, b) * kHeadDim + 8 * e);
       }
     }
 #pragma unroll
@@ -251,7 +246,6 @@ __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __r
                                                                 KvView kv, ScoreArgs a, const PrefillBatch pb,
                                                                 float* __restrict__ scores, int32_t* status) {
   __shared__ __align__(1024) uint8_t rows_s[kPsRows * kHeadDim * 2];
-  __shared__ uint8_t bad[kPsRows];  // rows whose page id is out of range
   const int h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // 8 tiles of one sequence: global tiles t0 .. t_end - 1, local tiles j0 ..
   const int seq = pb.seq_of_group(blockIdx.z);
@@ -270,15 +264,9 @@ __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __r
     const int j = tid + 256 * u;
     const int row = j >> 4, pc = j & 15;
     const int64_t b = chunk0 + row;
-    bool miss = false;
-    if (b < n_max && b < row_end) {
-      const int64_t prow = kv.pooled_row(seq, h, b, pc == 0 ? status : nullptr, kIdScore);
-      miss = prow < 0;
-      if (!miss)
-        cp_async16(rows_s + (pc >> 3) * (kPsRows * 128) + row * 128 + (((pc & 7) ^ (row & 7)) << 4),
-                   pooled + prow * kHeadDim + 8 * pc);
-    }
-    if (pc == 0) bad[row] = miss ? 1 : 0;
+    if (b < n_max && b < row_end)
+      cp_async16(rows_s + (pc >> 3) * (kPsRows * 128) + row * 128 + (((pc & 7) ^ (row & 7)) << 4),
+                 pooled + kv.pooled_row(seq, h, b) * kHeadDim + 8 * pc);
   }
   cp_async_commit();
   // B operands: column g = tile t0 + g
@@ -318,7 +306,7 @@ __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __r
     const int tile = t0 + 2 * c + (k & 1);
     if (b < row_end && tile < t_end) {
       const int64_t n_cand = diag0 + (tile - t0);
-      const bool ok = b < n_cand && !bad[b - chunk0];
+      const bool ok = b < n_cand;
       scores[(static_cast<int64_t>(tile) * a.hkv + h) * a.max_blocks + b] = ok ? hi[k] + lo[k] : -INFINITY;
     }
   }
@@ -553,11 +541,12 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
 
 // ---------------------------------------------------------------------------
 // Fused decode selection (k_scored <= 64). One CTA handles a chunk of a
-// unit's candidate blocks: a producer warp streams the chunk's summary rows
-// into a shared-memory ring with bulk copies (one 16 KB copy per 64 rows for a
-// contiguous cache, one 256-byte copy per row for a paged one); eight warps
-// score them (a half-warp per row) into 64-bit selection keys; block_topk
-// keeps the chunk's best. A unit spread over several chunks posts the chunk
+// unit's candidate blocks, whose summary rows are one contiguous run for
+// either cache layout: bf16 rows are copied into a swizzled shared-memory ring
+// by cp.async and scored on the tensor cores, fp32 rows are streamed by a
+// producer warp with one bulk copy per stage and scored by a half-warp per
+// row; the scores become 64-bit selection keys and the chunk's best are kept
+// (a sampled lower bound for bf16, the binned selection otherwise). A unit spread over several chunks posts the chunk
 // lists and its last CTA to finish (atomic ticket) selects among them.
 // grid (Hkv, batch, n_chunks); chunks past a sequence's candidates exit at
 // once and take no ticket.
@@ -726,7 +715,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
   extern __shared__ __align__(128) uint8_t sel_raw[];
   uint8_t* ring = sel_raw;                                                   // kSelStages x 16 KB
   uint64_t* keys = reinterpret_cast<uint64_t*>(sel_raw + kSelStages * kSelStageBytes);  // [max(chunk, 2048)]
-  int32_t* pages = reinterpret_cast<int32_t*>(keys + max(a.chunk, 2048));  // [chunk] page ids (paged caches)
   __shared__ uint64_t full[kSelStages], empty[kSelStages];
   __shared__ uint64_t top[64];
   __shared__ SelectScratch scr;
@@ -767,36 +755,14 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
     }
     fence_mbar_init();
   }
-  // bf16: the group's query rows are loaded now and summed once the page ids
-  // are in, so the two latencies overlap
+  // bf16: the group's query rows are loaded now and summed after the set-up
+  // barrier
   float xq[kMaxGroupHeads];
   if constexpr (sizeof(T) == 2) {
     if (tid < kHeadDim) {
       const T* qg = q + (static_cast<int64_t>(s) * a.hq + h * grp) * kHeadDim + tid;
 #pragma unroll
       for (int g = 0; g < kMaxGroupHeads; ++g) xq[g] = g < grp ? __bfloat162float(qg[g * kHeadDim]) : 0.f;
-    }
-  }
-  if (kv.layout == MSA_KV_PAGED) {
-    // the chunk's page ids, eight loads in flight per thread before any check
-    const int32_t* pt = kv.page_table + static_cast<int64_t>(s) * kv.max_pages + r0;
-    for (int b0 = 0; b0 < rows; b0 += 8 * kSelThreads) {
-      int32_t v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = b0 + u * kSelThreads + tid;
-        v[u] = i < rows ? pt[i] : 0;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = b0 + u * kSelThreads + tid;
-        if (i >= rows) continue;
-        if (v[u] < 0 || v[u] >= kv.num_pages) {
-          set_status(status, MSA_ERR_DEVICE_BOUNDS, kIdScore);
-          v[u] = -1;
-        }
-        pages[i] = v[u];
-      }
     }
   }
   __syncthreads();
@@ -815,7 +781,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
   uint64_t smax0 = 0ull, smax1 = 0ull;
   if constexpr (sizeof(T) == 2) {
     // bf16: every compute thread gathers 16-byte pieces of the stage's 64
-    // summary rows with cp.async (contiguous or one row per page alike) into
+    // summary rows (one contiguous run per unit, either cache layout) with cp.async into
     // a 4-stage ring, 128-byte swizzled as [64-dim half][row][128 B]; warps
     // 0-3 score 16 rows each on the tensor cores with the index query split
     // into a bf16 head and remainder (as in the fused step).
@@ -839,15 +805,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
           const int row = j >> 4, pc = j & 15;
           const int i = base + row;
           if (i >= rows) continue;
-          int64_t grow;
-          if (kv.layout == MSA_KV_CONTIGUOUS) {
-            grow = contig0 + i;
-          } else {
-            if (pages[i] < 0) continue;
-            grow = static_cast<int64_t>(pages[i]) * a.hkv + h;
-          }
           cp_async16(stage + (pc >> 3) * (kRows * 128) + row * 128 + (((pc & 7) ^ (row & 7)) << 4),
-                     pooled + grow * kHeadDim + 8 * pc);
+                     pooled + (contig0 + i) * kHeadDim + 8 * pc);
         }
       }
       cp_async_commit();
@@ -889,8 +848,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
           for (int hh = 0; hh < 2; ++hh) {
             const int i = base + 16 * warp + g + 8 * hh;
             if (i < rows) {
-              const bool ok = kv.layout == MSA_KV_CONTIGUOUS || pages[i] >= 0;
-              const uint64_t kx = emit(i, sacc[2 * hh] + sacc[2 * hh + 1], ok);
+              const uint64_t kx = emit(i, sacc[2 * hh] + sacc[2 * hh + 1], true);
               if (st & 1) smax1 = kx > smax1 ? kx : smax1;
               else smax0 = kx > smax0 ? kx : smax0;
             }
@@ -912,17 +870,16 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
       for (int i = 0; i < 8; ++i) qi[i] += x[i];
     }
   }
-  if (kv.layout == MSA_KV_CONTIGUOUS) {
+  {
     if (warp == kSelWarps) {
-      // ---------------- producer: one bulk copy per 64-row stage ----------------
+      // ---------------- producer: one bulk copy per stage ----------------
       if (lane == 0) {
         for (int st = 0; st < n_stages; ++st) {
           const int slot = st % kSelStages;
           if (st >= kSelStages && !mbar_wait(&empty[slot], ((st / kSelStages) - 1) & 1, status, kIdScore)) break;
           const int base = st * kStageRows;
           const int n = min(kStageRows, rows - base);
-          const T* src = pooled + ((static_cast<int64_t>(s) * a.hkv + h) * (kv.max_tokens / kBlock) + r0 + base) *
-                                      kHeadDim;
+          const T* src = pooled + ((static_cast<int64_t>(s) * a.hkv + h) * a.max_blocks + r0 + base) * kHeadDim;
           mbar_arrive_expect_tx(&full[slot], n * kRowBytes);
           bulk_load(ring + slot * kSelStageBytes, src, n * kRowBytes, &full[slot]);
         }
@@ -947,30 +904,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
-      }
-    }
-  } else if (warp < kSelWarps) {
-    // paged: summary rows are scattered one per page; direct 16-byte loads,
-    // 8 rows in flight per thread
-    constexpr int kRowsPerPass = 8 * (kSelWarps * 2);
-    for (int p0 = 0; p0 < rows; p0 += kRowsPerPass) {
-      RawRow<T> kp[8];
-      bool have[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = p0 + u * (kSelWarps * 2) + hw;
-        have[u] = i < rows && pages[i] >= 0;
-        if (have[u]) kp[u].load(pooled + (static_cast<int64_t>(pages[i]) * a.hkv + h) * kHeadDim + 8 * e);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = p0 + u * (kSelWarps * 2) + hw;
-        float part = have[u] ? kp[u].dot(qi) : 0.f;
-        part += __shfl_xor_sync(0xffffffffu, part, 8);
-        part += __shfl_xor_sync(0xffffffffu, part, 4);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        if (e == 0 && i < rows) emit(i, part, have[u]);
       }
     }
   }
@@ -1033,8 +966,7 @@ void select_decode_shape(int64_t max_blocks, int64_t units, int num_sms, int* ch
 
 size_t select_decode_smem(int chunk) {
   const int n = chunk > 2048 ? chunk : 2048;
-  return static_cast<size_t>(kSelStages) * kSelStageBytes + static_cast<size_t>(n) * sizeof(uint64_t) +
-         static_cast<size_t>(chunk) * sizeof(int32_t);
+  return static_cast<size_t>(kSelStages) * kSelStageBytes + static_cast<size_t>(n) * sizeof(uint64_t);
 }
 
 size_t select_decode_cand_bytes(int64_t units, int n_chunks) {

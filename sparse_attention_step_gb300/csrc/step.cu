@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   const int rank = blockIdx.x, C = gridDim.x, h = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t unit = static_cast<int64_t>(s) * a.hkv + h;
-  const int64_t max_blocks = kv.max_tokens / kBlock;
+  const int64_t max_blocks = kv.max_blocks();  // summary rows per unit
 
   // The producer sets up the ring and, as soon as the inputs are ready, starts
   // streaming the first stages of its chunk: their rows do not depend on the

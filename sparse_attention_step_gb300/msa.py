@@ -325,6 +325,6 @@ class Workspace:
 
 
 def pooled_shape(desc: KvDesc) -> tuple:
-    if desc.layout == MSA_KV_CONTIGUOUS:
-        return (desc.batch, desc.num_kv_heads, desc.max_tokens // 64, desc.head_dim)
-    return (desc.num_pages, desc.num_kv_heads, desc.head_dim)
+    """Summary keys: one row per (sequence, KV head, logical block), either cache layout."""
+    blocks = desc.max_tokens // 64 if desc.layout == MSA_KV_CONTIGUOUS else desc.max_pages_per_seq
+    return (desc.batch, desc.num_kv_heads, blocks, desc.head_dim)

@@ -59,11 +59,7 @@ def run_decode(inp, k_scored, k_total, force_local=True, want_scores=True, dense
 
 def gpu_pooled_rows(inp, res, s, h):
     n = inp.lens[s] // 64
-    p = res["pooled"]
-    if inp.layout == "contiguous":
-        return to64(p[s, h, :n])
-    pages = inp.page_table[s, :n].long()
-    return to64(p[pages, h])
+    return to64(res["pooled"][s, h, :n])
 
 
 def verify_units(inp, res, units, k_scored, k_total, force_local=True, stats=None, check_dense=False,
@@ -345,6 +341,20 @@ def run_step(inp, k_scored, k_total, force_local=True):
 ])
 def test_fused_step_small(dev, lens, hkv, hq, k_scored, k_total):
     inp = make_decode_inputs(lens, hkv, hq, "bf16", "contiguous", needles=3, seed=sum(lens) % 997, device=dev)
+    res = run_step(inp, k_scored, k_total)
+    assert res["status"] == 0
+    verify_units(inp, res, all_units(inp), k_scored, k_total)
+
+
+@pytest.mark.parametrize("lens,hkv,hq,k_scored,k_total", [
+    ([64 * 300 + 5, 64 * 77, 64 * 1024], 2, 16, 47, 48),   # few units: clusters of 16
+    ([64 * 200 + 33] * 20, 4, 32, 31, 32),                  # 80 units: clusters of 2
+    ([64 * 12, 10, 64], 2, 4, 5, 6),                        # tiny and partial sequences, G = 2
+])
+def test_fused_step_paged(dev, lens, hkv, hq, k_scored, k_total):
+    """The fused step on a paged cache (shuffled page table): the summaries are
+    per sequence, the K/V blocks are gathered through the page table."""
+    inp = make_decode_inputs(lens, hkv, hq, "bf16", "paged", needles=3, seed=sum(lens) % 991, device=dev)
     res = run_step(inp, k_scored, k_total)
     assert res["status"] == 0
     verify_units(inp, res, all_units(inp), k_scored, k_total)

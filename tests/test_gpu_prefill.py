@@ -56,9 +56,7 @@ def run_prefill(inp, k_scored, k_total, dense=False, sparse=True):
 
 
 def gpu_pooled_head(inp, res, h, n_full):
-    if inp.layout == "contiguous":
-        return to64(res["pooled"][0, h, :n_full])
-    return to64(res["pooled"][inp.page_table[0, :n_full].long(), h])
+    return to64(res["pooled"][0, h, :n_full])
 
 
 def verify_tiles(inp, res, tiles, heads, k_scored, k_total, rows_per_tile=None, stats=None, check_dense=False,

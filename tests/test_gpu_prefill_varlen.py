@@ -57,10 +57,9 @@ def run_single(inp, s, pooled, k_scored, k_total):
     dev = inp.q.device
     if c.layout == "contiguous":
         desc = msa.kv_desc(c.k[s:s + 1], c.v[s:s + 1], c.seq_lens[s:s + 1])
-        pool_s = pooled[s:s + 1]
     else:
         desc = msa.kv_desc(c.k, c.v, c.seq_lens[s:s + 1], c.page_table[s:s + 1])
-        pool_s = pooled
+    pool_s = pooled[s:s + 1]
     hq, hkv = c.num_q_heads, c.num_kv_heads
     n = inp.q_counts[s]
     n_tiles = msa.chunk_tiles(inp.q_starts[s], n)
@@ -88,8 +87,7 @@ def verify_against_oracle(inp, res, k_scored, k_total, rows_per_tile=7):
             kr, vr = c.kv_rows(s, h, "k").cpu(), c.kv_rows(s, h, "v").cpu()
             pooled, exact = O.pool_block_keys(kr, total, c.dtype)
             nf = total // 64
-            got_pool = res["pooled"][s, h, :nf] if c.layout == "contiguous" else \
-                res["pooled"][c.page_table[s, :nf].long(), h]
+            got_pool = res["pooled"][s, h, :nf]
             check_pooled(to64(got_pool), pooled, exact, c.dtype, to64(kr) if c.dtype == "f32" else None,
                          what=f"pooled keys seq {s} head {h}")
             for j, r0, r1 in O.prefill_tiles(q0, n):

@@ -1,8 +1,8 @@
 """GPU parity of the attention-sink selection (block 0 always kept, never
 scored, alongside the newest / diagonal block) against the CPU oracle, through
-the C ABI, on every selection path: the fused decode step, the chunked decode
-selection (paged cache), the radix top-k (k above 64, prefill tiles) and the
-token-max scores."""
+the C ABI, on every selection path: the fused decode step (contiguous and
+paged caches), the chunked decode selection, the radix top-k (k above 64,
+prefill tiles) and the token-max scores."""
 import numpy as np
 import pytest
 import torch
@@ -69,7 +69,8 @@ def run_decode_sink(inp, k_scored, k_total, step, kidx=None):
 
 @pytest.mark.parametrize("layout,k_scored,step", [
     ("contiguous", 5, True),     # fused decode step
-    ("paged", 5, True),          # chunked selection kernel + attention
+    ("paged", 5, True),          # fused decode step on a paged cache
+    ("paged", 5, False),         # chunked selection kernel + attention
     ("contiguous", 70, False),   # radix top-k (k above 64)
 ])
 def test_decode_sink(dev, layout, k_scored, step):

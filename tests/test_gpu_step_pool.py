@@ -71,16 +71,11 @@ def test_generation_loop_keeps_summaries_current(dev, layout, k_scored):
         full = _pool_full(msa, desc, inp.k, ws)
         torch.cuda.synchronize()
         filled = step == 1
-        if layout == "contiguous":
-            for s, n in enumerate(lens):
-                nbf = n // 64
-                assert torch.equal(pooled[s, :, :nbf], full[s, :, :nbf]), f"summaries differ, step {step}"
-                if filled:
-                    assert not torch.equal(pooled[s, :, nbf - 1], before[s, :, nbf - 1])
-        else:
-            for s, n in enumerate(lens):
-                pages = inp.page_table[s, :n // 64].long()
-                assert torch.equal(pooled[pages], full[pages]), f"summaries differ, step {step}"
+        for s, n in enumerate(lens):
+            nbf = n // 64
+            assert torch.equal(pooled[s, :, :nbf], full[s, :, :nbf]), f"summaries differ, step {step}"
+            if filled:
+                assert not torch.equal(pooled[s, :, nbf - 1], before[s, :, nbf - 1])
         # oracle: selection over the summaries of this length, attention over the GPU's list
         for s in range(b):
             for h in range(hkv):
