@@ -785,14 +785,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
     // a 4-stage ring, 128-byte swizzled as [64-dim half][row][128 B]; warps
     // 0-3 score 16 rows each on the tensor cores with the index query split
     // into a bf16 head and remainder (as in the fused step).
-    __shared__ float qsum[kHeadDim];
-    if (tid < kHeadDim) {
-      float acc = 0.f;
-#pragma unroll
-      for (int g = 0; g < kMaxGroupHeads; ++g) acc += xq[g];
-      qsum[tid] = acc;
-    }
-    __syncthreads();
     constexpr int kRows = kSelStageBytes / (kHeadDim * 2);  // 64 rows per stage
     const int64_t contig0 = (static_cast<int64_t>(s) * a.hkv + h) * a.max_blocks + r0;
     auto issue = [&](int st) {
@@ -811,6 +803,17 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
       }
       cp_async_commit();
     };
+    // the first stages are in flight before the index query is summed (its
+    // rows were loaded before the set-up barrier)
+    for (int st = 0; st < kSelStages - 1; ++st) issue(st);
+    __shared__ float qsum[kHeadDim];
+    if (tid < kHeadDim) {
+      float acc = 0.f;
+#pragma unroll
+      for (int g = 0; g < kMaxGroupHeads; ++g) acc += xq[g];
+      qsum[tid] = acc;
+    }
+    __syncthreads();
     const int g = lane >> 2, c = lane & 3;
     uint32_t qb[8][2];
 #pragma unroll
@@ -828,7 +831,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
     }
     const int krow = 16 * (warp & 3) + (lane & 7) + ((lane >> 3) & 1) * 8;
     const int kchunk = lane >> 4;
-    for (int st = 0; st < kSelStages - 1; ++st) issue(st);
     for (int st = 0; st < n_stages; ++st) {
       cp_async_wait<kSelStages - 2>();
       __syncthreads();  // stage st has landed for every thread; stage st - 1 is consumed
