@@ -951,7 +951,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
 }
 
 // Chunk size for the decode selection kernel: 2048 candidate rows (fewer,
-// longer CTAs amortise their fixed costs: page ids, index query, top-k),
+// longer CTAs amortise their fixed costs: index query, top-k, list merge),
 // halved down to 512 while the grid would hold fewer than two CTAs per SM,
 // then doubled while a unit would need more than 32 chunks (the last chunk of
 // a unit merges at most 32 lists of 64). Chunks past a short sequence's
