@@ -401,8 +401,7 @@ __device__ inline void digit_hist(const uint32_t* keys, int n, uint32_t prefix, 
       const uint32_t key = keys[i];
       if ((key & mask) == prefix) d = static_cast<int>((key >> shift) & dmask);
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, d);
-    if (d >= 0 && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&cnt[d], __popc(peers));
+    if (d >= 0) atomicAdd(&cnt[d], 1);
   }
   __syncthreads();
 }
@@ -443,7 +442,20 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   int32_t* out = idx_out + unit * a.k_total + (keep0 ? 1 : 0);
   uint32_t* cand = keys + a.max_blocks;
 
-  for (int i = tid; i < n; i += blockDim.x) keys[i] = float_to_key(sc[i]);
+  // eight loads in flight per thread before any store
+  for (int base = 0; base < n; base += 8 * static_cast<int>(blockDim.x)) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = base + u * blockDim.x + tid;
+      v[u] = i < n ? sc[i] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = base + u * blockDim.x + tid;
+      if (i < n) keys[i] = float_to_key(v[u]);
+    }
+  }
   if (tid == 0) n_cand_keys = 0;
   __syncthreads();
 
@@ -488,47 +500,46 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     take_equal = remaining;
   }
 
-  // Ordered compaction over contiguous per-thread ranges.
-  const int per = (n + blockDim.x - 1) / blockDim.x;
-  const int lo = min(n, tid * per);
-  const int hi = min(n, lo + per);
+  // Ordered compaction: warp w owns keys [w span, (w + 1) span) and its lanes
+  // read consecutive keys (no bank conflicts); ballots order a warp's picks,
+  // block scans over the warps' counts order the warps.
+  const int lane = tid & 31, nwarps = static_cast<int>(blockDim.x) >> 5;
+  const int span = ((n + nwarps - 1) / nwarps + 31) & ~31;
+  const int wlo = min(n, (tid >> 5) * span), whi = min(n, wlo + span);
+  const unsigned lt = (1u << lane) - 1u;
   int written = 0;
   if (k > 0) {
-    int eq_before = 0;
+    int eq_before = 0;  // keys equal to thresh in the warps before this one
     if (!all) {
       int my_eq = 0;
-      for (int i = lo; i < hi; ++i) my_eq += keys[i] == thresh;
+      for (int i = wlo + lane; i < whi; i += 32) my_eq += keys[i] == thresh ? 1 : 0;
+      my_eq = __reduce_add_sync(0xffffffffu, my_eq);
       int tot;
-      eq_before = block_inclusive_scan(my_eq, scan_tmp, &tot) - my_eq;
+      const int v = lane == 0 ? my_eq : 0;
+      eq_before = __shfl_sync(0xffffffffu, block_inclusive_scan(v, scan_tmp, &tot) - v, 0);
     }
-    int my_sel = 0;
-    {
-      int eq = eq_before;
-      for (int i = lo; i < hi; ++i) {
-        if (all) {
-          ++my_sel;
-        } else {
-          const uint32_t key = keys[i];
-          if (key > thresh) ++my_sel;
-          else if (key == thresh && eq++ < take_equal) ++my_sel;
-        }
+    // keep: above thresh, or equal to it and among the first take_equal such
+    // keys in block order
+    auto pass = [&](bool write, int pos) {
+      int eq = eq_before, nsel = 0;
+      for (int base = wlo; base < whi; base += 32) {
+        const int i = base + lane;
+        const uint32_t key = i < whi ? keys[i] : 0u;
+        const bool is_eq = !all && i < whi && key == thresh;
+        const unsigned me = __ballot_sync(0xffffffffu, is_eq);
+        const bool keep = i < whi && (all || key > thresh || (is_eq && eq + __popc(me & lt) < take_equal));
+        const unsigned mk = __ballot_sync(0xffffffffu, keep);
+        if (write && keep) out[pos + nsel + __popc(mk & lt)] = static_cast<int32_t>(i + skip);
+        nsel += __popc(mk);
+        eq += __popc(me);
       }
-    }
+      return nsel;
+    };
+    const int nsel = pass(false, 0);
     int tot;
-    int pos = block_inclusive_scan(my_sel, scan_tmp, &tot) - my_sel;
-    {
-      int eq = eq_before;
-      for (int i = lo; i < hi; ++i) {
-        bool keep;
-        if (all) {
-          keep = true;
-        } else {
-          const uint32_t key = keys[i];
-          keep = key > thresh || (key == thresh && eq++ < take_equal);
-        }
-        if (keep) out[pos++] = static_cast<int32_t>(i + skip);
-      }
-    }
+    const int v = lane == 0 ? nsel : 0;
+    const int pos = __shfl_sync(0xffffffffu, block_inclusive_scan(v, scan_tmp, &tot) - v, 0);
+    pass(true, pos);
     written = tot;
   }
   if (tid == 0) {
