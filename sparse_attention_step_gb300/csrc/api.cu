@@ -197,6 +197,10 @@ int forced_count(const msa_select_cfg* cfg) {
   return ((cfg->force_local & kForceLocal) ? 1 : 0) + ((cfg->force_local & kForceSink) ? 1 : 0);
 }
 
+// Queries and outputs move in 16-byte pieces (vector loads and stores,
+// cp.async, TMA), so their base addresses must be 16-byte aligned.
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
 msa_status check_q_heads(const msa_kv_desc* kv, int hq) {
   if (hq <= 0 || hq % kv->num_kv_heads != 0) return MSA_ERR_INVALID_ARG;
   if (hq / kv->num_kv_heads > 8) return MSA_ERR_UNSUPPORTED;
@@ -211,6 +215,7 @@ msa_status decode_common(const void* q, int hq, const msa_kv_desc* kv, const int
   if (q == nullptr || out == nullptr) return MSA_ERR_INVALID_ARG;
   if (idx != nullptr && k_total <= 0) return MSA_ERR_INVALID_ARG;
   if (!(scale > 0.f)) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out)) return MSA_ERR_INVALID_ARG;
   if (!decode_units_fit(kv)) return MSA_ERR_UNSUPPORTED;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != MSA_OK) return st;
@@ -275,6 +280,7 @@ msa_status prefill_common(const void* q, int hq, const PrefillBatch& pb, int64_t
   if (idx != nullptr && k_total <= 0) return MSA_ERR_INVALID_ARG;
   if (!(scale > 0.f)) return MSA_ERR_INVALID_ARG;
   if (kv->dtype != MSA_DTYPE_BF16) return MSA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(out)) return MSA_ERR_INVALID_ARG;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != MSA_OK) return st;
   if ((st = check_ws(ws, ws_bytes, kWsHeader)) != MSA_OK) return st;
@@ -383,6 +389,7 @@ msa_status check_select(const void* q, int32_t num_q_heads, const void* pooled, 
     return MSA_ERR_INVALID_ARG;
   if (cfg->force_local < 0 || cfg->force_local > (kForceLocal | kForceSink)) return MSA_ERR_INVALID_ARG;
   if (cfg->q_tile != 1 && cfg->q_tile != kBlock) return MSA_ERR_UNSUPPORTED;
+  if (!aligned16(q)) return MSA_ERR_INVALID_ARG;
   return MSA_OK;
 }
 // The failure-detection path on the device, exercised on purpose: one warp
@@ -557,6 +564,7 @@ msa_status decode_step_common(const void* q, int32_t num_q_heads, const void* po
   if ((st = check_q_heads(kv, num_q_heads)) != MSA_OK) return st;
   if (cfg->q_tile != 1) return MSA_ERR_UNSUPPORTED;
   if (!(scale > 0.f)) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out)) return MSA_ERR_INVALID_ARG;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != MSA_OK) return st;
   int C = 0, chunk = 0, bps = 0;
@@ -692,6 +700,7 @@ extern "C" msa_status msa_sparse_attn_decode_noalloc(const void* q, int32_t num_
   if ((st = check_q_heads(kv, num_q_heads)) != MSA_OK) return st;
   if (q == nullptr || out == nullptr || idx == nullptr || k_total <= 0) return MSA_ERR_INVALID_ARG;
   if (!(scale > 0.f)) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out)) return MSA_ERR_INVALID_ARG;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != MSA_OK) return st;
   uint8_t* ws = nullptr;

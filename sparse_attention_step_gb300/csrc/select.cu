@@ -640,6 +640,7 @@ __global__ void __launch_bounds__(kTopk64Threads) topk64_kernel(const float* __r
   const int h = blockIdx.x, outer = blockIdx.y;
   const int64_t unit = static_cast<int64_t>(outer) * a.hkv + h;
   const bool local = (a.force_local & kForceLocal) != 0, sink = (a.force_local & kForceSink) != 0;
+  pdl_wait();  // the scores come from the previous kernel
   int64_t n64, forced, nb;  // candidates, the kept newest / diagonal block, blocks in view
   if (!a.prefill) {
     const int64_t len = kv.seq_len(outer, status, kIdTopk);
@@ -663,6 +664,7 @@ __global__ void __launch_bounds__(kTopk64Threads) topk64_kernel(const float* __r
   __syncthreads();
   if (k > 0 && !block_select(tk, n, k, top, scr))
     block_topk(tk, n, k, tk + a.max_blocks, top, &count);
+  pdl_trigger();  // the attention kernel may start its set-up
   write_selection(top, max(k, 0), forced, keep0, a.k_total, idx_out + unit * a.k_total, sorted_blocks);
 }
 
@@ -994,9 +996,19 @@ size_t select_decode_cand_bytes(int64_t units, int n_chunks) {
 static cudaError_t launch_topk(const float* scores, const KvView& kv, const TopkArgs& ta, int outer,
                                int32_t* idx_out, int32_t* status, cudaStream_t stream) {
   if (ta.k_scored <= 64 && ta.max_blocks <= kTopk64MaxCand) {
-    topk64_kernel<<<dim3(kv.hkv, outer), kTopk64Threads, topk64_smem(ta.max_blocks), stream>>>(scores, kv, ta,
-                                                                                             idx_out, status);
-    return cudaGetLastError();
+    // programmatic dependent launch: the CTAs may be placed while the score
+    // kernel drains; they wait for its results before reading anything
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(kv.hkv, outer, 1);
+    lc.blockDim = dim3(kTopk64Threads, 1, 1);
+    lc.dynamicSmemBytes = topk64_smem(ta.max_blocks);
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, topk64_kernel, scores, kv, ta, idx_out, status);
   }
   const size_t smem = static_cast<size_t>(ta.max_blocks + kCandCap) * sizeof(uint32_t);
   topk_kernel<<<dim3(kv.hkv, outer), topk_threads(ta.max_blocks), smem, stream>>>(scores, kv, ta, idx_out, status);

@@ -24,7 +24,6 @@ constexpr int kTmThreads = 32 * (kTmWarps + 1);
 constexpr int kTmStages = 4;
 constexpr int kTmStage = kBlock * kHeadDim * 2;  // 16 KB: one block of index keys
 constexpr int kTmMaxChunk = 64;                  // candidate blocks per CTA, at most
-constexpr int kTmCtasPerSm = 3;                  // resident CTAs per SM (65 KB of shared memory each)
 constexpr int kTmMaxHeads = 8;
 
 }  // namespace
@@ -45,9 +44,16 @@ __global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __gri
   extern __shared__ __align__(1024) uint8_t tm_raw[];
   uint8_t* ring = smem_align1024(tm_raw);
   __shared__ uint64_t full[kTmStages], empty[kTmStages];
-  __shared__ float qsum[kTmMaxHeads][kHeadDim];
-  __shared__ int32_t rowid[kTmMaxChunk];                      // first index-key row of each block, -1 = bad page
-  __shared__ float part[kTmMaxChunk][kTmWarps][kTmMaxHeads];  // per-warp block maxima
+  __shared__ int32_t rowid[kTmMaxChunk];  // first index-key row of each block, -1 = bad page
+  // The index queries are needed only until the scoring warps hold them in
+  // registers, so the per-warp block maxima reuse their space (keeping three
+  // CTAs' shared memory within one SM).
+  __shared__ union {
+    float qsum[kTmMaxHeads][kHeadDim];
+    float part[kTmMaxChunk][kTmWarps][kTmMaxHeads];
+  } sh;
+  auto& qsum = sh.qsum;
+  auto& part = sh.part;
 
   const int s = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_wait();
@@ -60,45 +66,62 @@ __global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __gri
   if (b0 >= n_cand) return;
   const int nblk = static_cast<int>(min(static_cast<int64_t>(a.chunk), n_cand - b0));
 
-  if (tid == 0) {
+  // index-key row of candidate block j of this chunk (-1: bad page, never selected)
+  auto row_of = [&](int j) -> int32_t {
+    const int64_t b = b0 + j;
+    if (kv.layout == MSA_KV_CONTIGUOUS) return static_cast<int32_t>(static_cast<int64_t>(s) * kv.max_tokens + b * kBlock);
+    const int32_t p = kv.page(s, b, a.status, kIdScore);
+    return p < 0 ? -1 : p * kBlock;
+  };
+  // The producer sets up the ring and issues the first stages at once, so
+  // they are in flight while the index query is gathered.
+  const int n_pre = min(kTmStages, nblk);
+  if (warp == kTmWarps && lane == 0) {
     for (int i = 0; i < kTmStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kTmWarps);
     }
     fence_mbar_init();
+    tma_prefetch_desc(&tmi);
+    for (int j = 0; j < n_pre; ++j) {
+      const int32_t r = row_of(j);
+      uint8_t* dst = ring + j * kTmStage;
+      mbar_arrive_expect_tx(&full[j], kTmStage);
+      tma_load_2d(dst, &tmi, 0, r < 0 ? 0 : r, &full[j]);
+      tma_load_2d(dst + kTmStage / 2, &tmi, 64, r < 0 ? 0 : r, &full[j]);
+    }
   }
-  if (tid < kTmMaxChunk) {
-    int32_t r = -1;
-    if (tid < nblk) {
-      const int64_t b = b0 + tid;
-      if (kv.layout == MSA_KV_CONTIGUOUS) {
-        r = static_cast<int32_t>(static_cast<int64_t>(s) * kv.max_tokens + b * kBlock);
-      } else {
-        const int32_t p = kv.page(s, b, a.status, kIdScore);
-        r = p < 0 ? -1 : p * kBlock;
+  if (tid < kTmMaxChunk) rowid[tid] = tid < nblk ? row_of(tid) : -1;
+  if (tid < kTmMaxHeads * 16) {
+    // group h's index query, dims [8e, 8e + 8): the group's query heads are
+    // loaded at once (16 bytes each), then summed in head order
+    const int hh = tid >> 4, e = tid & 15;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    if (hh < a.hkv) {
+      const uint4* qg = reinterpret_cast<const uint4*>(a.q + (static_cast<int64_t>(s) * a.hq + hh * a.grp) * kHeadDim) + e;
+      uint4 x[kMaxGroupHeads];
+#pragma unroll
+      for (int g = 0; g < kMaxGroupHeads; ++g) x[g] = g < a.grp ? qg[g * (kHeadDim / 8)] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int g = 0; g < kMaxGroupHeads; ++g) {
+        const uint32_t w[4] = {x[g].x, x[g].y, x[g].z, x[g].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] += __uint_as_float(w[i] << 16);
+          acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+        }
       }
     }
-    rowid[tid] = r;
-  }
-  for (int i = tid; i < kTmMaxHeads * kHeadDim; i += blockDim.x) {
-    const int h = i / kHeadDim, d = i % kHeadDim;
-    float acc = 0.f;
-    if (h < a.hkv) {
-      const __nv_bfloat16* qg = a.q + (static_cast<int64_t>(s) * a.hq + h * a.grp) * kHeadDim + d;
-      float x[kMaxGroupHeads];
 #pragma unroll
-      for (int g = 0; g < kMaxGroupHeads; ++g) x[g] = g < a.grp ? __bfloat162float(qg[g * kHeadDim]) : 0.f;
-#pragma unroll
-      for (int g = 0; g < kMaxGroupHeads; ++g) acc += x[g];
-    }
-    qsum[h][d] = acc;
+    for (int i = 0; i < 8; ++i) qsum[hh][8 * e + i] = acc[i];
   }
   __syncthreads();
 
   if (warp == kTmWarps) {
     if (lane == 0) {
-      tma_prefetch_desc(&tmi);
-      for (int j = 0; j < nblk; ++j) {
+      for (int j = n_pre; j < nblk; ++j) {
         const int slot = j % kTmStages;
         if (j >= kTmStages && !mbar_wait(&empty[slot], ((j / kTmStages) - 1) & 1, a.status, kIdScore)) break;
         const int32_t y = rowid[j] < 0 ? 0 : rowid[j];
@@ -124,6 +147,7 @@ __global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __gri
         ql[kk][hlf] = pack_bf16(x0 - h0, x1 - h1);
       }
     }
+    bar_sync_warps(1, 32 * kTmWarps);  // every scoring warp has read qsum: part may overwrite it
     const int krow = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
     const int kchunk = lane >> 4;
     for (int j = 0; j < nblk; ++j) {
@@ -404,6 +428,9 @@ cudaError_t set_token_max_smem() {
   cudaError_t e = cudaFuncSetAttribute(token_max_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(token_max_smem_bytes()));
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(token_max_score_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(token_max_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(token_max_prefill_smem_bytes()));
 }
@@ -419,17 +446,32 @@ cudaError_t launch_token_max_scores(const CUtensorMap& tmi, const KvView& kv, in
   a.max_blocks = kv.max_blocks();
   a.scores = scores;
   a.status = status;
-  // one wave: the batch's blocks spread evenly over the resident CTAs
-  int num_sms = 0, dev = 0;
+  // one wave: the batch's blocks spread evenly over the CTAs the device keeps
+  // resident at once (its SMs x the CTAs that fit one SM, asked of the runtime)
+  int num_sms = 0, dev = 0, per_sm = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t slots = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * kTmCtasPerSm;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, token_max_score_kernel, kTmThreads,
+                                                    token_max_smem_bytes()) != cudaSuccess)
+    return cudaGetLastError();
+  const int64_t slots = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * (per_sm > 0 ? per_sm : 1);
   int64_t chunk = (static_cast<int64_t>(batch) * a.max_blocks + slots - 1) / slots;
   chunk = chunk < 8 ? 8 : chunk > kTmMaxChunk ? kTmMaxChunk : chunk;
   a.chunk = static_cast<int>(chunk);
   const unsigned chunks = static_cast<unsigned>((a.max_blocks + chunk - 1) / chunk);
-  token_max_score_kernel<<<dim3(chunks, batch), kTmThreads, token_max_smem_bytes(), stream>>>(tmi, kv, a);
-  return cudaGetLastError();
+  // programmatic dependent launch: the CTAs may be placed while the previous
+  // kernel drains; they wait for it before reading anything
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(chunks, batch, 1);
+  lc.blockDim = dim3(kTmThreads, 1, 1);
+  lc.dynamicSmemBytes = token_max_smem_bytes();
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, token_max_score_kernel, tmi, kv, a);
 }
 
 }  // namespace msa

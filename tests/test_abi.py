@@ -75,40 +75,58 @@ def test_head_and_selection_arguments(lib):
     d = _desc()
     cfg = msa.select_cfg(4)
     # Hq not a multiple of Hkv
-    assert lib.msa_select_topk_blocks(0x1, 15, 1, 0x1, ctypes.byref(d), ctypes.byref(cfg), 0x1, 5, None, 0x1, 1 << 20,
+    assert lib.msa_select_topk_blocks(0x10, 15, 1, 0x1, ctypes.byref(d), ctypes.byref(cfg), 0x1, 5, None, 0x1, 1 << 20,
                                       None) == msa.MSA_ERR_INVALID_ARG
     # more than 8 query heads per KV head
-    assert lib.msa_select_topk_blocks(0x1, 32, 1, 0x1, ctypes.byref(d), ctypes.byref(cfg), 0x1, 5, None, 0x1, 1 << 20,
+    assert lib.msa_select_topk_blocks(0x10, 32, 1, 0x1, ctypes.byref(d), ctypes.byref(cfg), 0x1, 5, None, 0x1, 1 << 20,
                                       None) == msa.MSA_ERR_UNSUPPORTED
     # k_total too small for k_scored + the forced block
-    assert lib.msa_select_topk_blocks(0x1, 16, 1, 0x1, ctypes.byref(d), ctypes.byref(cfg), 0x1, 4, None, 0x1, 1 << 20,
+    assert lib.msa_select_topk_blocks(0x10, 16, 1, 0x1, ctypes.byref(d), ctypes.byref(cfg), 0x1, 4, None, 0x1, 1 << 20,
                                       None) == msa.MSA_ERR_INVALID_ARG
     bad = msa.select_cfg(4, q_tile=3)
-    assert lib.msa_select_topk_blocks(0x1, 16, 1, 0x1, ctypes.byref(d), ctypes.byref(bad), 0x1, 5, None, 0x1, 1 << 20,
+    assert lib.msa_select_topk_blocks(0x10, 16, 1, 0x1, ctypes.byref(d), ctypes.byref(bad), 0x1, 5, None, 0x1, 1 << 20,
                                       None) == msa.MSA_ERR_UNSUPPORTED
     # a chunk may start anywhere, but must fit in the cache (1024 tokens) and not start before it
     d1 = _desc(batch=1)
     for q_start in (1000, -1):
         cfg_p = msa.select_cfg(4, q_tile=64, q_start=q_start)
-        assert lib.msa_select_topk_blocks(0x1, 16, 64, 0x1, ctypes.byref(d1), ctypes.byref(cfg_p), 0x1, 5, None, 0x1,
+        assert lib.msa_select_topk_blocks(0x10, 16, 64, 0x1, ctypes.byref(d1), ctypes.byref(cfg_p), 0x1, 5, None, 0x1,
                                           1 << 20, None) == msa.MSA_ERR_INVALID_ARG
 
 
 def test_decode_and_prefill_arguments(lib):
     d = _desc()
-    assert lib.msa_sparse_attn_decode(0x1, 16, ctypes.byref(d), None, 8, 0.1, 0x1, None, 0x1, 1 << 20,
+    assert lib.msa_sparse_attn_decode(0x10, 16, ctypes.byref(d), None, 8, 0.1, 0x1, None, 0x1, 1 << 20,
                                       None) == msa.MSA_ERR_INVALID_ARG
-    assert lib.msa_sparse_attn_decode(0x1, 16, ctypes.byref(d), 0x1, 8, -1.0, 0x1, None, 0x1, 1 << 20,
+    assert lib.msa_sparse_attn_decode(0x10, 16, ctypes.byref(d), 0x1, 8, -1.0, 0x1, None, 0x1, 1 << 20,
                                       None) == msa.MSA_ERR_INVALID_ARG
     # prefill: batch must be 1
-    assert lib.msa_sparse_attn_prefill(0x1, 16, 64, 0, ctypes.byref(d), 0x1, 5, 0.1, 0x1, None, 0x1, 1 << 20,
+    assert lib.msa_sparse_attn_prefill(0x10, 16, 64, 0, ctypes.byref(d), 0x1, 5, 0.1, 0x1, None, 0x1, 1 << 20,
                                        None) == msa.MSA_ERR_UNSUPPORTED
     d1 = _desc(batch=1)
     # any start, but the chunk must fit in the cache's 1024 tokens
-    assert lib.msa_dense_gqa_prefill(0x1, 16, 64, 980, ctypes.byref(d1), 0.1, 0x1, None, 0x1, 1 << 20,
+    assert lib.msa_dense_gqa_prefill(0x10, 16, 64, 980, ctypes.byref(d1), 0.1, 0x1, None, 0x1, 1 << 20,
                                      None) == msa.MSA_ERR_INVALID_ARG
-    assert lib.msa_dense_gqa_prefill(0x1, 16, 2000, 0, ctypes.byref(d1), 0.1, 0x1, None, 0x1, 1 << 20,
+    assert lib.msa_dense_gqa_prefill(0x10, 16, 2000, 0, ctypes.byref(d1), 0.1, 0x1, None, 0x1, 1 << 20,
                                      None) == msa.MSA_ERR_INVALID_ARG
+
+
+def test_queries_and_outputs_must_be_16_byte_aligned(lib):
+    """q and out move in 16-byte pieces: a misaligned base is an argument
+    error, found before any launch."""
+    d, d1 = _desc(), _desc(batch=1)
+    cfg = msa.select_cfg(4)
+    for q, out in ((0x18, 0x20), (0x20, 0x18)):
+        assert lib.msa_sparse_attn_decode(q, 16, ctypes.byref(d), 0x40, 8, 0.1, out, None, 0x40, 1 << 20,
+                                          None) == msa.MSA_ERR_INVALID_ARG
+        assert lib.msa_sparse_attn_decode_noalloc(q, 16, ctypes.byref(d), 0x40, 8, 0.1, out, None,
+                                                  None) == msa.MSA_ERR_INVALID_ARG
+        assert lib.msa_sparse_decode_step(q, 16, 0x40, ctypes.byref(d), ctypes.byref(cfg), 0x40, 5, 0.1, out, None,
+                                          0x40, 1 << 20, None) == msa.MSA_ERR_INVALID_ARG
+        assert lib.msa_sparse_attn_prefill(q, 16, 64, 0, ctypes.byref(d1), 0x40, 5, 0.1, out, None, 0x40, 1 << 20,
+                                           None) == msa.MSA_ERR_INVALID_ARG
+    assert lib.msa_select_topk_blocks(0x18, 16, 1, 0x40, ctypes.byref(d), ctypes.byref(cfg), 0x40, 5, None, 0x40,
+                                      1 << 20, None) == msa.MSA_ERR_INVALID_ARG
 
 
 def _batch(starts, counts):
