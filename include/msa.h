@@ -36,6 +36,9 @@
  *     and sets a sticky status word in the workspace, read with
  *     msa_read_device_status.
  *   - Head dimension D = 128 and block size 64 are the only supported values.
+ *   - q, out, k, v and the pooled keys are moved in 16-byte pieces (vector
+ *     loads and stores, asynchronous and tensor-memory-access copies): their
+ *     base addresses must be 16-byte aligned (MSA_ERR_INVALID_ARG otherwise).
  *
  * Layouts (row-major, innermost last):
  *   q (decode)   [batch, num_q_heads, 128]         KV dtype

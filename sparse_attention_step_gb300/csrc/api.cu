@@ -106,12 +106,18 @@ msa_status make_q_map(CUtensorMap* map, const void* base, int64_t n_tokens, int 
   return r == CUDA_SUCCESS ? MSA_OK : MSA_ERR_CUDA;
 }
 
+// Queries, outputs, keys, values and pooled keys move in 16-byte pieces
+// (vector loads and stores, cp.async, TMA), so their base addresses must be
+// 16-byte aligned.
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
 msa_status validate_kv(const msa_kv_desc* kv) {
   if (kv == nullptr) return MSA_ERR_INVALID_ARG;
   if (kv->layout != MSA_KV_CONTIGUOUS && kv->layout != MSA_KV_PAGED) return MSA_ERR_INVALID_ARG;
   if (kv->dtype != MSA_DTYPE_F32 && kv->dtype != MSA_DTYPE_BF16) return MSA_ERR_INVALID_ARG;
   if (kv->batch <= 0 || kv->num_kv_heads <= 0) return MSA_ERR_INVALID_ARG;
   if (kv->k == nullptr || kv->v == nullptr || kv->seq_lens == nullptr) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(kv->k) || !aligned16(kv->v)) return MSA_ERR_INVALID_ARG;
   if (kv->head_dim != kHeadDim || kv->block_size != kBlock) return MSA_ERR_UNSUPPORTED;
   if (kv->layout == MSA_KV_CONTIGUOUS) {
     if (kv->max_tokens <= 0 || kv->max_tokens % kBlock != 0) return MSA_ERR_INVALID_ARG;
@@ -196,10 +202,6 @@ msa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_E
 int forced_count(const msa_select_cfg* cfg) {
   return ((cfg->force_local & kForceLocal) ? 1 : 0) + ((cfg->force_local & kForceSink) ? 1 : 0);
 }
-
-// Queries and outputs move in 16-byte pieces (vector loads and stores,
-// cp.async, TMA), so their base addresses must be 16-byte aligned.
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 msa_status check_q_heads(const msa_kv_desc* kv, int hq) {
   if (hq <= 0 || hq % kv->num_kv_heads != 0) return MSA_ERR_INVALID_ARG;
@@ -389,7 +391,7 @@ msa_status check_select(const void* q, int32_t num_q_heads, const void* pooled, 
     return MSA_ERR_INVALID_ARG;
   if (cfg->force_local < 0 || cfg->force_local > (kForceLocal | kForceSink)) return MSA_ERR_INVALID_ARG;
   if (cfg->q_tile != 1 && cfg->q_tile != kBlock) return MSA_ERR_UNSUPPORTED;
-  if (!aligned16(q)) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(pooled)) return MSA_ERR_INVALID_ARG;
   return MSA_OK;
 }
 // The failure-detection path on the device, exercised on purpose: one warp
@@ -462,7 +464,7 @@ msa_status msa_pool_block_keys(const msa_kv_desc* kv, int64_t first_block, int64
                                size_t ws_bytes, msa_stream_t stream) {
   msa_status st = validate_kv(kv);
   if (st != MSA_OK) return st;
-  if (pooled == nullptr || first_block < 0 || n_blocks < -1) return MSA_ERR_INVALID_ARG;
+  if (pooled == nullptr || first_block < 0 || n_blocks < -1 || !aligned16(pooled)) return MSA_ERR_INVALID_ARG;
   if (ws != nullptr && ws_bytes < kWsHeader) return MSA_ERR_WORKSPACE;
   KvView view = view_of(kv);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -564,7 +566,7 @@ msa_status decode_step_common(const void* q, int32_t num_q_heads, const void* po
   if ((st = check_q_heads(kv, num_q_heads)) != MSA_OK) return st;
   if (cfg->q_tile != 1) return MSA_ERR_UNSUPPORTED;
   if (!(scale > 0.f)) return MSA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(out)) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(pooled)) return MSA_ERR_INVALID_ARG;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != MSA_OK) return st;
   int C = 0, chunk = 0, bps = 0;

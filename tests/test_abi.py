@@ -127,6 +127,13 @@ def test_queries_and_outputs_must_be_16_byte_aligned(lib):
                                            None) == msa.MSA_ERR_INVALID_ARG
     assert lib.msa_select_topk_blocks(0x18, 16, 1, 0x40, ctypes.byref(d), ctypes.byref(cfg), 0x40, 5, None, 0x40,
                                       1 << 20, None) == msa.MSA_ERR_INVALID_ARG
+    # pooled keys and the cache's k, v
+    assert lib.msa_select_topk_blocks(0x20, 16, 1, 0x48, ctypes.byref(d), ctypes.byref(cfg), 0x40, 5, None, 0x40,
+                                      1 << 20, None) == msa.MSA_ERR_INVALID_ARG
+    assert lib.msa_pool_block_keys(ctypes.byref(d), 0, -1, 0x48, None, 0, None) == msa.MSA_ERR_INVALID_ARG
+    for field in ("k", "v"):
+        bad = _desc(**{field: 0x1008})
+        assert lib.msa_pool_block_keys(ctypes.byref(bad), 0, -1, 0x4000, None, 0, None) == msa.MSA_ERR_INVALID_ARG
 
 
 def _batch(starts, counts):
