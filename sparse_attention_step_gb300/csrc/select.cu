@@ -613,61 +613,6 @@ __device__ inline void choose_top(const uint64_t* keys, int n, int k, uint8_t* r
   block_topk(keys, n, k, reinterpret_cast<uint64_t*>(ring), top, count);
 }
 
-// Top-k for k_scored <= 64 and at most 4096 candidates (prefill tiles, and
-// decode scores computed apart, as in token-max mode): the scores become
-// 64-bit selection keys (score, then lower block first) in shared memory;
-// the binned selection picks the k best, the threshold sort (block_topk)
-// takes the keys that crowd one bin. The list is written as the radix top-k
-// writes it. grid (Hkv, outer) with outer = batch (decode) or n_tiles
-// (prefill), 256 threads; dynamic shared memory topk64_smem(max_blocks).
-constexpr int kTopk64Threads = 256;
-constexpr int kTopk64MaxCand = 4096;
-__host__ __device__ inline int topk64_pad(int64_t n) {
-  int lists = 1;
-  while (static_cast<int64_t>(lists) * 64 < n) lists <<= 1;
-  return lists * 64 > 128 ? lists * 64 : 128;
-}
-size_t topk64_smem(int64_t max_blocks) {
-  return static_cast<size_t>(max_blocks + 2 * topk64_pad(max_blocks) + 64) * sizeof(uint64_t);
-}
-__global__ void __launch_bounds__(kTopk64Threads) topk64_kernel(const float* __restrict__ scores, KvView kv, TopkArgs a,
-                                                              int32_t* __restrict__ idx_out, int32_t* status) {
-  extern __shared__ __align__(16) uint64_t tk[];  // keys [max_blocks], then the threshold sort's scratch
-  __shared__ uint64_t top[64];
-  __shared__ SelectScratch scr;
-  __shared__ int sorted_blocks[64];
-  __shared__ int count;
-  const int h = blockIdx.x, outer = blockIdx.y;
-  const int64_t unit = static_cast<int64_t>(outer) * a.hkv + h;
-  const bool local = (a.force_local & kForceLocal) != 0, sink = (a.force_local & kForceSink) != 0;
-  pdl_wait();  // the scores come from the previous kernel
-  int64_t n64, forced, nb;  // candidates, the kept newest / diagonal block, blocks in view
-  if (!a.prefill) {
-    const int64_t len = kv.seq_len(outer, status, kIdTopk);
-    nb = (len + kBlock - 1) / kBlock;
-    const int64_t nbf = len / kBlock;
-    n64 = local ? min(nbf, nb - 1) : nbf;
-    forced = (local && nb > 0) ? nb - 1 : -1;
-  } else {
-    const int seq = a.pb.seq_of_tile(outer);
-    n64 = a.pb.q_start[seq] / kBlock + (outer - a.pb.tile_off[seq]);  // blocks before the diagonal
-    nb = n64 + 1;
-    forced = local ? n64 : -1;
-  }
-  if (n64 < 0) n64 = 0;
-  const int skip = (sink && n64 > 0) ? 1 : 0;  // attention sink: block 0 kept, not scored
-  const bool keep0 = sink && nb > 0 && forced != 0;
-  const int n = static_cast<int>(n64) - skip;
-  const int k = min(a.k_scored, n);
-  const float* sc = scores + unit * a.max_blocks;
-  for (int i = threadIdx.x; i < n; i += kTopk64Threads) tk[i] = sel_key(sc[i + skip], i + skip);
-  __syncthreads();
-  if (k > 0 && !block_select(tk, n, k, top, scr))
-    block_topk(tk, n, k, tk + a.max_blocks, top, &count);
-  pdl_trigger();  // the attention kernel may start its set-up
-  write_selection(top, max(k, 0), forced, keep0, a.k_total, idx_out + unit * a.k_total, sorted_blocks);
-}
-
 // The k best of n distinct keys through a sampled lower bound: the k-th
 // largest of ns sample keys (each the largest of a group of the keys, so
 // real keys) bounds the k-th best key from below; the keys at or above it
@@ -716,6 +661,90 @@ __device__ inline bool sampled_top(const uint64_t* keys, int n, int k, const uin
   }
   __syncthreads();
   return true;
+}
+
+// Top-k for k_scored <= 64 and at most 4096 candidates (prefill tiles, and
+// decode scores computed apart, as in token-max mode): the scores become
+// 64-bit selection keys (score, then lower block first) in shared memory;
+// the k best come from a sampled lower bound (the largest key of each of 64
+// groups of consecutive keys as the samples), else from the binned
+// selection, else (keys crowding one bin) from the threshold sort
+// (block_topk). The list is written as the radix top-k writes it. grid (Hkv, outer) with outer = batch (decode) or n_tiles
+// (prefill), 256 threads; dynamic shared memory topk64_smem(max_blocks).
+constexpr int kTopk64Threads = 256;
+constexpr int kTopk64MaxCand = 4096;
+static_assert(kTopk64Threads == 4 * 64, "64 sample groups of four threads each");
+__host__ __device__ inline int topk64_pad(int64_t n) {
+  int lists = 1;
+  while (static_cast<int64_t>(lists) * 64 < n) lists <<= 1;
+  return lists * 64 > 128 ? lists * 64 : 128;
+}
+size_t topk64_smem(int64_t max_blocks) {
+  return static_cast<size_t>(max_blocks + 2 * topk64_pad(max_blocks) + 64) * sizeof(uint64_t);
+}
+__global__ void __launch_bounds__(kTopk64Threads) topk64_kernel(const float* __restrict__ scores, KvView kv, TopkArgs a,
+                                                              int32_t* __restrict__ idx_out, int32_t* status) {
+  extern __shared__ __align__(16) uint64_t tk[];  // keys [max_blocks], then the threshold sort's scratch
+  __shared__ uint64_t top[64];
+  __shared__ SelectScratch scr;
+  __shared__ uint64_t smp[64], lb;
+  __shared__ int sorted_blocks[64];
+  __shared__ int count, n_surv;
+  const int h = blockIdx.x, outer = blockIdx.y;
+  const int64_t unit = static_cast<int64_t>(outer) * a.hkv + h;
+  const bool local = (a.force_local & kForceLocal) != 0, sink = (a.force_local & kForceSink) != 0;
+  pdl_wait();  // the scores come from the previous kernel
+  int64_t n64, forced, nb;  // candidates, the kept newest / diagonal block, blocks in view
+  if (!a.prefill) {
+    const int64_t len = kv.seq_len(outer, status, kIdTopk);
+    nb = (len + kBlock - 1) / kBlock;
+    const int64_t nbf = len / kBlock;
+    n64 = local ? min(nbf, nb - 1) : nbf;
+    forced = (local && nb > 0) ? nb - 1 : -1;
+  } else {
+    const int seq = a.pb.seq_of_tile(outer);
+    n64 = a.pb.q_start[seq] / kBlock + (outer - a.pb.tile_off[seq]);  // blocks before the diagonal
+    nb = n64 + 1;
+    forced = local ? n64 : -1;
+  }
+  if (n64 < 0) n64 = 0;
+  const int skip = (sink && n64 > 0) ? 1 : 0;  // attention sink: block 0 kept, not scored
+  const bool keep0 = sink && nb > 0 && forced != 0;
+  const int n = static_cast<int>(n64) - skip;
+  const int k = min(a.k_scored, n);
+  const float* sc = scores + unit * a.max_blocks;
+  {
+    // every score load in flight at once, then the keys
+    constexpr int kPer = kTopk64MaxCand / kTopk64Threads;
+    float v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = threadIdx.x + u * kTopk64Threads;
+      v[u] = i < n ? sc[i + skip] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int i = threadIdx.x + u * kTopk64Threads;
+      if (i < n) tk[i] = sel_key(v[u], i + skip);
+    }
+  }
+  __syncthreads();
+  {
+    // sample g: the largest key of keys [g G, (g + 1) G), four threads a group
+    const int G = (n + 63) / 64, g = threadIdx.x >> 2, part = threadIdx.x & 3;
+    const int end = min(n, (g + 1) * G);
+    uint64_t m = 0ull;
+    for (int i = g * G + part; i < end; i += 4) m = tk[i] > m ? tk[i] : m;
+    uint64_t o = shfl_xor_u64(m, 1);
+    m = o > m ? o : m;
+    o = shfl_xor_u64(m, 2);
+    m = o > m ? o : m;
+    if (part == 0) smp[g] = m;
+  }
+  if (k > 0 && !sampled_top(tk, n, k, smp, 64, scr.cand, top, &lb, &n_surv) && !block_select(tk, n, k, top, scr))
+    block_topk(tk, n, k, tk + a.max_blocks, top, &count);
+  pdl_trigger();  // the attention kernel may start its set-up
+  write_selection(top, max(k, 0), forced, keep0, a.k_total, idx_out + unit * a.k_total, sorted_blocks);
 }
 
 template <typename T>
