@@ -193,24 +193,28 @@ __global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __gri
 // tiles of a chunk batch, on the 5th-generation tensor cores. A CTA takes a
 // chunk of index-key blocks of one sequence and a group of up to 16 of its
 // tiles, for every KV head: the 128 index queries (tile x head) are the rows
-// of A, the block's 64 index-key tokens the columns of B, so
-//   D[query, token] = q_idx . K_idx[token]     tcgen05.mma M128 N64, fp32 in TMEM
+// of A, the 128 index-key tokens of a pair of blocks the columns of B, so
+//   D[query, token] = q_idx . K_idx[token]     tcgen05.mma M128 N128, fp32 in TMEM
 // with the fp32 index queries split into a bf16 head (k-steps 0-7) and a bf16
 // remainder (k-steps 8-15) accumulated into the same D, which reproduces the
 // fp32 products to ~2^-16 relative (rows of absent tiles or heads are zeros).
-// Each query row sits in one TMEM lane, so the block maximum over the 64
+// Each query row sits in one TMEM lane, so the maximum over a block's 64
 // tokens is a reduction inside one thread. Warps: 0-3 read D (TMEM lanes
-// 0-127), 4 the TMA producer (4-stage ring of index-key blocks), 5 the TMEM
+// 0-127), 4 the TMA producer (4-stage ring of block pairs), 5 the TMEM
 // allocator and MMA issuer; D is double-buffered. The index queries come from
 // the workspace (the prefill index-query kernel). grid (block chunks, groups
-// of 16 tiles of one sequence).
+// of 16 tiles of one sequence), the chunk sized so the grid is about one wave.
 // ---------------------------------------------------------------------------
 namespace {
 constexpr int kTpTiles = 16;       // tiles per group (x 8 heads = the MMA's 128 rows)
-constexpr int kTpChunk = 64;       // index-key blocks per CTA
+constexpr int kTpMaxChunk = 128;   // index-key blocks per CTA, at most (an even count)
 constexpr int kTpThreads = 192;
 constexpr int kTpProducer = 4, kTpMma = 5;  // warps
 constexpr int kTpStages = 4;
+// A stage holds a pair of blocks as the 128 rows of B: [block 2p, dims 0-63 |
+// block 2p + 1, dims 0-63 | block 2p, dims 64-127 | block 2p + 1, dims 64-127],
+// 8 KB each (64 rows of 128 bytes, 128-byte swizzle)
+constexpr int kTpStage = 2 * kTmStage;
 constexpr int kTpABytes = 65536;   // A: head and remainder, 128 rows x 128 dims bf16 each
 struct TpTail {
   uint64_t kv_full[kTpStages];
@@ -219,14 +223,15 @@ struct TpTail {
   uint64_t s_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
-  int32_t rowid[kTpChunk];
+  int32_t rowid[kTpMaxChunk];
 };
-constexpr size_t kTpSmem = 1024 + kTpABytes + static_cast<size_t>(kTpStages) * kTmStage + sizeof(TpTail);
+constexpr size_t kTpSmem = 1024 + kTpABytes + static_cast<size_t>(kTpStages) * kTpStage + sizeof(TpTail);
 }  // namespace
 
 struct TokenMaxPrefillArgs {
   const float* qidx;  // [tiles, hkv, 128] fp32
   int hkv;
+  int chunk;  // index-key blocks per CTA: even, <= kTpMaxChunk
   int64_t max_blocks;
   float* scores;  // [tiles, hkv, max_blocks]
   int32_t* status;
@@ -238,8 +243,8 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
   extern __shared__ __align__(1024) uint8_t tp_raw[];
   uint8_t* base = smem_align1024(tp_raw);
   uint8_t* qa = base;                  // A operands, 128-byte swizzled, K-major
-  uint8_t* ring = base + kTpABytes;    // index-key blocks
-  TpTail& st = *reinterpret_cast<TpTail*>(ring + kTpStages * kTmStage);
+  uint8_t* ring = base + kTpABytes;    // index-key block pairs
+  TpTail& st = *reinterpret_cast<TpTail*>(ring + kTpStages * kTpStage);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // the group's sequence: groups are counted sequence by sequence
@@ -255,9 +260,10 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
   const int t_end = min(t0 + kTpTiles, pb.tile_off[seq + 1]);
   const int64_t diag0 = pb.q_start[seq] / kBlock + j0;           // candidates of tile t0 + t: blocks < diag0 + t
   const int64_t n_max = diag0 + (t_end - t0) - 1;                // the group's most candidates
-  const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kTpChunk;
+  const int64_t b0 = static_cast<int64_t>(blockIdx.x) * a.chunk;
   if (b0 >= n_max) return;  // the whole CTA leaves before any barrier or allocation
-  const int nblk = static_cast<int>(min(static_cast<int64_t>(kTpChunk), n_max - b0));
+  const int nblk = static_cast<int>(min(static_cast<int64_t>(a.chunk), n_max - b0));
+  const int npair = (nblk + 1) / 2;
   pdl_wait();
 
   if (tid == 0) {
@@ -272,7 +278,7 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
     mbar_init(&st.drain, 1);
     fence_mbar_init();
   }
-  if (tid < kTpChunk) {
+  if (tid < kTpMaxChunk) {
     int32_t r = -1;
     if (tid < nblk) {
       const int64_t b = b0 + tid;
@@ -313,7 +319,7 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
   }
   fence_proxy_async();  // the tensor core reads A through the async proxy
   if (warp == kTpMma) {
-    tc::alloc(&st.tmem_base, 128);
+    tc::alloc(&st.tmem_base, 256);
     tc::relinquish();
   }
   tc::fence_before();
@@ -326,36 +332,42 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
     if (lane == 0) {
       tma_prefetch_desc(&tmi);
       int issued = 0;
-      for (int j = 0; j < nblk; ++j) {
-        const int slot = j % kTpStages;
-        if (j >= kTpStages && !mbar_wait(&st.kv_empty[slot], ((j / kTpStages) - 1) & 1, a.status, kIdScore)) break;
-        const int32_t y = st.rowid[j] < 0 ? 0 : st.rowid[j];
-        uint8_t* dst = ring + slot * kTmStage;
-        mbar_arrive_expect_tx(&st.kv_full[slot], kTmStage);
-        tma_load_2d(dst, &tmi, 0, y, &st.kv_full[slot]);
-        tma_load_2d(dst + kTmStage / 2, &tmi, 64, y, &st.kv_full[slot]);
-        issued = j + 1;
+      for (int p = 0; p < npair; ++p) {
+        const int slot = p % kTpStages;
+        if (p >= kTpStages && !mbar_wait(&st.kv_empty[slot], ((p / kTpStages) - 1) & 1, a.status, kIdScore)) break;
+        const int nb_p = min(2, nblk - 2 * p);  // the last pair of an odd chunk has one block
+        uint8_t* dst = ring + slot * kTpStage;
+        mbar_arrive_expect_tx(&st.kv_full[slot], nb_p * kTmStage);
+        for (int e = 0; e < nb_p; ++e) {
+          const int32_t r = st.rowid[2 * p + e];
+          const int32_t y = r < 0 ? 0 : r;
+          tma_load_2d(dst + e * 8192, &tmi, 0, y, &st.kv_full[slot]);
+          tma_load_2d(dst + 16384 + e * 8192, &tmi, 64, y, &st.kv_full[slot]);
+        }
+        issued = p + 1;
       }
       // every load this thread issued has landed before the CTA may exit
-      for (int j = issued - kTpStages < 0 ? 0 : issued - kTpStages; j < issued; ++j)
-        mbar_wait(&st.kv_full[j % kTpStages], (j / kTpStages) & 1, a.status, kIdScore);
+      for (int p = issued - kTpStages < 0 ? 0 : issued - kTpStages; p < issued; ++p)
+        mbar_wait(&st.kv_full[p % kTpStages], (p / kTpStages) & 1, a.status, kIdScore);
     }
   } else if (warp == kTpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kId = tc::idesc_bf16(128, 64, 0, 0);
+      // N = 128: the pair's two blocks (in an odd chunk's last pair, rows
+      // 64-127 of B are stale and the columns they produce are not read)
+      constexpr uint32_t kId = tc::idesc_bf16(128, 128, 0, 0);
       const uint32_t a_addr = smem_u32(qa), r_addr = smem_u32(ring);
-      for (int j = 0; j < nblk; ++j) {
-        const int slot = j % kTpStages, buf = j & 1;
-        if (!mbar_wait(&st.kv_full[slot], (j / kTpStages) & 1, a.status, kIdScore)) break;
-        if (j >= 2 && !mbar_wait(&st.s_empty[buf], ((j >> 1) - 1) & 1, a.status, kIdScore)) break;
+      for (int p = 0; p < npair; ++p) {
+        const int slot = p % kTpStages, buf = p & 1;
+        if (!mbar_wait(&st.kv_full[slot], (p / kTpStages) & 1, a.status, kIdScore)) break;
+        if (p >= 2 && !mbar_wait(&st.s_empty[buf], ((p >> 1) - 1) & 1, a.status, kIdScore)) break;
         tc::fence_after();
-        const uint32_t d = tmem + buf * 64;
+        const uint32_t d = tmem + buf * 128;
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
           const int k8 = kk & 7;  // k-steps 8-15 repeat the dims with the remainder of the queries
           const uint64_t ad = tc::sdesc_sw128(a_addr + (kk >> 3) * 32768 + (k8 >> 2) * 16384 + (k8 & 3) * 32, 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(r_addr + slot * kTmStage + (k8 >> 2) * 8192 + (k8 & 3) * 32, 16, 1024);
+          const uint64_t bd = tc::sdesc_sw128(r_addr + slot * kTpStage + (k8 >> 2) * 16384 + (k8 & 3) * 32, 16, 1024);
           tc::mma_ss(d, ad, bd, kId, kk > 0 ? 1u : 0u);
         }
         tc::commit(&st.kv_empty[slot]);
@@ -372,22 +384,27 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
     const int64_t n_cand = diag0 + g;  // this tile's candidates
     const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
     float* out = a.scores + (static_cast<int64_t>(live ? t0 + g : 0) * a.hkv + h) * a.max_blocks;
-    for (int j = 0; j < nblk; ++j) {
-      const int buf = j & 1;
-      if (!mbar_wait_warp(&st.s_full[buf], (j >> 1) & 1, a.status, kIdScore)) break;
+    for (int p = 0; p < npair; ++p) {
+      const int buf = p & 1;
+      if (!mbar_wait_warp(&st.s_full[buf], (p >> 1) & 1, a.status, kIdScore)) break;
       tc::fence_after();
-      uint32_t r0[32], r1[32];
-      tc::ld32(tmem + lane_base + buf * 64, r0);
-      tc::ld32(tmem + lane_base + buf * 64 + 32, r1);
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      tc::ld64(tmem + lane_base + buf * 128, r0, r1);       // block 2p
+      tc::ld64(tmem + lane_base + buf * 128 + 64, r2, r3);  // block 2p + 1
       tc::wait_ld();
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&st.s_empty[buf]);
-      float m = -INFINITY;
+      float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) m = fmaxf(m, fmaxf(__uint_as_float(r0[c]), __uint_as_float(r1[c])));
+      for (int c = 0; c < 32; ++c) {
+        m0 = fmaxf(m0, fmaxf(__uint_as_float(r0[c]), __uint_as_float(r1[c])));
+        m1 = fmaxf(m1, fmaxf(__uint_as_float(r2[c]), __uint_as_float(r3[c])));
+      }
+      const int j = 2 * p;
       const int64_t b = b0 + j;
-      if (live && b < n_cand) out[b] = st.rowid[j] < 0 ? -INFINITY : m;  // bad page: never selected
+      if (live && b < n_cand) out[b] = st.rowid[j] < 0 ? -INFINITY : m0;  // bad page: never selected
+      if (live && j + 1 < nblk && b + 1 < n_cand) out[b + 1] = st.rowid[j + 1] < 0 ? -INFINITY : m1;
     }
   }
   pdl_trigger();
@@ -395,7 +412,7 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
   __syncthreads();
   if (warp == kTpMma) {
     tc::fence_after();
-    tc::dealloc(tmem, 128);
+    tc::dealloc(tmem, 256);
   }
 }
 
@@ -416,7 +433,16 @@ cudaError_t launch_token_max_prefill_scores(const CUtensorMap& tmi, const KvView
   int groups = 0;  // groups of kTpTiles tiles, sequence by sequence
   for (int s = 0; s < pb.n_seqs; ++s) groups += (pb.tile_off[s + 1] - pb.tile_off[s] + kTpTiles - 1) / kTpTiles;
   if (last <= 0 || groups == 0) return cudaSuccess;  // no candidates anywhere
-  const unsigned chunks = static_cast<unsigned>((last + kTpChunk - 1) / kTpChunk);
+  // about one wave: one CTA per SM, the groups sharing the SMs
+  int num_sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t per_group = max(static_cast<int64_t>(1), static_cast<int64_t>(num_sms > 0 ? num_sms : 1) / groups);
+  int64_t chunk = (last + per_group - 1) / per_group;
+  chunk = (chunk + 1) / 2 * 2;
+  chunk = chunk < 16 ? 16 : chunk > kTpMaxChunk ? kTpMaxChunk : chunk;
+  a.chunk = static_cast<int>(chunk);
+  const unsigned chunks = static_cast<unsigned>((last + chunk - 1) / chunk);
   token_max_prefill_kernel<<<dim3(chunks, groups), kTpThreads, token_max_prefill_smem_bytes(), stream>>>(tmi, kv, a,
                                                                                                           pb);
   return cudaGetLastError();
