@@ -72,16 +72,19 @@ __global__ void __launch_bounds__(256) qidx_prefill_kernel(const T* __restrict__
 }
 
 // bf16 q: the tile's rows (64 tokens x G heads, 256 bytes each; a token's G
-// heads are contiguous) are pulled into shared memory with 16-byte cp.async,
-// every piece in flight at once and no registers held while they travel, then
-// summed like the kernel above: 16 row slots per 16-byte piece of the dims,
+// heads are contiguous) are pulled into shared memory with 16-byte cp.async in
+// chunks of 64 rows through a 4-stage ring (three chunks in flight while one
+// is summed, three CTAs per SM), then summed like the kernel above: 16 row
+// slots per 16-byte piece of the dims, each slot's rows in ascending order,
 // the slots' partial sums added in slot order. grid (Hkv, n_tiles), 256
-// threads, dynamic shared memory 64 G x 256 bytes.
+// threads, dynamic shared memory kQidxStages x 16 KB.
 constexpr int kQidxThreads = 256;
+constexpr int kQidxChunkRows = 64;  // 16 KB of rows per chunk
+constexpr int kQidxStages = 4;
 __global__ void __launch_bounds__(kQidxThreads) qidx_prefill_bf16_kernel(const __nv_bfloat16* __restrict__ q, int hq,
                                                                        int hkv, const PrefillBatch pb,
                                                                        float* __restrict__ qidx) {
-  extern __shared__ __align__(16) uint8_t qrows[];  // [n_rows][256 B]
+  extern __shared__ __align__(16) uint8_t qrows[];  // [kQidxStages][kQidxChunkRows][256 B]
   __shared__ float part[16][kHeadDim + 4];
   const int h = blockIdx.x;
   const int tile = blockIdx.y;  // global tile
@@ -90,25 +93,40 @@ __global__ void __launch_bounds__(kQidxThreads) qidx_prefill_bf16_kernel(const _
   const int j0 = max(pb.tile_row0(s, tile), 0);  // the tile's first token within its sequence's chunk
   const int r0 = pb.q_off[s] + j0;
   const int n_rows = (min(pb.q_cnt[s], pb.tile_row0(s, tile) + kBlock) - j0) * grp;  // token-major, head-minor
+  const int n_ch = (n_rows + kQidxChunkRows - 1) / kQidxChunkRows;
   const int tid = threadIdx.x;
-  for (int i = tid; i < n_rows * 16; i += kQidxThreads) {
-    const int row = i >> 4, pc = i & 15;
-    const int t = row / grp, g = row - t * grp;
-    cp_async16(qrows + row * 256 + pc * 16,
-               q + (static_cast<int64_t>(r0 + t) * hq + h * grp + g) * kHeadDim + 8 * pc);
-  }
-  cp_async_commit();
-  cp_async_wait<0>();
-  __syncthreads();
+  // chunk c (rows [64 c, 64 c + 64)) into stage c mod kQidxStages; one commit
+  // group per call, empty past the last chunk, so the wait count is uniform
+  auto issue = [&](int c) {
+    if (c < n_ch) {
+      uint8_t* stage = qrows + (c % kQidxStages) * (kQidxChunkRows * 256);
+      const int rows = min(kQidxChunkRows, n_rows - c * kQidxChunkRows);
+      for (int i = tid; i < rows * 16; i += kQidxThreads) {
+        const int lr = i >> 4, pc = i & 15;
+        const int row = c * kQidxChunkRows + lr;
+        const int t = row / grp, g = row - t * grp;
+        cp_async16(stage + lr * 256 + pc * 16, q + (static_cast<int64_t>(r0 + t) * hq + h * grp + g) * kHeadDim + 8 * pc);
+      }
+    }
+    cp_async_commit();
+  };
+  for (int c = 0; c < kQidxStages - 1; ++c) issue(c);
   const int e = tid & 15, slot = tid >> 4;
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int c = 0; c < n_ch; ++c) {
+    cp_async_wait<kQidxStages - 2>();  // chunk c has landed (this thread's pieces)
+    __syncthreads();                   // every thread's pieces; chunk c - 1's stage is free again
+    issue(c + kQidxStages - 1);
+    const uint8_t* stage = qrows + (c % kQidxStages) * (kQidxChunkRows * 256);
+    const int rows = min(kQidxChunkRows, n_rows - c * kQidxChunkRows);
 #pragma unroll 4
-  for (int row = slot; row < n_rows; row += 16) {
-    RawRow<__nv_bfloat16> x;
-    x.w = *reinterpret_cast<const uint4*>(qrows + row * 256 + 16 * e);
-    x.add_to(acc);
+    for (int lr = slot; lr < rows; lr += 16) {  // 64 rows per chunk: each slot's rows stay ascending
+      RawRow<__nv_bfloat16> x;
+      x.w = *reinterpret_cast<const uint4*>(stage + lr * 256 + 16 * e);
+      x.add_to(acc);
+    }
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) part[slot][8 * e + j] = acc[j];
@@ -120,7 +138,7 @@ __global__ void __launch_bounds__(kQidxThreads) qidx_prefill_bf16_kernel(const _
     qidx[(static_cast<int64_t>(tile) * hkv + h) * kHeadDim + tid] = t;
   }
 }
-constexpr size_t kQidxSmemMax = static_cast<size_t>(kBlock) * kMaxGroupHeads * 256;
+constexpr size_t kQidxSmemMax = static_cast<size_t>(kQidxStages) * kQidxChunkRows * 256;
 
 // ---------------------------------------------------------------------------
 // Block scores.
@@ -668,25 +686,20 @@ __device__ inline bool sampled_top(const uint64_t* keys, int n, int k, const uin
 // 64-bit selection keys (score, then lower block first) in shared memory;
 // the k best come from a sampled lower bound (the largest key of each of 64
 // groups of consecutive keys as the samples), else from the binned
-// selection, else (keys crowding one bin) from the threshold sort
-// (block_topk). The list is written as the radix top-k writes it. grid (Hkv, outer) with outer = batch (decode) or n_tiles
+// selection, else (keys crowding one bin) from a radix select of the k-th
+// key, which needs no scratch beyond the keys. The list is written as the
+// radix top-k writes it. grid (Hkv, outer) with outer = batch (decode) or n_tiles
 // (prefill), 256 threads; dynamic shared memory topk64_smem(max_blocks).
 constexpr int kTopk64Threads = 256;
 constexpr int kTopk64MaxCand = 4096;
 static_assert(kTopk64Threads == 4 * 64, "64 sample groups of four threads each");
-__host__ __device__ inline int topk64_pad(int64_t n) {
-  int lists = 1;
-  while (static_cast<int64_t>(lists) * 64 < n) lists <<= 1;
-  return lists * 64 > 128 ? lists * 64 : 128;
-}
-size_t topk64_smem(int64_t max_blocks) {
-  return static_cast<size_t>(max_blocks + 2 * topk64_pad(max_blocks) + 64) * sizeof(uint64_t);
-}
-__global__ void __launch_bounds__(kTopk64Threads) topk64_kernel(const float* __restrict__ scores, KvView kv, TopkArgs a,
+size_t topk64_smem(int64_t max_blocks) { return static_cast<size_t>(max_blocks) * sizeof(uint64_t); }
+__global__ void __launch_bounds__(kTopk64Threads, 6) topk64_kernel(const float* __restrict__ scores, KvView kv, TopkArgs a,
                                                               int32_t* __restrict__ idx_out, int32_t* status) {
-  extern __shared__ __align__(16) uint64_t tk[];  // keys [max_blocks], then the threshold sort's scratch
+  extern __shared__ __align__(16) uint64_t tk[];  // keys [max_blocks]
   __shared__ uint64_t top[64];
   __shared__ SelectScratch scr;
+  __shared__ RadixScratch radix;
   __shared__ uint64_t smp[64], lb;
   __shared__ int sorted_blocks[64];
   __shared__ int count, n_surv;
@@ -742,7 +755,7 @@ __global__ void __launch_bounds__(kTopk64Threads) topk64_kernel(const float* __r
     if (part == 0) smp[g] = m;
   }
   if (k > 0 && !sampled_top(tk, n, k, smp, 64, scr.cand, top, &lb, &n_surv) && !block_select(tk, n, k, top, scr))
-    block_topk(tk, n, k, tk + a.max_blocks, top, &count);
+    block_compact_ge(tk, n, block_kth_largest(tk, n, k, radix), top, 64, &count);  // exactly the k best
   pdl_trigger();  // the attention kernel may start its set-up
   write_selection(top, max(k, 0), forced, keep0, a.k_total, idx_out + unit * a.k_total, sorted_blocks);
 }
@@ -1086,7 +1099,7 @@ cudaError_t launch_select(const T* q, int hq, const PrefillBatch* pb, const T* p
     outer = n_tiles;
     sa.n_tiles = n_tiles;
     if constexpr (sizeof(T) == 2) {
-      const size_t smem = static_cast<size_t>(kBlock) * (hq / kv.hkv) * 256;
+      const size_t smem = kQidxSmemMax;
       qidx_prefill_bf16_kernel<<<dim3(kv.hkv, n_tiles), kQidxThreads, smem, stream>>>(q, hq, kv.hkv, *pb, qidx_ws);
     } else {
       qidx_prefill_kernel<T><<<dim3(kv.hkv, n_tiles), 256, 0, stream>>>(q, hq, kv.hkv, *pb, qidx_ws);
@@ -1127,7 +1140,7 @@ cudaError_t launch_select_token_max_prefill(const CUtensorMap& tmi, const __nv_b
                                             int32_t* idx_out, int k_total, float* scores, float* qidx_ws,
                                             int32_t* status, cudaStream_t stream) {
   const int n_tiles = pb.total_tiles();
-  const size_t smem = static_cast<size_t>(kBlock) * (hq / kv.hkv) * 256;
+  const size_t smem = kQidxSmemMax;
   qidx_prefill_bf16_kernel<<<dim3(kv.hkv, n_tiles), kQidxThreads, smem, stream>>>(q, hq, kv.hkv, pb, qidx_ws);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
