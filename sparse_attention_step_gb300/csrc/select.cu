@@ -254,7 +254,9 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const T* __restric
 // 128 summary rows into shared memory with cp.async (128-byte swizzle, two
 // 64-dim halves) and each warp scores 16 of them against the index queries of
 // 8 tiles at once: mma.sync with the 8 tiles as the N columns, the fp32 index
-// queries split into a bf16 head and a bf16 remainder (two n-tiles).
+// queries split into a bf16 head and a bf16 remainder (two n-tiles). The 8
+// index queries are read once per CTA (coalesced) into shared memory, where
+// every warp takes its operand fragments.
 // ---------------------------------------------------------------------------
 constexpr int kPsRows = 128;
 constexpr int kPsTiles = 8;
@@ -264,6 +266,7 @@ __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __r
                                                                 KvView kv, ScoreArgs a, const PrefillBatch pb,
                                                                 float* __restrict__ scores, int32_t* status) {
   __shared__ __align__(1024) uint8_t rows_s[kPsRows * kHeadDim * 2];
+  __shared__ __align__(16) float qs[kPsTiles][kHeadDim + 8];  // padded: conflict-free 8-byte fragment reads
   const int h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // 8 tiles of one sequence: global tiles t0 .. t_end - 1, local tiles j0 ..
   const int seq = pb.seq_of_group(blockIdx.z);
@@ -287,25 +290,31 @@ __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __r
                  pooled + kv.pooled_row(seq, h, b) * kHeadDim + 8 * pc);
   }
   cp_async_commit();
+  {
+    // the 8 tiles' index queries (zeros past the last tile), one float4 a thread
+    const int tt = tid >> 5, d4 = tid & 31;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t0 + tt < t_end)
+      x = reinterpret_cast<const float4*>(qidx_ws + (static_cast<int64_t>(t0 + tt) * a.hkv + h) * kHeadDim)[d4];
+    *reinterpret_cast<float4*>(&qs[tt][4 * d4]) = x;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
   // B operands: column g = tile t0 + g
   const int g = lane >> 2, c = lane & 3;
-  const bool live = t0 + g < t_end;
-  const float* qg = qidx_ws + (static_cast<int64_t>(live ? t0 + g : 0) * a.hkv + h) * kHeadDim;
   uint32_t qh[8][2], ql[8][2];
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
 #pragma unroll
     for (int hlf = 0; hlf < 2; ++hlf) {
       const int d = 16 * kk + 2 * c + 8 * hlf;
-      const float x0 = live ? qg[d] : 0.f, x1 = live ? qg[d + 1] : 0.f;
-      const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
-      const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
+      const float2 x = *reinterpret_cast<const float2*>(&qs[g][d]);
+      const float h0 = __bfloat162float(__float2bfloat16_rn(x.x));
+      const float h1 = __bfloat162float(__float2bfloat16_rn(x.y));
       qh[kk][hlf] = pack_bf16(h0, h1);
-      ql[kk][hlf] = pack_bf16(x0 - h0, x1 - h1);
+      ql[kk][hlf] = pack_bf16(x.x - h0, x.y - h1);
     }
   }
-  cp_async_wait<0>();
-  __syncthreads();
   const uint32_t sbase = smem_u32(rows_s);
   const int krow = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
   const int kchunk = lane >> 4;
