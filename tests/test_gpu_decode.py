@@ -191,6 +191,17 @@ def test_decode_many_splits_and_chunks(dev):
     verify_units(inp, res, all_units(inp), 40, 48, check_dense=True)
 
 
+@pytest.mark.parametrize("layout", ["contiguous", "paged"])
+def test_decode_long_lists_few_units(dev, layout):
+    """Few units with long lists: each unit's list over a 16-CTA cluster with
+    a long slice per CTA (the two-quartet attention kernel), ragged lengths."""
+    lens = [64 * 2000 + 29]
+    inp = make_decode_inputs(lens, 8, 64, "bf16", layout, needles=4, seed=41, device=dev)
+    res = run_decode(inp, 300, 301, dense=True)
+    assert res["status"] == 0
+    verify_units(inp, res, all_units(inp), 300, 301, check_dense=True)
+
+
 @pytest.mark.parametrize("k_scored", [0, 1, 10_000])
 def test_decode_k_extremes(dev, k_scored):
     lens = [64 * 30 + 7, 64 * 5]
