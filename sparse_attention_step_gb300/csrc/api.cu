@@ -574,7 +574,14 @@ msa_status decode_step_common(const void* q, int32_t num_q_heads, const void* po
   // A paged cache takes the fused step only when its grid is one wave (a
   // ragged batch of long and short sequences is left to the chunked selection,
   // which sizes its pieces per sequence).
-  const bool fused = kv->dtype == MSA_DTYPE_BF16 && cfg->mode == MSA_SCORE_MEAN_POOLED_KEYS && cfg->k_scored >= 0 &&
+  // Token-max scores (the shared index-key cache comes in place of the
+  // summaries) are computed by their own kernel first; the fused step then
+  // reads them in place of scoring summary rows.
+  const bool token_max = cfg->mode == MSA_SCORE_TOKEN_MAX;
+  const bool fused = kv->dtype == MSA_DTYPE_BF16 &&
+                     (cfg->mode == MSA_SCORE_MEAN_POOLED_KEYS ||
+                      (token_max && pooled_update == nullptr && kv->num_kv_heads <= 8)) &&
+                     cfg->k_scored >= 0 &&
                      k_total >= std::min<int64_t>(cfg->k_scored, kv_max_blocks(kv)) + forced_count(cfg) &&
                      step_shape(units, kv_max_blocks(kv), cfg->k_scored, k_total, dev->num_sms, dev->step_clusters, &C,
                                 &chunk, &bps) &&
@@ -592,20 +599,36 @@ msa_status decode_step_common(const void* q, int32_t num_q_heads, const void* po
     return cuda_status(launch_pool_newest(static_cast<const float*>(kv->k), view_of(kv), kv->batch,
                                           static_cast<float*>(pooled_update), ws_status(ws), s));
   }
-  if ((st = check_ws(ws, ws_bytes, kWsHeader)) != MSA_OK) return st;
   const int64_t rows = kv_rows(kv);
   if (rows >= (int64_t(1) << 31)) return MSA_ERR_UNSUPPORTED;
-  // summary rows: [batch * hkv * max_blocks, 128], 128-row boxes
   CUtensorMap tmk, tmv, tmp;
   if ((st = make_kv_map(&tmk, kv->k, rows)) != MSA_OK) return st;
   if ((st = make_kv_map(&tmv, kv->v, rows)) != MSA_OK) return st;
-  if ((st = make_kv_map(&tmp, pooled, units * kv_max_blocks(kv), 128)) != MSA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const float* pre_scores = nullptr;
+  if (token_max) {
+    // index-key rows: [batch * max_tokens, 128] or [num_pages * 64, 128]
+    const SelectLayout SL = select_layout(kv, 0, 0);
+    if ((st = check_ws(ws, ws_bytes, SL.total)) != MSA_OK) return st;
+    const int64_t idx_rows = kv->layout == MSA_KV_CONTIGUOUS ? static_cast<int64_t>(kv->batch) * kv->max_tokens
+                                                             : static_cast<int64_t>(kv->num_pages) * kBlock;
+    if (idx_rows >= (int64_t(1) << 31)) return MSA_ERR_UNSUPPORTED;
+    if ((st = make_kv_map(&tmp, pooled, idx_rows)) != MSA_OK) return st;
+    float* scores = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + SL.scores);
+    if ((st = cuda_status(launch_token_max_scores(tmp, view_of(kv), kv->batch, static_cast<const __nv_bfloat16*>(q),
+                                                  num_q_heads, cfg->force_local, scores, ws_status(ws), s))) != MSA_OK)
+      return st;
+    pre_scores = scores;
+  } else {
+    if ((st = check_ws(ws, ws_bytes, kWsHeader)) != MSA_OK) return st;
+    // summary rows: [batch * hkv * max_blocks, 128], 128-row boxes
+    if ((st = make_kv_map(&tmp, pooled, units * kv_max_blocks(kv), 128)) != MSA_OK) return st;
+  }
   return cuda_status(launch_decode_step(tmk, tmv, tmp, view_of(kv), kv->batch, static_cast<const __nv_bfloat16*>(q),
                                         num_q_heads, *cfg, k_total, C, chunk, bps, scale * kLog2e, idx_out,
                                         static_cast<__nv_bfloat16*>(out), lse, ws_status(ws),
                                         static_cast<const __nv_bfloat16*>(kv->k),
-                                        static_cast<__nv_bfloat16*>(pooled_update),
-                                        reinterpret_cast<cudaStream_t>(stream)));
+                                        static_cast<__nv_bfloat16*>(pooled_update), pre_scores, s));
 }
 
 }  // namespace

@@ -143,6 +143,7 @@ cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, c
                                const KvView& kv, int batch, const __nv_bfloat16* q, int hq, const msa_select_cfg& cfg,
                                int k_total, int C, int chunk, int bps, float scale_log2,
                                int32_t* idx_out, __nv_bfloat16* out, float* lse, int32_t* status,
-                               const __nv_bfloat16* k, __nv_bfloat16* pooled_out, cudaStream_t stream);
+                               const __nv_bfloat16* k, __nv_bfloat16* pooled_out, const float* pre_scores,
+                               cudaStream_t stream);
 
 }  // namespace msa

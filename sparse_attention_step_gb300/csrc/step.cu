@@ -26,6 +26,10 @@
 //      shared memory: every CTA pushes piece p (one head, 8 dims) of its
 //      partial into the shared memory of CTA p % C, and after one cluster
 //      barrier CTA r merges and writes output pieces r, r + C, ...
+// With scores computed apart (the token-max scores of the guide's Step 1 as
+// drawn, by the kernel before this one), phase 1 reads each CTA's chunk of
+// block scores instead of streaming and scoring summary rows; phases 2-4 are
+// the same.
 #include <float.h>
 
 #include <algorithm>
@@ -68,10 +72,12 @@ struct StepArgs {
   int32_t* status;
   const __nv_bfloat16* k;        // keys (for pooling the newest block)
   __nv_bfloat16* pooled_out;     // nullable: summary of the newest block when it has just filled
+  const float* pre_scores;       // scores computed apart: [batch, hkv, max_blocks] (kPre kernels only)
 };
 
-// grid (C, Hkv, batch), cluster (C, 1, 1). kStages: depth of the shared-memory ring.
-template <int kStages>
+// grid (C, Hkv, batch), cluster (C, 1, 1). kStages: depth of the shared-memory
+// ring; kPre: the block scores come from a.pre_scores.
+template <int kStages, bool kPre>
 __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid_constant__ CUtensorMap tmk,
                                                                    const __grid_constant__ CUtensorMap tmv,
                                                                    const __grid_constant__ CUtensorMap tmpool, KvView kv,
@@ -101,7 +107,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   // streaming the first stages of its chunk: their rows do not depend on the
   // sequence length, which is read meanwhile (stages past the candidates are
   // drained unread).
-  const int n_pre = min(kStages, (a.chunk + kStRowsPerStage - 1) / kStRowsPerStage);
+  const int n_pre = kPre ? 0 : min(kStages, (a.chunk + kStRowsPerStage - 1) / kStRowsPerStage);
   const int32_t y0 = static_cast<int32_t>(unit * max_blocks + static_cast<int64_t>(rank) * a.chunk);
   if (warp == kStWarps && lane == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -121,7 +127,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     }
   }
   pdl_wait();
-  if (tid < kHeadDim) {
+  if (!kPre && tid < kHeadDim) {
     // all G loads in flight at once, then summed in head order
     const __nv_bfloat16* qg = a.q + (static_cast<int64_t>(s) * a.hq + h * a.grp) * kHeadDim + tid;
     float x[kStG];
@@ -143,7 +149,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   const int keep0 = (sink && nb > 0 && forced != 0) ? 1 : 0;
   const int64_t r0 = static_cast<int64_t>(rank) * a.chunk;
   const int rows = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(a.chunk), n_cand - r0)));
-  const int n_st = (rows + kStRowsPerStage - 1) / kStRowsPerStage;
+  const int n_st = kPre ? 0 : (rows + kStRowsPerStage - 1) / kStRowsPerStage;
   if (rank == 0 && warp == kStWarps && lane >= 28 && forced >= 0) {
     // the newest block is always attended: pull it into L2 during scoring
     const int64_t row = kv.block_row(s, h, forced, a.status, kIdDecode);
@@ -153,7 +159,34 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
 
   // ---------------------------------------------------------------- 1. scores
   uint64_t lmax = 0ull;  // compute warps: the largest key this lane produced
-  if (warp == kStWarps) {
+  if constexpr (kPre) {
+    if (warp < kStWarps) {
+      // this CTA's chunk of the unit's scores, every load in flight at once;
+      // lanes 4j fold in the keys of lanes 4j + 1 .. 4j + 3, as the samples
+      // are taken from lanes 4j
+      constexpr int kPer = kStMaxChunk / (32 * kStWarps);
+      const float* sc = a.pre_scores + unit * max_blocks + r0;
+      float v[kPer];
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int i = tid + 32 * kStWarps * u;
+        v[u] = i < rows ? sc[i] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int i = tid + 32 * kStWarps * u;
+        if (i < rows) {
+          const uint64_t key = (skip && r0 + i == 0) ? 0ull : sel_key(v[u], static_cast<int>(r0 + i));
+          keys[i] = key;
+          lmax = key > lmax ? key : lmax;
+        }
+      }
+      uint64_t o = shfl_xor_u64(lmax, 1);
+      lmax = o > lmax ? o : lmax;
+      o = shfl_xor_u64(lmax, 2);
+      lmax = o > lmax ? o : lmax;
+    }
+  } else if (warp == kStWarps) {
     if (lane == 0) {
       // 128 summary rows per stage as two 64-column boxes (128-byte swizzle);
       // rows past the CTA's chunk are loaded but never scored
@@ -694,22 +727,22 @@ int max_clusters_of(int C) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, decode_step_kernel<kStages>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, decode_step_kernel<kStages, false>, &cfg) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
   }
   return n;
 }
 
-template <int kStages>
+template <int kStages, bool kPre>
 cudaError_t set_smem_of() {
-  cudaError_t e = cudaFuncSetAttribute(decode_step_kernel<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(decode_step_kernel<kStages, kPre>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(step_smem(kStages)));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_step_kernel<kStages>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(decode_step_kernel<kStages, kPre>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(decode_step_kernel<kStages>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return cudaFuncSetAttribute(decode_step_kernel<kStages, kPre>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
 }  // namespace
@@ -718,13 +751,17 @@ cudaError_t set_smem_of() {
 // at once (0 if the query fails). Needs set_step_smem() first.
 int step_max_clusters(int C) { return max_clusters_of<kStStages>(C); }
 
-cudaError_t set_step_smem() { return set_smem_of<kStStages>(); }
+cudaError_t set_step_smem() {
+  const cudaError_t e = set_smem_of<kStStages, false>();
+  return e != cudaSuccess ? e : set_smem_of<kStStages, true>();
+}
 
 cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, const CUtensorMap& tmpool,
                                const KvView& kv, int batch, const __nv_bfloat16* q, int hq, const msa_select_cfg& cfg,
                                int k_total, int C, int chunk, int bps, float scale_log2,
                                int32_t* idx_out, __nv_bfloat16* out, float* lse, int32_t* status,
-                               const __nv_bfloat16* k, __nv_bfloat16* pooled_out, cudaStream_t stream) {
+                               const __nv_bfloat16* k, __nv_bfloat16* pooled_out, const float* pre_scores,
+                               cudaStream_t stream) {
   StepArgs a;
   a.q = q;
   a.hq = hq;
@@ -747,6 +784,7 @@ cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, c
   a.status = status;
   a.k = k;
   a.pooled_out = pooled_out;
+  a.pre_scores = pre_scores;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(C, kv.hkv, batch);
   lc.blockDim = dim3(kStThreads, 1, 1);
@@ -761,7 +799,8 @@ cudaError_t launch_decode_step(const CUtensorMap& tmk, const CUtensorMap& tmv, c
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 2;
-  return cudaLaunchKernelEx(&lc, decode_step_kernel<kStStages>, tmk, tmv, tmpool, kv, a);
+  if (pre_scores != nullptr) return cudaLaunchKernelEx(&lc, decode_step_kernel<kStStages, true>, tmk, tmv, tmpool, kv, a);
+  return cudaLaunchKernelEx(&lc, decode_step_kernel<kStStages, false>, tmk, tmv, tmpool, kv, a);
 }
 
 }  // namespace msa

@@ -21,7 +21,7 @@ def dev(lib):
     return torch.device("cuda:0")
 
 
-def run_token_max(inp, ik, k_scored, k_total, step=False):
+def run_token_max(inp, ik, k_scored, k_total, step=False, sink=False):
     from sparse_attention_step_gb300 import msa
     dev = inp.q.device
     desc = msa.kv_desc(inp.k, inp.v, inp.seq_lens, inp.page_table)
@@ -34,7 +34,7 @@ def run_token_max(inp, ik, k_scored, k_total, step=False):
     scores = torch.full((b * hkv, max_blocks), float("nan"), dtype=torch.float32, device=dev)
     out = torch.full_like(inp.q, float("nan"))
     lse = torch.full((b, hq), float("nan"), dtype=torch.float32, device=dev)
-    cfg = msa.select_cfg(k_scored, mode=msa.MSA_SCORE_TOKEN_MAX)
+    cfg = msa.select_cfg(k_scored, mode=msa.MSA_SCORE_TOKEN_MAX, sink=sink)
     if step:
         msa.msa_sparse_decode_step(inp.q, hq, ik.kidx, desc, cfg, idx, k_total, SCALE, out, lse, ws.buf, ws.nbytes)
         scores = None
@@ -75,12 +75,35 @@ def test_token_max_select_and_attend(dev, layout, hkv, hq):
     verify(inp, ik, res, [(s, h) for s in range(inp.batch) for h in range(hkv)], 6, 7)
 
 
-def test_token_max_through_the_decode_step(dev):
-    inp = make_decode_inputs([64 * 200 + 5, 64 * 64], 4, 32, "bf16", "contiguous", seed=43, device=dev)
+@pytest.mark.parametrize("layout", ["contiguous", "paged"])
+def test_token_max_through_the_decode_step(dev, layout):
+    """The decode step in token-max mode: the scores from their own kernel,
+    then the fused step reads them in place of scoring summaries. Its lists
+    equal those of the two-kernel form (the same scores and keys) and its
+    outputs the oracle's."""
+    inp = make_decode_inputs([64 * 200 + 5, 64 * 64, 64 * 3 + 1], 4, 32, "bf16", layout, seed=43, device=dev)
     ik = make_index_keys(inp, needles=3, seed=44)
     res = run_token_max(inp, ik, 11, 12, step=True)
-    assert res["status"] == 0
-    verify(inp, ik, res, [(s, h) for s in range(2) for h in range(4)], 11, 12)
+    ref = run_token_max(inp, ik, 11, 12)
+    assert res["status"] == 0 and ref["status"] == 0
+    assert torch.equal(res["idx"], ref["idx"])
+    verify(inp, ik, res, [(s, h) for s in range(3) for h in range(4)], 11, 12)
+
+
+def test_token_max_decode_step_sink(dev):
+    from tests.test_gpu_sink import check_sink_row
+    inp = make_decode_inputs([64 * 150 + 9, 64 * 40], 2, 16, "bf16", "contiguous", seed=47, device=dev)
+    ik = make_index_keys(inp, needles=2, seed=48)
+    res = run_token_max(inp, ik, 7, 9, step=True, sink=True)
+    ref = run_token_max(inp, ik, 7, 9, sink=True)
+    assert res["status"] == 0 and ref["status"] == 0
+    assert torch.equal(res["idx"], ref["idx"])
+    grp = inp.num_q_heads // inp.num_kv_heads
+    for s in range(2):
+        kidx = to64(ik.rows(inp, s))
+        for h in range(2):
+            r = O.select_token_max(to64(inp.q[s, h * grp:(h + 1) * grp]), kidx, inp.lens[s], 7, 9)
+            check_sink_row(res["idx"][s, h].cpu().numpy(), r["scores"], 7, r["forced"], 9, True)
 
 
 def test_token_max_short_and_empty_sequences(dev):
@@ -101,6 +124,11 @@ def test_token_max_decode_128k_sampled(dev):
     assert res["status"] == 0
     stats = SelectionStats()
     verify(inp, ik, res, [(0, 0), (3, 5), (7, 7)], 31, 32, stats)
+    # the benchmark's launch: the fused step, its lists equal to the two-kernel form's on every unit
+    res_step = run_token_max(inp, ik, 31, 32, step=True)
+    assert res_step["status"] == 0
+    assert torch.equal(res_step["idx"], res["idx"])
+    verify(inp, ik, res_step, [(1, 2), (6, 0)], 31, 32)
     del inp, ik
     torch.cuda.empty_cache()
 
