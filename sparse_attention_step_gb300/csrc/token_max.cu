@@ -266,7 +266,28 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
   const int npair = (nblk + 1) / 2;
   pdl_wait();
 
-  if (tid == 0) {
+  // index-key row of block j of this chunk, -1 for a bad page
+  auto row_of = [&](int j) -> int32_t {
+    const int64_t b = b0 + j;
+    if (kv.layout == MSA_KV_CONTIGUOUS) return static_cast<int32_t>(static_cast<int64_t>(seq) * kv.max_tokens + b * kBlock);
+    const int32_t p = kv.page(seq, b, a.status, kIdScore);
+    return p < 0 ? -1 : p * kBlock;
+  };
+  auto issue_pair = [&](int p, int slot) {  // the producer: block pair p into ring slot `slot`
+    const int nb_p = min(2, nblk - 2 * p);  // the last pair of an odd chunk has one block
+    uint8_t* dst = ring + slot * kTpStage;
+    mbar_arrive_expect_tx(&st.kv_full[slot], nb_p * kTmStage);
+    for (int e = 0; e < nb_p; ++e) {
+      const int32_t r = row_of(2 * p + e);
+      const int32_t y = r < 0 ? 0 : r;
+      tma_load_2d(dst + e * 8192, &tmi, 0, y, &st.kv_full[slot]);
+      tma_load_2d(dst + 16384 + e * 8192, &tmi, 64, y, &st.kv_full[slot]);
+    }
+  };
+  // The producer sets up the barriers and issues the first pairs at once, so
+  // they travel while A is built.
+  const int n_pre = min(kTpStages, npair);
+  if (warp == kTpProducer && lane == 0) {
     for (int i = 0; i < kTpStages; ++i) {
       mbar_init(&st.kv_full[i], 1);
       mbar_init(&st.kv_empty[i], 1);
@@ -277,34 +298,34 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
     }
     mbar_init(&st.drain, 1);
     fence_mbar_init();
+    tma_prefetch_desc(&tmi);
+    for (int p = 0; p < n_pre; ++p) issue_pair(p, p);
   }
-  if (tid < kTpMaxChunk) {
-    int32_t r = -1;
-    if (tid < nblk) {
-      const int64_t b = b0 + tid;
-      if (kv.layout == MSA_KV_CONTIGUOUS) {
-        r = static_cast<int32_t>(static_cast<int64_t>(seq) * kv.max_tokens + b * kBlock);
-      } else {
-        const int32_t p = kv.page(seq, b, a.status, kIdScore);
-        r = p < 0 ? -1 : p * kBlock;
-      }
-    }
-    st.rowid[tid] = r;
-  }
+  if (tid < kTpMaxChunk) st.rowid[tid] = tid < nblk ? row_of(tid) : -1;
   // A: row r = 8 (tile) + head; 16-byte piece c16 of a row's 256 bytes goes to
-  // [operand][dim half][row][(c16 mod 8) ^ (row mod 8)] (the TMA 128-byte swizzle)
-  for (int i = tid; i < 128 * 16; i += kTpThreads) {
-    const int row = i >> 4, c16 = i & 15;
-    float x[8];
+  // [operand][dim half][row][(c16 mod 8) ^ (row mod 8)] (the TMA 128-byte swizzle).
+  // Every index-query load of this thread is in flight before the first is used.
+  constexpr int kAIt = (128 * 16 + kTpThreads - 1) / kTpThreads;
+  float4 qu[kAIt], qv[kAIt];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = 0.f;
+  for (int it = 0; it < kAIt; ++it) {
+    const int i = tid + it * kTpThreads;
+    const int row = i >> 4, c16 = i & 15;
     const int g = row >> 3, h = row & 7;
-    if (h < a.hkv && t0 + g < t_end) {
+    qu[it] = qv[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i < 128 * 16 && h < a.hkv && t0 + g < t_end) {
       const float4* qi = reinterpret_cast<const float4*>(a.qidx + (static_cast<int64_t>(t0 + g) * a.hkv + h) * kHeadDim +
                                                          8 * c16);
-      const float4 u = qi[0], v = qi[1];
-      x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w; x[4] = v.x; x[5] = v.y; x[6] = v.z; x[7] = v.w;
+      qu[it] = qi[0];
+      qv[it] = qi[1];
     }
+  }
+#pragma unroll
+  for (int it = 0; it < kAIt; ++it) {
+    const int i = tid + it * kTpThreads;
+    if (i >= 128 * 16) break;
+    const int row = i >> 4, c16 = i & 15;
+    const float x[8] = {qu[it].x, qu[it].y, qu[it].z, qu[it].w, qv[it].x, qv[it].y, qv[it].z, qv[it].w};
     uint32_t hi[4], lo[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -330,20 +351,11 @@ __global__ void __launch_bounds__(kTpThreads, 1) token_max_prefill_kernel(const 
   if (warp == kTpProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmi);
-      int issued = 0;
-      for (int p = 0; p < npair; ++p) {
+      int issued = n_pre;
+      for (int p = n_pre; p < npair; ++p) {
         const int slot = p % kTpStages;
         if (p >= kTpStages && !mbar_wait(&st.kv_empty[slot], ((p / kTpStages) - 1) & 1, a.status, kIdScore)) break;
-        const int nb_p = min(2, nblk - 2 * p);  // the last pair of an odd chunk has one block
-        uint8_t* dst = ring + slot * kTpStage;
-        mbar_arrive_expect_tx(&st.kv_full[slot], nb_p * kTmStage);
-        for (int e = 0; e < nb_p; ++e) {
-          const int32_t r = st.rowid[2 * p + e];
-          const int32_t y = r < 0 ? 0 : r;
-          tma_load_2d(dst + e * 8192, &tmi, 0, y, &st.kv_full[slot]);
-          tma_load_2d(dst + 16384 + e * 8192, &tmi, 64, y, &st.kv_full[slot]);
-        }
+        issue_pair(p, slot);
         issued = p + 1;
       }
       // every load this thread issued has landed before the CTA may exit
