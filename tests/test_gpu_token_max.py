@@ -196,3 +196,33 @@ def test_token_max_prefill_sink(dev):
             q_tile = to64(inp.q[64 * j:min(131, 64 * j + 64), 8 * h:8 * h + 8])
             ref = O.prefill_tile_select_token_max(q_tile, j, 64 * 12, kidx, 4, 6)
             check_sink_row(res["idx"][j, h].cpu().numpy(), ref["scores"], 4, ref["diag"], 6, True)
+
+
+def test_token_max_prefill_8k_on_128k_sampled(dev):
+    """The benchmark's chunk (8192 new tokens on a 131072-token prefix, 8 KV /
+    64 query heads, top-32 + diagonal) in token-max mode, in the launch the
+    benchmark times: the scores and selections of 32 (tile, head) units spread
+    over the chunk and the heads against the oracle."""
+    from synth import make_prefill_batch_inputs
+    from tests.parity import record
+    q0, n_new, k_scored, k_total = 131072, 8192, 32, 33
+    inp = make_prefill_batch_inputs([q0], [n_new], 8, 64, "bf16", "contiguous", seed=1004, device=dev)
+    ik = make_index_keys(inp.cache, needles=0, seed=4007)
+    res = run_token_max_prefill(inp, ik, k_scored, k_total)
+    assert res["status"] == 0
+    kidx = to64(ik.rows(inp.cache, 0))
+    qs = inp.q_rows(0)
+    tiles = list(O.prefill_tiles(q0, n_new))
+    stats = SelectionStats()
+    for i in range(32):
+        j, lo, hi = tiles[(i * 37) % len(tiles)]
+        h = i % 8
+        q_tile = to64(qs[lo:hi, 8 * h:8 * h + 8])
+        ref = O.prefill_tile_select_token_max(q_tile, j, q0, kidx, k_scored, k_total)
+        got = to64(res["scores"][j * 8 + h, :ref["diag"]])
+        lim = 1e-5 * np.maximum(1.0, np.abs(ref["scores"])) + 1e-5 * np.abs(ref["q_idx"]).sum()
+        assert (np.abs(got - ref["scores"]) <= lim).all(), f"token-max scores differ, tile {j} head {h}"
+        check_selection(res["idx"][j, h].cpu().numpy(), ref["scores"], k_scored, ref["diag"], k_total, stats)
+    record("prefill_8k_on_128k token-max (sampled)", units=stats.units, near_ties=stats.near_ties)
+    del inp, ik, res
+    torch.cuda.empty_cache()
