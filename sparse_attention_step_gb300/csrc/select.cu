@@ -703,7 +703,7 @@ constexpr int kTopk64Threads = 256;
 constexpr int kTopk64MaxCand = 4096;
 static_assert(kTopk64Threads == 4 * 64, "64 sample groups of four threads each");
 size_t topk64_smem(int64_t max_blocks) { return static_cast<size_t>(max_blocks) * sizeof(uint64_t); }
-__global__ void __launch_bounds__(kTopk64Threads, 6) topk64_kernel(const float* __restrict__ scores, KvView kv, TopkArgs a,
+__global__ void __launch_bounds__(kTopk64Threads, 8) topk64_kernel(const float* __restrict__ scores, KvView kv, TopkArgs a,
                                                               int32_t* __restrict__ idx_out, int32_t* status) {
   extern __shared__ __align__(16) uint64_t tk[];  // keys [max_blocks]
   __shared__ uint64_t top[64];
@@ -735,18 +735,17 @@ __global__ void __launch_bounds__(kTopk64Threads, 6) topk64_kernel(const float* 
   const int n = static_cast<int>(n64) - skip;
   const int k = min(a.k_scored, n);
   const float* sc = scores + unit * a.max_blocks;
-  {
-    // every score load in flight at once, then the keys
-    constexpr int kPer = kTopk64MaxCand / kTopk64Threads;
-    float v[kPer];
+  // the score loads eight at a time in flight, then their keys
+  for (int base = 0; base < n; base += 8 * kTopk64Threads) {
+    float v[8];
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int i = threadIdx.x + u * kTopk64Threads;
+    for (int u = 0; u < 8; ++u) {
+      const int i = base + threadIdx.x + u * kTopk64Threads;
       v[u] = i < n ? sc[i + skip] : 0.f;
     }
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int i = threadIdx.x + u * kTopk64Threads;
+    for (int u = 0; u < 8; ++u) {
+      const int i = base + threadIdx.x + u * kTopk64Threads;
       if (i < n) tk[i] = sel_key(v[u], i + skip);
     }
   }

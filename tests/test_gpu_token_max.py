@@ -106,11 +106,12 @@ def test_token_max_decode_step_sink(dev):
             check_sink_row(res["idx"][s, h].cpu().numpy(), r["scores"], 7, r["forced"], 9, True)
 
 
-def test_token_max_short_and_empty_sequences(dev):
+@pytest.mark.parametrize("step", [False, True])
+def test_token_max_short_and_empty_sequences(dev, step):
     # no candidates (one partial block), exactly one complete block, and k above the candidates
     inp = make_decode_inputs([40, 64, 64 * 3 + 2], 2, 16, "bf16", "contiguous", seed=45, device=dev)
     ik = make_index_keys(inp, seed=46)
-    res = run_token_max(inp, ik, 5, 6)
+    res = run_token_max(inp, ik, 5, 6, step=step)
     assert res["status"] == 0
     verify(inp, ik, res, [(s, h) for s in range(3) for h in range(2)], 5, 6)
 
