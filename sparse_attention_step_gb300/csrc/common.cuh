@@ -126,6 +126,17 @@ __device__ inline bool mbar_wait_warp_limit(uint64_t* bar, uint32_t parity, int3
   return __all_sync(0xffffffffu, mbar_wait_limit(bar, parity, status, where, limit_cycles));
 }
 
+// Waits (bounded) until the copies of the last `stages` ring stages issued so
+// far (stage i in slot i % stages, i < issued) have landed. A producer calls
+// it before its CTA moves on: in a normal run the consumers have already
+// waited for them all and it returns at once; after a bounded wait gave up
+// somewhere it keeps copies still in flight from landing in shared memory
+// that is reused or released.
+__device__ inline void mbar_drain(uint64_t* full, int stages, int issued, int32_t* status, int where) {
+  for (int i = issued > stages ? issued - stages : 0; i < issued; ++i)
+    mbar_wait(&full[i % stages], static_cast<uint32_t>((i / stages) & 1), status, where);
+}
+
 // ---------------------------------------------------------------------------
 // TMA: 2-D tiled bulk tensor copy global -> shared, completing on an mbarrier.
 // x is the innermost coordinate (elements), y the row.

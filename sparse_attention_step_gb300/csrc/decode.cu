@@ -328,9 +328,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_bf16_kernel(const __grid_c
   if (warp == kDecConsumers) {
     // ---------------- producer ----------------
     if (lane == 0) {
+      int issued = 0;
       for (int i = 0; i < nblk; ++i) {
         const int stg = i % kStages;
         if (i >= kStages && !mbar_wait(&st.empty[stg], ((i / kStages) - 1) & 1, a.status, kIdDecode)) break;
+        issued = i + 1;
         const int64_t row = kv.block_row(s, h, a.idx ? st.blocks[i] : st.dense_lo + i, a.status, kIdDecode);
         uint8_t* dst = ring + stg * kStageBytes;
         mbar_arrive_expect_tx(&st.full[stg], kStageBytes);
@@ -340,6 +342,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_bf16_kernel(const __grid_c
         tma_load_2d(dst + 16384, &tmv, 0, y, &st.full[stg]);
         tma_load_2d(dst + 24576, &tmv, 64, y, &st.full[stg]);
       }
+      mbar_drain(st.full, kStages, issued, a.status, kIdDecode);
     }
   } else {
     // ---------------- consumers ----------------

@@ -86,9 +86,11 @@ __global__ void __launch_bounds__(kPfThreads) prefill_bf16_kernel(const __grid_c
     if (lane == 0) {
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
+      int issued = 0;
       for (int i = 0; i < nblk; ++i) {
         const int stg = i % kPfStages;
         if (i >= kPfStages && !mbar_wait(&st.empty[stg], ((i / kPfStages) - 1) & 1, a.status, kIdPrefill)) break;
+        issued = i + 1;
         const int b = dense ? i : st.blocks[i];
         const int64_t row = kv.block_row(seq, h, b, a.status, kIdPrefill);
         uint8_t* dst = ring + stg * kPfStageBytes;
@@ -99,6 +101,7 @@ __global__ void __launch_bounds__(kPfThreads) prefill_bf16_kernel(const __grid_c
         tma_load_2d(dst + 16384, &tmv, 0, y, &st.full[stg]);
         tma_load_2d(dst + 24576, &tmv, 64, y, &st.full[stg]);
       }
+      mbar_drain(st.full, kPfStages, issued, a.status, kIdPrefill);
     }
     return;  // the producer takes no part in the epilogue
   }

@@ -939,6 +939,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
     if (warp == kSelWarps) {
       // ---------------- producer: one bulk copy per stage ----------------
       if (lane == 0) {
+        int issued = 0;
         for (int st = 0; st < n_stages; ++st) {
           const int slot = st % kSelStages;
           if (st >= kSelStages && !mbar_wait(&empty[slot], ((st / kSelStages) - 1) & 1, status, kIdScore)) break;
@@ -947,7 +948,9 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
           const T* src = pooled + ((static_cast<int64_t>(s) * a.hkv + h) * a.max_blocks + r0 + base) * kHeadDim;
           mbar_arrive_expect_tx(&full[slot], n * kRowBytes);
           bulk_load(ring + slot * kSelStageBytes, src, n * kRowBytes, &full[slot]);
+          issued = st + 1;
         }
+        mbar_drain(full, kSelStages, issued, status, kIdScore);
       }
     } else {
       // ---------------- scorers ----------------

@@ -190,6 +190,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     if (lane == 0) {
       // 128 summary rows per stage as two 64-column boxes (128-byte swizzle);
       // rows past the CTA's chunk are loaded but never scored
+      int issued = n_pre;
       for (int st = n_pre; st < n_st; ++st) {
         const int slot = st % kStages;
         if (st >= kStages && !mbar_wait(&empty[slot], ((st / kStages) - 1) & 1, a.status, kIdDecode)) break;
@@ -197,9 +198,11 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
         mbar_arrive_expect_tx(&full[slot], kStStage);
         tma_load_2d(dst, &tmpool, 0, y0 + st * kStRowsPerStage, &full[slot]);
         tma_load_2d(dst + kStStage / 2, &tmpool, 64, y0 + st * kStRowsPerStage, &full[slot]);
+        issued = st + 1;
       }
-      // early stages beyond this chunk's candidates: wait until they land
-      for (int st = n_st; st < n_pre; ++st) mbar_wait(&full[st], 0, a.status, kIdDecode);
+      // every stage issued has landed, the early ones beyond this chunk's
+      // candidates (never read) included, before the ring is reused
+      mbar_drain(full, kStages, issued, a.status, kIdDecode);
     }
   } else {
     // S = K_pool q_idx on the tensor cores, warp w taking rows 16w..16w+15 of
@@ -437,9 +440,11 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
   for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   if (warp == kStWarps) {
     if (lane == 0) {
+      int issued = 0;
       for (int i = 0; i < nblk; ++i) {
         const int slot = i % kStages;
         if (i >= kStages && !mbar_wait(&empty[slot], ((i / kStages) - 1) & 1, a.status, kIdDecode)) break;
+        issued = i + 1;
         const int32_t b = slice_at(lo + i);
         if (b >= nb) set_status(a.status, MSA_ERR_DEVICE_BOUNDS, kIdDecode);  // its keys are masked below
         const int64_t row = b < nb ? kv.block_row(s, h, b, a.status, kIdDecode) : -1;
@@ -451,6 +456,7 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
         tma_load_2d(dst + 16384, &tmv, 0, y, &full[slot]);
         tma_load_2d(dst + 24576, &tmv, 64, y, &full[slot]);
       }
+      mbar_drain(full, kStages, issued, a.status, kIdDecode);
     }
   } else if (warp < kStAttnWarps) {
     uint32_t qb[8][2];

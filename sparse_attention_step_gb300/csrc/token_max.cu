@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __gri
 
   if (warp == kTmWarps) {
     if (lane == 0) {
+      int issued = n_pre;
       for (int j = n_pre; j < nblk; ++j) {
         const int slot = j % kTmStages;
         if (j >= kTmStages && !mbar_wait(&empty[slot], ((j / kTmStages) - 1) & 1, a.status, kIdScore)) break;
@@ -129,7 +130,9 @@ __global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __gri
         mbar_arrive_expect_tx(&full[slot], kTmStage);
         tma_load_2d(dst, &tmi, 0, y, &full[slot]);
         tma_load_2d(dst + kTmStage / 2, &tmi, 64, y, &full[slot]);
+        issued = j + 1;
       }
+      mbar_drain(full, kTmStages, issued, a.status, kIdScore);
     }
   } else {
     const int g = lane >> 2, c = lane & 3;
