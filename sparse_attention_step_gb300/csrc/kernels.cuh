@@ -12,7 +12,7 @@ namespace msa {
 // sit in: tile j holds the chunk rows r with (q_start[s] + r) / 64 ==
 // q_start[s] / 64 + j (its diagonal block), so a chunk that starts inside a
 // block has a shorter first tile. They are global tiles tile_off[s] ..
-// tile_off[s + 1] - 1, and the prefill scorer takes them in groups of 8
+// tile_off[s + 1] - 1, and the prefill scorer takes them in groups of 16
 // (global groups grp_off[s] .. grp_off[s + 1] - 1).
 constexpr int kMaxPrefillSeqs = 64;
 struct PrefillBatch {

@@ -250,16 +250,16 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const T* __restric
 
 // ---------------------------------------------------------------------------
 // Prefill block scores on the tensor cores (bf16 summaries).
-// grid (ceil(rows / 128), Hkv, ceil(n_tiles / 8)), 256 threads. The CTA copies
-// 128 summary rows into shared memory with cp.async (128-byte swizzle, two
-// 64-dim halves) and each warp scores 16 of them against the index queries of
-// 8 tiles at once: mma.sync with the 8 tiles as the N columns, the fp32 index
-// queries split into a bf16 head and a bf16 remainder (two n-tiles). The 8
-// index queries are read once per CTA (coalesced) into shared memory, where
-// every warp takes its operand fragments.
+// grid (ceil(rows / 128), Hkv, ceil(n_tiles / 16)), 256 threads. The CTA
+// copies 128 summary rows into shared memory with cp.async (128-byte swizzle,
+// two 64-dim halves) and each warp scores 16 of them against the index queries
+// of 16 tiles at once: mma.sync with the tiles as the N columns (two n-tiles
+// of 8), the fp32 index queries split into a bf16 head and a bf16 remainder.
+// The 16 index queries are read once per CTA (coalesced) into shared memory,
+// where every warp takes its operand fragments.
 // ---------------------------------------------------------------------------
 constexpr int kPsRows = 128;
-constexpr int kPsTiles = 8;
+constexpr int kPsTiles = 16;
 
 __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __restrict__ qidx_ws,
                                                                 const __nv_bfloat16* __restrict__ pooled,
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __r
   __shared__ __align__(1024) uint8_t rows_s[kPsRows * kHeadDim * 2];
   __shared__ __align__(16) float qs[kPsTiles][kHeadDim + 8];  // padded: conflict-free 8-byte fragment reads
   const int h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // 8 tiles of one sequence: global tiles t0 .. t_end - 1, local tiles j0 ..
+  // 16 tiles of one sequence: global tiles t0 .. t_end - 1, local tiles j0 ..
   const int seq = pb.seq_of_group(blockIdx.z);
   const int j0 = (blockIdx.z - pb.grp_off[seq]) * kPsTiles;
   const int t0 = pb.tile_off[seq] + j0;
@@ -290,9 +290,10 @@ __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __r
                  pooled + kv.pooled_row(seq, h, b) * kHeadDim + 8 * pc);
   }
   cp_async_commit();
-  {
-    // the 8 tiles' index queries (zeros past the last tile), one float4 a thread
-    const int tt = tid >> 5, d4 = tid & 31;
+#pragma unroll
+  for (int u = 0; u < kPsTiles / 8; ++u) {
+    // the 16 tiles' index queries (zeros past the last tile), one float4 a thread each time
+    const int tt = 8 * u + (tid >> 5), d4 = tid & 31;
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
     if (t0 + tt < t_end)
       x = reinterpret_cast<const float4*>(qidx_ws + (static_cast<int64_t>(t0 + tt) * a.hkv + h) * kHeadDim)[d4];
@@ -300,41 +301,44 @@ __global__ void __launch_bounds__(256) score_prefill_mma_kernel(const float* __r
   }
   cp_async_wait<0>();
   __syncthreads();
-  // B operands: column g = tile t0 + g
-  const int g = lane >> 2, c = lane & 3;
-  uint32_t qh[8][2], ql[8][2];
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-    for (int hlf = 0; hlf < 2; ++hlf) {
-      const int d = 16 * kk + 2 * c + 8 * hlf;
-      const float2 x = *reinterpret_cast<const float2*>(&qs[g][d]);
-      const float h0 = __bfloat162float(__float2bfloat16_rn(x.x));
-      const float h1 = __bfloat162float(__float2bfloat16_rn(x.y));
-      qh[kk][hlf] = pack_bf16(h0, h1);
-      ql[kk][hlf] = pack_bf16(x.x - h0, x.y - h1);
-    }
-  }
   const uint32_t sbase = smem_u32(rows_s);
   const int krow = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8;
   const int kchunk = lane >> 4;
-  float hi[4] = {0.f, 0.f, 0.f, 0.f}, lo[4] = {0.f, 0.f, 0.f, 0.f};
+  const int g = lane >> 2, c = lane & 3;
+  // one n-tile of 8 tiles at a time; B operands: column g = tile t0 + 8 nt + g
+#pragma unroll 1
+  for (int nt = 0; nt < kPsTiles / 8; ++nt) {
+    uint32_t qh[8][2], ql[8][2];
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    uint32_t a0, a1, a2, a3;
-    ldsm_x4(sbase + (kk >> 2) * (kPsRows * 128) + swz128(krow, (kk & 3) * 2 + kchunk), a0, a1, a2, a3);
-    mma_bf16(hi, a0, a1, a2, a3, qh[kk][0], qh[kk][1]);
-    mma_bf16(lo, a0, a1, a2, a3, ql[kk][0], ql[kk][1]);
-  }
-  // lane: rows 16 warp + g (+8), tiles 2c and 2c + 1
+    for (int kk = 0; kk < 8; ++kk) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int64_t b = chunk0 + 16 * warp + g + 8 * (k >> 1);
-    const int tile = t0 + 2 * c + (k & 1);
-    if (b < row_end && tile < t_end) {
-      const int64_t n_cand = diag0 + (tile - t0);
-      const bool ok = b < n_cand;
-      scores[(static_cast<int64_t>(tile) * a.hkv + h) * a.max_blocks + b] = ok ? hi[k] + lo[k] : -INFINITY;
+      for (int hlf = 0; hlf < 2; ++hlf) {
+        const int d = 16 * kk + 2 * c + 8 * hlf;
+        const float2 x = *reinterpret_cast<const float2*>(&qs[8 * nt + g][d]);
+        const float h0 = __bfloat162float(__float2bfloat16_rn(x.x));
+        const float h1 = __bfloat162float(__float2bfloat16_rn(x.y));
+        qh[kk][hlf] = pack_bf16(h0, h1);
+        ql[kk][hlf] = pack_bf16(x.x - h0, x.y - h1);
+      }
+    }
+    float hi[4] = {0.f, 0.f, 0.f, 0.f}, lo[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(sbase + (kk >> 2) * (kPsRows * 128) + swz128(krow, (kk & 3) * 2 + kchunk), a0, a1, a2, a3);
+      mma_bf16(hi, a0, a1, a2, a3, qh[kk][0], qh[kk][1]);
+      mma_bf16(lo, a0, a1, a2, a3, ql[kk][0], ql[kk][1]);
+    }
+    // lane: rows 16 warp + g (+8), tiles 8 nt + 2c and 8 nt + 2c + 1
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t b = chunk0 + 16 * warp + g + 8 * (k >> 1);
+      const int tile = t0 + 8 * nt + 2 * c + (k & 1);
+      if (b < row_end && tile < t_end) {
+        const int64_t n_cand = diag0 + (tile - t0);
+        const bool ok = b < n_cand;
+        scores[(static_cast<int64_t>(tile) * a.hkv + h) * a.max_blocks + b] = ok ? hi[k] + lo[k] : -INFINITY;
+      }
     }
   }
 }
