@@ -266,7 +266,10 @@ msa_status msa_sparse_attn_prefill_varlen(const void* q, int32_t num_q_heads, in
  * device): one thread-block cluster per (sequence, KV head) scores the
  * summaries, selects and attends, exchanging the lists and the partial
  * results through distributed shared memory (nothing round-trips through the
- * workspace); otherwise it launches the two kernels in turn. ws must hold
+ * workspace); otherwise it launches the two kernels in turn. In token-max mode
+ * (cfg->mode, pooled = the index-key cache, Hkv <= 8) the token scores are
+ * written to the workspace by their own kernel first and the cluster kernel
+ * selects and attends on them. ws must hold
  * msa_workspace_size(MSA_OP_DECODE_STEP, ...) bytes. */
 msa_status msa_sparse_decode_step(const void* q, int32_t num_q_heads, const void* pooled,
                                   const msa_kv_desc* kv /* host */, const msa_select_cfg* cfg /* host */,
