@@ -118,6 +118,13 @@ __global__ void __launch_bounds__(kStThreads, 2) decode_step_kernel(const __grid
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
     tma_prefetch_desc(&tmpool);
+    // While the kernel before this one finishes, its first stages' rows are
+    // pulled into L2 (a prefetch has no result: if that kernel writes any of
+    // them, the loads below, issued after it has completed, read its values).
+    for (int st = 0; st < n_pre; ++st) {
+      tma_prefetch_2d(&tmpool, 0, y0 + st * kStRowsPerStage);
+      tma_prefetch_2d(&tmpool, 64, y0 + st * kStRowsPerStage);
+    }
     pdl_wait();
     for (int st = 0; st < n_pre; ++st) {
       uint8_t* dst = ring + st * kStStage;
