@@ -56,6 +56,18 @@ __global__ void __launch_bounds__(kTmThreads) token_max_score_kernel(const __gri
   auto& part = sh.part;
 
   const int s = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (kv.layout == MSA_KV_CONTIGUOUS && warp == kTmWarps && lane == 0) {
+    // While the kernel before this one finishes, the first blocks of this
+    // chunk are pulled into L2 (a prefetch has no result: if that kernel
+    // writes any of them, the loads, issued after it has completed, read its
+    // values).
+    const int64_t bp = static_cast<int64_t>(blockIdx.x) * a.chunk;
+    for (int j = 0; j < kTmStages && bp + j < a.max_blocks; ++j) {
+      const int32_t r = static_cast<int32_t>(static_cast<int64_t>(s) * kv.max_tokens + (bp + j) * kBlock);
+      tma_prefetch_2d(&tmi, 0, r);
+      tma_prefetch_2d(&tmi, 64, r);
+    }
+  }
   pdl_wait();
   const int64_t len = kv.seq_len(s, a.status, kIdScore);
   const int64_t nb = (len + kBlock - 1) / kBlock;
