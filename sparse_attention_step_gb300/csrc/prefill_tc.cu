@@ -18,10 +18,11 @@
 // An M128 MMA costs about the same at N = 64 as at N = 128, so scoring a pair
 // at once halves the tensor time of Q K^T against one block at a time.
 // Warp roles: warps 0-7 softmax of tile 0 and warps 8-15 of tile 1; within a
-// tile, warps 0-3 take the pair's first block (score columns 0-63) and warps
-// 4-7 its second (columns 64-127) for the rows in TMEM lanes 32 (w mod 4) ..
-// (a warp reaches only those lanes); the two halves of a row exchange their
-// maxima and sums through shared memory (a named barrier per tile). Warp 16 is
+// tile, warp w takes 16 rows of the TMEM lanes 32 (w mod 4) .. (a warp
+// reaches only those lanes), both halves of each: its threads j < 16 hold the
+// pair's first block (score columns 0-63) and threads j + 16 the second
+// (columns 64-127) of the same row (the 16x32bx2 TMEM access shape), so the
+// halves exchange their maxima and sums with a shuffle. Warp 16 is
 // the TMA producer (Q once, then 2-stage K and V rings of one pair each; K of
 // a stage is released once both tiles' S are computed, V once both tiles'
 // O += P V are), warp 17 the TMEM allocator and MMA issuer. The two tiles
@@ -304,13 +305,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
     }
   } else {
     // ------------------------------------------------------------ softmax
-    __shared__ float xmax[2][kTcTiles][2][128];  // [pair parity][tile][half][row]
-    __shared__ float xsum[kTcTiles][2][128];
+    // Each warp takes 16 rows of its TMEM lane quadrant, both halves of each
+    // row: thread j < 16 the scores of the pair's first block (columns
+    // [0, 64)), thread j + 16 those of the second (columns [64, 128)) of the
+    // same row, so the two halves meet by a shuffle.
     const int t = warp >> 3;                // tile
-    const int hf = (warp >> 2) & 1;         // block of the pair: score columns [64 hf, 64 hf + 64)
-    const int q4 = warp & 3;                // TMEM lane quadrant
-    const int r = 32 * q4 + lane;           // row within the tile = TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+    const int q4 = warp & 3;                // TMEM lane quadrant (the lanes this warp may access)
+    const int sub = (warp >> 2) & 1;        // its lanes [16 sub, 16 sub + 16) of the quadrant
+    const int hf = lane >> 4;               // block of the pair: score columns [64 hf, 64 hf + 64)
+    const int r = 32 * q4 + 16 * sub + (lane & 15);  // row within the tile = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q4 + 16 * sub) << 16;
     const int bar_id = 1 + t;               // the tile's 8 softmax warps
     const int tt = rh * (kTcTiles * 16) + 16 * t + (r >> 3);  // token within the 64-token tile
     const int head = h * 8 + (r & 7);
@@ -327,11 +331,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       tc::fence_after();
       const bool have = hf < blocks_in(i);  // the odd last pair has no second block
       uint32_t sa[32], sb[32];
-      if (ok && have) {
-        const uint32_t sad = tmem + lane_base + t * 128 + 64 * hf;
-        tc::ld64(sad, sa, sb);
+      if (ok) {  // the whole warp loads (columns 64 hf .. 64 hf + 63 of its rows)
+        tc::ld64_h2(tmem + lane_base + t * 128, sa, sb);
         tc::wait_ld();
-      } else {
+      }
+      if (!(ok && have)) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) sa[c] = sb[c] = __float_as_uint(-INFINITY);
       }
@@ -355,14 +359,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
         w[7] = u[21];
         mx = fmax3(fmax3(w[0], w[1], w[2]), fmax3(w[3], w[4], w[5]), fmaxf(w[6], w[7]));
       }
-      xmax[i & 1][t][hf][r] = mx;
-      named_bar_sync(bar_id, 256);
-      mx = fmaxf(mx, xmax[i & 1][t][hf ^ 1][r]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // the row's other half
       const float m_blk = mx * a.scale_log2;  // -inf stays -inf
       const float m_new = fmaxf(m, m_blk);
       const bool need = (m == -INFINITY) ? (m_new != -INFINITY) : (m_new > m + kRescaleLog2);
-      // the rows of this warp (the same rows as the partner warp of the other
-      // half, so both take the same decision) move to the new max together
+      // the rows of this warp (both halves of each are in it, so both take the
+      // same decision) move to the new max together
       const bool resc = __any_sync(0xffffffffu, need);
       float alpha = 1.f;
       if (resc) {
@@ -374,9 +376,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nr2 = make_float2(neg_ref, neg_ref);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0;
       // P replaces the scores it came from: columns [32 hf, 32 hf + 32) of the
-      // tile's S buffer hold keys [64 hf, 64 hf + 64) in pairs (the other
-      // half read those columns before the barrier above). The next S into
-      // the buffer is issued after O += P V of this pair.
+      // tile's S buffer hold keys [64 hf, 64 hf + 64) in pairs (the row's
+      // other half, in this warp, read those columns in the load above; no
+      // other warp touches these rows). The next S into the buffer is issued
+      // after O += P V of this pair.
       auto exp_store = [&](const uint32_t (&sr)[32], uint32_t col) {
         uint32_t pk[16];
 #pragma unroll
@@ -387,10 +390,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
           else acc0 = fadd2(acc0, pp);
           pk[c] = pack_bf16(pp.x, pp.y);
         }
-        if (ok && have) tc::st16(tmem + lane_base + t * 128 + col, pk);
+        // threads j < 16 store at `col`, threads j + 16 at `col` + 32 (for a
+        // missing second block they store zeros, which nothing reads)
+        if (ok) tc::st16_h2<32>(tmem + lane_base + t * 128 + col, pk);
       };
-      exp_store(sa, 32 * hf);
-      exp_store(sb, 32 * hf + 16);
+      exp_store(sa, 0);
+      exp_store(sb, 16);
       const float2 acc = fadd2(acc0, acc1);
       const float sum = acc.x + acc.y;
       // O of this half rescaled to the new max (after the scores are consumed,
@@ -399,12 +404,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
 #pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t o[32];
-          const uint32_t oa = tmem + lane_base + 256 + t * 128 + 64 * hf + cc * 32;
-          tc::ld32(oa, o);
+          const uint32_t oa = tmem + lane_base + 256 + t * 128 + cc * 32;  // columns + 64 hf
+          tc::ld32_h2(oa, o);
           tc::wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-          tc::st32(oa, o);
+          tc::st32_h2<64>(oa, o);
         }
       }
       tc::wait_st();
@@ -414,9 +419,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
       if (lane == 0 && ok) mbar_arrive(&st.p_full[t]);
     }
     // epilogue: the row's two half sums, then O / l in bf16 and the lse
-    xsum[t][hf][r] = l;
-    named_bar_sync(bar_id, 256);
-    const float L = l + xsum[t][hf ^ 1][r];
+    const float L = l + __shfl_xor_sync(0xffffffffu, l, 16);
     ok = __all_sync(0xffffffffu, ok && wait_or_abort(&st.o_final[t], 0, abort, a.status));
     tc::fence_after();
     const float inv = (L > 0.f) ? 1.f / L : 0.f;
@@ -428,7 +431,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
 #pragma unroll 1
     for (int cc = 0; cc < 2; ++cc) {
       uint32_t o[32];
-      tc::ld32(tmem + lane_base + 256 + t * 128 + 64 * hf + cc * 32, o);
+      tc::ld32_h2(tmem + lane_base + 256 + t * 128 + cc * 32, o);  // columns + 64 hf
       tc::wait_ld();
       if (nblk == 0 || !ok) {
 #pragma unroll
