@@ -9,7 +9,8 @@
 // and compute S[token, group] = K_idx q_idx^T with mma.sync, the fp32 index
 // queries of up to 8 groups split into a bf16 head (one n-tile) and a bf16
 // remainder (a second n-tile), then reduce the max over their tokens. The
-// block maxima go to the score buffer that the top-k kernel reads.
+// block maxima go to the score buffer that the fused decode step (or the
+// top-k kernel) reads.
 #include <float.h>
 
 #include "kernels.cuh"
