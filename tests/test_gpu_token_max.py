@@ -76,18 +76,19 @@ def test_token_max_select_and_attend(dev, layout, hkv, hq):
 
 
 @pytest.mark.parametrize("layout", ["contiguous", "paged"])
-def test_token_max_through_the_decode_step(dev, layout):
+@pytest.mark.parametrize("hkv,hq", [(4, 32), (2, 8), (1, 8)])
+def test_token_max_through_the_decode_step(dev, layout, hkv, hq):
     """The decode step in token-max mode: the scores from their own kernel,
     then the fused step reads them in place of scoring summaries. Its lists
     equal those of the two-kernel form (the same scores and keys) and its
-    outputs the oracle's."""
-    inp = make_decode_inputs([64 * 200 + 5, 64 * 64, 64 * 3 + 1], 4, 32, "bf16", layout, seed=43, device=dev)
+    outputs the oracle's; group sizes 8 and 4, one to four KV heads."""
+    inp = make_decode_inputs([64 * 200 + 5, 64 * 64, 64 * 3 + 1], hkv, hq, "bf16", layout, seed=43, device=dev)
     ik = make_index_keys(inp, needles=3, seed=44)
     res = run_token_max(inp, ik, 11, 12, step=True)
     ref = run_token_max(inp, ik, 11, 12)
     assert res["status"] == 0 and ref["status"] == 0
     assert torch.equal(res["idx"], ref["idx"])
-    verify(inp, ik, res, [(s, h) for s in range(3) for h in range(4)], 11, 12)
+    verify(inp, ik, res, [(s, h) for s in range(3) for h in range(hkv)], 11, 12)
 
 
 def test_token_max_decode_step_sink(dev):
