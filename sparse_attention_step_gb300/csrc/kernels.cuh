@@ -112,6 +112,7 @@ struct PrefillArgs {
   __nv_bfloat16* out;
   float* lse;
   int32_t* status;
+  int num_sms;  // the device's SMs (the tcgen05 kernel's prefetch for the next wave of CTAs)
 };
 cudaError_t set_prefill_smem();
 cudaError_t set_prefill_tc_smem();

@@ -225,6 +225,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
             tma_load_2d(vs + stg * kPairBytes + hd * 16384 + j * 8192, &tmv, 64 * hd, j ? y1 : y0, &st.v_full[stg]);
         issued_v = i + 1;
       }
+      // The CTA that starts when this one ends is, in the dispatch order, one
+      // wave (a CTA per SM) later: its Q and first pair of K/V blocks are
+      // pulled into L2 now, while this CTA's last pairs compute, so its
+      // set-up does not wait on HBM. (Only a prefetch: nothing depends on the
+      // guess.)
+      {
+        const int64_t nx = static_cast<int64_t>(blockIdx.x) + gridDim.x * (blockIdx.y + static_cast<int64_t>(gridDim.y) * blockIdx.z) +
+                           a.num_sms;
+        if (nx < static_cast<int64_t>(gridDim.x) * gridDim.y * gridDim.z) {
+          const int rh2 = static_cast<int>(nx % gridDim.x), h2 = static_cast<int>((nx / gridDim.x) % gridDim.y);
+          const int tile2 = static_cast<int>(nx / (static_cast<int64_t>(gridDim.x) * gridDim.y));
+          const int seq2 = a.batch.seq_of_tile(tile2);
+          const int64_t diag2 = a.batch.q_start[seq2] / kBlock + (tile2 - a.batch.tile_off[seq2]);
+          const int32_t tok2 = a.batch.q_off[seq2] + a.batch.tile_row0(seq2, tile2) + rh2 * (kTcTiles * 16);
+          for (int t = 0; t < kTcTiles; ++t)
+            for (int half = 0; half < 2; ++half) tma_prefetch_3d(&tmq, 64 * half, h2 * 8, tok2 + 16 * t);
+          for (int j = 0; j < 2; ++j) {
+            const int32_t b = a.idx == nullptr ? j : a.idx[(static_cast<int64_t>(tile2) * a.hkv + h2) * a.k_total + j];
+            if (b < 0 || b > diag2 || j >= a.k_total) continue;
+            if (kv.layout != MSA_KV_CONTIGUOUS) continue;  // paged: the page lookup is left to the CTA itself
+            const int32_t y = static_cast<int32_t>(kv.block_row(seq2, h2, b, nullptr, kIdPrefill));
+            for (int hd = 0; hd < 2; ++hd) {
+              tma_prefetch_2d(&tmk, 64 * hd, y);
+              tma_prefetch_2d(&tmv, 64 * hd, y);
+            }
+          }
+        }
+      }
       // drain: every load this thread issued has landed before the CTA may exit
       mbar_wait(&st.q_full, 0, a.status, kIdPrefill);
       for (int i = issued_k - kTcStages < 0 ? 0 : issued_k - kTcStages; i < issued_k; ++i)
@@ -488,7 +516,11 @@ cudaError_t set_prefill_tc_smem() {
 cudaError_t launch_prefill_tc(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                               const KvView& kv, const PrefillArgs& a, cudaStream_t stream) {
   dim3 grid(2, kv.hkv, a.batch.total_tiles());
-  prefill_tc_kernel<<<grid, kTcThreads, kTcSmem, stream>>>(tmq, tmk, tmv, kv, a);
+  PrefillArgs args = a;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&args.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) args.num_sms = 1;
+  prefill_tc_kernel<<<grid, kTcThreads, kTcSmem, stream>>>(tmq, tmk, tmv, kv, args);
   return cudaGetLastError();
 }
 

@@ -152,6 +152,14 @@ __device__ inline uint32_t taddr(uint32_t base, uint32_t lane, uint32_t col) { r
 
 }  // namespace tc
 
+// Pull one 3-D tile into L2 (no shared memory, no completion to wait for).
+__device__ inline void tma_prefetch_3d(const CUtensorMap* map, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // 3-D tiled TMA load (x innermost).
 __device__ inline void tma_load_3d(void* smem_dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
                                    uint64_t* bar) {
