@@ -241,9 +241,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const __grid_
           const int32_t tok2 = a.batch.q_off[seq2] + a.batch.tile_row0(seq2, tile2) + rh2 * (kTcTiles * 16);
           for (int t = 0; t < kTcTiles; ++t)
             for (int half = 0; half < 2; ++half) tma_prefetch_3d(&tmq, 64 * half, h2 * 8, tok2 + 16 * t);
-          for (int j = 0; j < 2; ++j) {
+          const int n_first = a.idx == nullptr ? 2 : min(2, a.k_total);  // the dense list is 0 .. diag
+          for (int j = 0; j < n_first; ++j) {
             const int32_t b = a.idx == nullptr ? j : a.idx[(static_cast<int64_t>(tile2) * a.hkv + h2) * a.k_total + j];
-            if (b < 0 || b > diag2 || j >= a.k_total) continue;
+            if (b < 0 || b > diag2) continue;
             if (kv.layout != MSA_KV_CONTIGUOUS) continue;  // paged: the page lookup is left to the CTA itself
             const int32_t y = static_cast<int32_t>(kv.block_row(seq2, h2, b, nullptr, kIdPrefill));
             for (int hd = 0; hd < 2; ++hd) {
