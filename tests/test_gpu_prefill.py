@@ -185,6 +185,20 @@ def test_prefill_paged_cache(dev, hq, hkv):
     verify_tiles(inp, res, range(n_tiles), range(hkv), 6, 7, rows_per_tile=9, check_dense=True)
 
 
+def test_prefill_diagonal_only_list(dev):
+    """k_scored = 0: every tile's list is its diagonal block alone (k_total =
+    1). 13 tiles x 8 KV heads on the tcgen05 kernel is 208 CTAs, more than
+    one per SM, so the CTAs that prefetch for one a wave later reach the
+    last unit's one-entry list."""
+    inp = make_prefill_inputs(64 * 20 + 9, 64 * 12 + 40, 8, 64, "bf16", seed=17, device=dev)
+    res = run_prefill(inp, 0, 1)
+    assert res["status"] == 0
+    n_tiles = msa_tiles(inp)
+    for j in range(n_tiles):
+        assert res["idx"][j].cpu().tolist() == [[inp.q_start // 64 + j]] * 8, f"tile {j}"
+    verify_tiles(inp, res, range(n_tiles), [0, 7], 0, 1, rows_per_tile=7)
+
+
 def test_prefill_all_blocks_equals_dense(dev):
     inp = make_prefill_inputs(64 * 6, 64 * 2 + 5, 2, 16, "bf16", seed=3, device=dev)
     res = run_prefill(inp, 1000, 1001, dense=True)
