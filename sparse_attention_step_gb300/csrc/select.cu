@@ -619,20 +619,25 @@ __device__ inline int pow2_at_least(int x) {
 }
 
 // Writes the final list of a unit: the blocks of the kk best keys ascending,
-// the forced block, then -1 padding. Called by every thread.
+// the forced block, then -1 padding. Called by every thread (at least 64);
+// top[0..kk) must be visible to all of them. A selected block's position is
+// the number of selected blocks below it (the blocks are distinct), counted
+// by one thread per block.
 __device__ inline void write_selection(const uint64_t* top, int kk, int64_t forced, bool keep0, int k_total,
-                                       int32_t* out, int* sorted_tmp) {
-  if (threadIdx.x < 32) warp_sort64_blocks_asc(top, kk, sorted_tmp);
-  __syncthreads();
+                                       int32_t* out) {
   const int o = keep0 ? 1 : 0;  // block 0 (attention sink) leads the list
+  if (static_cast<int>(threadIdx.x) < kk) {
+    // ascending blocks == descending complements (the key's low word)
+    const uint32_t me = static_cast<uint32_t>(top[threadIdx.x]);
+    int pos = 0;
+#pragma unroll 4
+    for (int j = 0; j < kk; ++j) pos += static_cast<uint32_t>(top[j]) > me ? 1 : 0;
+    out[o + pos] = static_cast<int>(~me);
+  }
   for (int i = threadIdx.x; i < k_total; i += blockDim.x) {
     const int j = i - o;
-    int v;
-    if (j < 0) v = 0;
-    else if (j < kk) v = sorted_tmp[j];
-    else if (j == kk && forced >= 0) v = static_cast<int>(forced);
-    else v = -1;
-    out[i] = v;
+    if (j >= 0 && j < kk) continue;  // a selected block, written above
+    out[i] = j < 0 ? 0 : (j == kk && forced >= 0 ? static_cast<int>(forced) : -1);
   }
 }
 
@@ -714,7 +719,6 @@ __global__ void __launch_bounds__(kTopk64Threads, 8) topk64_kernel(const float* 
   __shared__ SelectScratch scr;
   __shared__ RadixScratch radix;
   __shared__ uint64_t smp[64], lb;
-  __shared__ int sorted_blocks[64];
   __shared__ int count, n_surv;
   const int h = blockIdx.x, outer = blockIdx.y;
   const int64_t unit = static_cast<int64_t>(outer) * a.hkv + h;
@@ -769,7 +773,7 @@ __global__ void __launch_bounds__(kTopk64Threads, 8) topk64_kernel(const float* 
   if (k > 0 && !sampled_top(tk, n, k, smp, 64, scr.cand, top, &lb, &n_surv) && !block_select(tk, n, k, top, scr))
     block_compact_ge(tk, n, block_kth_largest(tk, n, k, radix), top, 64, &count);  // exactly the k best
   pdl_trigger();  // the attention kernel may start its set-up
-  write_selection(top, max(k, 0), forced, keep0, a.k_total, idx_out + unit * a.k_total, sorted_blocks);
+  write_selection(top, max(k, 0), forced, keep0, a.k_total, idx_out + unit * a.k_total);
 }
 
 template <typename T>
@@ -785,7 +789,6 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
   __shared__ uint64_t full[kSelStages], empty[kSelStages];
   __shared__ uint64_t top[64];
   __shared__ SelectScratch scr;
-  __shared__ int sorted_blocks[64];
   __shared__ int count, is_last;
 
   // chunk pieces are dispatched deepest first (grid z descending): the long
@@ -999,7 +1002,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
     if (!done) choose_top(keys, rows, kk_local, ring, top, scr, &count);
   }
   if (my_chunks == 1) {
-    write_selection(top, kk, forced, keep0, a.k_total, out, sorted_blocks);
+    write_selection(top, kk, forced, keep0, a.k_total, out);
     return;
   }
   // post this chunk's list; the unit's last CTA selects among them
@@ -1016,7 +1019,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_decode_kernel(const T* 
   for (int i = tid; i < n_all; i += blockDim.x) keys[i] = __ldcg(all + i);
   __syncthreads();
   if (kk > 0) choose_top(keys, n_all, kk, ring, top, scr, &count);
-  write_selection(top, kk, forced, keep0, a.k_total, out, sorted_blocks);
+  write_selection(top, kk, forced, keep0, a.k_total, out);
   if (tid == 0) a.tickets[unit] = 0;  // ready for the next call
 }
 

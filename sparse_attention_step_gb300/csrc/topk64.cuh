@@ -529,22 +529,4 @@ __device__ inline int block_compact_ge(const uint64_t* keys, int n, uint64_t t, 
   return min(*count, cap);
 }
 
-// One warp: sort up to 64 block ids ascending (entries >= n are padding).
-__device__ inline void warp_sort64_blocks_asc(const uint64_t* top, int n, int* out) {
-  const int lane = threadIdx.x & 31;
-  // ascending blocks == descending complements (the key's low word); 0 pads
-  uint32_t x[2];
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int e = 2 * lane + r;
-    x[r] = e < n ? static_cast<uint32_t>(top[e]) : 0u;
-  }
-  warp_sort64_desc(x);
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int e = 2 * lane + r;
-    if (e < n) out[e] = static_cast<int>(~x[r]);
-  }
-}
-
 }  // namespace msa
