@@ -72,6 +72,8 @@ def run_decode_sink(inp, k_scored, k_total, step, kidx=None):
     ("paged", 5, True),          # fused decode step on a paged cache
     ("paged", 5, False),         # chunked selection kernel + attention
     ("contiguous", 70, False),   # radix top-k (k above 64)
+    ("paged", 64, False),        # chunked selection at its largest k: the list fills k_total
+    ("contiguous", 64, True),    # fused decode step at its largest k
 ])
 def test_decode_sink(dev, layout, k_scored, step):
     lens = [64 * 150 + 7, 64 * 12, 64 + 3, 40]
